@@ -1,0 +1,442 @@
+"""Benchmark of the 8-bit paged KV cache hot path on GB300: one step = kvq_store + kvq_decode.
+
+Default workload (``qwen3_1p7b``): a Qwen3-1.7B-shaped attention layer -- Hq=16, Hkv=8, head_dim=128,
+page 16 -- storing 8 x 2048 new rows and decoding batch 8 over contexts drawn uniformly from
+[1024, 16384], fp8_e4m3.  Inputs are seeded synthetic tensors (workloads.py).  Prints one JSON line.
+
+Metric: algorithmic HBM bytes moved by the step per second (GB/s), i.e. store bytes (bf16 in, codes
+and fp16 scales out, slot mapping) plus decode bytes (codes and scales of every valid token, q,
+block table, output), divided by the device time of the step.  L2 is flushed between steps.
+
+``--impl reference`` times the CPU oracle (the plain C reference of the same computation) on the
+host cores, on a bounded sample of the same workload, and prints the same line with
+``"impl": "reference"``.
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="qwen3_1p7b",
+                    choices=["qwen3_1p7b", "long_gqa", "mla", "serving", "tiny"])
+    ap.add_argument("--kind", default="fp8_e4m3", choices=["fp8_e4m3", "q8_0"])
+    ap.add_argument("--batch", type=int, default=None, help="long_gqa / serving batch override")
+    ap.add_argument("--ctx", type=int, default=None, help="long_gqa / mla context override")
+    ap.add_argument("--path", type=int, default=0, help="decode path: 0 auto, 1 CUDA cores, 2 tcgen05")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--seed", type=int, default=None)
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------------------------------ setup
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() and args.impl == "ours" else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return world, rank
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def make_case(args, device):
+    from block_quantized_bit_gb300 import workloads
+    kw = {}
+    if args.seed is not None:
+        kw["seed"] = args.seed
+    if args.workload == "long_gqa":
+        kw.update(batch=args.batch or 1, ctx=args.ctx or 262144)
+    elif args.workload == "mla":
+        kw.update(ctx=args.ctx or 163840)
+    elif args.workload == "serving" and args.batch:
+        kw.update(batch=args.batch)
+    return workloads.make(args.workload, kind=args.kind, device=device, **kw)
+
+
+def valid_tokens(case):
+    """Tokens the decode reads: t < seq_len whose page is not masked."""
+    bt = case.block_table.cpu()
+    lens = case.seq_lens.cpu().tolist()
+    P = case.page_size
+    total = 0
+    for b, L in enumerate(lens):
+        n = (L + P - 1) // P
+        pages = bt[b, :n]
+        full = int((pages >= 0).sum())
+        last_masked = n > 0 and int(pages[n - 1]) < 0
+        tail = L - (n - 1) * P if n > 0 else 0
+        total += full * P - ((P - tail) if (n > 0 and not last_masked) else 0)
+    return total
+
+
+def algorithmic_bytes(case):
+    """(store_bytes, decode_bytes) of one step -- the method's own traffic."""
+    n_kv = 1 if case.mla else 2
+    row_elems = n_kv * case.num_kv_heads * case.head_dim
+    if case.new_k is not None:
+        store_rows = int(case.new_k.shape[0])
+    else:
+        store_rows = int(case.k.shape[0])
+    store = store_rows * (row_elems * (2 + 1 + 2 / 32) + 8)
+    toks = valid_tokens(case)
+    pages = sum((int(L) + case.page_size - 1) // case.page_size for L in case.seq_lens.cpu().tolist())
+    decode = toks * row_elems * 17 / 16 + case.q.numel() * 2 + case.batch * case.num_q_heads * case.v_dim * 2 \
+        + pages * 4 + case.batch * 4
+    return store, decode, store_rows, toks
+
+
+# ------------------------------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while the timed region runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index=0):
+        self.proc = None
+        self.gpu = gpu_index
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons = [], [], set()
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for name, val in zip(("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"),
+                                 f[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------------------------------ ours
+def run_ours(args, world, rank):
+    from block_quantized_bit_gb300 import kvq
+    dev = torch.device("cuda", torch.cuda.current_device())
+    case = make_case(args, "cuda")
+    L = kvq.Layout(case.num_pages, case.page_size, case.num_kv_heads, case.head_dim, case.v_dim, case.mla)
+    codes, scales = kvq.alloc_pool(L, dev)
+    codes.zero_()
+    scales.zero_()
+    # fill the cached context (untimed)
+    kvq.kvq_store(codes, scales, case.k, case.v, case.slot_mapping, L, case.kind)
+    if case.new_k is not None:
+        sk, sv, ss = case.new_k, case.new_v, case.new_slots
+    else:  # the store step re-stores the context rows
+        sk, sv, ss = case.k, case.v, case.slot_mapping
+    out = torch.empty(case.batch, case.num_q_heads, case.v_dim, dtype=torch.bfloat16, device=dev)
+    ws = kvq.alloc_workspace(L, case.batch, case.num_q_heads, case.max_pages, dev, path=args.path)
+    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)  # 4x L2
+    stream = torch.cuda.current_stream()
+
+    def step():
+        kvq.kvq_store(codes, scales, sk, sv, ss, L, case.kind)
+        kvq.kvq_decode(case.q, codes, scales, case.block_table, case.seq_lens, out, ws, L, case.kind,
+                       case.sm_scale, path=args.path)
+
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        step()
+    torch.cuda.synchronize()
+    st = kvq.kvq_workspace_status(ws)
+    if st != 0:
+        raise RuntimeError("decode reported status %d" % st)
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    for i in range(K):
+        flush.fill_(i & 0xFF)
+        ev[i][0].record(stream)
+        kvq.kvq_store(codes, scales, sk, sv, ss, L, case.kind)
+        ev[i][1].record(stream)
+        kvq.kvq_decode(case.q, codes, scales, case.block_table, case.seq_lens, out, ws, L, case.kind,
+                       case.sm_scale, path=args.path)
+        ev[i][2].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    store_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
+    dec_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K)]
+    step_ms = [a + b for a, b in zip(store_ms, dec_ms)]
+    total_ms = max_over_ranks(sum(step_ms), world)
+    ms_per_step = total_ms / K
+
+    store_b, dec_b, store_rows, toks = algorithmic_bytes(case)
+    value = world * (store_b + dec_b) * K / (total_ms / 1e3) / 1e9
+    peaks = load_peaks()
+    hbm = peaks.get("hbm_gbs")
+    dec_avg_s = statistics.mean(dec_ms) / 1e3
+    store_avg_s = statistics.mean(store_ms) / 1e3
+    dec_gbs = dec_b / dec_avg_s / 1e9
+    store_gbs = store_b / store_avg_s / 1e9
+
+    # end to end through the public API: host inputs (pinned) in, host output back, every step
+    e2e = run_e2e(args, case, L, codes, scales, sk, sv, ss, ws, flush, world)
+    e2e["value"] = world * (store_b + dec_b) / e2e.pop("step_s") / 1e9
+    e2e["unit"] = "GB/s"
+
+    launches_per_step = 3  # store kernel, decode split kernel, merge kernel
+    res = {
+        "metric": "quantized-KV decode attention HBM GB/s (% of GB300 peak); kvq_store GB/s",
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "u8" if args.kind == "q8_0" else "fp8_e4m3",
+        "data": "synthetic (seeded; workloads.py)",
+        "config": {"workload": args.workload, "kind": args.kind, "batch": case.batch,
+                   "num_q_heads": case.num_q_heads, "num_kv_heads": case.num_kv_heads,
+                   "head_dim": case.head_dim, "v_dim": case.v_dim, "page_size": case.page_size,
+                   "store_rows": store_rows, "decode_tokens": toks,
+                   "seq_lens": [int(x) for x in case.seq_lens.cpu().tolist()][:16],
+                   "l2": "flushed between steps (512 MB write)", "parallelism": "replicas" if world > 1 else "1 gpu"},
+        "store_gbs": round(store_gbs, 1),
+        "store_frac_hbm": round(store_gbs / hbm, 4) if hbm else None,
+        "decode_gbs": round(dec_gbs, 1),
+        "decode_frac_hbm": round(dec_gbs / hbm, 4) if hbm else None,
+        "decode_us": round(dec_avg_s * 1e6, 2),
+        "decode_us_per_token": round(dec_avg_s * 1e6 / case.batch, 3),
+        "store_us": round(store_avg_s * 1e6, 2),
+        "roofline": {"bound": "hbm", "kernel": "kvq_decode (split kernel + merge)",
+                     "achieved": round(dec_gbs, 1), "peak": hbm, "unit": "GB/s",
+                     "frac": round(dec_gbs / hbm, 4) if hbm else None,
+                     "peak_source": "MEASURED_PEAKS.json hbm_gbs (of measured)" if hbm else "fallback 6800",
+                     "traffic": None},
+        "clocks": clk,
+        "e2e": e2e,
+        "gpu_launches": launches_per_step * K,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        res["cpu_baseline"] = cpu_baseline(case, args)
+    return res
+
+
+def run_e2e(args, case, L, codes, scales, sk, sv, ss, ws, flush, world):
+    from block_quantized_bit_gb300 import kvq
+    dev = codes.device
+    hk = sk.cpu().pin_memory()
+    hv = None if sv is None else sv.cpu().pin_memory()
+    hs = ss.cpu().pin_memory()
+    hq = case.q.cpu().pin_memory()
+    hbt = case.block_table.cpu().pin_memory()
+    hsl = case.seq_lens.cpu().pin_memory()
+    hout = torch.empty((case.batch, case.num_q_heads, case.v_dim), dtype=torch.bfloat16).pin_memory()
+    dk, dv, ds = torch.empty_like(sk), None if sv is None else torch.empty_like(sv), torch.empty_like(ss)
+    dq, dbt, dsl = torch.empty_like(case.q), torch.empty_like(case.block_table), torch.empty_like(case.seq_lens)
+    dout = torch.empty((case.batch, case.num_q_heads, case.v_dim), dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def one():
+        dk.copy_(hk, non_blocking=True)
+        if dv is not None:
+            dv.copy_(hv, non_blocking=True)
+        ds.copy_(hs, non_blocking=True)
+        dq.copy_(hq, non_blocking=True)
+        dbt.copy_(hbt, non_blocking=True)
+        dsl.copy_(hsl, non_blocking=True)
+        kvq.kvq_store(codes, scales, dk, dv, ds, L, case.kind)
+        kvq.kvq_decode(dq, codes, scales, dbt, dsl, dout, ws, L, case.kind, case.sm_scale, path=args.path)
+        hout.copy_(dout, non_blocking=True)
+
+    for _ in range(max(3, args.warmup)):
+        one()
+    torch.cuda.synchronize()
+    K = args.steps
+    tot = 0.0
+    for _ in range(K):
+        flush.fill_(3)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        one()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        tot += e0.elapsed_time(e1)
+    tot = max_over_ranks(tot, world)
+    h2d = sum(t.numel() * t.element_size() for t in (hk, hs, hq, hbt, hsl)) + (0 if hv is None else
+                                                                               hv.numel() * hv.element_size())
+    d2h = hout.numel() * hout.element_size()
+    return {"step_s": tot / K / 1e3, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+
+
+def load_peaks():
+    try:
+        return json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "_fallback": True}
+
+
+# ------------------------------------------------------------------------------------------ oracle
+def oracle_sample(case, budget_rows=None, max_seqs=None):
+    """A bounded sample of the workload for the CPU oracle: the store rows and the sequences decoded."""
+    n_rows = int((case.new_k if case.new_k is not None else case.k).shape[0])
+    if budget_rows is not None:
+        n_rows = min(n_rows, budget_rows)
+    seqs = list(range(case.batch if max_seqs is None else min(case.batch, max_seqs)))
+    return n_rows, seqs
+
+
+def oracle_step(case, codes, scales, n_rows, seqs, threads):
+    """One oracle step over the sample: store n_rows rows, decode the chosen sequences.  Returns bytes."""
+    import oracle as O
+    bits = lambda t: t.contiguous().view(torch.int16).numpy().view(np.uint16)  # noqa: E731
+    if case.new_k is not None:
+        k, v, s = case.new_k[:n_rows], None if case.new_v is None else case.new_v[:n_rows], case.new_slots[:n_rows]
+    else:
+        k, v, s = case.k[:n_rows], None if case.v is None else case.v[:n_rows], case.slot_mapping[:n_rows]
+    O.store(codes, scales, bits(k), None if v is None else bits(v), s.numpy(), num_kv_heads=case.num_kv_heads,
+            head_dim=case.head_dim, page_size=case.page_size, mla=case.mla, kind=case.kind)
+    idx = torch.tensor(seqs, dtype=torch.long)
+    O.decode(bits(case.q[idx]), codes, scales, case.block_table[idx].numpy(), case.seq_lens[idx].numpy(),
+             num_q_heads=case.num_q_heads, num_kv_heads=case.num_kv_heads, head_dim=case.head_dim,
+             v_dim=case.v_dim, page_size=case.page_size, mla=case.mla, kind=case.kind, sm_scale=case.sm_scale,
+             nthreads=threads)
+    n_kv = 1 if case.mla else 2
+    row = n_kv * case.num_kv_heads * case.head_dim
+    sub = type(case)(**{**case.__dict__, "seq_lens": case.seq_lens[idx], "block_table": case.block_table[idx],
+                        "q": case.q[idx]})
+    toks = valid_tokens(sub)
+    return n_rows * (row * (2 + 1 + 2 / 32) + 8) + toks * row * 17 / 16
+
+
+def prepare_oracle(case):
+    import oracle as O
+    from oracle import build_oracle
+    build_oracle.build()
+    cpu = type(case)(**{k: (v.cpu() if isinstance(v, torch.Tensor) else v) for k, v in case.__dict__.items()})
+    codes = np.zeros((cpu.num_pages, 1 if cpu.mla else 2, cpu.num_kv_heads, cpu.page_size, cpu.head_dim), np.uint8)
+    scales = np.zeros(codes.shape[:-1] + (cpu.head_dim // 32,), np.uint16)
+    return O, cpu, codes, scales
+
+
+def cpu_baseline(case, args):
+    """The oracle, as it stands, on a bounded sample of the same workload (~10-30 s of CPU work)."""
+    O, cpu, codes, scales = prepare_oracle(case)
+    threads = max(1, O.openmp_threads())
+    n_rows, seqs = oracle_sample(cpu, budget_rows=2048, max_seqs=2)
+    t0 = time.perf_counter()
+    nbytes = oracle_step(cpu, codes, scales, n_rows, seqs, threads)
+    dt = time.perf_counter() - t0
+    return {"value": round(nbytes / dt / 1e9, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "sample": "store of %d rows + fp64 decode of %d of %d sequences (all heads), one pass, %.1f s"
+                      % (n_rows, len(seqs), cpu.batch, dt)}
+
+
+def run_reference(args, world, rank):
+    """Reference arm: the CPU oracle on the host cores, same workload/metric, bounded sample per step."""
+    if rank != 0:
+        return None
+    case = make_case(args, "cpu")
+    O, cpu, codes, scales = prepare_oracle(case)
+    threads = max(1, O.openmp_threads())
+    n_rows, seqs = oracle_sample(cpu, budget_rows=512, max_seqs=1)
+    for _ in range(args.warmup):
+        oracle_step(cpu, codes, scales, n_rows, seqs, threads)
+    t0 = time.perf_counter()
+    nb = 0.0
+    for _ in range(args.steps):
+        nb += oracle_step(cpu, codes, scales, n_rows, seqs, threads)
+    dt = time.perf_counter() - t0
+    value = nb / dt / 1e9
+    sample = "store of %d rows + fp64 decode of %d of %d sequences (all heads) per step" % (n_rows, len(seqs),
+                                                                                          cpu.batch)
+    return {
+        "impl": "reference",
+        "metric": "quantized-KV decode attention HBM GB/s (% of GB300 peak); kvq_store GB/s",
+        "value": round(value, 5), "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(dt / args.steps * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded; workloads.py)",
+        "config": {"workload": args.workload, "kind": args.kind, "sample": sample},
+        "cpu_baseline": {"value": round(value, 5), "unit": "GB/s", "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 5), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    args = parse()
+    world, rank = dist_setup(args)
+    if args.impl == "reference":
+        res = run_reference(args, world, rank)
+    else:
+        if not torch.cuda.is_available():
+            raise SystemExit("bench.py needs a CUDA GPU for --impl ours")
+        from __graft_entry__ import build
+        build()
+        res = run_ours(args, world, rank)
+    if rank == 0 and res is not None:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

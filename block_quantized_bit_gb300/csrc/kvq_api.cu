@@ -1,0 +1,283 @@
+// kvq_api.cu -- the C ABI of libkvq: argument validation, the pool cost model, workspace sizing and
+// kernel dispatch.  Every check runs on the host before any launch; a rejected call touches nothing.
+//
+// Cost model: "feat(kvcache): 8-bit KV cache (q8_0 / fp8_e4m3) behind --kv-cache-dtype", section "What"
+// (1.0625 bytes per element: one code byte plus an fp16 scale per 32 elements) and its review comment's
+// "End-to-end numbers" (the KV pool grows by 2 / 1.0625 at the same budget).  "feat(kvcache): 8-bit
+// DSV4 window/compressed KV", section "One ordering trap": the budget must be priced with the same
+// bytes-per-token the pool uses, which is why both come from this one function.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdint>
+#include <limits>
+
+#include "../../include/kvq.h"
+#include "kvq_internal.h"
+
+namespace kvq {
+
+namespace {
+
+constexpr size_t kAlign = 16;
+constexpr uint32_t kStatusTimeoutWord = 0x7100u;  // written by a kernel that gave up a bounded wait
+
+bool aligned(const void* p) { return (reinterpret_cast<uintptr_t>(p) % kAlign) == 0; }
+
+int n_kv_of(const kvq_layout& L) { return L.mla ? 1 : 2; }
+
+kvq_status check_layout(const kvq_layout* L) {
+  if (L == nullptr) return KVQ_EINVAL;
+  if (L->num_pages < 0 || L->page_size <= 0 || L->num_kv_heads <= 0) return KVQ_EINVAL;
+  if (L->mla != 0 && L->mla != 1) return KVQ_EINVAL;
+  if (L->head_dim <= 0 || L->head_dim % 32 != 0) return KVQ_EHEADDIM;
+  if (L->v_dim <= 0 || L->v_dim % 32 != 0) return KVQ_EHEADDIM;
+  if (!L->mla && L->v_dim != L->head_dim) return KVQ_EINVAL;
+  if (L->mla && L->v_dim > L->head_dim) return KVQ_EINVAL;
+  // element count must fit comfortably in int64 / size_t
+  const double elems = static_cast<double>(L->num_pages) * n_kv_of(*L) * L->num_kv_heads * L->page_size *
+                       static_cast<double>(L->head_dim);
+  if (elems > 4.0e18) return KVQ_EINVAL;
+  return KVQ_OK;
+}
+
+bool kind_ok(int kind) { return kind == KVQ_FP8_E4M3 || kind == KVQ_Q8_0; }
+
+size_t elems_of(const kvq_layout& L) {
+  return static_cast<size_t>(L.num_pages) * n_kv_of(L) * L.num_kv_heads * L.page_size * L.head_dim;
+}
+
+struct WorkspacePlan {
+  int32_t heads_per_item;
+  int32_t query_groups;
+  int64_t max_items;
+  size_t acc_offset, ml_offset, total;
+};
+
+int32_t choose_path(const kvq_layout& L, int32_t num_q_heads, const kvq_decode_options* opt) {
+  (void)L;
+  (void)num_q_heads;
+  const int32_t want = opt ? opt->path : 0;
+  if (want == 2) return -1;  // no tensor-core kernel in this build
+  return 1;
+}
+
+bool plan_workspace(const kvq_layout& L, int32_t batch, int32_t num_q_heads, int32_t max_pages,
+                    const kvq_decode_options* opt, WorkspacePlan* w) {
+  if (batch < 0 || num_q_heads <= 0 || max_pages <= 0) return false;
+  if (num_q_heads % L.num_kv_heads != 0) return false;
+  const int32_t group = num_q_heads / L.num_kv_heads;
+  const int32_t pps = opt ? opt->pages_per_split : 0;
+  if (pps < 0) return false;
+  w->heads_per_item = cc_heads_per_item(group, L.head_dim, L.mla);
+  w->query_groups = L.num_kv_heads * (group / w->heads_per_item);
+  w->max_items = max_work_items(batch, w->query_groups, max_pages, pps);
+  const size_t acc = static_cast<size_t>(w->max_items) * w->heads_per_item * L.v_dim * sizeof(float);
+  const size_t ml = static_cast<size_t>(w->max_items) * w->heads_per_item * 2 * sizeof(float);
+  w->acc_offset = kWorkspaceHeader;
+  w->ml_offset = w->acc_offset + ((acc + 255) / 256) * 256;
+  w->total = w->ml_offset + ((ml + 255) / 256) * 256;
+  return true;
+}
+
+}  // namespace
+
+int64_t max_work_items(int32_t batch, int32_t query_groups, int32_t max_pages, int32_t pages_per_split) {
+  const int64_t per_seq = static_cast<int64_t>(query_groups);
+  if (pages_per_split > 0)
+    return static_cast<int64_t>(batch) * per_seq * ((max_pages + pages_per_split - 1) / pages_per_split);
+  const int64_t upper = static_cast<int64_t>(batch) * per_seq * ((max_pages + kMinPagesPerSplit - 1) / kMinPagesPerSplit);
+  return std::min<int64_t>(upper, kTargetItems + static_cast<int64_t>(batch) * per_seq);
+}
+
+}  // namespace kvq
+
+using namespace kvq;
+
+extern "C" {
+
+const char* kvq_version(void) { return "0.1.0"; }
+
+const char* kvq_strerror(kvq_status s) {
+  switch (s) {
+    case KVQ_OK: return "ok";
+    case KVQ_EINVAL: return "invalid argument";
+    case KVQ_EKIND: return "unknown quantization kind (expected KVQ_FP8_E4M3 or KVQ_Q8_0)";
+    case KVQ_EHEADDIM: return "head_dim and v_dim must be positive multiples of 32 (the quantization block)";
+    case KVQ_EALIGN: return "device pointers must be 16-byte aligned";
+    case KVQ_EWORKSPACE: return "workspace smaller than kvq_decode_workspace_bytes()";
+    case KVQ_EARCH: return "current device is not compute capability 10.3 (GB300, sm_103a)";
+    case KVQ_ECUDA: return "a CUDA call or kernel launch failed";
+    case KVQ_EUNSUPPORTED: return "no decode kernel for this page size / head_dim / path";
+    case KVQ_ETIMEOUT: return "a kernel gave up a bounded wait; its output is not valid";
+  }
+  return "unknown status";
+}
+
+size_t kvq_pool_bytes(const kvq_layout* layout) {
+  if (check_layout(layout) != KVQ_OK) return 0;
+  return elems_of(*layout);
+}
+
+size_t kvq_scale_bytes(const kvq_layout* layout) {
+  if (check_layout(layout) != KVQ_OK) return 0;
+  return elems_of(*layout) / 32 * 2;
+}
+
+double kvq_bytes_per_token(const kvq_layout* layout) {
+  if (check_layout(layout) != KVQ_OK) return -1.0;
+  const double elems = static_cast<double>(n_kv_of(*layout)) * layout->num_kv_heads * layout->head_dim;
+  return elems + elems / 32.0 * 2.0;
+}
+
+int64_t kvq_num_pages(const kvq_layout* layout, size_t budget_bytes) {
+  if (check_layout(layout) != KVQ_OK) return -1;
+  const uint64_t elems_per_page =
+      static_cast<uint64_t>(n_kv_of(*layout)) * layout->num_kv_heads * layout->page_size * layout->head_dim;
+  const uint64_t bytes_per_page = elems_per_page + elems_per_page / 32 * 2;
+  return static_cast<int64_t>(budget_bytes / bytes_per_page);
+}
+
+kvq_status kvq_device_check(void) {
+  int dev = 0, major = 0, minor = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return KVQ_ECUDA;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess) return KVQ_ECUDA;
+  if (cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) return KVQ_ECUDA;
+  if (major != 10 || minor != 3) return KVQ_EARCH;
+  return KVQ_OK;
+}
+
+kvq_status kvq_store(void* pool, void* scales, const void* k, const void* v, const int64_t* slot_mapping,
+                     int64_t num_tokens, const kvq_layout* layout, kvq_kind kind, void* stream) {
+  kvq_status st = check_layout(layout);
+  if (st != KVQ_OK) return st;
+  if (!kind_ok(kind)) return KVQ_EKIND;
+  if (num_tokens < 0) return KVQ_EINVAL;
+  if (layout->mla ? (v != nullptr) : false) return KVQ_EINVAL;
+  if (num_tokens == 0) return KVQ_OK;
+  if (!pool || !scales || !k || !slot_mapping || (!layout->mla && !v)) return KVQ_EINVAL;
+  if (!aligned(pool) || !aligned(scales) || !aligned(k) || (v && !aligned(v)) ||
+      (reinterpret_cast<uintptr_t>(slot_mapping) % 8) != 0)
+    return KVQ_EALIGN;
+  st = kvq_device_check();
+  if (st != KVQ_OK) return st;
+  return launch_store(pool, scales, k, v, slot_mapping, num_tokens, *layout, kind,
+                      static_cast<cudaStream_t>(stream));
+}
+
+size_t kvq_decode_workspace_bytes_ex(const kvq_layout* layout, int32_t batch, int32_t num_q_heads,
+                                     int32_t max_pages_per_seq, const kvq_decode_options* options) {
+  if (check_layout(layout) != KVQ_OK) return 0;
+  WorkspacePlan w;
+  if (!plan_workspace(*layout, batch, num_q_heads, max_pages_per_seq, options, &w)) return 0;
+  return w.total;
+}
+
+size_t kvq_decode_workspace_bytes(const kvq_layout* layout, int32_t batch, int32_t num_q_heads,
+                                  int32_t max_pages_per_seq) {
+  return kvq_decode_workspace_bytes_ex(layout, batch, num_q_heads, max_pages_per_seq, nullptr);
+}
+
+kvq_status kvq_decode_ex(const void* q, const void* pool, const void* scales, const int32_t* block_table,
+                         int32_t max_pages_per_seq, const int32_t* seq_lens, int32_t batch, int32_t num_q_heads,
+                         float sm_scale, void* out, kvq_out_dtype out_dtype, void* workspace,
+                         size_t workspace_bytes, const kvq_layout* layout, kvq_kind kind,
+                         const kvq_decode_options* options, void* stream) {
+  kvq_status st = check_layout(layout);
+  if (st != KVQ_OK) return st;
+  if (!kind_ok(kind)) return KVQ_EKIND;
+  if (out_dtype != KVQ_OUT_BF16 && out_dtype != KVQ_OUT_F32) return KVQ_EINVAL;
+  if (batch < 0 || num_q_heads <= 0 || max_pages_per_seq <= 0) return KVQ_EINVAL;
+  if (num_q_heads % layout->num_kv_heads != 0) return KVQ_EINVAL;
+  if (!(sm_scale == sm_scale) || sm_scale > std::numeric_limits<float>::max() ||
+      sm_scale < -std::numeric_limits<float>::max())
+    return KVQ_EINVAL;
+  if (options && (options->pages_per_split < 0 || options->path < 0 || options->path > 2)) return KVQ_EINVAL;
+  if (layout->page_size != kPageTokens) return KVQ_EUNSUPPORTED;
+  if (!decode_cc_supported(layout->head_dim, layout->v_dim, layout->mla)) return KVQ_EUNSUPPORTED;
+  const int32_t path = choose_path(*layout, num_q_heads, options);
+  if (path < 0) return KVQ_EUNSUPPORTED;
+  WorkspacePlan w;
+  if (!plan_workspace(*layout, batch, num_q_heads, max_pages_per_seq, options, &w)) return KVQ_EINVAL;
+  if (batch == 0) return KVQ_OK;
+  if (!q || !pool || !scales || !block_table || !seq_lens || !out || !workspace) return KVQ_EINVAL;
+  if (workspace_bytes < w.total) return KVQ_EWORKSPACE;
+  if (!aligned(q) || !aligned(pool) || !aligned(scales) || !aligned(out) || !aligned(workspace) ||
+      (reinterpret_cast<uintptr_t>(block_table) % 4) != 0 || (reinterpret_cast<uintptr_t>(seq_lens) % 4) != 0)
+    return KVQ_EALIGN;
+  st = kvq_device_check();
+  if (st != KVQ_OK) return st;
+
+  DecodeArgs a;
+  a.q = q;
+  a.codes = static_cast<const uint8_t*>(pool);
+  a.scales = static_cast<const uint16_t*>(scales);
+  a.block_table = block_table;
+  a.num_pages = layout->num_pages;
+  a.max_pages = max_pages_per_seq;
+  a.seq_lens = seq_lens;
+  a.batch = batch;
+  a.num_q_heads = num_q_heads;
+  a.num_kv_heads = layout->num_kv_heads;
+  a.head_dim = layout->head_dim;
+  a.v_dim = layout->v_dim;
+  a.mla = layout->mla;
+  a.sm_scale = sm_scale;
+  a.out = out;
+  a.out_dtype = out_dtype;
+  a.kind = kind;
+  a.pages_per_split = options ? options->pages_per_split : 0;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  a.status = reinterpret_cast<uint32_t*>(ws);
+  a.part_acc = reinterpret_cast<float*>(ws + w.acc_offset);
+  a.part_ml = reinterpret_cast<float*>(ws + w.ml_offset);
+  a.max_items = w.max_items;
+  a.heads_per_item = w.heads_per_item;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(ws, 0, sizeof(uint32_t), s) != cudaSuccess) return KVQ_ECUDA;
+  st = launch_decode_cc(a, s);
+  if (st != KVQ_OK) return st;
+  return launch_merge(a, w.query_groups, s);
+}
+
+kvq_status kvq_decode(const void* q, const void* pool, const void* scales, const int32_t* block_table,
+                      int32_t max_pages_per_seq, const int32_t* seq_lens, int32_t batch, int32_t num_q_heads,
+                      float sm_scale, void* out, kvq_out_dtype out_dtype, void* workspace, size_t workspace_bytes,
+                      const kvq_layout* layout, kvq_kind kind, void* stream) {
+  return kvq_decode_ex(q, pool, scales, block_table, max_pages_per_seq, seq_lens, batch, num_q_heads, sm_scale, out,
+                       out_dtype, workspace, workspace_bytes, layout, kind, nullptr, stream);
+}
+
+kvq_status kvq_workspace_status(const void* workspace, void* stream) {
+  if (!workspace) return KVQ_EINVAL;
+  uint32_t word = 0;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(&word, workspace, sizeof(word), cudaMemcpyDeviceToHost, s) != cudaSuccess) return KVQ_ECUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return KVQ_ECUDA;
+  if (word == 0) return KVQ_OK;
+  return word == kStatusTimeoutWord ? KVQ_ETIMEOUT : KVQ_EINVAL;
+}
+
+kvq_status kvq_encode_probe(kvq_kind kind, const float* y, uint8_t* codes, int64_t n, void* stream) {
+  if (!kind_ok(kind)) return KVQ_EKIND;
+  if (n < 0) return KVQ_EINVAL;
+  if (n == 0) return KVQ_OK;
+  if (!y || !codes) return KVQ_EINVAL;
+  kvq_status st = kvq_device_check();
+  if (st != KVQ_OK) return st;
+  return launch_encode_probe(kind, y, codes, n, static_cast<cudaStream_t>(stream));
+}
+
+kvq_status kvq_dequant_probe(kvq_kind kind, const uint8_t* codes, const uint16_t* scales, uint16_t* out, int64_t n,
+                             void* stream) {
+  if (!kind_ok(kind)) return KVQ_EKIND;
+  if (n < 0 || n % 16 != 0) return KVQ_EINVAL;
+  if (n == 0) return KVQ_OK;
+  if (!codes || !scales || !out) return KVQ_EINVAL;
+  if (!aligned(codes) || !aligned(out)) return KVQ_EALIGN;
+  kvq_status st = kvq_device_check();
+  if (st != KVQ_OK) return st;
+  return launch_dequant_probe(kind, codes, scales, out, n, static_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"

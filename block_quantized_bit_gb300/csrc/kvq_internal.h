@@ -1,0 +1,61 @@
+// kvq_internal.h -- launchers shared between the libkvq translation units (host side).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/kvq.h"
+
+namespace kvq {
+
+// Arguments of one decode call after host validation.
+struct DecodeArgs {
+  const void* q;
+  const uint8_t* codes;
+  const uint16_t* scales;
+  const int32_t* block_table;
+  int64_t num_pages;
+  int32_t max_pages;
+  const int32_t* seq_lens;
+  int32_t batch;
+  int32_t num_q_heads;
+  int32_t num_kv_heads;
+  int32_t head_dim;
+  int32_t v_dim;
+  int32_t mla;
+  float sm_scale;
+  void* out;
+  kvq_out_dtype out_dtype;
+  kvq_kind kind;
+  int32_t pages_per_split;  // 0 = automatic
+  // workspace carve-up
+  uint32_t* status;
+  float* part_acc;   // [max_items][heads_per_item][v_dim]
+  float* part_ml;    // [max_items][heads_per_item][2]
+  int64_t max_items;
+  int32_t heads_per_item;  // query heads one work item covers (a tile of the group)
+};
+
+// Tokens per page the decode kernels support, and the workspace's leading status block.
+constexpr int kPageTokens = 16;
+constexpr size_t kWorkspaceHeader = 256;
+
+// Work-item planning constants shared by the host (workspace bound) and the kernels.
+constexpr int kTargetItems = 1216;  // 8 items per SM on a 152-SM GB300
+constexpr int kMinPagesPerSplit = 4;
+
+// Heads of one query group that a CUDA-core work item covers.
+int32_t cc_heads_per_item(int32_t group, int32_t head_dim, int32_t mla);
+// Upper bound on work items for the given sizes (used for workspace sizing and the grid).
+int64_t max_work_items(int32_t batch, int32_t query_groups, int32_t max_pages, int32_t pages_per_split);
+
+kvq_status launch_store(void* pool, void* scales, const void* k, const void* v, const int64_t* slot_mapping,
+                        int64_t num_tokens, const kvq_layout& L, kvq_kind kind, cudaStream_t stream);
+kvq_status launch_encode_probe(kvq_kind kind, const float* y, uint8_t* codes, int64_t n, cudaStream_t stream);
+kvq_status launch_dequant_probe(kvq_kind kind, const uint8_t* codes, const uint16_t* scales, uint16_t* out,
+                                int64_t n, cudaStream_t stream);
+bool decode_cc_supported(int32_t head_dim, int32_t v_dim, int32_t mla);
+kvq_status launch_decode_cc(const DecodeArgs& a, cudaStream_t stream);
+kvq_status launch_merge(const DecodeArgs& a, int32_t query_groups, cudaStream_t stream);
+
+}  // namespace kvq

@@ -1,0 +1,227 @@
+"""Thin ctypes binding of libkvq (``include/kvq.h``), with the same entry-point names.
+
+Argument marshalling only: torch tensors are passed as raw device pointers plus sizes, and the
+current torch CUDA stream as the ``stream`` argument.  Every step of the store and the decode runs
+in libkvq's CUDA kernels.  If the library has not been built, importing works but every call raises
+``RuntimeError`` -- there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+from typing import Optional
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libkvq.so")
+
+KVQ_FP8_E4M3 = 1
+KVQ_Q8_0 = 2
+KIND = {"fp8_e4m3": KVQ_FP8_E4M3, "q8_0": KVQ_Q8_0}
+KVQ_OUT_BF16 = 0
+KVQ_OUT_F32 = 1
+
+STATUS = {0: "KVQ_OK", -1: "KVQ_EINVAL", -2: "KVQ_EKIND", -3: "KVQ_EHEADDIM", -4: "KVQ_EALIGN",
+          -5: "KVQ_EWORKSPACE", -6: "KVQ_EARCH", -7: "KVQ_ECUDA", -8: "KVQ_EUNSUPPORTED", -9: "KVQ_ETIMEOUT"}
+
+EXPORTS = ["kvq_pool_bytes", "kvq_scale_bytes", "kvq_bytes_per_token", "kvq_num_pages", "kvq_store",
+           "kvq_decode_workspace_bytes", "kvq_decode_workspace_bytes_ex", "kvq_decode", "kvq_decode_ex",
+           "kvq_workspace_status", "kvq_encode_probe", "kvq_dequant_probe", "kvq_strerror",
+           "kvq_device_check", "kvq_version"]
+
+
+class kvq_layout(ctypes.Structure):
+    _fields_ = [("num_pages", ctypes.c_int64), ("page_size", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("v_dim", ctypes.c_int32), ("mla", ctypes.c_int32)]
+
+
+class kvq_decode_options(ctypes.Structure):
+    _fields_ = [("pages_per_split", ctypes.c_int32), ("path", ctypes.c_int32)]
+
+
+class KvqError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__("%s failed: %s (%s)" % (where, STATUS.get(status, status), strerror(status)))
+
+
+_lib = None
+
+
+def lib():
+    """The loaded libkvq (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError("libkvq.so is not built (%s); run __graft_entry__.build()" % LIB_PATH)
+        L = ctypes.CDLL(LIB_PATH)
+        P, i64, i32, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_size_t
+        LP = ctypes.POINTER(kvq_layout)
+        OP = ctypes.POINTER(kvq_decode_options)
+        sig = {
+            "kvq_pool_bytes": (sz, [LP]),
+            "kvq_scale_bytes": (sz, [LP]),
+            "kvq_bytes_per_token": (ctypes.c_double, [LP]),
+            "kvq_num_pages": (i64, [LP, sz]),
+            "kvq_store": (i32, [P, P, P, P, P, i64, LP, i32, P]),
+            "kvq_decode_workspace_bytes": (sz, [LP, i32, i32, i32]),
+            "kvq_decode_workspace_bytes_ex": (sz, [LP, i32, i32, i32, OP]),
+            "kvq_decode": (i32, [P, P, P, P, i32, P, i32, i32, ctypes.c_float, P, i32, P, sz, LP, i32, P]),
+            "kvq_decode_ex": (i32, [P, P, P, P, i32, P, i32, i32, ctypes.c_float, P, i32, P, sz, LP, i32, OP, P]),
+            "kvq_workspace_status": (i32, [P, P]),
+            "kvq_encode_probe": (i32, [i32, P, P, i64, P]),
+            "kvq_dequant_probe": (i32, [i32, P, P, P, i64, P]),
+            "kvq_strerror": (ctypes.c_char_p, [i32]),
+            "kvq_device_check": (i32, []),
+            "kvq_version": (ctypes.c_char_p, []),
+        }
+        for name, (res, args) in sig.items():
+            f = getattr(L, name)
+            f.restype = res
+            f.argtypes = args
+        _lib = L
+    return _lib
+
+
+def strerror(status: int) -> str:
+    return lib().kvq_strerror(int(status)).decode()
+
+
+def _check(status: int, where: str):
+    if status != 0:
+        raise KvqError(status, where)
+
+
+def _kind(kind) -> int:
+    return KIND[kind] if isinstance(kind, str) else int(kind)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+@dataclass
+class Layout:
+    """Python view of ``kvq_layout``."""
+    num_pages: int
+    page_size: int
+    num_kv_heads: int
+    head_dim: int
+    v_dim: int
+    mla: bool = False
+
+    def c(self) -> kvq_layout:
+        return kvq_layout(self.num_pages, self.page_size, self.num_kv_heads, self.head_dim, self.v_dim,
+                          int(bool(self.mla)))
+
+    @property
+    def n_kv(self) -> int:
+        return 1 if self.mla else 2
+
+    def codes_shape(self):
+        return (self.num_pages, self.n_kv, self.num_kv_heads, self.page_size, self.head_dim)
+
+    def scales_shape(self):
+        return (self.num_pages, self.n_kv, self.num_kv_heads, self.page_size, self.head_dim // 32)
+
+
+# ---------------------------------------------------------------------------- cost model
+def kvq_pool_bytes(layout: Layout) -> int:
+    return lib().kvq_pool_bytes(ctypes.byref(layout.c()))
+
+
+def kvq_scale_bytes(layout: Layout) -> int:
+    return lib().kvq_scale_bytes(ctypes.byref(layout.c()))
+
+
+def kvq_bytes_per_token(layout: Layout) -> float:
+    return lib().kvq_bytes_per_token(ctypes.byref(layout.c()))
+
+
+def kvq_num_pages(layout: Layout, budget_bytes: int) -> int:
+    return lib().kvq_num_pages(ctypes.byref(layout.c()), int(budget_bytes))
+
+
+def alloc_pool(layout: Layout, device="cuda"):
+    """(codes uint8, scales as int16 bit patterns) tensors of the pool's shapes on ``device``."""
+    codes = torch.empty(layout.codes_shape(), dtype=torch.uint8, device=device)
+    scales = torch.empty(layout.scales_shape(), dtype=torch.int16, device=device)
+    return codes, scales
+
+
+# ---------------------------------------------------------------------------- store
+def kvq_store(pool: torch.Tensor, scales: torch.Tensor, k: torch.Tensor, v: Optional[torch.Tensor],
+              slot_mapping: torch.Tensor, layout: Layout, kind, stream=None):
+    """Quantize rows ``k`` / ``v`` ([T, Hkv, D] bf16) and scatter them to ``slot_mapping`` ([T] int64)."""
+    _check(lib().kvq_store(_ptr(pool), _ptr(scales), _ptr(k), _ptr(v), _ptr(slot_mapping), int(k.shape[0]),
+                           ctypes.byref(layout.c()), _kind(kind), _stream(stream)), "kvq_store")
+
+
+# ---------------------------------------------------------------------------- decode
+def _opts(pages_per_split=0, path=0):
+    return kvq_decode_options(int(pages_per_split), int(path))
+
+
+def kvq_decode_workspace_bytes(layout: Layout, batch: int, num_q_heads: int, max_pages_per_seq: int,
+                               pages_per_split=0, path=0) -> int:
+    o = _opts(pages_per_split, path)
+    return lib().kvq_decode_workspace_bytes_ex(ctypes.byref(layout.c()), int(batch), int(num_q_heads),
+                                               int(max_pages_per_seq), ctypes.byref(o))
+
+
+def alloc_workspace(layout: Layout, batch, num_q_heads, max_pages_per_seq, device="cuda", **opts):
+    n = kvq_decode_workspace_bytes(layout, batch, num_q_heads, max_pages_per_seq, **opts)
+    if n == 0:
+        raise KvqError(-1, "kvq_decode_workspace_bytes")
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def kvq_decode(q: torch.Tensor, pool: torch.Tensor, scales: torch.Tensor, block_table: torch.Tensor,
+               seq_lens: torch.Tensor, out: torch.Tensor, workspace: torch.Tensor, layout: Layout, kind,
+               sm_scale: float = 1.0, pages_per_split: int = 0, path: int = 0, stream=None):
+    """Decode attention; writes ``out`` ([B, Hq, v_dim], bf16 or float32)."""
+    if out.dtype == torch.bfloat16:
+        od = KVQ_OUT_BF16
+    elif out.dtype == torch.float32:
+        od = KVQ_OUT_F32
+    else:
+        raise TypeError("out must be bfloat16 or float32")
+    o = _opts(pages_per_split, path)
+    _check(lib().kvq_decode_ex(_ptr(q), _ptr(pool), _ptr(scales), _ptr(block_table), int(block_table.shape[1]),
+                               _ptr(seq_lens), int(seq_lens.shape[0]), int(q.shape[1]), float(sm_scale), _ptr(out),
+                               od, _ptr(workspace), int(workspace.numel() * workspace.element_size()),
+                               ctypes.byref(layout.c()), _kind(kind), ctypes.byref(o), _stream(stream)),
+           "kvq_decode")
+
+
+def kvq_workspace_status(workspace: torch.Tensor, stream=None) -> int:
+    return lib().kvq_workspace_status(_ptr(workspace), _stream(stream))
+
+
+# ---------------------------------------------------------------------------- probes
+def kvq_encode_probe(kind, y: torch.Tensor, codes: torch.Tensor, stream=None):
+    _check(lib().kvq_encode_probe(_kind(kind), _ptr(y), _ptr(codes), int(y.numel()), _stream(stream)),
+           "kvq_encode_probe")
+
+
+def kvq_dequant_probe(kind, codes: torch.Tensor, scales: torch.Tensor, out: torch.Tensor, stream=None):
+    _check(lib().kvq_dequant_probe(_kind(kind), _ptr(codes), _ptr(scales), _ptr(out), int(codes.numel()),
+                                   _stream(stream)), "kvq_dequant_probe")
+
+
+def kvq_device_check() -> int:
+    return lib().kvq_device_check()
+
+
+def kvq_version() -> str:
+    return lib().kvq_version().decode()

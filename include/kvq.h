@@ -1,0 +1,182 @@
+/*
+ * kvq.h -- C ABI of libkvq: an 8-bit block-scaled paged KV cache for one GB300 (sm_103a).
+ *
+ * Two operations, taken from the pull-request pages on the 8-bit KV cache:
+ *
+ *   kvq_store   quantize incoming bf16 K/V rows and scatter them into a page pool
+ *               ("feat(kvcache): 8-bit KV cache (q8_0 / fp8_e4m3) behind --kv-cache-dtype",
+ *               section "What": one fp16 scale per 32 elements along head_dim, s = max/448 for
+ *               fp8_e4m3 and s = max/127 for q8_0, 1.0625 bytes per element; review comment
+ *               "A bug on sm_89": int8 rounds half away from zero then clamps to +-127, fp8 is
+ *               clamped to +-448 then rounded once to nearest-even).
+ *   kvq_decode  split-K decode attention over that pool: bf16 queries, K and V dequantized to bf16
+ *               before the dot (same page, "What": the scale varies along the reduction dim), an fp32
+ *               online softmax, split partials merged at the end ("feat(kvcache): 8-bit DSV4
+ *               window/compressed KV", section "Testing": split-k decode kernel, masked -1 columns).
+ *               GQA pools keep separate K and V rows; MLA pools keep one latent row per token that
+ *               serves as both (same page, "What this adds").
+ *
+ * Conventions for every entry point:
+ *   - Pointers named as device pointers must point to device memory of the current device; host
+ *     pointers (kvq_layout) are read during the call only.  The caller owns every buffer; the
+ *     library allocates nothing and keeps no state between calls.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Calls are asynchronous on it.
+ *   - Arguments are validated on the host before anything is launched.  A failed validation returns
+ *     a negative kvq_status and leaves every buffer untouched.  A launch failure returns KVQ_ECUDA.
+ *   - Device pointers must be 16-byte aligned (KVQ_EALIGN otherwise).
+ */
+#ifndef KVQ_H
+#define KVQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Code format.  Both use one fp16 scale per 32 elements. */
+typedef enum {
+    KVQ_FP8_E4M3 = 1, /* OCP E4M3 "fn" codes, s = amax / 448 */
+    KVQ_Q8_0 = 2      /* int8 codes,          s = amax / 127 */
+} kvq_kind;
+
+/* Element type of kvq_decode's output. */
+typedef enum {
+    KVQ_OUT_BF16 = 0, /* round-to-nearest-even bf16 */
+    KVQ_OUT_F32 = 1   /* fp32, no final rounding to bf16 */
+} kvq_out_dtype;
+
+typedef enum {
+    KVQ_OK = 0,
+    KVQ_EINVAL = -1,       /* null pointer, negative size, bad layout, Hq % Hkv != 0, ... */
+    KVQ_EKIND = -2,        /* kind is not a kvq_kind */
+    KVQ_EHEADDIM = -3,     /* head_dim (or v_dim) not a positive multiple of 32 */
+    KVQ_EALIGN = -4,       /* a device pointer is not 16-byte aligned */
+    KVQ_EWORKSPACE = -5,   /* workspace smaller than kvq_decode_workspace_bytes() */
+    KVQ_EARCH = -6,        /* current device is not compute capability 10.3 */
+    KVQ_ECUDA = -7,        /* a CUDA call or launch failed */
+    KVQ_EUNSUPPORTED = -8, /* valid, but no kernel for this shape (see kvq_decode) */
+    KVQ_ETIMEOUT = -9      /* a kernel gave up a bounded wait (reported by kvq_workspace_status) */
+} kvq_status;
+
+/*
+ * Pool layout (one layer).  With n_kv = 2 for GQA (K and V) and n_kv = 1 for MLA:
+ *   codes : uint8  [num_pages][n_kv][num_kv_heads][page_size][head_dim]
+ *   scales: fp16   [num_pages][n_kv][num_kv_heads][page_size][head_dim / 32]
+ * Token slot s lives in page s / page_size at offset s % page_size.  Each (page, kv, head) chunk is
+ * contiguous, so one page of one head is one bulk copy.
+ */
+typedef struct {
+    int64_t num_pages;
+    int32_t page_size;    /* tokens per page; kvq_decode supports 16 */
+    int32_t num_kv_heads; /* Hkv (1 for MLA) */
+    int32_t head_dim;     /* K row width D, a multiple of 32 (576 for the MLA latent row) */
+    int32_t v_dim;        /* V width: == head_dim for GQA; <= head_dim for MLA (V = row[0:v_dim]) */
+    int32_t mla;          /* 0: separate K and V rows; 1: one latent row serves as K and V */
+} kvq_layout;
+
+/* ---------------------------------------------------------------- cost model (host only) */
+/* Bytes of the codes array / the scales array for `layout->num_pages` pages. 0 if the layout is invalid. */
+size_t kvq_pool_bytes(const kvq_layout* layout);
+size_t kvq_scale_bytes(const kvq_layout* layout);
+/* Bytes one cached token costs: n_kv * Hkv * head_dim * 17/16 (codes + fp16 scales).  -1 if invalid.
+ * ("What": 1.0625 bytes per element against bf16's 2; the review's +88% pool growth = 2 / 1.0625.) */
+double kvq_bytes_per_token(const kvq_layout* layout);
+/* Whole pages (codes + scales) that fit in `budget_bytes`; num_pages of `layout` is ignored.  -1 if invalid. */
+int64_t kvq_num_pages(const kvq_layout* layout, size_t budget_bytes);
+
+/* ---------------------------------------------------------------- store */
+/*
+ * Quantize and scatter `num_tokens` rows.
+ *   pool, scales  device, the arrays described by kvq_layout (written in place)
+ *   k             device bf16 [num_tokens][num_kv_heads][head_dim]
+ *   v             device bf16, same shape as k; must be NULL when layout->mla (the latent row is k)
+ *   slot_mapping  device int64 [num_tokens]; row t goes to slot slot_mapping[t]; -1 skips the row.
+ *                 Slots must be unique within one call; a slot >= num_pages * page_size is skipped
+ *                 (never written).
+ * Per 32-element block: amax in fp32; s = fp16_RNE(min(amax / Q, 65504)) with IEEE fp32 division;
+ * a block whose fp16 scale is 0 stores zero codes and a zero scale; otherwise every element is
+ * y = x / s (IEEE fp32) and the code is E4M3 nearest-even of clamp(y, +-448) (fp8) or
+ * clamp(round-half-away(y), +-127) (q8_0).
+ */
+kvq_status kvq_store(void* pool, void* scales, const void* k, const void* v, const int64_t* slot_mapping,
+                     int64_t num_tokens, const kvq_layout* layout, kvq_kind kind, void* stream);
+
+/* ---------------------------------------------------------------- decode */
+/* Options for kvq_decode_ex.  Zero-initialise for the defaults. */
+typedef struct {
+    int32_t pages_per_split; /* 0 = automatic; else every split covers this many pages */
+    int32_t path;            /* 0 = automatic; 1 = CUDA-core kernel; 2 = tensor-core (tcgen05) kernel */
+} kvq_decode_options;
+
+/* Workspace bytes kvq_decode needs for these sizes (an upper bound independent of seq_lens). 0 if invalid. */
+size_t kvq_decode_workspace_bytes(const kvq_layout* layout, int32_t batch, int32_t num_q_heads,
+                                  int32_t max_pages_per_seq);
+size_t kvq_decode_workspace_bytes_ex(const kvq_layout* layout, int32_t batch, int32_t num_q_heads,
+                                     int32_t max_pages_per_seq, const kvq_decode_options* options);
+
+/*
+ * Decode attention for one new query token per sequence.
+ *   q            device bf16 [batch][num_q_heads][head_dim]
+ *   pool, scales device, filled by kvq_store
+ *   block_table  device int32 [batch][max_pages_per_seq]; entry j is the physical page of tokens
+ *                [16j, 16j+16); -1 masks that whole page.  Entries at or beyond ceil(seq_len/16) are
+ *                never read.  An entry >= layout->num_pages is treated as masked and makes
+ *                kvq_workspace_status report KVQ_EINVAL.
+ *   seq_lens     device int32 [batch], each in [0, max_pages_per_seq * page_size]
+ *   sm_scale     multiplies q.k before the softmax
+ *   out          device [batch][num_q_heads][v_dim], bf16 or fp32 per out_dtype
+ *   workspace    device scratch of at least kvq_decode_workspace_bytes(); its content on entry is
+ *                irrelevant; it holds the split partials and a status word after the call.
+ * Query head h reads kv head h / (num_q_heads / num_kv_heads).  For every (b, h) the result is
+ * softmax(sm_scale * q.K^T) V over the valid tokens t < seq_lens[b] whose page is not masked, with
+ * K and V dequantized to bf16 (RNE of code * scale) and fp32 accumulation; a sequence without a
+ * valid token outputs zeros.  Supported: page_size 16 and head_dim in {64, 128, 256} with v_dim ==
+ * head_dim (GQA), or the MLA row head_dim 576 / v_dim 512; other shapes return KVQ_EUNSUPPORTED.
+ */
+kvq_status kvq_decode(const void* q, const void* pool, const void* scales, const int32_t* block_table,
+                      int32_t max_pages_per_seq, const int32_t* seq_lens, int32_t batch, int32_t num_q_heads,
+                      float sm_scale, void* out, kvq_out_dtype out_dtype, void* workspace,
+                      size_t workspace_bytes, const kvq_layout* layout, kvq_kind kind, void* stream);
+kvq_status kvq_decode_ex(const void* q, const void* pool, const void* scales, const int32_t* block_table,
+                         int32_t max_pages_per_seq, const int32_t* seq_lens, int32_t batch,
+                         int32_t num_q_heads, float sm_scale, void* out, kvq_out_dtype out_dtype,
+                         void* workspace, size_t workspace_bytes, const kvq_layout* layout, kvq_kind kind,
+                         const kvq_decode_options* options, void* stream);
+
+/*
+ * Status word a decode left in its workspace: KVQ_OK; KVQ_ETIMEOUT if a kernel gave up a bounded
+ * wait (its output is then not valid); KVQ_EINVAL if a block-table entry pointed past the pool.
+ * Synchronizes `stream`.
+ */
+kvq_status kvq_workspace_status(const void* workspace, void* stream);
+
+/* ---------------------------------------------------------------- rounding probes */
+/*
+ * Elementwise code step of the store on already-scaled fp32 values (device arrays of n):
+ * codes[i] = E4M3_RNE(clamp(y[i], +-448)) for fp8, or int8 clamp(round-half-away(y[i]), +-127) for
+ * q8_0.  Exposes the store kernel's own conversion so that it can be checked exhaustively.
+ */
+kvq_status kvq_encode_probe(kvq_kind kind, const float* y, uint8_t* codes, int64_t n, void* stream);
+/*
+ * Dequant step of the decode, by the decode kernels' own routine, on n codes (n a multiple of 16)
+ * in chunks of 16 that share one scale: out[i] = bf16 bits of RNE_bf16(value(codes[i]) *
+ * fp16(scales[i / 16])).  codes and out 16-byte aligned device arrays of n; scales a device array
+ * of n / 16 fp16 bit patterns.
+ */
+kvq_status kvq_dequant_probe(kvq_kind kind, const uint8_t* codes, const uint16_t* scales, uint16_t* out,
+                             int64_t n, void* stream);
+
+/* ---------------------------------------------------------------- misc */
+/* Message for a status code (static string). */
+const char* kvq_strerror(kvq_status status);
+/* KVQ_OK if the current device is sm_103 and the library's kernels load on it, else KVQ_EARCH / KVQ_ECUDA. */
+kvq_status kvq_device_check(void);
+/* Library version, e.g. "0.1.0". */
+const char* kvq_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* KVQ_H */

@@ -1,0 +1,134 @@
+"""Host-side checks of the C ABI: the library loads, exports what include/kvq.h declares, prices the
+pool correctly, and rejects bad arguments before touching the GPU (no GPU needed)."""
+import ctypes
+import json
+import math
+import os
+import re
+
+import pytest
+
+import oracle as O
+from block_quantized_bit_gb300 import build_lib, kvq
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+GOLDEN = json.load(open(os.path.join(ROOT, "tests", "golden", "page_facts.json")))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build_lib.build()
+    return kvq.lib()
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "kvq.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(kvq_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_library_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert len(names) >= 14
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(kvq.EXPORTS) == set(names)
+    assert kvq.kvq_version() == "0.1.0"
+
+
+def L(**kw):
+    base = dict(num_pages=10, page_size=16, num_kv_heads=2, head_dim=128, v_dim=128, mla=False)
+    base.update(kw)
+    return kvq.Layout(**base)
+
+
+@pytest.mark.parametrize("hkv,d,mla", [(8, 128, False), (2, 256, False), (1, 576, True), (4, 64, False)])
+def test_cost_model_matches_the_oracle_and_the_pages(lib, hkv, d, mla):
+    lay = L(num_kv_heads=hkv, head_dim=d, v_dim=512 if mla else d, mla=mla)
+    n_kv = 1 if mla else 2
+    bpt = kvq.kvq_bytes_per_token(lay)
+    assert bpt == O.bytes_per_token(n_kv, hkv, d)
+    assert bpt == GOLDEN["bytes_per_element_8bit"]["value"] * n_kv * hkv * d
+    assert kvq.kvq_pool_bytes(lay) == 10 * 16 * n_kv * hkv * d
+    assert kvq.kvq_scale_bytes(lay) == 10 * 16 * n_kv * hkv * d // 32 * 2
+    budget = 123_456_789
+    pages = kvq.kvq_num_pages(lay, budget)
+    assert pages == budget // int(16 * bpt)
+
+
+def test_pool_growth_against_bf16_at_equal_bytes(lib):
+    """Pool tokens grow by exactly 32/17 = 2/1.0625 (review comment 'End-to-end numbers': +88%)."""
+    lay = L(num_kv_heads=2, head_dim=256, v_dim=256)
+    bf16_per_token = 2 * 2 * 2 * 256
+    for budget in (10 ** 9, 37 * 10 ** 9, 2 ** 40):
+        q_tokens = kvq.kvq_num_pages(lay, budget) * 16
+        b_tokens = budget // (bf16_per_token * 16) * 16
+        assert abs(q_tokens / b_tokens - 32 / 17) < 1e-4
+    pool = GOLDEN["kv_pool_tokens"]
+    # a budget of [305730, 305731) bf16 tokens holds [305730, 305731) * 32/17 8-bit tokens
+    assert math.floor(pool["bf16"] * 32 / 17) <= pool["fp8_e4m3"] <= math.floor((pool["bf16"] + 1) * 32 / 17)
+
+
+def test_invalid_layouts_are_rejected(lib):
+    assert kvq.kvq_pool_bytes(L(head_dim=100, v_dim=100)) == 0
+    assert kvq.kvq_bytes_per_token(L(head_dim=0, v_dim=0)) == -1.0
+    assert kvq.kvq_num_pages(L(num_kv_heads=0), 10 ** 6) == -1
+    assert kvq.kvq_decode_workspace_bytes(L(), 4, 7, 10) == 0       # Hq % Hkv != 0
+    assert kvq.kvq_decode_workspace_bytes(L(), 4, 8, 10) > 0
+
+
+FAKE = 0x10000  # an aligned host address that must never be dereferenced: validation fails first
+
+
+def _store(lib, layout, kind=1, k=FAKE, v=FAKE, sm=FAKE, pool=FAKE, scales=FAKE, n=4):
+    P = ctypes.c_void_p
+    return lib.kvq_store(P(pool), P(scales), P(k), P(v) if v else None, P(sm), n, ctypes.byref(layout.c()), kind,
+                         None)
+
+
+def test_store_argument_errors(lib):
+    assert _store(lib, L(), kind=3) == -2                        # KVQ_EKIND
+    assert _store(lib, L(head_dim=48, v_dim=48)) == -3           # KVQ_EHEADDIM
+    assert _store(lib, L(), k=0) == -1                           # null k
+    assert _store(lib, L(), v=0) == -1                           # GQA needs v
+    assert _store(lib, L(mla=True, num_kv_heads=1, head_dim=576, v_dim=512)) == -1   # MLA must not pass v
+    assert _store(lib, L(), k=FAKE + 8) == -4                    # KVQ_EALIGN
+    assert _store(lib, L(), pool=FAKE + 4) == -4
+    assert _store(lib, L(), n=-1) == -1
+    assert _store(lib, L(), n=0) == 0                            # nothing to do, nothing launched
+
+
+def _decode(lib, layout, *, q=FAKE, ws_bytes=None, batch=2, hq=8, maxp=10, kind=1, out_dtype=0, ws=FAKE, opts=None):
+    P = ctypes.c_void_p
+    if ws_bytes is None:
+        ws_bytes = lib.kvq_decode_workspace_bytes(ctypes.byref(layout.c()), batch, hq, maxp)
+    o = ctypes.byref(opts) if opts is not None else None
+    return lib.kvq_decode_ex(P(q), P(FAKE), P(FAKE), P(FAKE), maxp, P(FAKE), batch, hq, 1.0, P(FAKE), out_dtype,
+                             P(ws), ws_bytes, ctypes.byref(layout.c()), kind, o, None)
+
+
+def test_decode_argument_errors(lib):
+    assert _decode(lib, L(), kind=0) == -2
+    assert _decode(lib, L(), hq=7) == -1
+    assert _decode(lib, L(), ws_bytes=16) == -5                  # KVQ_EWORKSPACE
+    assert _decode(lib, L(), q=FAKE + 2) == -4                   # KVQ_EALIGN
+    assert _decode(lib, L(), ws=FAKE + 8) == -4
+    assert _decode(lib, L(), out_dtype=5) == -1
+    assert _decode(lib, L(page_size=32)) == -8                   # KVQ_EUNSUPPORTED
+    assert _decode(lib, L(head_dim=96, v_dim=96)) == -8
+    assert _decode(lib, L(), batch=0) == 0
+    bad = kvq.kvq_decode_options(-3, 0)
+    assert _decode(lib, L(), opts=bad) == -1
+
+
+def test_workspace_bound_covers_every_split_choice(lib):
+    lay = L(num_kv_heads=8, head_dim=128, v_dim=128)
+    auto = kvq.kvq_decode_workspace_bytes(lay, 8, 16, 1024)
+    forced = kvq.kvq_decode_workspace_bytes(lay, 8, 16, 1024, pages_per_split=1)
+    assert forced > auto > 0
+
+
+def test_strerror_has_a_message_for_every_status(lib):
+    for code, name in kvq.STATUS.items():
+        msg = kvq.strerror(code)
+        assert msg and msg != "unknown status", name

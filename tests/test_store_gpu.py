@@ -1,0 +1,142 @@
+"""GPU store parity: the CUDA store is bit-exact against the oracle (every code byte, every scale bit),
+and its rounding primitives agree with the oracle exhaustively on their domains."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from block_quantized_bit_gb300 import kvq, workloads
+
+from parity import bits, gpu_pool, gpu_store, oracle_pool, oracle_store
+
+pytestmark = pytest.mark.gpu
+KINDS = ["fp8_e4m3", "q8_0"]
+
+# reduced sizes of every workload family: several warps' worth of blocks and a ragged tail
+CASES = {
+    "tiny": dict(),
+    "qwen3_1p7b": dict(batch=3, ctx_lo=100, ctx_hi=900, new_rows_per_seq=97),
+    "long_gqa": dict(batch=2, ctx=2100, mask_frac=0.02),
+    "mla": dict(ctx=1037),
+    "serving": dict(batch=6, median=300, lo=40, hi=2000),
+}
+
+
+def _case(name, kind, **kw):
+    return workloads.make(name, kind=kind, device="cpu", **{**CASES[name], **kw})
+
+
+@pytest.mark.parametrize("kind", KINDS)
+@pytest.mark.parametrize("name", list(CASES))
+def test_store_bit_exact(name, kind):
+    case = _case(name, kind)
+    L, codes, scales = gpu_pool(case)
+    oc, osc = oracle_pool(case)
+    gpu_store(case, codes, scales)
+    oracle_store(case, oc, osc)
+    if case.new_k is not None:
+        gpu_store(case, codes, scales, rows="new")
+        oracle_store(case, oc, osc, rows="new")
+    torch.cuda.synchronize()
+    gc = codes.cpu().numpy()
+    gs = scales.cpu().numpy().view(np.uint16)
+    assert np.array_equal(gc, oc), "code bytes differ at %d places" % int((gc != oc).sum())
+    assert np.array_equal(gs, osc), "scale bits differ at %d places" % int((gs != osc).sum())
+    # never a NaN code
+    if kind == "fp8_e4m3":
+        written = gs != 0xA5A5
+        assert not np.any((gc[np.repeat(written, 32, axis=-1)] & 0x7F) == 0x7F)
+
+
+@pytest.mark.parametrize("kind", KINDS)
+def test_store_edge_cases(kind):
+    case = workloads.tiny(kind=kind, ctx=37)
+    L, codes, scales = gpu_pool(case)
+    dev = "cuda"
+    # zero rows: nothing happens
+    kvq.kvq_store(codes, scales, case.k[:0].to(dev), case.v[:0].to(dev), case.slot_mapping[:0].to(dev), L, kind)
+    # every slot skipped: the poisoned pool stays as it was
+    skip = torch.full_like(case.slot_mapping, -1)
+    kvq.kvq_store(codes, scales, case.k.to(dev), case.v.to(dev), skip.to(dev), L, kind)
+    torch.cuda.synchronize()
+    assert bool((codes == 0xA5).all()) and bool((scales.view(torch.int16) == np.int16(np.uint16(0xA5A5))).all())
+    # a single row, then the rest in reverse order
+    one = slice(5, 6)
+    kvq.kvq_store(codes, scales, case.k[one].to(dev), case.v[one].to(dev), case.slot_mapping[one].to(dev), L, kind)
+    idx = torch.arange(case.k.shape[0] - 1, -1, -1)
+    kvq.kvq_store(codes, scales, case.k[idx].to(dev), case.v[idx].to(dev), case.slot_mapping[idx].to(dev), L, kind)
+    oc, osc = oracle_pool(case)
+    oracle_store(case, oc, osc)
+    torch.cuda.synchronize()
+    assert np.array_equal(codes.cpu().numpy(), oc)
+    assert np.array_equal(scales.cpu().numpy().view(np.uint16), osc)
+
+
+def test_store_special_blocks_of_the_tiny_workload():
+    """All-zero block -> zero scale and codes; +-1000 block saturates to 0x7E/0xFE (fp8) or +-127 (q8_0)."""
+    for kind in KINDS:
+        case = workloads.tiny(kind=kind)
+        L, codes, scales = gpu_pool(case)
+        gpu_store(case, codes, scales)
+        torch.cuda.synchronize()
+        c = codes.cpu().numpy()
+        s = scales.cpu().numpy().view(np.uint16)
+        assert s[0, 0, 0, 0, 0] == 0 and not c[0, 0, 0, 0, 0:32].any()     # token 0, K, head 0, block 0
+        blk = c[0, 1, 1, 1, 32:64]                                          # token 1, V, head 1, block 1
+        if kind == "fp8_e4m3":
+            assert blk[8] == 0x7E and blk[19] == 0xFE
+        else:
+            assert blk.view(np.int8)[8] == 127 and blk.view(np.int8)[19] == -127
+
+
+def _fp32_sweep():
+    """fp32 values covering every E4M3 binade: a strided sweep of all bit patterns plus every
+    midpoint between adjacent E4M3 values with its 64 neighbours on each side."""
+    pats = np.arange(0, 1 << 32, 257, dtype=np.uint64).astype(np.uint32).view(np.float32)
+    pats = pats[np.isfinite(pats)]
+    vals = sorted({O.e4m3_value(c) for c in range(0x7F)})
+    mids = np.array([(a + b) / 2 for a, b in zip(vals[:-1], vals[1:])] + [448.0, 464.0], np.float32)
+    near = [mids]
+    for d in range(1, 65):
+        near.append(np.nextafter(mids, np.float32(np.inf)) if d == 1 else
+                    (mids.view(np.uint32) + d).view(np.float32))
+        near.append((mids.view(np.uint32) - d).view(np.float32))
+    near = np.concatenate(near)
+    special = np.array([0.0, -0.0, np.inf, -np.inf, 1e-45, -1e-45, 0.49999997, 0.5, 126.5, 127.5, -127.5, 1e30],
+                       np.float32)
+    y = np.concatenate([pats, near, -near, special, np.linspace(-130, 130, 1 << 20, dtype=np.float32)])
+    return y
+
+
+@pytest.mark.parametrize("kind", KINDS)
+def test_encode_probe_matches_oracle_on_fp32_sweep(kind):
+    """The store's code step (hardware satfinite RNE for fp8; roundf + clamp for q8_0) vs the oracle."""
+    y = _fp32_sweep()
+    yd = torch.from_numpy(y).cuda()
+    codes = torch.empty(y.size, dtype=torch.uint8, device="cuda")
+    kvq.kvq_encode_probe(kind, yd, codes)
+    torch.cuda.synchronize()
+    got = codes.cpu().numpy()
+    ref = O.e4m3_sat_rne(y) if kind == "fp8_e4m3" else O.q8_rhaz(y).view(np.uint8)
+    bad = np.nonzero(got != ref)[0]
+    assert bad.size == 0, [(float(y[i]), int(got[i]), int(ref[i])) for i in bad[:10]]
+
+
+@pytest.mark.parametrize("kind", KINDS)
+def test_dequant_probe_matches_oracle_for_every_code_and_scale(kind):
+    """The decode's dequant routine vs RNE_bf16(code * scale) for all codes x all finite positive fp16 scales."""
+    codes = np.arange(256, dtype=np.uint8)
+    if kind == "fp8_e4m3":
+        codes = codes[(codes != 0x7F) & (codes != 0xFF)]
+    codes = np.concatenate([codes, np.zeros((-codes.size) % 16, np.uint8)])  # whole 16-code chunks
+    s16 = np.arange(0, 0x7C00, dtype=np.uint32).astype(np.uint16)
+    chunk_codes = np.tile(codes, s16.size)
+    chunk_scales = np.repeat(s16, codes.size // 16)
+    got = torch.empty(chunk_codes.size, dtype=torch.int16, device="cuda")
+    kvq.kvq_dequant_probe(kind, torch.from_numpy(chunk_codes).cuda(),
+                          torch.from_numpy(chunk_scales.view(np.int16)).cuda(), got)
+    torch.cuda.synchronize()
+    g = got.cpu().numpy().view(np.uint16)
+    ref = O.dequant(kind, chunk_codes, np.repeat(s16, codes.size))
+    ref_bits = O.bf16_rne(ref)
+    assert np.array_equal(g, ref_bits), int((g != ref_bits).sum())
