@@ -29,7 +29,7 @@ STATUS = {0: "KVQ_OK", -1: "KVQ_EINVAL", -2: "KVQ_EKIND", -3: "KVQ_EHEADDIM", -4
 EXPORTS = ["kvq_pool_bytes", "kvq_scale_bytes", "kvq_bytes_per_token", "kvq_num_pages", "kvq_store",
            "kvq_decode_workspace_bytes", "kvq_decode_workspace_bytes_ex", "kvq_decode", "kvq_decode_ex",
            "kvq_workspace_status", "kvq_encode_probe", "kvq_dequant_probe", "kvq_strerror",
-           "kvq_device_check", "kvq_version"]
+           "kvq_device_check", "kvq_version", "kvq_decode_noalloc"]
 
 
 class kvq_layout(ctypes.Structure):
@@ -76,6 +76,7 @@ def lib():
             "kvq_strerror": (ctypes.c_char_p, [i32]),
             "kvq_device_check": (i32, []),
             "kvq_version": (ctypes.c_char_p, []),
+            "kvq_decode_noalloc": (i32, [P, P, P, P, i32, P, i32, i32, ctypes.c_float, P, i32, LP, i32, P]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -202,6 +203,21 @@ def kvq_decode(q: torch.Tensor, pool: torch.Tensor, scales: torch.Tensor, block_
                                od, _ptr(workspace), int(workspace.numel() * workspace.element_size()),
                                ctypes.byref(layout.c()), _kind(kind), ctypes.byref(o), _stream(stream)),
            "kvq_decode")
+
+
+def kvq_decode_noalloc(q: torch.Tensor, pool: torch.Tensor, scales: torch.Tensor, block_table: torch.Tensor,
+                       seq_lens: torch.Tensor, out: torch.Tensor, layout: Layout, kind, sm_scale: float = 1.0,
+                       stream=None):
+    """kvq_decode without a workspace argument, for callers that cannot allocate device memory.
+
+    The split-K scratch is the library's fixed device array (KVQ_NOALLOC_SCRATCH_BYTES); calls that
+    overlap on the GPU share it and race.
+    """
+    od = KVQ_OUT_BF16 if out.dtype == torch.bfloat16 else KVQ_OUT_F32
+    _check(lib().kvq_decode_noalloc(_ptr(q), _ptr(pool), _ptr(scales), _ptr(block_table), int(block_table.shape[1]),
+                                    _ptr(seq_lens), int(seq_lens.shape[0]), int(q.shape[1]), float(sm_scale),
+                                    _ptr(out), od, ctypes.byref(layout.c()), _kind(kind), _stream(stream)),
+           "kvq_decode_noalloc")
 
 
 def kvq_workspace_status(workspace: torch.Tensor, stream=None) -> int:

@@ -146,6 +146,27 @@ kvq_status kvq_decode_ex(const void* q, const void* pool, const void* scales, co
                          const kvq_decode_options* options, void* stream);
 
 /*
+ * kvq_decode for callers that cannot allocate device memory.  The pages have no counterpart to
+ * this entry point.  It exists because some callers cannot call cudaMalloc when they decode: a
+ * serving loop that reserved all of its memory up front, a plugin running under another
+ * framework's allocator, or code that has no allocator at all.  Arguments and results are those of
+ * kvq_decode without the workspace: the split-K scratch is a fixed array of
+ * KVQ_NOALLOC_SCRATCH_BYTES in the library's own device memory, which every GPU that loads the
+ * library keeps until the process exits.  Sizes whose kvq_decode_workspace_bytes() exceeds that
+ * return KVQ_EWORKSPACE.  Nothing is allocated.
+ * The first call on each device looks up the array's device address (cudaGetSymbolAddress) with
+ * that device current; make that first call before capturing any stream.  Every call shares the
+ * array and it keeps the previous call's contents (the call clears what must start at zero); calls
+ * whose kernels overlap on the GPU -- different streams, or host threads without ordering -- race
+ * on it and give wrong results.
+ */
+#define KVQ_NOALLOC_SCRATCH_BYTES (8u << 20)
+kvq_status kvq_decode_noalloc(const void* q, const void* pool, const void* scales, const int32_t* block_table,
+                              int32_t max_pages_per_seq, const int32_t* seq_lens, int32_t batch,
+                              int32_t num_q_heads, float sm_scale, void* out, kvq_out_dtype out_dtype,
+                              const kvq_layout* layout, kvq_kind kind, void* stream);
+
+/*
  * Status word a decode left in its workspace: KVQ_OK; KVQ_ETIMEOUT if a kernel gave up a bounded
  * wait (its output is then not valid); KVQ_EINVAL if a block-table entry pointed past the pool.
  * Synchronizes `stream`.
