@@ -268,6 +268,17 @@ kvq_status kvq_encode_probe(kvq_kind kind, const float* y, uint8_t* codes, int64
   return launch_encode_probe(kind, y, codes, n, static_cast<cudaStream_t>(stream));
 }
 
+kvq_status kvq_quantize_probe(kvq_kind kind, const uint16_t* x, int64_t nx, const uint16_t* s, int64_t ns,
+                              uint8_t* codes, void* stream) {
+  if (!kind_ok(kind)) return KVQ_EKIND;
+  if (nx < 0 || ns < 0) return KVQ_EINVAL;
+  if (nx == 0 || ns == 0) return KVQ_OK;
+  if (!x || !s || !codes) return KVQ_EINVAL;
+  kvq_status st = kvq_device_check();
+  if (st != KVQ_OK) return st;
+  return launch_quantize_probe(kind, x, nx, s, ns, codes, static_cast<cudaStream_t>(stream));
+}
+
 kvq_status kvq_dequant_probe(kvq_kind kind, const uint8_t* codes, const uint16_t* scales, uint16_t* out, int64_t n,
                              void* stream) {
   if (!kind_ok(kind)) return KVQ_EKIND;

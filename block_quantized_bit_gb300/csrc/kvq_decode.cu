@@ -27,7 +27,7 @@ namespace kvq {
 namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr int kPlanThreads = 128;
+
 
 struct KParams {
   const __nv_bfloat16* q;
@@ -56,7 +56,7 @@ __device__ __forceinline__ int32_t seq_pages(const KParams& p, int32_t b) {
 }
 
 // Block-wide plan: pages per split C, and for `want_b` (or the sequence that owns item `want_item`)
-// its first item index and split count.  Must be called by all kPlanThreads threads of the CTA.
+// its first item index and split count.  Every thread of the CTA must call it (blockDim a multiple of 32).
 struct Plan {
   int32_t C;
   int32_t b;        // sequence
@@ -66,13 +66,13 @@ struct Plan {
 };
 
 __device__ Plan make_plan(const KParams& p, int32_t want_item, int32_t want_b) {
-  __shared__ long long s_red[kPlanThreads / 32];
-  __shared__ int32_t s_scan[kPlanThreads / 32];
+  __shared__ long long s_red[32];
+  __shared__ int32_t s_scan[32];
   __shared__ Plan s_plan;
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, nthr = blockDim.x, nwarp = nthr >> 5;
   const int lane = tid & 31, warp = tid >> 5;
   const int32_t groups = p.num_kv_heads * p.head_tiles;
-  const int32_t per = (p.batch + kPlanThreads - 1) / kPlanThreads;
+  const int32_t per = (p.batch + nthr - 1) / nthr;
   const int32_t b0 = tid * per, b1 = min(b0 + per, p.batch);
   // 1) total page-units
   long long units = 0;
@@ -81,7 +81,7 @@ __device__ Plan make_plan(const KParams& p, int32_t want_item, int32_t want_b) {
   if (lane == 0) s_red[warp] = units;
   __syncthreads();
   long long tot = 0;
-  for (int w = 0; w < kPlanThreads / 32; ++w) tot += s_red[w];
+  for (int w = 0; w < nwarp; ++w) tot += s_red[w];
   tot *= groups;
   int32_t C = p.pages_per_split;
   if (C <= 0) {
@@ -99,7 +99,7 @@ __device__ Plan make_plan(const KParams& p, int32_t want_item, int32_t want_b) {
   if (lane == 31) s_scan[warp] = incl;
   __syncthreads();
   int32_t warp_off = 0, total_items = 0;
-  for (int w = 0; w < kPlanThreads / 32; ++w) {
+  for (int w = 0; w < nwarp; ++w) {
     if (w < warp) warp_off += s_scan[w];
     total_items += s_scan[w];
   }
@@ -142,6 +142,15 @@ struct RowGeom {
   static_assert(32 % LPT == 0, "lanes per token must divide the warp");
 };
 
+template <int N>
+struct Log2 {
+  static constexpr int value = 1 + Log2<N / 2>::value;
+};
+template <>
+struct Log2<1> {
+  static constexpr int value = 0;
+};
+
 template <int D, int DV, int GT, int KIND, bool MLA, int WARPS, int STAGES>
 struct CCConfig {
   using G = RowGeom<D>;
@@ -154,16 +163,56 @@ struct CCConfig {
   static constexpr int DATA_BYTES = PIPE_BYTES > COMBINE_BYTES ? PIPE_BYTES : COMBINE_BYTES;
   static constexpr int SMEM_BYTES = DATA_BYTES + WARPS * STAGES * 8 + WARPS * STAGES * 4;
   static constexpr int CPL_V = (DV / 16 + 31) / 32;       // value chunks per lane
+  static constexpr int LOG_GT = Log2<GT>::value;
   static_assert(CODE_BYTES % 16 == 0 && SCALE_BYTES % 16 == 0, "bulk copy sizes");
+  static_assert(GT <= G::LPT, "a token's lanes must cover every head of the tile");
 };
 
-template <int D, int DV, int GT, int KIND, bool MLA, int WARPS, int STAGES>
-__global__ void __launch_bounds__(WARPS * 32) decode_cc_kernel(KParams p) {
+// Lane (within a token group) that ends up holding head h after the transposed reduction.
+template <int LPT, int GT>
+__device__ __forceinline__ int head_lane(int h) {
+  constexpr int LG = Log2<GT>::value;
+  int c = 0;
+#pragma unroll
+  for (int k = 0; k < LG; ++k)
+    if ((h >> (LG - 1 - k)) & 1) c |= LPT >> (k + 1);
+  return c;
+}
+
+// Sum v[h] over the LPT lanes of a token while distributing heads: after the call, v[0] of a lane
+// holds the full dot for head H(lane) (the first log2(GT) xor steps exchange half of the remaining
+// heads each, the rest add the single value).  Every lane of the warp must call it.
+template <int LPT, int GT>
+__device__ __forceinline__ float reduce_heads(float (&v)[GT], int lane) {
+  constexpr int LG = Log2<GT>::value;
+#pragma unroll
+  for (int k = 0; k < LG; ++k) {
+    const int o = LPT >> (k + 1);
+    const bool upper = (lane & o) != 0;
+    constexpr int dummy = 0;
+    (void)dummy;
+    const int n = GT >> k;
+#pragma unroll
+    for (int i = 0; i < GT / 2; ++i) {
+      if (i < n / 2) {
+        const float send = upper ? v[i] : v[i + n / 2];
+        const float keep = upper ? v[i + n / 2] : v[i];
+        v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+      }
+    }
+  }
+  float r = v[0];
+#pragma unroll
+  for (int o = LPT >> (LG + 1); o >= 1; o >>= 1) r += __shfl_xor_sync(0xffffffffu, r, o);
+  return r;
+}
+
+template <int D, int DV, int GT, int KIND, bool MLA, int WARPS, int STAGES, int MINB>
+__global__ void __launch_bounds__(WARPS * 32, MINB) decode_cc_kernel(KParams p) {
   using Cfg = CCConfig<D, DV, GT, KIND, MLA, WARPS, STAGES>;
   using Geo = RowGeom<D>;
   constexpr int NCH = Geo::NCH, LPT = Geo::LPT, CPL = Geo::CPL, TPI = Geo::TPI, ITERS = Geo::ITERS;
-  constexpr int NB = Geo::NB;
-  static_assert(WARPS * 32 == kPlanThreads, "plan helper assumes 128 threads");
+  constexpr int NB = Geo::NB, CPL_V = Cfg::CPL_V, LG = Cfg::LOG_GT;
 
   extern __shared__ __align__(128) uint8_t smem[];
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Cfg::DATA_BYTES);
@@ -174,7 +223,6 @@ __global__ void __launch_bounds__(WARPS * 32) decode_cc_kernel(KParams p) {
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int32_t b = plan.b;
-  const int32_t groups = p.num_kv_heads * p.head_tiles;
   const int32_t local = static_cast<int32_t>(blockIdx.x) - plan.base;
   const int32_t qg = local / plan.nsplit;
   const int32_t split = local - qg * plan.nsplit;
@@ -185,52 +233,46 @@ __global__ void __launch_bounds__(WARPS * 32) decode_cc_kernel(KParams p) {
   const int32_t pg0 = split * plan.C;
   const int32_t pg1 = min(pg0 + plan.C, npages);
   const int32_t head0 = g * p.group + ht * GT;  // first query head of this item
-  (void)groups;
 
   if (tid < WARPS * STAGES) mbar_init(&bars[tid], 1);
   fence_mbar_init();
   __syncthreads();
 
-  // Query rows of this item's heads, for the chunk(s) this lane owns.
   const int tg = lane / LPT;  // token group within the warp
-  const int c0 = lane % LPT;  // first chunk of this lane
-  float qreg[GT][CPL][16];
+  const int c0 = lane % LPT;  // first 16-element chunk of this lane
+  // head whose score this lane ends up owning after reduce_heads
+  int my_head = 0;
+#pragma unroll
+  for (int k = 0; k < LG; ++k)
+    if (c0 & (LPT >> (k + 1))) my_head |= GT >> (k + 1);
+
+  // q rows of this item's heads for the lane's chunk(s), as packed bf16 pairs
+  uint32_t qb[GT][CPL][8];
 #pragma unroll
   for (int h = 0; h < GT; ++h) {
     const __nv_bfloat16* qrow = p.q + (static_cast<int64_t>(b) * p.num_q_heads + head0 + h) * D;
 #pragma unroll
     for (int k = 0; k < CPL; ++k) {
       const int c = c0 + 32 * k;
-#pragma unroll
-      for (int i = 0; i < 16; ++i) qreg[h][k][i] = 0.0f;
+      uint4 a = make_uint4(0u, 0u, 0u, 0u), bq = a;
       if (c < NCH) {
         const uint4* src = reinterpret_cast<const uint4*>(qrow + c * 16);
-        const uint4 a = __ldg(src), bq = __ldg(src + 1);
-        const __nv_bfloat162* pa = reinterpret_cast<const __nv_bfloat162*>(&a);
-        const __nv_bfloat162* pb = reinterpret_cast<const __nv_bfloat162*>(&bq);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float2 x = __bfloat1622float2(pa[i]);
-          const float2 y = __bfloat1622float2(pb[i]);
-          qreg[h][k][2 * i] = x.x;
-          qreg[h][k][2 * i + 1] = x.y;
-          qreg[h][k][8 + 2 * i] = y.x;
-          qreg[h][k][8 + 2 * i + 1] = y.y;
-        }
+        a = __ldg(src);
+        bq = __ldg(src + 1);
       }
+      qb[h][k][0] = a.x; qb[h][k][1] = a.y; qb[h][k][2] = a.z; qb[h][k][3] = a.w;
+      qb[h][k][4] = bq.x; qb[h][k][5] = bq.y; qb[h][k][6] = bq.z; qb[h][k][7] = bq.w;
     }
   }
 
-  float m[GT], l[GT], acc[GT][Cfg::CPL_V][16];
+  float m = -INFINITY, l = 0.0f;  // online-softmax state of head my_head
+  float2 acc[GT][CPL_V][8];
 #pragma unroll
-  for (int h = 0; h < GT; ++h) {
-    m[h] = -INFINITY;
-    l[h] = 0.0f;
+  for (int h = 0; h < GT; ++h)
 #pragma unroll
-    for (int k = 0; k < Cfg::CPL_V; ++k)
+    for (int k = 0; k < CPL_V; ++k)
 #pragma unroll
-      for (int i = 0; i < 16; ++i) acc[h][k][i] = 0.0f;
-  }
+      for (int e = 0; e < 8; ++e) acc[h][k][e] = make_float2(0.0f, 0.0f);
 
   // Pages of this warp: pg0 + warp + i * WARPS.
   const int32_t np = pg1 - pg0;
@@ -286,79 +328,88 @@ __global__ void __launch_bounds__(WARPS * 32) decode_cc_kernel(KParams p) {
       const int32_t pg = pg0 + warp + i * WARPS;
       const uint8_t* kc = wbuf + s * Cfg::STAGE_BYTES;
       const uint8_t* vc = MLA ? kc : kc + Cfg::CODE_BYTES;
-      const __half* ks = reinterpret_cast<const __half*>(kc + Cfg::NKV * Cfg::CODE_BYTES);
-      const __half* vs = MLA ? ks : ks + kPage * NB;
+      const uint16_t* ks = reinterpret_cast<const uint16_t*>(kc + Cfg::NKV * Cfg::CODE_BYTES);
+      const uint16_t* vs = MLA ? ks : ks + kPage * NB;
 
-      // ---- scores for the 16 tokens of the page
-      float sc[ITERS][GT];
+      // ---- scores of this lane's head for its tokens of the page
+      float sc[ITERS];
 #pragma unroll
       for (int it = 0; it < ITERS; ++it) {
         const int t = it * TPI + tg;
-        float part[GT];
+        float part[GT][2];
 #pragma unroll
-        for (int h = 0; h < GT; ++h) part[h] = 0.0f;
+        for (int h = 0; h < GT; ++h) part[h][0] = part[h][1] = 0.0f;
 #pragma unroll
         for (int k = 0; k < CPL; ++k) {
           const int c = c0 + 32 * k;
           if (c < NCH) {
             const uint4 code = *reinterpret_cast<const uint4*>(kc + t * D + c * 16);
-            const float sf = __half2float(ks[t * NB + (c >> 1)]);
-            float kd[16];
-            dequant16<KIND>(code, sf, kd);
+            uint32_t kd[8];
+            dequant16<KIND>(code, ks[t * NB + (c >> 1)], kd);
 #pragma unroll
-            for (int h = 0; h < GT; ++h)
+            for (int e = 0; e < 8; ++e)
 #pragma unroll
-              for (int e = 0; e < 16; ++e) part[h] = fmaf(qreg[h][k][e], kd[e], part[h]);
+              for (int h = 0; h < GT; ++h) {
+                part[h][0] = fma_f32_bf16(lo16(qb[h][k][e]), lo16(kd[e]), part[h][0]);
+                part[h][1] = fma_f32_bf16(hi16(qb[h][k][e]), hi16(kd[e]), part[h][1]);
+              }
           }
         }
+        float v[GT];
+#pragma unroll
+        for (int h = 0; h < GT; ++h) v[h] = part[h][0] + part[h][1];
+        const float dot = reduce_heads<LPT, GT>(v, lane);
+        sc[it] = (pg * kPage + t < L) ? dot * p.score_scale : -INFINITY;
+      }
+      // ---- online softmax for this lane's head; the page max is uniform over the head's lanes
+      float mx = -INFINITY;
+#pragma unroll
+      for (int it = 0; it < ITERS; ++it) mx = fmaxf(mx, sc[it]);
+#pragma unroll
+      for (int o = LPT; o < 32; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      const float mnew = fmaxf(m, mx);
+      const float alpha = (mnew == -INFINITY) ? 1.0f : exp2f(m - mnew);
+      m = mnew;
+      l *= alpha;
+#pragma unroll
+      for (int it = 0; it < ITERS; ++it) {
+        sc[it] = (sc[it] == -INFINITY) ? 0.0f : exp2f(sc[it] - mnew);
+        l += sc[it];
+      }
+      if (__any_sync(0xffffffffu, alpha != 1.0f)) {
 #pragma unroll
         for (int h = 0; h < GT; ++h) {
+          const float ah = __shfl_sync(0xffffffffu, alpha, tg * LPT + head_lane<LPT, GT>(h));
 #pragma unroll
-          for (int o = 1; o < LPT; o <<= 1) part[h] += __shfl_xor_sync(0xffffffffu, part[h], o);
-          const bool valid = pg * kPage + t < L;
-          sc[it][h] = valid ? part[h] * p.score_scale : -INFINITY;
-        }
-      }
-      // ---- online softmax update (page max is warp-uniform)
+          for (int k = 0; k < CPL_V; ++k)
 #pragma unroll
-      for (int h = 0; h < GT; ++h) {
-        float mx = -INFINITY;
-#pragma unroll
-        for (int it = 0; it < ITERS; ++it) mx = fmaxf(mx, sc[it][h]);
-#pragma unroll
-        for (int o = LPT; o < 32; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-        const float mnew = fmaxf(m[h], mx);
-        const float alpha = (mnew == -INFINITY) ? 1.0f : exp2f(m[h] - mnew);
-        m[h] = mnew;
-        l[h] *= alpha;
-#pragma unroll
-        for (int k = 0; k < Cfg::CPL_V; ++k)
-#pragma unroll
-          for (int e = 0; e < 16; ++e) acc[h][k][e] *= alpha;
-#pragma unroll
-        for (int it = 0; it < ITERS; ++it) {
-          const float pr = (sc[it][h] == -INFINITY) ? 0.0f : exp2f(sc[it][h] - mnew);
-          sc[it][h] = pr;
-          l[h] += pr;
+            for (int e = 0; e < 8; ++e) {
+              acc[h][k][e].x *= ah;
+              acc[h][k][e].y *= ah;
+            }
         }
       }
       // ---- P.V
 #pragma unroll
       for (int it = 0; it < ITERS; ++it) {
         const int t = it * TPI + tg;
+        float ph[GT];
+#pragma unroll
+        for (int h = 0; h < GT; ++h) ph[h] = __shfl_sync(0xffffffffu, sc[it], tg * LPT + head_lane<LPT, GT>(h));
         if (pg * kPage + t >= L) continue;  // never touch rows past the sequence end
 #pragma unroll
-        for (int k = 0; k < Cfg::CPL_V; ++k) {
+        for (int k = 0; k < CPL_V; ++k) {
           const int c = c0 + 32 * k;
           if (c * 16 < DV) {
             const uint4 code = *reinterpret_cast<const uint4*>(vc + t * D + c * 16);
-            const float sf = __half2float(vs[t * NB + (c >> 1)]);
-            float vd[16];
-            dequant16<KIND>(code, sf, vd);
+            uint32_t vd[8];
+            dequant16<KIND>(code, vs[t * NB + (c >> 1)], vd);
 #pragma unroll
-            for (int h = 0; h < GT; ++h)
+            for (int e = 0; e < 8; ++e) {
+              const float2 v2 = unpack_bf16x2(vd[e]);
 #pragma unroll
-              for (int e = 0; e < 16; ++e) acc[h][k][e] = fmaf(sc[it][h], vd[e], acc[h][k][e]);
+              for (int h = 0; h < GT; ++h) acc[h][k][e] = ffma2(v2, make_float2(ph[h], ph[h]), acc[h][k][e]);
+            }
           }
         }
       }
@@ -379,40 +430,44 @@ __global__ void __launch_bounds__(WARPS * 32) decode_cc_kernel(KParams p) {
 
   // ---- reduce over token groups inside the warp
 #pragma unroll
-  for (int h = 0; h < GT; ++h) {
+  for (int o = LPT; o < 32; o <<= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
 #pragma unroll
-    for (int o = LPT; o < 32; o <<= 1) l[h] += __shfl_xor_sync(0xffffffffu, l[h], o);
+  for (int h = 0; h < GT; ++h)
 #pragma unroll
-    for (int k = 0; k < Cfg::CPL_V; ++k)
+    for (int k = 0; k < CPL_V; ++k)
 #pragma unroll
-      for (int e = 0; e < 16; ++e)
+      for (int e = 0; e < 8; ++e)
 #pragma unroll
-        for (int o = LPT; o < 32; o <<= 1) acc[h][k][e] += __shfl_xor_sync(0xffffffffu, acc[h][k][e], o);
-  }
+        for (int o = LPT; o < 32; o <<= 1) {
+          acc[h][k][e].x += __shfl_xor_sync(0xffffffffu, acc[h][k][e].x, o);
+          acc[h][k][e].y += __shfl_xor_sync(0xffffffffu, acc[h][k][e].y, o);
+        }
 
   // ---- combine warps through shared memory (pipeline buffers are free now)
   __syncthreads();
   float* cm = reinterpret_cast<float*>(smem);            // [WARPS][GT] m
   float* cl = cm + WARPS * GT;                             // [WARPS][GT] l
   float* ca = cl + WARPS * GT;                             // [WARPS][GT][DV]
-  if (lane == 0) {
+  if (tg == 0 && lane < LPT) {
 #pragma unroll
-    for (int h = 0; h < GT; ++h) {
-      cm[warp * GT + h] = m[h];
-      cl[warp * GT + h] = l[h];
-    }
+    for (int h = 0; h < GT; ++h)
+      if (c0 == head_lane<LPT, GT>(h)) {
+        cm[warp * GT + h] = m;
+        cl[warp * GT + h] = l;
+      }
   }
   if (tg == 0) {
 #pragma unroll
     for (int h = 0; h < GT; ++h)
 #pragma unroll
-      for (int k = 0; k < Cfg::CPL_V; ++k) {
+      for (int k = 0; k < CPL_V; ++k) {
         const int c = c0 + 32 * k;
         if (c * 16 < DV) {
           float4* dst = reinterpret_cast<float4*>(ca + (warp * GT + h) * DV + c * 16);
 #pragma unroll
           for (int e = 0; e < 4; ++e)
-            dst[e] = make_float4(acc[h][k][4 * e], acc[h][k][4 * e + 1], acc[h][k][4 * e + 2], acc[h][k][4 * e + 3]);
+            dst[e] = make_float4(acc[h][k][2 * e].x, acc[h][k][2 * e].y, acc[h][k][2 * e + 1].x,
+                                 acc[h][k][2 * e + 1].y);
         }
       }
   }
@@ -443,43 +498,93 @@ __global__ void __launch_bounds__(WARPS * 32) decode_cc_kernel(KParams p) {
 }
 
 // ------------------------------------------------------------------------------------- merge
-// One CTA per (b, query group): combine the group's split partials per head and write the output.
+// One CTA per (b, query group, head of the group, 32-dim slice of the output).  Its 256 threads are
+// 8 float4 columns x 32 split groups: every thread accumulates its columns over the splits
+// s = group, group + 32, ... with weights exp2(m_s - M), and the groups are summed in shared memory.
+constexpr int kMergeThreads = 256;
+constexpr int kMergeCols = 8;                    // float4 columns = 32 dims per CTA
+constexpr int kMergeGroups = kMergeThreads / kMergeCols;
+
 template <typename OutT>
-__global__ void __launch_bounds__(kPlanThreads) merge_kernel(KParams p, OutT* __restrict__ out, int32_t heads_per_item,
-                                                             int32_t DV) {
+__global__ void __launch_bounds__(kMergeThreads) merge_kernel(KParams p, OutT* __restrict__ out, int32_t heads_per_item,
+                                                              int32_t DV) {
+  __shared__ float s_red[kMergeThreads];
+  __shared__ float4 s_acc[kMergeGroups][kMergeCols];
   const int32_t groups = p.num_kv_heads * p.head_tiles;
-  const int32_t b = blockIdx.x / groups;
-  const int32_t qg = blockIdx.x - b * groups;
+  const int32_t slices = DV / 32;
+  int32_t rest = blockIdx.x;
+  const int32_t slice = rest % slices;
+  rest /= slices;
+  const int32_t h = rest % heads_per_item;
+  rest /= heads_per_item;
+  const int32_t qg = rest % groups;
+  const int32_t b = rest / groups;
   const Plan plan = make_plan(p, -1, b);
   const int32_t g = qg / p.head_tiles, ht = qg - g * p.head_tiles;
-  const int32_t head0 = g * p.group + ht * heads_per_item;
+  const int32_t head = g * p.group + ht * heads_per_item + h;
   int32_t ns = plan.nsplit;
   const int64_t first = static_cast<int64_t>(plan.base) + static_cast<int64_t>(qg) * ns;
   if (first + ns > p.max_items) {  // cannot happen when the workspace bound holds; never read past it
     if (threadIdx.x == 0) set_status(p.status, kStatusBadPage);
     ns = 0;
   }
-  for (int idx = threadIdx.x; idx < heads_per_item * DV; idx += blockDim.x) {
-    const int h = idx / DV, d = idx - h * DV;
-    float M = -INFINITY;
-    for (int32_t s = 0; s < ns; ++s) M = fmaxf(M, p.part_ml[((first + s) * heads_per_item + h) * 2]);
-    float a = 0.0f, lsum = 0.0f;
-    if (M != -INFINITY) {
-      for (int32_t s = 0; s < ns; ++s) {
-        const int64_t it = (first + s) * heads_per_item + h;
-        const float ms = p.part_ml[it * 2];
-        if (ms == -INFINITY) continue;
-        const float w = exp2f(ms - M);
-        lsum = fmaf(p.part_ml[it * 2 + 1], w, lsum);
-        a = fmaf(p.part_acc[it * DV + d], w, a);
-      }
+  const int tid = threadIdx.x;
+  // global max of the split maxima
+  float M = -INFINITY;
+  for (int32_t s = tid; s < ns; s += kMergeThreads) M = fmaxf(M, p.part_ml[((first + s) * heads_per_item + h) * 2]);
+  s_red[tid] = M;
+  __syncthreads();
+  for (int o = kMergeThreads / 2; o > 0; o >>= 1) {
+    if (tid < o) s_red[tid] = fmaxf(s_red[tid], s_red[tid + o]);
+    __syncthreads();
+  }
+  M = s_red[0];
+  __syncthreads();
+  const int col = tid % kMergeCols, grp = tid / kMergeCols;
+  const int d = slice * 32 + col * 4;
+  float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+  float lsum = 0.0f;
+  if (M != -INFINITY) {
+#pragma unroll 4
+    for (int32_t s = grp; s < ns; s += kMergeGroups) {
+      const int64_t it = (first + s) * heads_per_item + h;
+      const float2 ml = *reinterpret_cast<const float2*>(p.part_ml + it * 2);
+      const float w = (ml.x == -INFINITY) ? 0.0f : exp2f(ml.x - M);
+      const float4 v = *reinterpret_cast<const float4*>(p.part_acc + it * DV + d);
+      a.x = fmaf(v.x, w, a.x);
+      a.y = fmaf(v.y, w, a.y);
+      a.z = fmaf(v.z, w, a.z);
+      a.w = fmaf(v.w, w, a.w);
+      lsum = fmaf(ml.y, w, lsum);
     }
-    const float o = (lsum > 0.0f) ? a / lsum : 0.0f;
-    const int64_t dst = (static_cast<int64_t>(b) * p.num_q_heads + head0 + h) * DV + d;
-    if constexpr (sizeof(OutT) == 2)
-      out[dst] = __float2bfloat16_rn(o);
-    else
-      out[dst] = o;
+  }
+  s_acc[grp][col] = a;
+  s_red[tid] = (col == 0) ? lsum : 0.0f;
+  __syncthreads();
+  for (int o = kMergeThreads / 2; o > 0; o >>= 1) {
+    if (tid < o) s_red[tid] += s_red[tid + o];
+    __syncthreads();
+  }
+  const float L = s_red[0];
+  if (tid < kMergeCols) {
+    float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int gi = 0; gi < kMergeGroups; ++gi) {
+      const float4 v = s_acc[gi][tid];
+      t.x += v.x;
+      t.y += v.y;
+      t.z += v.z;
+      t.w += v.w;
+    }
+    const float inv = (L > 0.0f) ? 1.0f / L : 0.0f;
+    const float o4[4] = {t.x * inv, t.y * inv, t.z * inv, t.w * inv};
+    const int64_t dst = (static_cast<int64_t>(b) * p.num_q_heads + head) * DV + slice * 32 + tid * 4;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      if constexpr (sizeof(OutT) == 2)
+        out[dst + e] = __float2bfloat16_rn(o4[e]);
+      else
+        out[dst + e] = o4[e];
+    }
   }
 }
 
@@ -491,10 +596,11 @@ __global__ void dequant_probe_kernel(const uint8_t* __restrict__ codes, const ui
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   for (int64_t c = i; c < nchunks; c += stride) {
     const uint4 code = reinterpret_cast<const uint4*>(codes)[c];
-    float v[16];
-    dequant16<KIND>(code, half_bits_to_float(scales[c]), v);
-#pragma unroll
-    for (int e = 0; e < 16; ++e) out[c * 16 + e] = __bfloat16_as_ushort(__float2bfloat16_rn(v[e]));
+    uint32_t kd[8];
+    dequant16<KIND>(code, scales[c], kd);
+    uint4* dst = reinterpret_cast<uint4*>(out + c * 16);
+    dst[0] = make_uint4(kd[0], kd[1], kd[2], kd[3]);
+    dst[1] = make_uint4(kd[4], kd[5], kd[6], kd[7]);
   }
 }
 
@@ -521,10 +627,11 @@ KParams make_kparams(const DecodeArgs& a) {
   return p;
 }
 
-template <int D, int DV, int GT, int KIND, bool MLA, int WARPS, int STAGES>
+template <int D, int DV, int GT, int KIND, bool MLA, int STAGES, int MINB>
 kvq_status launch_cc(const DecodeArgs& a, cudaStream_t stream) {
+  constexpr int WARPS = 4;
   using Cfg = CCConfig<D, DV, GT, KIND, MLA, WARPS, STAGES>;
-  auto kern = decode_cc_kernel<D, DV, GT, KIND, MLA, WARPS, STAGES>;
+  auto kern = decode_cc_kernel<D, DV, GT, KIND, MLA, WARPS, STAGES, MINB>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES) != cudaSuccess)
     return KVQ_ECUDA;
   const KParams p = make_kparams(a);
@@ -532,10 +639,10 @@ kvq_status launch_cc(const DecodeArgs& a, cudaStream_t stream) {
   return cudaGetLastError() == cudaSuccess ? KVQ_OK : KVQ_ECUDA;
 }
 
-template <int D, int DV, int GT, bool MLA, int STAGES>
+template <int D, int DV, int GT, bool MLA, int STAGES, int MINB>
 kvq_status launch_cc_kind(const DecodeArgs& a, cudaStream_t stream) {
-  if (a.kind == KVQ_FP8_E4M3) return launch_cc<D, DV, GT, KVQ_FP8_E4M3, MLA, 4, STAGES>(a, stream);
-  return launch_cc<D, DV, GT, KVQ_Q8_0, MLA, 4, STAGES>(a, stream);
+  if (a.kind == KVQ_FP8_E4M3) return launch_cc<D, DV, GT, KVQ_FP8_E4M3, MLA, STAGES, MINB>(a, stream);
+  return launch_cc<D, DV, GT, KVQ_Q8_0, MLA, STAGES, MINB>(a, stream);
 }
 
 }  // namespace
@@ -556,31 +663,32 @@ bool decode_cc_supported(int32_t head_dim, int32_t v_dim, int32_t mla) {
 kvq_status launch_decode_cc(const DecodeArgs& a, cudaStream_t stream) {
   const int gt = a.heads_per_item;
   if (a.mla) {
-    if (gt == 1) return launch_cc_kind<576, 512, 1, true, 2>(a, stream);
-    return launch_cc_kind<576, 512, 2, true, 2>(a, stream);
+    if (gt == 1) return launch_cc_kind<576, 512, 1, true, 2, 1>(a, stream);
+    return launch_cc_kind<576, 512, 2, true, 2, 1>(a, stream);
   }
-#define KVQ_CC_CASE(DD, STG)                                                        \
+#define KVQ_CC_CASE(DD, STG, MB)                                                    \
   if (a.head_dim == DD) {                                                           \
-    if (gt == 1) return launch_cc_kind<DD, DD, 1, false, STG>(a, stream);           \
-    if (gt == 2) return launch_cc_kind<DD, DD, 2, false, STG>(a, stream);           \
-    return launch_cc_kind<DD, DD, 4, false, STG>(a, stream);                        \
+    if (gt == 1) return launch_cc_kind<DD, DD, 1, false, STG, MB>(a, stream);       \
+    if (gt == 2) return launch_cc_kind<DD, DD, 2, false, STG, MB>(a, stream);       \
+    return launch_cc_kind<DD, DD, 4, false, STG, MB>(a, stream);                    \
   }
-  KVQ_CC_CASE(64, 4)
-  KVQ_CC_CASE(128, 4)
-  KVQ_CC_CASE(256, 3)
+  KVQ_CC_CASE(64, 4, 4)
+  KVQ_CC_CASE(128, 3, 4)
+  KVQ_CC_CASE(256, 2, 3)
 #undef KVQ_CC_CASE
   return KVQ_EUNSUPPORTED;
 }
 
 kvq_status launch_merge(const DecodeArgs& a, int32_t query_groups, cudaStream_t stream) {
   const KParams p = make_kparams(a);
-  const unsigned grid = static_cast<unsigned>(static_cast<int64_t>(a.batch) * query_groups);
+  const int64_t grid = static_cast<int64_t>(a.batch) * query_groups * a.heads_per_item * (a.v_dim / 32);
   if (grid == 0) return KVQ_OK;
   if (a.out_dtype == KVQ_OUT_BF16)
-    merge_kernel<__nv_bfloat16><<<grid, kPlanThreads, 0, stream>>>(p, static_cast<__nv_bfloat16*>(a.out),
-                                                                    a.heads_per_item, a.v_dim);
+    merge_kernel<__nv_bfloat16><<<static_cast<unsigned>(grid), kMergeThreads, 0, stream>>>(
+        p, static_cast<__nv_bfloat16*>(a.out), a.heads_per_item, a.v_dim);
   else
-    merge_kernel<float><<<grid, kPlanThreads, 0, stream>>>(p, static_cast<float*>(a.out), a.heads_per_item, a.v_dim);
+    merge_kernel<float><<<static_cast<unsigned>(grid), kMergeThreads, 0, stream>>>(p, static_cast<float*>(a.out),
+                                                                                 a.heads_per_item, a.v_dim);
   return cudaGetLastError() == cudaSuccess ? KVQ_OK : KVQ_ECUDA;
 }
 

@@ -9,6 +9,7 @@
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
 #include <stdint.h>
+#include <string.h>
 
 #include "../../include/kvq.h"
 #include "kvq_internal.h"
@@ -116,36 +117,86 @@ __device__ __forceinline__ uint8_t encode_q8(float y) {
 }
 
 // --------------------------------------------------------------------------- decode dequantization
-// Value of one code pair as exact fp32 (fp8: via the hardware E4M3 -> f16 conversion, exact).
-__device__ __forceinline__ float2 fp8x2_to_float2(uint16_t two) {
-  __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two), __NV_E4M3);
-  __half2 hh = *reinterpret_cast<__half2*>(&h);
-  return __half22float2(hh);
+// Dequantize to bf16: kd = RNE_bf16(value(code) * s), where s is the block's fp16 scale.
+//   1. the codes become exact f16 values: fp8 through the hardware E4M3 -> f16x2 conversion; q8_0
+//      through the 1024-offset f16 pattern 0x6400 | (q + 128), whose offset is removed in step 2;
+//   2. one mixed-precision FMA per element, f16 x f16 + f32 -> f32, forms code * s exactly (an
+//      11-bit by 11-bit product fits fp32's 24 bits; for q8_0 the addend -1152 * s removes the offset
+//      exactly, because (q + 1152) * s and 1152 * s are exact and the result q * s is representable);
+//   3. one bf16x2 conversion rounds the pair to nearest-even.
+// The result is packed bf16x2 (element 2p in the low half), exactly the bf16 numbers of the oracle.
+__device__ __forceinline__ uint32_t cvt_f16x2_e4m3x2(uint32_t two_codes) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(static_cast<uint16_t>(two_codes)));
+  return r;
 }
 
-// bf16 RNE of an exact fp32 product, returned widened back to fp32.
-__device__ __forceinline__ float round_bf16(float x) { return __bfloat162float(__float2bfloat16_rn(x)); }
+__device__ __forceinline__ float fma_f32_f16(uint16_t a, uint16_t b, float c) {
+  float d;
+  asm("fma.rn.f32.f16 %0, %1, %2, %3;" : "=f"(d) : "h"(a), "h"(b), "f"(c));
+  return d;
+}
 
-// Dequantize 16 codes (one 16-byte chunk) of one scale block into fp32 values that are exactly the
-// bf16 numbers RNE(code * scale).  The code * scale product is exact in fp32 (<= 18 significant bits).
+__device__ __forceinline__ float fma_f32_bf16(uint16_t a, uint16_t b, float c) {
+  float d;
+  asm("fma.rn.f32.bf16 %0, %1, %2, %3;" : "=f"(d) : "h"(a), "h"(b), "f"(c));
+  return d;
+}
+
+// bf16x2 of (lo, hi), round to nearest-even; lo lands in the low half.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Packed fp32 FMA on two lanes of a 64-bit register pair (d = a * b + c elementwise).
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+  uint64_t A, B, C, D;
+  memcpy(&A, &a, 8);
+  memcpy(&B, &b, 8);
+  memcpy(&C, &c, 8);
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(D) : "l"(A), "l"(B), "l"(C));
+  float2 d;
+  memcpy(&d, &D, 8);
+  return d;
+}
+
+__device__ __forceinline__ float2 unpack_bf16x2(uint32_t v) {
+  return make_float2(__uint_as_float(v << 16), __uint_as_float(v & 0xFFFF0000u));
+}
+
+__device__ __forceinline__ uint16_t lo16(uint32_t v) { return static_cast<uint16_t>(v & 0xFFFFu); }
+__device__ __forceinline__ uint16_t hi16(uint32_t v) { return static_cast<uint16_t>(v >> 16); }
+
+// Addend that completes step 2 for a block with fp16 scale bits s_bits.
 template <int KIND>
-__device__ __forceinline__ void dequant16(const uint4 c, float scale, float out[16]) {
+__device__ __forceinline__ float dequant_addend(uint16_t s_bits) {
+  if (KIND == KVQ_FP8_E4M3) return -0.0f;
+  return -1152.0f * __half2float(__ushort_as_half(s_bits));
+}
+
+// Exact f16 values of codes (2w, 2w+1) of a 32-bit word of four codes; `half` selects bytes 0-1 or 2-3.
+template <int KIND>
+__device__ __forceinline__ uint32_t codes_to_f16x2(uint32_t word, int half) {
+  if (KIND == KVQ_FP8_E4M3) return cvt_f16x2_e4m3x2(half ? (word >> 16) : (word & 0xFFFFu));
+  const uint32_t u = word ^ 0x80808080u;  // q + 128 in each byte
+  return __byte_perm(u, 0x64646464u, half ? 0x5342u : 0x5140u);
+}
+
+// Dequantize 16 codes (one 16-byte chunk, one scale) into 8 bf16x2 words.
+template <int KIND>
+__device__ __forceinline__ void dequant16(const uint4 c, uint16_t s_bits, uint32_t kd[8]) {
+  const float z = dequant_addend<KIND>(s_bits);
   const uint32_t w[4] = {c.x, c.y, c.z, c.w};
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    if (KIND == KVQ_FP8_E4M3) {
-      float2 lo = fp8x2_to_float2(static_cast<uint16_t>(w[i] & 0xFFFFu));
-      float2 hi = fp8x2_to_float2(static_cast<uint16_t>(w[i] >> 16));
-      out[4 * i + 0] = round_bf16(lo.x * scale);
-      out[4 * i + 1] = round_bf16(lo.y * scale);
-      out[4 * i + 2] = round_bf16(hi.x * scale);
-      out[4 * i + 3] = round_bf16(hi.y * scale);
-    } else {
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int8_t q = static_cast<int8_t>((w[i] >> (8 * j)) & 0xFFu);
-        out[4 * i + j] = round_bf16(static_cast<float>(q) * scale);
-      }
+    for (int hh = 0; hh < 2; ++hh) {
+      const uint32_t c2 = codes_to_f16x2<KIND>(w[i], hh);
+      const float a = fma_f32_f16(lo16(c2), s_bits, z);
+      const float b = fma_f32_f16(hi16(c2), s_bits, z);
+      kd[2 * i + hh] = pack_bf16x2(a, b);
     }
   }
 }

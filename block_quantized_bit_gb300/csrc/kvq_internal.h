@@ -52,6 +52,8 @@ int64_t max_work_items(int32_t batch, int32_t query_groups, int32_t max_pages, i
 kvq_status launch_store(void* pool, void* scales, const void* k, const void* v, const int64_t* slot_mapping,
                         int64_t num_tokens, const kvq_layout& L, kvq_kind kind, cudaStream_t stream);
 kvq_status launch_encode_probe(kvq_kind kind, const float* y, uint8_t* codes, int64_t n, cudaStream_t stream);
+kvq_status launch_quantize_probe(kvq_kind kind, const uint16_t* x, int64_t nx, const uint16_t* s, int64_t ns,
+                                 uint8_t* codes, cudaStream_t stream);
 kvq_status launch_dequant_probe(kvq_kind kind, const uint8_t* codes, const uint16_t* scales, uint16_t* out,
                                 int64_t n, cudaStream_t stream);
 bool decode_cc_supported(int32_t head_dim, int32_t v_dim, int32_t mla);

@@ -5,11 +5,19 @@
 // and its review comment "A bug on sm_89" (int8 rounds half away from zero then clamps; fp8 clamps
 // then rounds once to nearest-even -- never through a truncated fp16).
 //
-// Mapping: four lanes own one 32-element block (8 bf16 = one 16-byte load each).  The input is
-// walked as a flat stream of blocks, K first then V, so every warp load is 512 contiguous bytes.
-// amax is a 2-step xor shuffle inside the 4-lane group; each lane writes its 8 code bytes, the
-// group's first lane the fp16 scale.  UNROLL independent blocks per lane are loaded before any is
-// processed, to keep enough bytes in flight for HBM.
+// Mapping: one lane owns one 32-element block (four 16-byte loads, 64 contiguous bytes).  The input
+// is walked as a flat stream of blocks, K first then V; a warp covers 2 KiB of contiguous input per
+// sweep and each lane keeps UNROLL blocks in flight.  The lane computes amax, the fp16 scale, the 32
+// codes (two 16-byte stores) and the scale without any cross-lane traffic.
+//
+// Division.  The codes must be those of the IEEE fp32 quotient x / s.  Per block the lane takes
+// r = RN(1/s) (IEEE reciprocal) once; per element it forms q0 = x*r, the exact remainder
+// e = q0*s - x by FMA, and y = q0 - e*r (one Newton-Raphson step with an FMA remainder, Markstein,
+// "Computation of elementary functions on the IBM RISC System/6000 processor", IBM J. Res. Dev.
+// 34(1), 1990).  y is not the correctly rounded quotient for every (x, s), but its fp8 and q8_0 codes
+// equal the codes of the IEEE quotient for every bf16 x and every fp16 s; the GPU test sweeps all of
+// them through kvq_quantize_probe against the oracle's IEEE division.  The operand order keeps the
+// sign of zero (x = -0 gives y = -0, code 0x80).
 #include <algorithm>
 
 #include "kvq_device.cuh"
@@ -22,83 +30,129 @@ namespace {
 constexpr int kStoreThreads = 256;
 constexpr int kStoreUnroll = 4;
 
-template <int KIND, int UNROLL>
-__global__ void __launch_bounds__(kStoreThreads)
-    store_kernel(uint8_t* __restrict__ codes, __half* __restrict__ scales, const uint4* __restrict__ k,
-                 const uint4* __restrict__ v, const int64_t* __restrict__ slot_mapping, int32_t T,
-                 int32_t Hkv, int32_t D, int32_t P, int32_t n_kv, int64_t num_slots) {
-  const int32_t nb = D >> 5;
-  const int32_t row_blocks = Hkv * nb;            // blocks in one token row (all heads)
-  const int32_t blocks_per_kv = T * row_blocks;   // host guarantees n_kv * this < 2^31
-  const int32_t total = blocks_per_kv * n_kv;
-  const int lane = threadIdx.x & 31;
-  const int sub = lane & 3;
-  const int32_t warp_global = (blockIdx.x * kStoreThreads + threadIdx.x) >> 5;
-  const int32_t nwarps = (gridDim.x * kStoreThreads) >> 5;
-  const int32_t step = nwarps * 8;  // groups per sweep of all warps
+// Unsigned division by a run-time constant d >= 1 via a multiply-high (Granlund & Montgomery,
+// "Division by invariant integers using multiplication", PLDI 1994): q = (umulhi(n, m) + n) >> s,
+// valid for n < 2^31.
+struct FastDiv {
+  uint32_t m, s, d;
+};
 
-  for (int32_t wbase = warp_global * 8; wbase < total; wbase += step * UNROLL) {
-    uint4 x[UNROLL];
-    int32_t blk[UNROLL];
+FastDiv make_fastdiv(uint32_t d) {
+  uint32_t s = 0;
+  while ((1ull << s) < d) ++s;  // s = ceil(log2 d)
+  const uint64_t m = ((1ull << 32) * ((1ull << s) - d)) / d + 1;
+  return FastDiv{static_cast<uint32_t>(m), s, d};
+}
+
+__device__ __forceinline__ uint32_t fdiv(uint32_t n, const FastDiv& f) {
+  return (__umulhi(n, f.m) + n) >> f.s;
+}
+
+// Code step shared by the store kernel and kvq_quantize_probe.
+__device__ __forceinline__ float quotient(float x, float s, float r) {
+  const float q0 = x * r;
+  const float e = fmaf(q0, s, -x);
+  return fmaf(e, -r, q0);
+}
+
+template <int KIND>
+__device__ __forceinline__ uint32_t encode4(float a, float b, float c, float d) {
+  if (KIND == KVQ_FP8_E4M3) {
+    return static_cast<uint32_t>(encode_fp8x2(a, b)) | (static_cast<uint32_t>(encode_fp8x2(c, d)) << 16);
+  } else {
+    return static_cast<uint32_t>(encode_q8(a)) | (static_cast<uint32_t>(encode_q8(b)) << 8) |
+           (static_cast<uint32_t>(encode_q8(c)) << 16) | (static_cast<uint32_t>(encode_q8(d)) << 24);
+  }
+}
+
+struct StoreArgs {
+  uint8_t* codes;
+  __half* scales;
+  const uint4* k;
+  const uint4* v;
+  const int64_t* slot_mapping;
+  int32_t blocks_per_kv;  // T * Hkv * nb
+  int32_t total;          // blocks_per_kv * n_kv  (< 2^31)
+  FastDiv row_blocks;     // Hkv * nb
+  FastDiv nb;             // blocks per row of one head
+  int32_t Hkv, D, n_kv;
+  int32_t page_shift;     // log2(page_size) if a power of two, else -1
+  int32_t P;
+  int64_t num_slots;
+};
+
+template <int KIND, int UNROLL>
+__global__ void __launch_bounds__(kStoreThreads) store_kernel(StoreArgs a) {
+  const int32_t stride = gridDim.x * kStoreThreads;
+  for (int32_t base = blockIdx.x * kStoreThreads + threadIdx.x; base < a.total; base += stride * UNROLL) {
+    uint4 x[UNROLL][4];
 #pragma unroll
     for (int u = 0; u < UNROLL; ++u) {
-      blk[u] = wbase + u * step + (lane >> 2);
-      x[u] = make_uint4(0u, 0u, 0u, 0u);
-      if (blk[u] < total) {
-        const int kv = blk[u] >= blocks_per_kv;
-        const int32_t local = blk[u] - (kv ? blocks_per_kv : 0);
-        x[u] = __ldcs((kv ? v : k) + (static_cast<int64_t>(local) * 4 + sub));
+      const int32_t blk = base + u * stride;
+      if (blk < a.total) {
+        const int kv = blk >= a.blocks_per_kv;
+        const int32_t local = blk - (kv ? a.blocks_per_kv : 0);
+        const uint4* src = (kv ? a.v : a.k) + static_cast<int64_t>(local) * 4;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) x[u][i] = __ldcs(src + i);
       }
     }
 #pragma unroll
     for (int u = 0; u < UNROLL; ++u) {
-      float f[8];
-      const __nv_bfloat162* xp = reinterpret_cast<const __nv_bfloat162*>(&x[u]);
+      const int32_t blk = base + u * stride;
+      if (blk >= a.total) continue;
+      const int kv = blk >= a.blocks_per_kv;
+      const uint32_t local = static_cast<uint32_t>(blk - (kv ? a.blocks_per_kv : 0));
+      const uint32_t t = fdiv(local, a.row_blocks);
+      const uint32_t in_row = local - t * a.row_blocks.d;
+      const uint32_t h = fdiv(in_row, a.nb);
+      const uint32_t j = in_row - h * a.nb.d;
+      const int64_t slot = __ldg(a.slot_mapping + t);
+      if (slot < 0 || slot >= a.num_slots) continue;  // -1 skips; out-of-range slots are never written
+      int64_t page, off;
+      if (a.page_shift >= 0) {
+        page = slot >> a.page_shift;
+        off = slot & (a.P - 1);
+      } else {
+        page = slot / a.P;
+        off = slot - page * a.P;
+      }
+      const int64_t dst_row = ((page * a.n_kv + kv) * a.Hkv + h) * a.P + off;
+
+      float f[32];
       float amax = 0.0f;
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        const float2 t = __bfloat1622float2(xp[i]);
-        f[2 * i] = t.x;
-        f[2 * i + 1] = t.y;
-        amax = fmaxf(amax, fmaxf(fabsf(t.x), fabsf(t.y)));
-      }
-      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-      if (blk[u] >= total) continue;
-      const int kv = blk[u] >= blocks_per_kv;
-      const int32_t local = blk[u] - (kv ? blocks_per_kv : 0);
-      const int32_t t = local / row_blocks;
-      const int32_t in_row = local - t * row_blocks;
-      const int32_t h = in_row / nb;
-      const int32_t j = in_row - h * nb;
-      const int64_t slot = __ldg(slot_mapping + t);
-      if (slot < 0 || slot >= num_slots) continue;  // -1 skips; out-of-range slots are never written
-      const int64_t page = slot / P;
-      const int32_t off = static_cast<int32_t>(slot - page * P);
-      const int64_t dst_row = ((page * n_kv + kv) * Hkv + h) * P + off;
-
-      const __half s16 = block_scale<KIND>(amax);
-      const float sf = __half2float(s16);
-      uint2 out = make_uint2(0u, 0u);
-      if (sf != 0.0f) {
-        float y[8];
+        const uint32_t w[4] = {x[u][i].x, x[u][i].y, x[u][i].z, x[u][i].w};
 #pragma unroll
-        for (int i = 0; i < 8; ++i) y[i] = __fdiv_rn(f[i], sf);
-        if (KIND == KVQ_FP8_E4M3) {
-          out.x = static_cast<uint32_t>(encode_fp8x2(y[0], y[1])) |
-                  (static_cast<uint32_t>(encode_fp8x2(y[2], y[3])) << 16);
-          out.y = static_cast<uint32_t>(encode_fp8x2(y[4], y[5])) |
-                  (static_cast<uint32_t>(encode_fp8x2(y[6], y[7])) << 16);
-        } else {
-          out.x = static_cast<uint32_t>(encode_q8(y[0])) | (static_cast<uint32_t>(encode_q8(y[1])) << 8) |
-                  (static_cast<uint32_t>(encode_q8(y[2])) << 16) | (static_cast<uint32_t>(encode_q8(y[3])) << 24);
-          out.y = static_cast<uint32_t>(encode_q8(y[4])) | (static_cast<uint32_t>(encode_q8(y[5])) << 8) |
-                  (static_cast<uint32_t>(encode_q8(y[6])) << 16) | (static_cast<uint32_t>(encode_q8(y[7])) << 24);
+        for (int e = 0; e < 4; ++e) {
+          f[8 * i + 2 * e] = __uint_as_float(w[e] << 16);
+          f[8 * i + 2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u);
         }
       }
-      uint2* dst = reinterpret_cast<uint2*>(codes + dst_row * D + (j << 5) + (sub << 3));
-      __stcs(dst, out);
-      if (sub == 0) scales[dst_row * nb + j] = (sf != 0.0f) ? s16 : __ushort_as_half(0);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(f[i]));
+      const __half s16 = block_scale<KIND>(amax);
+      const float sf = __half2float(s16);
+      uint4 o0 = make_uint4(0u, 0u, 0u, 0u), o1 = o0;
+      if (sf != 0.0f) {
+        const float r = __frcp_rn(sf);
+        float y[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) y[i] = quotient(f[i], sf, r);
+        o0.x = encode4<KIND>(y[0], y[1], y[2], y[3]);
+        o0.y = encode4<KIND>(y[4], y[5], y[6], y[7]);
+        o0.z = encode4<KIND>(y[8], y[9], y[10], y[11]);
+        o0.w = encode4<KIND>(y[12], y[13], y[14], y[15]);
+        o1.x = encode4<KIND>(y[16], y[17], y[18], y[19]);
+        o1.y = encode4<KIND>(y[20], y[21], y[22], y[23]);
+        o1.z = encode4<KIND>(y[24], y[25], y[26], y[27]);
+        o1.w = encode4<KIND>(y[28], y[29], y[30], y[31]);
+      }
+      uint4* dst = reinterpret_cast<uint4*>(a.codes + dst_row * a.D + (static_cast<int64_t>(j) << 5));
+      __stcs(dst, o0);
+      __stcs(dst + 1, o1);
+      a.scales[dst_row * (a.D >> 5) + j] = (sf != 0.0f) ? s16 : __ushort_as_half(0);
     }
   }
 }
@@ -115,6 +169,21 @@ __global__ void encode_probe_kernel(const float* __restrict__ y, uint8_t* __rest
   }
 }
 
+// codes[i * nx + j] = code of x[j] against the nonzero fp16 scale s[i], by the store's own routine.
+template <int KIND>
+__global__ void quantize_probe_kernel(const uint16_t* __restrict__ x, int64_t nx, const uint16_t* __restrict__ s,
+                                      int64_t ns, uint8_t* __restrict__ codes) {
+  const int64_t n = nx * ns;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; e < n; e += stride) {
+    const int64_t i = e / nx, j = e - i * nx;
+    const float sf = half_bits_to_float(s[i]);
+    const float xf = __uint_as_float(static_cast<uint32_t>(x[j]) << 16);
+    const float y = quotient(xf, sf, __frcp_rn(sf));
+    codes[e] = static_cast<uint8_t>(encode4<KIND>(y, 0.0f, 0.0f, 0.0f) & 0xFFu);
+  }
+}
+
 int sm_count() {
   int dev = 0, n = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 152;
@@ -127,30 +196,38 @@ int sm_count() {
 kvq_status launch_store(void* pool, void* scales, const void* k, const void* v, const int64_t* slot_mapping,
                         int64_t num_tokens, const kvq_layout& L, kvq_kind kind, cudaStream_t stream) {
   const int n_kv = L.mla ? 1 : 2;
-  const int64_t row_blocks = static_cast<int64_t>(L.num_kv_heads) * (L.head_dim / 32);
+  const int32_t nb = L.head_dim / 32;
+  const int64_t row_blocks = static_cast<int64_t>(L.num_kv_heads) * nb;
   const int64_t max_rows = std::max<int64_t>(1, ((int64_t(1) << 30) / (row_blocks * n_kv)));
   const int64_t row_elems = static_cast<int64_t>(L.num_kv_heads) * L.head_dim;
   const int sms = sm_count();
-  const int64_t num_slots = L.num_pages * L.page_size;
+  int page_shift = -1;
+  for (int s = 0; s < 31; ++s)
+    if ((1 << s) == L.page_size) page_shift = s;
   for (int64_t t0 = 0; t0 < num_tokens; t0 += max_rows) {
-    const int32_t T = static_cast<int32_t>(std::min(max_rows, num_tokens - t0));
-    const int64_t total_blocks = static_cast<int64_t>(T) * row_blocks * n_kv;
-    const int64_t groups_per_cta = kStoreThreads / 4;
-    int64_t grid = (total_blocks + groups_per_cta * kStoreUnroll - 1) / (groups_per_cta * kStoreUnroll);
-    grid = std::min<int64_t>(grid, static_cast<int64_t>(sms) * 8);
-    grid = std::max<int64_t>(grid, 1);
-    const uint4* kp = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(k) + t0 * row_elems);
-    const uint4* vp =
-        v ? reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(v) + t0 * row_elems) : nullptr;
-    const int64_t* sm = slot_mapping + t0;
+    const int64_t T = std::min(max_rows, num_tokens - t0);
+    StoreArgs a;
+    a.codes = static_cast<uint8_t*>(pool);
+    a.scales = static_cast<__half*>(scales);
+    a.k = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(k) + t0 * row_elems);
+    a.v = v ? reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(v) + t0 * row_elems) : nullptr;
+    a.slot_mapping = slot_mapping + t0;
+    a.blocks_per_kv = static_cast<int32_t>(T * row_blocks);
+    a.total = a.blocks_per_kv * n_kv;
+    a.row_blocks = make_fastdiv(static_cast<uint32_t>(row_blocks));
+    a.nb = make_fastdiv(static_cast<uint32_t>(nb));
+    a.Hkv = L.num_kv_heads;
+    a.D = L.head_dim;
+    a.n_kv = n_kv;
+    a.page_shift = page_shift;
+    a.P = L.page_size;
+    a.num_slots = L.num_pages * L.page_size;
+    int64_t grid = (static_cast<int64_t>(a.total) + kStoreThreads * kStoreUnroll - 1) / (kStoreThreads * kStoreUnroll);
+    grid = std::max<int64_t>(1, std::min<int64_t>(grid, static_cast<int64_t>(sms) * 8));
     if (kind == KVQ_FP8_E4M3)
-      store_kernel<KVQ_FP8_E4M3, kStoreUnroll><<<static_cast<unsigned>(grid), kStoreThreads, 0, stream>>>(
-          static_cast<uint8_t*>(pool), static_cast<__half*>(scales), kp, vp, sm, T, L.num_kv_heads, L.head_dim,
-          L.page_size, n_kv, num_slots);
+      store_kernel<KVQ_FP8_E4M3, kStoreUnroll><<<static_cast<unsigned>(grid), kStoreThreads, 0, stream>>>(a);
     else
-      store_kernel<KVQ_Q8_0, kStoreUnroll><<<static_cast<unsigned>(grid), kStoreThreads, 0, stream>>>(
-          static_cast<uint8_t*>(pool), static_cast<__half*>(scales), kp, vp, sm, T, L.num_kv_heads, L.head_dim,
-          L.page_size, n_kv, num_slots);
+      store_kernel<KVQ_Q8_0, kStoreUnroll><<<static_cast<unsigned>(grid), kStoreThreads, 0, stream>>>(a);
     if (cudaGetLastError() != cudaSuccess) return KVQ_ECUDA;
   }
   return KVQ_OK;
@@ -164,6 +241,19 @@ kvq_status launch_encode_probe(kvq_kind kind, const float* y, uint8_t* codes, in
     encode_probe_kernel<KVQ_FP8_E4M3><<<static_cast<unsigned>(grid), threads, 0, stream>>>(y, codes, n);
   else
     encode_probe_kernel<KVQ_Q8_0><<<static_cast<unsigned>(grid), threads, 0, stream>>>(y, codes, n);
+  return cudaGetLastError() == cudaSuccess ? KVQ_OK : KVQ_ECUDA;
+}
+
+kvq_status launch_quantize_probe(kvq_kind kind, const uint16_t* x, int64_t nx, const uint16_t* s, int64_t ns,
+                                 uint8_t* codes, cudaStream_t stream) {
+  const int64_t n = nx * ns;
+  if (n == 0) return KVQ_OK;
+  const int threads = 256;
+  const int64_t grid = std::min<int64_t>((n + threads - 1) / threads, static_cast<int64_t>(sm_count()) * 16);
+  if (kind == KVQ_FP8_E4M3)
+    quantize_probe_kernel<KVQ_FP8_E4M3><<<static_cast<unsigned>(grid), threads, 0, stream>>>(x, nx, s, ns, codes);
+  else
+    quantize_probe_kernel<KVQ_Q8_0><<<static_cast<unsigned>(grid), threads, 0, stream>>>(x, nx, s, ns, codes);
   return cudaGetLastError() == cudaSuccess ? KVQ_OK : KVQ_ECUDA;
 }
 

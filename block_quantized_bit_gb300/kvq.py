@@ -28,7 +28,7 @@ STATUS = {0: "KVQ_OK", -1: "KVQ_EINVAL", -2: "KVQ_EKIND", -3: "KVQ_EHEADDIM", -4
 
 EXPORTS = ["kvq_pool_bytes", "kvq_scale_bytes", "kvq_bytes_per_token", "kvq_num_pages", "kvq_store",
            "kvq_decode_workspace_bytes", "kvq_decode_workspace_bytes_ex", "kvq_decode", "kvq_decode_ex",
-           "kvq_workspace_status", "kvq_encode_probe", "kvq_dequant_probe", "kvq_strerror",
+           "kvq_workspace_status", "kvq_encode_probe", "kvq_quantize_probe", "kvq_dequant_probe", "kvq_strerror",
            "kvq_device_check", "kvq_version", "kvq_decode_noalloc"]
 
 
@@ -73,6 +73,7 @@ def lib():
             "kvq_workspace_status": (i32, [P, P]),
             "kvq_encode_probe": (i32, [i32, P, P, i64, P]),
             "kvq_dequant_probe": (i32, [i32, P, P, P, i64, P]),
+            "kvq_quantize_probe": (i32, [i32, P, i64, P, i64, P, P]),
             "kvq_strerror": (ctypes.c_char_p, [i32]),
             "kvq_device_check": (i32, []),
             "kvq_version": (ctypes.c_char_p, []),
@@ -228,6 +229,12 @@ def kvq_workspace_status(workspace: torch.Tensor, stream=None) -> int:
 def kvq_encode_probe(kind, y: torch.Tensor, codes: torch.Tensor, stream=None):
     _check(lib().kvq_encode_probe(_kind(kind), _ptr(y), _ptr(codes), int(y.numel()), _stream(stream)),
            "kvq_encode_probe")
+
+
+def kvq_quantize_probe(kind, x_bits: torch.Tensor, s_bits: torch.Tensor, codes: torch.Tensor, stream=None):
+    """codes[i * nx + j] = the store's code of bf16 x[j] against nonzero fp16 scale s[i]."""
+    _check(lib().kvq_quantize_probe(_kind(kind), _ptr(x_bits), int(x_bits.numel()), _ptr(s_bits), int(s_bits.numel()),
+                                    _ptr(codes), _stream(stream)), "kvq_quantize_probe")
 
 
 def kvq_dequant_probe(kind, codes: torch.Tensor, scales: torch.Tensor, out: torch.Tensor, stream=None):

@@ -181,6 +181,14 @@ kvq_status kvq_workspace_status(const void* workspace, void* stream);
  */
 kvq_status kvq_encode_probe(kvq_kind kind, const float* y, uint8_t* codes, int64_t n, void* stream);
 /*
+ * Division-and-rounding step of the store, by the store kernel's own routine, for every pairing of
+ * nx bf16 elements with ns nonzero fp16 scales (device arrays of bit patterns):
+ * codes[i * nx + j] = code of x[j] / s[i] (fp8_e4m3 or q8_0, as kvq_store computes it).  Exposes the
+ * store's quotient so that its codes can be checked against IEEE division on every (x, s).
+ */
+kvq_status kvq_quantize_probe(kvq_kind kind, const uint16_t* x, int64_t nx, const uint16_t* s, int64_t ns,
+                              uint8_t* codes, void* stream);
+/*
  * Dequant step of the decode, by the decode kernels' own routine, on n codes (n a multiple of 16)
  * in chunks of 16 that share one scale: out[i] = bf16 bits of RNE_bf16(value(codes[i]) *
  * fp16(scales[i / 16])).  codes and out 16-byte aligned device arrays of n; scales a device array

@@ -263,6 +263,16 @@ uint16_t kvo_block_scale(int kind, const uint16_t* x_bits, int n)
     return kvo_f16_rne((double)s32);
 }
 
+/* Code of one element x (bf16 bits) against a nonzero fp16 block scale s16: y = x / s in IEEE binary32,
+ * then the fp8 or q8_0 rounding. */
+uint8_t kvo_code_of(int kind, uint16_t x_bits, uint16_t s16)
+{
+    float sf = (float)kvo_f16_value(s16);
+    float y = bf16_bits_to_float(x_bits) / sf; /* IEEE binary32 division */
+    if (kind == KVO_FP8_E4M3) return kvo_e4m3_sat_rne(y);
+    return (uint8_t)kvo_q8_rhaz(y);
+}
+
 void kvo_quantize_block(int kind, const uint16_t* x_bits, int n, uint8_t* codes, uint16_t* scale_out)
 {
     uint16_t s16 = kvo_block_scale(kind, x_bits, n);
@@ -271,14 +281,21 @@ void kvo_quantize_block(int kind, const uint16_t* x_bits, int n, uint8_t* codes,
         memset(codes, 0, (size_t)n);
         return;
     }
-    float sf = (float)kvo_f16_value(s16);
-    for (int i = 0; i < n; ++i) {
-        float y = bf16_bits_to_float(x_bits[i]) / sf; /* IEEE binary32 division */
-        if (kind == KVO_FP8_E4M3)
-            codes[i] = kvo_e4m3_sat_rne(y);
-        else
-            codes[i] = (uint8_t)kvo_q8_rhaz(y);
-    }
+    for (int i = 0; i < n; ++i) codes[i] = kvo_code_of(kind, x_bits[i], s16);
+}
+
+/* Every pairing of ns scales with nx elements: codes[i * nx + j] = code of x[j] against s[i]. */
+void kvo_code_table(int kind, const uint16_t* x_bits, int64_t nx, const uint16_t* s_bits, int64_t ns,
+                    uint8_t* codes, int nthreads)
+{
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#pragma omp parallel for schedule(static)
+#else
+    (void)nthreads;
+#endif
+    for (int64_t i = 0; i < ns; ++i)
+        for (int64_t j = 0; j < nx; ++j) codes[i * nx + j] = kvo_code_of(kind, x_bits[j], s_bits[i]);
 }
 
 /* ------------------------------------------------------------------------------------------ */

@@ -48,6 +48,8 @@ def lib():
             "kvo_q8_rhaz_batch": (None, [P, P, i64]),
             "kvo_dequant_batch": (None, [i32, P, P, P, i64]),
             "kvo_has_openmp": (i32, []),
+            "kvo_code_of": (ctypes.c_uint8, [i32, ctypes.c_uint16, ctypes.c_uint16]),
+            "kvo_code_table": (None, [i32, P, i64, P, i64, P, i32]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -148,6 +150,15 @@ def quantize_block(kind, x_bits):
     lib().kvo_quantize_block(_kind(kind), px, x.size, codes.ctypes.data_as(ctypes.c_void_p),
                              s.ctypes.data_as(ctypes.c_void_p))
     return codes, int(s[0])
+
+
+def code_table(kind, x_bits, s_bits, nthreads=0):
+    """codes[i, j] = code of bf16 x[j] against nonzero fp16 scale s[i] (IEEE fp32 division, then rounding)."""
+    x, px = _c(x_bits, np.uint16)
+    s, ps = _c(s_bits, np.uint16)
+    out = np.empty((s.size, x.size), np.uint8)
+    lib().kvo_code_table(_kind(kind), px, x.size, ps, s.size, out.ctypes.data_as(ctypes.c_void_p), int(nthreads))
+    return out
 
 
 def bytes_per_token(n_kv, num_kv_heads, head_dim):

@@ -139,4 +139,35 @@ def test_dequant_probe_matches_oracle_for_every_code_and_scale(kind):
     g = got.cpu().numpy().view(np.uint16)
     ref = O.dequant(kind, chunk_codes, np.repeat(s16, codes.size))
     ref_bits = O.bf16_rne(ref)
+    if kind == "q8_0":
+        # A zero scale only ever comes with zero codes (zero block).  For a negative int8 code the exact
+        # product is -0; the offset form of the routine returns +0 there: the same number.
+        zero = np.repeat(s16, codes.size) == 0
+        assert np.all(g[zero] & 0x7FFF == 0) and np.all(ref_bits[zero] & 0x7FFF == 0)
+        g, ref_bits = g[~zero], ref_bits[~zero]
     assert np.array_equal(g, ref_bits), int((g != ref_bits).sum())
+
+
+@pytest.mark.parametrize("kind", KINDS)
+def test_store_quotient_gives_ieee_codes_for_every_bf16_and_fp16_scale(kind):
+    """The store's division (reciprocal + FMA-remainder correction) yields, for every finite bf16 x and
+    every nonzero finite fp16 scale s with |x / s| <= 2^64, the same code as the oracle's IEEE fp32 x / s.
+
+    Larger quotients cannot occur in a block: |x| <= amax, and the scale s = fp16(amax / Q) is at
+    least amax / (1.5 Q) even when it is subnormal, so |x / s| <= 1.5 * 448."""
+    xb = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    xb = xb[((xb >> 7) & 0xFF) != 0xFF]                          # finite bf16 only
+    sb = np.arange(1, 0x7C00, dtype=np.uint32).astype(np.uint16)  # every nonzero finite fp16 scale
+    x_d = torch.from_numpy(xb.view(np.int16)).cuda()
+    chunk = 2048
+    for i0 in range(0, sb.size, chunk):
+        s = sb[i0:i0 + chunk]
+        out = torch.empty(s.size * xb.size, dtype=torch.uint8, device="cuda")
+        kvq.kvq_quantize_probe(kind, x_d, torch.from_numpy(s.view(np.int16)).cuda(), out)
+        got = out.cpu().numpy().reshape(s.size, xb.size)
+        ref = O.code_table(kind, xb, s)
+        xf = np.abs((xb.astype(np.uint32) << 16).view(np.float32).astype(np.float64))
+        sf = s.view(np.float16).astype(np.float64)
+        reachable = xf[None, :] <= (2.0 ** 64) * sf[:, None]
+        bad = np.argwhere((got != ref) & reachable)
+        assert bad.size == 0, [(hex(int(s[i])), hex(int(xb[j])), int(got[i, j]), int(ref[i, j])) for i, j in bad[:8]]
