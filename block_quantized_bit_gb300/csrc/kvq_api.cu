@@ -48,18 +48,25 @@ size_t elems_of(const kvq_layout& L) {
 }
 
 struct WorkspacePlan {
+  int32_t path;
+  int32_t split_align;
   int32_t heads_per_item;
   int32_t query_groups;
   int64_t max_items;
   size_t acc_offset, ml_offset, total;
 };
 
-int32_t choose_path(const kvq_layout& L, int32_t num_q_heads, const kvq_decode_options* opt) {
-  (void)L;
-  (void)num_q_heads;
+// 1 = CUDA-core kernel, 2 = tensor-core kernel, -1 = the requested path has no kernel for this shape.
+// Automatic: tensor cores where QK^T and PV are dense enough (8..16 query heads per kv head).
+int32_t choose_path(const kvq_layout& L, int32_t batch, int32_t num_q_heads, const kvq_decode_options* opt) {
+  const int32_t group = num_q_heads / L.num_kv_heads;
+  const bool tc = decode_tc_supported(L.head_dim, L.v_dim, L.mla, group, batch);
+  const bool cc = decode_cc_supported(L.head_dim, L.v_dim, L.mla);
   const int32_t want = opt ? opt->path : 0;
-  if (want == 2) return -1;  // no tensor-core kernel in this build
-  return 1;
+  if (want == 2) return tc ? 2 : -1;
+  if (want == 1) return cc ? 1 : -1;
+  if (tc) return 2;
+  return cc ? 1 : -1;
 }
 
 bool plan_workspace(const kvq_layout& L, int32_t batch, int32_t num_q_heads, int32_t max_pages,
@@ -69,7 +76,10 @@ bool plan_workspace(const kvq_layout& L, int32_t batch, int32_t num_q_heads, int
   const int32_t group = num_q_heads / L.num_kv_heads;
   const int32_t pps = opt ? opt->pages_per_split : 0;
   if (pps < 0) return false;
-  w->heads_per_item = cc_heads_per_item(group, L.head_dim, L.mla);
+  const int32_t path = choose_path(L, batch, num_q_heads, opt);
+  w->path = path;
+  w->heads_per_item = (path == 2) ? group : cc_heads_per_item(group, L.head_dim, L.mla);
+  w->split_align = (path == 2) ? 8 : 1;
   w->query_groups = L.num_kv_heads * (group / w->heads_per_item);
   w->max_items = max_work_items(batch, w->query_groups, max_pages, pps);
   const size_t acc = static_cast<size_t>(w->max_items) * w->heads_per_item * L.v_dim * sizeof(float);
@@ -194,11 +204,9 @@ kvq_status kvq_decode_ex(const void* q, const void* pool, const void* scales, co
     return KVQ_EINVAL;
   if (options && (options->pages_per_split < 0 || options->path < 0 || options->path > 2)) return KVQ_EINVAL;
   if (layout->page_size != kPageTokens) return KVQ_EUNSUPPORTED;
-  if (!decode_cc_supported(layout->head_dim, layout->v_dim, layout->mla)) return KVQ_EUNSUPPORTED;
-  const int32_t path = choose_path(*layout, num_q_heads, options);
-  if (path < 0) return KVQ_EUNSUPPORTED;
   WorkspacePlan w;
   if (!plan_workspace(*layout, batch, num_q_heads, max_pages_per_seq, options, &w)) return KVQ_EINVAL;
+  if (w.path < 0) return KVQ_EUNSUPPORTED;
   if (batch == 0) return KVQ_OK;
   if (!q || !pool || !scales || !block_table || !seq_lens || !out || !workspace) return KVQ_EINVAL;
   if (workspace_bytes < w.total) return KVQ_EWORKSPACE;
@@ -233,9 +241,10 @@ kvq_status kvq_decode_ex(const void* q, const void* pool, const void* scales, co
   a.part_ml = reinterpret_cast<float*>(ws + w.ml_offset);
   a.max_items = w.max_items;
   a.heads_per_item = w.heads_per_item;
+  a.split_align = w.split_align;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (cudaMemsetAsync(ws, 0, sizeof(uint32_t), s) != cudaSuccess) return KVQ_ECUDA;
-  st = launch_decode_cc(a, s);
+  st = (w.path == 2) ? launch_decode_tc(a, s) : launch_decode_cc(a, s);
   if (st != KVQ_OK) return st;
   return launch_merge(a, w.query_groups, s);
 }

@@ -34,6 +34,7 @@ struct DecodeArgs {
   float* part_ml;    // [max_items][heads_per_item][2]
   int64_t max_items;
   int32_t heads_per_item;  // query heads one work item covers (a tile of the group)
+  int32_t split_align;     // automatic split sizes are a multiple of this many pages
 };
 
 // Tokens per page the decode kernels support, and the workspace's leading status block.
@@ -57,6 +58,8 @@ kvq_status launch_quantize_probe(kvq_kind kind, const uint16_t* x, int64_t nx, c
 kvq_status launch_dequant_probe(kvq_kind kind, const uint8_t* codes, const uint16_t* scales, uint16_t* out,
                                 int64_t n, cudaStream_t stream);
 bool decode_cc_supported(int32_t head_dim, int32_t v_dim, int32_t mla);
+bool decode_tc_supported(int32_t head_dim, int32_t v_dim, int32_t mla, int32_t group, int32_t batch);
+kvq_status launch_decode_tc(const DecodeArgs& a, cudaStream_t stream);
 kvq_status launch_decode_cc(const DecodeArgs& a, cudaStream_t stream);
 kvq_status launch_merge(const DecodeArgs& a, int32_t query_groups, cudaStream_t stream);
 

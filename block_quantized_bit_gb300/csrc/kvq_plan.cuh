@@ -1,0 +1,150 @@
+// kvq_plan.cuh -- work-item planning shared by the decode kernels and the merge kernel.
+//
+// A decode work item is (sequence b, query group, split): a query group is a kv head together with a
+// tile of the query heads that read it, and a split is a run of C consecutive pages of the sequence.
+// C = pages_per_split when the caller fixes it; otherwise C = max(4, ceil(sum_b pages_b * groups /
+// 1216)) rounded up to `split_align` pages.  Every CTA derives the same plan from seq_lens on the
+// device, so no planning launch and no host read-back are needed.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "kvq_device.cuh"
+#include "kvq_internal.h"
+
+namespace kvq {
+namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+
+struct KParams {
+  int32_t split_align;    // automatic split sizes are rounded up to a multiple of this
+  const __nv_bfloat16* q;
+  const uint8_t* codes;
+  const __half* scales;
+  const int32_t* block_table;
+  const int32_t* seq_lens;
+  float* part_acc;
+  float* part_ml;
+  uint32_t* status;
+  int64_t num_pages;      // pages in the pool: larger block-table entries are treated as masked
+  int64_t max_items;      // work items the workspace holds
+  int32_t max_pages;
+  int32_t batch;
+  int32_t num_q_heads;
+  int32_t num_kv_heads;
+  int32_t group;          // Hq / Hkv
+  int32_t head_tiles;     // group / heads_per_item
+  int32_t pages_per_split;
+  float score_scale;      // sm_scale * log2(e)
+};
+
+__device__ __forceinline__ int32_t seq_pages(const KParams& p, int32_t b) {
+  const int32_t L = max(__ldg(p.seq_lens + b), 0);
+  return min((L + kPage - 1) / kPage, p.max_pages);
+}
+
+// Block-wide plan: pages per split C, and for `want_b` (or the sequence that owns item `want_item`)
+// its first item index and split count.  Every thread of the CTA must call it (blockDim a multiple of 32).
+struct Plan {
+  int32_t C;
+  int32_t b;        // sequence
+  int32_t base;     // first item of sequence b
+  int32_t nsplit;   // splits per query group of sequence b
+  int32_t n_items;  // items over the whole batch
+};
+
+__device__ Plan make_plan(const KParams& p, int32_t want_item, int32_t want_b) {
+  __shared__ long long s_red[32];
+  __shared__ int32_t s_scan[32];
+  __shared__ Plan s_plan;
+  const int tid = threadIdx.x, nthr = blockDim.x, nwarp = nthr >> 5;
+  const int lane = tid & 31, warp = tid >> 5;
+  const int32_t groups = p.num_kv_heads * p.head_tiles;
+  const int32_t per = (p.batch + nthr - 1) / nthr;
+  const int32_t b0 = tid * per, b1 = min(b0 + per, p.batch);
+  // 1) total page-units
+  long long units = 0;
+  for (int32_t b = b0; b < b1; ++b) units += seq_pages(p, b);
+  for (int o = 16; o > 0; o >>= 1) units += __shfl_xor_sync(0xffffffffu, units, o);
+  if (lane == 0) s_red[warp] = units;
+  __syncthreads();
+  long long tot = 0;
+  for (int w = 0; w < nwarp; ++w) tot += s_red[w];
+  tot *= groups;
+  int32_t C = p.pages_per_split;
+  if (C <= 0) {
+    long long c = (tot + kTargetItems - 1) / kTargetItems;
+    C = static_cast<int32_t>(c > kMinPagesPerSplit ? c : static_cast<long long>(kMinPagesPerSplit));
+    C = (C + p.split_align - 1) / p.split_align * p.split_align;
+  }
+  // 2) items per sequence, exclusive scan over the batch
+  int32_t mine = 0;
+  for (int32_t b = b0; b < b1; ++b) mine += groups * ((seq_pages(p, b) + C - 1) / C);
+  int32_t incl = mine;
+  for (int o = 1; o < 32; o <<= 1) {
+    const int32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) s_scan[warp] = incl;
+  __syncthreads();
+  int32_t warp_off = 0, total_items = 0;
+  for (int w = 0; w < nwarp; ++w) {
+    if (w < warp) warp_off += s_scan[w];
+    total_items += s_scan[w];
+  }
+  int32_t run = warp_off + incl - mine;  // first item of b0
+  for (int32_t b = b0; b < b1; ++b) {
+    const int32_t ns = (seq_pages(p, b) + C - 1) / C;
+    const int32_t n = groups * ns;
+    const bool hit = (want_b >= 0) ? (b == want_b) : (want_item >= run && want_item < run + n);
+    if (hit) {
+      s_plan.C = C;
+      s_plan.b = b;
+      s_plan.base = run;
+      s_plan.nsplit = ns;
+    }
+    run += n;
+  }
+  if (tid == 0 && want_b < 0 && want_item >= total_items) {
+    s_plan.C = C;
+    s_plan.b = -1;
+    s_plan.base = 0;
+    s_plan.nsplit = 0;
+  }
+  __syncthreads();
+  Plan r = s_plan;
+  r.n_items = total_items;
+  r.C = C;
+  __syncthreads();
+  return r;
+}
+
+inline KParams make_kparams(const DecodeArgs& a) {
+  KParams p;
+  p.q = static_cast<const __nv_bfloat16*>(a.q);
+  p.codes = a.codes;
+  p.scales = reinterpret_cast<const __half*>(a.scales);
+  p.block_table = a.block_table;
+  p.seq_lens = a.seq_lens;
+  p.part_acc = a.part_acc;
+  p.part_ml = a.part_ml;
+  p.status = a.status;
+  p.num_pages = a.num_pages;
+  p.max_items = a.max_items;
+  p.max_pages = a.max_pages;
+  p.batch = a.batch;
+  p.num_q_heads = a.num_q_heads;
+  p.num_kv_heads = a.num_kv_heads;
+  p.group = a.num_q_heads / a.num_kv_heads;
+  p.head_tiles = p.group / a.heads_per_item;
+  p.pages_per_split = a.pages_per_split;
+  p.score_scale = a.sm_scale * kLog2e;
+  p.split_align = a.split_align;
+  return p;
+}
+
+}  // namespace
+}  // namespace kvq

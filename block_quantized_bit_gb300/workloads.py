@@ -186,9 +186,10 @@ def qwen3_1p7b(kind="fp8_e4m3", seed=1002, device="cpu", batch=8, ctx_lo=1024, c
                 new_k=_bf16(nk), new_v=_bf16(nv), new_slots=new_slots.to(device))
 
 
-def long_gqa(kind="fp8_e4m3", seed=1003, device="cpu", batch=1, ctx=9000, mask_frac=0.005):
+def long_gqa(kind="fp8_e4m3", seed=1003, device="cpu", batch=1, ctx=9000, mask_frac=0.005, num_q_heads=16,
+             num_kv_heads=2, head_dim=256):
     g = _gen(device, seed)
-    Hq, Hkv, D = 16, 2, 256
+    Hq, Hkv, D = num_q_heads, num_kv_heads, head_dim
     seq_lens = torch.full((batch,), ctx, dtype=torch.int32)
     bt, sm, num_pages = _layout_context(seq_lens, seed, permute_pages=True, mask_frac=mask_frac)
     T = int(seq_lens.sum())

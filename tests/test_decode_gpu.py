@@ -45,12 +45,18 @@ def test_decode_matches_oracle(name, kind):
     assert_decode_close(got16, ref, rel=2.0 ** -8)
 
 
+@pytest.mark.parametrize("path", [1, 2])
 @pytest.mark.parametrize("pps", [1, 3, 16])
-def test_decode_is_invariant_to_the_split_size(pps):
+def test_decode_is_invariant_to_the_split_size(pps, path):
+    """Any split size gives the oracle's answer.  The CUDA-core path keeps fp32 probabilities, so its
+    splits agree to fp32 rounding; the tensor-core path rounds P to bf16 against a split-dependent
+    running max, so its splits agree to that rounding."""
     case, codes, scales, oc, osc = _stored("long_gqa", "fp8_e4m3")
-    auto = gpu_decode(case, codes, scales)
-    forced = gpu_decode(case, codes, scales, pages_per_split=pps)
-    np.testing.assert_allclose(forced, auto, rtol=0, atol=2e-5)
+    ref = oracle_decode(case, oc, osc)
+    auto = gpu_decode(case, codes, scales, path=path)
+    forced = gpu_decode(case, codes, scales, pages_per_split=pps, path=path)
+    assert_decode_close(forced, ref)
+    np.testing.assert_allclose(forced, auto, rtol=0, atol=2e-5 if path == 1 else 5e-3)
 
 
 def test_decode_never_reads_nan_bytes_past_a_sequence_end():
@@ -95,3 +101,46 @@ def test_decode_sm_scale_is_applied():
     case, codes, scales, oc, osc = _stored("tiny", "fp8_e4m3")
     case.sm_scale = 0.3
     assert_decode_close(gpu_decode(case, codes, scales), oracle_decode(case, oc, osc))
+
+
+# ------------------------------------------------------------------ tensor-core (tcgen05) path
+TC_CASES = [
+    dict(batch=2, ctx=9000),                                              # G = 8, D = 256
+    dict(batch=3, ctx=2500, num_q_heads=32, num_kv_heads=2, head_dim=128),  # G = 16, D = 128
+    dict(batch=2, ctx=3001, num_q_heads=16, num_kv_heads=2, head_dim=128, mask_frac=0.03),
+]
+
+
+@pytest.mark.parametrize("kind", KINDS)
+@pytest.mark.parametrize("ci", range(len(TC_CASES)))
+def test_tensor_core_decode_matches_oracle(ci, kind):
+    case, codes, scales, oc, osc = _stored("long_gqa", kind, **TC_CASES[ci])
+    ref = oracle_decode(case, oc, osc)
+    got = gpu_decode(case, codes, scales, path=2)
+    assert_decode_close(got, ref)
+
+
+@pytest.mark.parametrize("pps", [8, 12, 40])
+def test_tensor_core_decode_split_sizes_and_many_items_per_cta(pps):
+    """Split sizes that are not whole 128-token tiles (ragged last tile) and enough items that every
+    persistent CTA runs several of them, against the oracle and the CUDA-core path."""
+    case, codes, scales, oc, osc = _stored("long_gqa", "fp8_e4m3", batch=3, ctx=9000, mask_frac=0.01)
+    ref = oracle_decode(case, oc, osc)
+    tc = gpu_decode(case, codes, scales, path=2, pages_per_split=pps)
+    assert_decode_close(tc, ref)
+    cc = gpu_decode(case, codes, scales, path=1, pages_per_split=pps)
+    np.testing.assert_allclose(tc, cc, rtol=0, atol=5e-3)
+
+
+def test_tensor_core_decode_nan_poisoned_tails_and_empty_sequences():
+    case = workloads.long_gqa(kind="q8_0", batch=4, ctx=1000 + 9, mask_frac=0.0)
+    case.block_table[1, :] = -1
+    case.seq_lens[2] = 0
+    L, codes, scales = gpu_pool(case, poison_codes=0xFF)
+    gpu_store(case, codes, scales)
+    oc, osc = oracle_pool(case, poison_codes=0xFF)
+    oracle_store(case, oc, osc)
+    got = gpu_decode(case, codes, scales, path=2)
+    ref = oracle_decode(case, oc, osc)
+    assert not got[1].any() and not got[2].any()
+    assert_decode_close(got, ref)
