@@ -48,13 +48,13 @@ constexpr int kN = 16;            // MMA N: query heads, padded
 constexpr int kSmWarps = 4;
 constexpr int kDwWarps = 8;
 constexpr int kMmaWarp = kSmWarps + kDwWarps;          // warp 12
-constexpr int kProdWarp = kMmaWarp + 1;                // warp 13
-constexpr int kThreads = (kProdWarp + 1) * 32;         // 14 warps: at most 4 per sub-partition
+constexpr int kProdWarp = kMmaWarp + 1;                // warps 13 (K ring) and 14 (V ring)
+constexpr int kThreads = (kProdWarp + 2) * 32;         // 15 warps: at most 4 per sub-partition
 constexpr int kDwThreads = kDwWarps * 32;
 constexpr int kMaxPlanBatch = 2048;   // sequences whose item bases fit the shared table
 constexpr float kLazyRescale = 8.0f;  // log2 headroom before the running max must move
 constexpr int kTmemCols = 512;
-constexpr int kBox = 2 * kPage * 128;  // one TMA box: 16 tokens x 128 code bytes, of K and of V
+constexpr int kBox = kPage * 128;  // one TMA box: 16 tokens x 128 code bytes of K or of V
 
 template <int D>
 struct TcCfg {
@@ -70,39 +70,40 @@ struct TcCfg {
   static constexpr int NSL = D / 128;               // 128-byte column slices of a code row
   static constexpr int O_CHUNKS = D / 128;          // M=128 slices of O^T
   static constexpr int KCOLS = D / 2;               // TMEM columns of one K tile
-  static constexpr int STAGES = (D == 128) ? 4 : 2; // staging ring depth (tiles)
-  // one stage: codes [page][slice][kv][token][128 B] as TMA wrote them (128-byte swizzle), then the
-  // scales [page][kv][token][NB] (fp16)
-  static constexpr int SC_KV = kPage * NB * 2;      // scale bytes of one page, K or V
-  static constexpr int ST_SC = kPagesPerTile * NSL * kBox;
-  static constexpr int STAGE_BYTES = ST_SC + kPagesPerTile * 2 * SC_KV;
-  static constexpr int ST_OFF = 0;                  // 1024-byte aligned: swizzle atoms
-  static constexpr int V_OFF = ST_OFF + STAGES * STAGE_BYTES;
+  static constexpr int STAGES = (D == 128) ? 4 : 2; // depth of each staging ring (tiles)
+  // one ring slot (K ring and V ring alike): codes [page][slice][token][128 B] as TMA wrote them
+  // (128-byte swizzle), then the scales [page][token][NB] (fp16)
+  static constexpr int SC_KV = kPage * NB * 2;      // scale bytes of one page
+  static constexpr int SL_SC = kPagesPerTile * NSL * kBox;
+  static constexpr int SLOT_BYTES = SL_SC + kPagesPerTile * SC_KV;
+  static constexpr int KR_OFF = 0;                  // 1024-byte aligned: swizzle atoms
+  static constexpr int VR_OFF = KR_OFF + STAGES * SLOT_BYTES;
+  static constexpr int V_OFF = VR_OFF + STAGES * SLOT_BYTES;
   static constexpr int Q_OFF = V_OFF + TILE_BYTES;
   static constexpr int P_OFF = Q_OFF + Q_BYTES;
   static constexpr int RED_OFF = P_OFF + 2 * P_BYTES;
   static constexpr int FLAG_OFF = RED_OFF + kSmWarps * kN * 4;  // per-warp "max moved" votes
   static constexpr int VAL_OFF = FLAG_OFF + 16;                  // token validity of each K buffer's tile
-  static constexpr int META_OFF = VAL_OFF + 2 * kTile;           // valid tokens per page of each stage
-  static constexpr int TAB_OFF = META_OFF + STAGES * kPagesPerTile * 4;
-  static constexpr int NBARS = 9 + 2 * STAGES;
+  static constexpr int META_OFF = VAL_OFF + 2 * kTile;           // valid tokens per page: [ring][slot][page]
+  static constexpr int TAB_OFF = META_OFF + 2 * STAGES * kPagesPerTile * 4;
+  static constexpr int NBARS = 11 + 4 * STAGES;
   static constexpr int BAR_OFF = TAB_OFF + kMaxPlanBatch * 4;
   static constexpr int SMEM_BYTES = BAR_OFF + NBARS * 8 + 16 + 1024;  // + slack to align the base
   static_assert(D % 128 == 0, "tensor-core decode needs head_dim a multiple of 128");
-  static_assert(STAGE_BYTES % 1024 == 0, "stages keep the boxes 1024-byte aligned");
+  static_assert(SLOT_BYTES % 1024 == 0, "slots keep the boxes 1024-byte aligned");
   static_assert(NCH_T % 2 == 0, "32 codes per tcgen05.st");
-  static_assert(64 + 2 * KCOLS <= kTmemCols && 32 + O_CHUNKS * kN <= 64, "TMEM columns");
+  static_assert(96 + 2 * KCOLS <= kTmemCols && O_CHUNKS * kN <= 32, "TMEM columns");
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
 };
 
 // TMA tile load of one box of the code pool: the 128-byte slice `slice` of the rows `row`..`row+15`
-// (row = kv head * 16 + token) of K and V in physical page `page`, completing on `bar`.
-__device__ __forceinline__ void tma_load_codes(uint32_t dst, const CUtensorMap* map, int slice, int row, int page,
-                                               uint64_t* bar) {
+// (row = kv head * 16 + token) of K (kv = 0) or V (kv = 1) in physical page `page`, completing on `bar`.
+__device__ __forceinline__ void tma_load_codes(uint32_t dst, const CUtensorMap* map, int slice, int row, int kv,
+                                               int page, uint64_t* bar) {
   asm volatile(
       "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5, "
       "%6}], [%7];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(slice), "r"(row), "r"(0), "r"(page), "r"(smem_u32(bar))
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(slice), "r"(row), "r"(kv), "r"(page), "r"(smem_u32(bar))
       : "memory");
 }
 
@@ -231,6 +232,26 @@ __device__ __forceinline__ void tile_load_item(TileIter& t, const int32_t* tab, 
   t.i = 0;
 }
 
+// N consecutive fp16 scales (2 or 4, naturally aligned) in one shared-memory load.
+template <int N>
+__device__ __forceinline__ void load_scales(const uint8_t* src, uint16_t (&sc)[N]) {
+  static_assert(N == 2 || N == 4, "scale vector");
+  if constexpr (N == 4) {
+    const uint2 v = *reinterpret_cast<const uint2*>(src);
+    sc[0] = static_cast<uint16_t>(v.x);
+    sc[1] = static_cast<uint16_t>(v.x >> 16);
+    sc[2] = static_cast<uint16_t>(v.y);
+    sc[3] = static_cast<uint16_t>(v.y >> 16);
+  } else {
+    const uint32_t v = *reinterpret_cast<const uint32_t*>(src);
+    sc[0] = static_cast<uint16_t>(v);
+    sc[1] = static_cast<uint16_t>(v >> 16);
+  }
+}
+
+// Which of the two O accumulators an item uses: items alternate within a CTA.
+__device__ __forceinline__ int item_obuf(int32_t item) { return ((item - static_cast<int32_t>(blockIdx.x)) / gridDim.x) & 1; }
+
 __device__ __forceinline__ void tile_first(TileIter& t, const int32_t* tab, const KParams& p, int32_t groups,
                                            int32_t C, int32_t n_items) {
   t.item = blockIdx.x;
@@ -255,11 +276,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const KParams p,
   uint8_t* sV = smem + Cfg::V_OFF;
   uint8_t* sQ = smem + Cfg::Q_OFF;
   uint8_t* sP = smem + Cfg::P_OFF;  // [2] buffers
-  uint8_t* sSt = smem + Cfg::ST_OFF;
+  uint8_t* sKr = smem + Cfg::KR_OFF;  // K ring
+  uint8_t* sVr = smem + Cfg::VR_OFF;  // V ring
   float* sRed = reinterpret_cast<float*>(smem + Cfg::RED_OFF);
   int32_t* sFlag = reinterpret_cast<int32_t*>(smem + Cfg::FLAG_OFF);
   int32_t* sTab = reinterpret_cast<int32_t*>(smem + Cfg::TAB_OFF);
-  int32_t* sMeta = reinterpret_cast<int32_t*>(smem + Cfg::META_OFF);
+  int32_t* sMeta = reinterpret_cast<int32_t*>(smem + Cfg::META_OFF);  // [ring][slot][page]
   uint8_t* sValid = smem + Cfg::VAL_OFF;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Cfg::BAR_OFF);
   // Every barrier completes once per use of its buffer, so a waiter names an unambiguous phase.
@@ -268,8 +290,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const KParams p,
   uint64_t* bar_p_full = bars + 4;   // [2] P buffer b written, S buffer b read, O rescaled (softmax warps)
   uint64_t* bar_pv_done = bars + 6;  // [2] PV that read P buffer b completed (commit)
   uint64_t* bar_v_full = bars + 8;   // V tile written (dequant warps), once per tile
-  uint64_t* bar_full = bars + 9;               // [STAGES] stage s landed (producer arrival + bytes)
-  uint64_t* bar_empty = bars + 9 + Cfg::STAGES;  // [STAGES] stage s read by every dequant warp
+  uint64_t* bar_pv_lo = bars + 9;    // [2] the PV MMAs of O^T slice 0 (d < 128) reading P buffer b completed
+  uint64_t* bar_full = bars + 11;                     // [ring][STAGES] slot landed (producer arrival + bytes)
+  uint64_t* bar_empty = bars + 11 + 2 * Cfg::STAGES;  // [ring][STAGES] slot read by every dequant warp
   uint32_t* sTmem = reinterpret_cast<uint32_t*>(smem + Cfg::BAR_OFF + Cfg::NBARS * 8);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -290,9 +313,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const KParams p,
       mbar_init(&bar_qk_done[b], 1);
       mbar_init(&bar_p_full[b], kSmWarps);
       mbar_init(&bar_pv_done[b], 1);
+      mbar_init(&bar_pv_lo[b], 1);
     }
     mbar_init(bar_v_full, kDwWarps);
-    for (int s = 0; s < Cfg::STAGES; ++s) {
+    for (int s = 0; s < 2 * Cfg::STAGES; ++s) {
       mbar_init(&bar_full[s], 1);
       mbar_init(&bar_empty[s], kDwWarps);
     }
@@ -311,66 +335,70 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const KParams p,
   tc_fence_after();
   const uint32_t tmem = *sTmem;
   const uint32_t tS = tmem;       // S^T buffers: columns [16 b, 16 b + 16)
-  const uint32_t tO = tmem + 32;  // O^T slices: columns [32 + 16 c, 48 + 16 c)
-  const uint32_t tK = tmem + 64;  // K tiles: buffer b at columns [64 + b * KCOLS, 64 + (b + 1) * KCOLS)
+  const uint32_t tO = tmem + 32;  // O^T of item parity o, slice c: columns [32 + 32 o + 16 c, +16)
+  const uint32_t tK = tmem + 96;  // K tiles: buffer b at columns [96 + b * KCOLS, 96 + (b + 1) * KCOLS)
   const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
 
   bool ok = true;
   uint32_t gtile = 0;  // tiles processed by this CTA so far
 
-  if (warp == kProdWarp) {
-    // ===================================================================== producer
-    // Lane pi (< 8) owns page pi of the tile: block-table entry, valid tokens, and its copies.
-    const uint32_t st_base = smem_u32(sSt);
+  if (warp >= kProdWarp) {
+    // ===================================================================== producers
+    // Warp 13 fills the K ring, warp 14 the V ring, each running ahead on its own ring.  Lane pi (< 8)
+    // owns page pi of a tile: block-table entry (requested one tile ahead), valid tokens, its copies.
+    const int kv = warp - kProdWarp;
+    uint8_t* ring_base = kv ? sVr : sKr;
     TileIter t;
     tile_first(t, sTab, p, groups, C, n_items);
-    uint32_t n = 0;  // tiles issued
+    auto page_entry = [&](const TileIter& ti) -> int32_t {
+      if (!ti.live || lane >= kPagesPerTile) return -1;
+      const int32_t pg = ti.pg0 + ti.i * kPagesPerTile + lane;
+      return pg < ti.pg1 ? __ldg(p.block_table + static_cast<int64_t>(ti.b) * p.max_pages + pg) : -1;
+    };
+    uint32_t n = 0;              // tiles issued
+    int32_t bt = page_entry(t);  // block-table entry of tile n
     while (ok && t.live) {
-      const int st = n % Cfg::STAGES;
-      const uint32_t use = n / Cfg::STAGES;
-      if (use > 0 && !mbar_wait_bounded(&bar_empty[st], (use - 1) & 1)) { ok = false; break; }
-      int32_t phys = -1, nvalid = 0;
-      if (lane < kPagesPerTile) {
-        const int32_t pg = t.pg0 + t.i * kPagesPerTile + lane;
-        if (pg < t.pg1) {
-          phys = __ldg(p.block_table + static_cast<int64_t>(t.b) * p.max_pages + pg);
-          if (phys >= p.num_pages) {
-            set_status(p.status, kStatusBadPage);
-            phys = -1;
-          }
-          if (phys >= 0) nvalid = min(kPage, t.L - pg * kPage);  // >= 1: pg < the sequence's page count
-        }
+      int32_t phys = bt, nvalid = 0;
+      if (phys >= p.num_pages) {
+        set_status(p.status, kStatusBadPage);
+        phys = -1;
       }
+      if (phys >= 0) nvalid = min(kPage, t.L - (t.pg0 + t.i * kPagesPerTile + lane) * kPage);  // >= 1
+      TileIter nx = t;
+      tile_next(nx, sTab, p, groups, C, n_items);
+      bt = page_entry(nx);
+      const int sl = n % Cfg::STAGES;
+      const int ring = kv * Cfg::STAGES + sl;
+      const uint32_t use = n / Cfg::STAGES;
+      if (use > 0 && !mbar_wait_bounded(&bar_empty[ring], (use - 1) & 1)) { ok = false; break; }
       const uint32_t bytes =
-          __reduce_add_sync(0xffffffffu, phys >= 0 ? static_cast<uint32_t>(Cfg::NSL * kBox + 2 * Cfg::SC_KV) : 0u);
+          __reduce_add_sync(0xffffffffu, phys >= 0 ? static_cast<uint32_t>(Cfg::NSL * kBox + Cfg::SC_KV) : 0u);
       int32_t nv[kPagesPerTile];
 #pragma unroll
       for (int i = 0; i < kPagesPerTile; ++i) nv[i] = __shfl_sync(0xffffffffu, nvalid, i);
       if (lane == 0) {
 #pragma unroll
-        for (int i = 0; i < kPagesPerTile; ++i) sMeta[st * kPagesPerTile + i] = nv[i];
-        mbar_arrive_expect_tx(&bar_full[st], bytes);  // releases sMeta with the stage
+        for (int i = 0; i < kPagesPerTile; ++i) sMeta[ring * kPagesPerTile + i] = nv[i];
+        mbar_arrive_expect_tx(&bar_full[ring], bytes);  // releases the page counts with the slot
       }
       __syncwarp();
       if (phys >= 0) {
-        const uint32_t dst = st_base + st * Cfg::STAGE_BYTES;
+        uint8_t* slot = ring_base + sl * Cfg::SLOT_BYTES;
 #pragma unroll
-        for (int sl = 0; sl < Cfg::NSL; ++sl)
-          tma_load_codes(dst + (lane * Cfg::NSL + sl) * kBox, &tmap, sl, t.g * kPage, phys, &bar_full[st]);
-        const uint8_t* sk = reinterpret_cast<const uint8_t*>(p.scales) +
-                            ((static_cast<int64_t>(phys) * 2 * p.num_kv_heads + t.g) * kPage) * Cfg::NB * 2;
-        const uint8_t* sv = sk + static_cast<int64_t>(p.num_kv_heads) * Cfg::SC_KV;
-        uint8_t* sdst = sSt + st * Cfg::STAGE_BYTES + Cfg::ST_SC + lane * 2 * Cfg::SC_KV;
-        bulk_g2s(sdst, sk, Cfg::SC_KV, &bar_full[st]);
-        bulk_g2s(sdst + Cfg::SC_KV, sv, Cfg::SC_KV, &bar_full[st]);
+        for (int c = 0; c < Cfg::NSL; ++c)
+          tma_load_codes(smem_u32(slot + (lane * Cfg::NSL + c) * kBox), &tmap, c, t.g * kPage, kv, phys,
+                         &bar_full[ring]);
+        const uint8_t* src = reinterpret_cast<const uint8_t*>(p.scales) +
+                             ((static_cast<int64_t>(phys) * 2 + kv) * p.num_kv_heads + t.g) * Cfg::SC_KV;
+        bulk_g2s(slot + Cfg::SL_SC + lane * Cfg::SC_KV, src, Cfg::SC_KV, &bar_full[ring]);
       }
-      tile_next(t, sTab, p, groups, C, n_items);
+      t = nx;
       ++n;
     }
     // no copy may still be in flight when the CTA exits
     for (uint32_t j = 1; j <= n && j <= static_cast<uint32_t>(Cfg::STAGES); ++j) {
       const uint32_t m = n - j;
-      (void)mbar_wait_bounded(&bar_full[m % Cfg::STAGES], (m / Cfg::STAGES) & 1);
+      (void)mbar_wait_bounded(&bar_full[kv * Cfg::STAGES + m % Cfg::STAGES], (m / Cfg::STAGES) & 1);
     }
   } else if (warp >= kSmWarps && warp < kMmaWarp) {
     // ===================================================================== dequant warps
@@ -380,44 +408,71 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const KParams p,
     const int pi = tt / kPage, off = tt % kPage;
     const int swz = off & 7;              // 128-byte swizzle phase of this token's staging rows
     const uint32_t voff = (tt % 8) * 16 + (tt / 8) * Cfg::RS;
-    // staging address of 16-code chunk k of this thread's part of the K (kv = 0) or V (kv = 1) row
-    auto chunk_addr = [&](const uint8_t* sb, int kv, int k) -> const uint4* {
+    // address, in a ring slot, of 16-code chunk k of this thread's part of its token's row
+    auto chunk_addr = [&](const uint8_t* slot, int k) -> const uint4* {
       const int c = part * Cfg::NCH_T + k;  // chunk index along the row
       const int sl = c / 8, cw = c % 8;
-      return reinterpret_cast<const uint4*>(sb + (pi * Cfg::NSL + sl) * kBox + (kv * kPage + off) * 128 +
-                                            ((cw ^ swz) * 16));
+      return reinterpret_cast<const uint4*>(slot + (pi * Cfg::NSL + sl) * kBox + off * 128 + ((cw ^ swz) * 16));
     };
-    TileIter tc;
-    tile_first(tc, sTab, p, groups, C, n_items);
-    while (ok && tc.live) {
-      const int st = gtile % Cfg::STAGES;  // staging stage
-      const int kb = gtile & 1;            // K buffer = S / P buffer = validity slot of this tile
-      if (!mbar_wait_bounded(&bar_full[st], (gtile / Cfg::STAGES) & 1)) { ok = false; break; }
-      const uint8_t* sb = sSt + st * Cfg::STAGE_BYTES;
-      const bool v_ok = off < sMeta[st * kPagesPerTile + pi];
-      const uint16_t* scl = reinterpret_cast<const uint16_t*>(sb + Cfg::ST_SC + pi * 2 * Cfg::SC_KV) +
-                            off * Cfg::NB + part * Cfg::NBT;  // K scales; V scales SC_KV bytes on
-      // ---- K tile into TMEM buffer kb, once the QK that last read that buffer is complete
-      if (gtile >= 2 && !mbar_wait_bounded(&bar_qk_done[kb], ((gtile >> 1) - 1) & 1)) { ok = false; break; }
-      if (tc.i == 0) {
-        // this item's q rows; the previous tile's QK must have read the old ones
-        if (gtile >= 1 && !mbar_wait_bounded(&bar_qk_done[(gtile - 1) & 1], ((gtile - 1) >> 1) & 1)) {
-          ok = false;
-          break;
-        }
-        const int32_t head0 = tc.g * p.group;
-        for (int idx = dw; idx < GN * (D / 8); idx += kDwThreads) {
+    const int sc_off = Cfg::SL_SC + pi * Cfg::SC_KV + (off * Cfg::NB + part * Cfg::NBT) * 2;
+    // q rows of an item (GN x D bf16), QPT 16-byte pieces per thread, loaded one tile ahead of use
+    constexpr int QPIECES = GN * (D / 8);
+    constexpr int QPT = (QPIECES + kDwThreads - 1) / kDwThreads;
+    uint4 qreg[QPT];
+    auto load_q = [&](const TileIter& t) {
+      const int32_t head0 = t.g * p.group;
+#pragma unroll
+      for (int j = 0; j < QPT; ++j) {
+        const int idx = dw + j * kDwThreads;
+        if (idx < QPIECES) {
           const int h = idx / (D / 8), c8 = idx % (D / 8);
-          const uint4 v = __ldg(reinterpret_cast<const uint4*>(
-              p.q + (static_cast<int64_t>(tc.b) * p.num_q_heads + head0 + h) * D + c8 * 8));
-          *reinterpret_cast<uint4*>(sQ + (h % 8) * 16 + (h / 8) * Cfg::RS + c8 * 128) = v;
+          qreg[j] = __ldg(reinterpret_cast<const uint4*>(
+              p.q + (static_cast<int64_t>(t.b) * p.num_q_heads + head0 + h) * D + c8 * 8));
         }
-        fence_proxy_async_smem();
       }
-      // the validity slot kb was last read by the softmax of tile gtile - 2
-      if (gtile >= 2 && !mbar_wait_bounded(&bar_p_full[kb], ((gtile >> 1) - 1) & 1)) { ok = false; break; }
-      if (part == 0) sValid[kb * kTile + tt] = v_ok ? 1 : 0;  // published to the softmax warps with k_full
-      {
+    };
+    // K of tile n+1 is dequantized before V of tile n: the PV that frees the V tile for tile n+1 then
+    // has two dequant steps of slack instead of none.
+    TileIter tk;  // next tile whose K is dequantized
+    tile_first(tk, sTab, p, groups, C, n_items);
+    if (tk.live) load_q(tk);
+    uint32_t nk = 0, nv = 0;  // tiles whose K / V have been written
+    while (ok && (tk.live || nv < nk)) {
+      if (tk.live) {
+        // ================================================================ K of tile nk -> TMEM buffer kb
+        const int kb = nk & 1;  // K buffer = S / P buffer = validity slot of this tile
+        const int ring = nk % Cfg::STAGES;
+        if (!mbar_wait_bounded(&bar_full[ring], (nk / Cfg::STAGES) & 1)) { ok = false; break; }
+        const uint8_t* slot = sKr + ring * Cfg::SLOT_BYTES;
+        const bool v_ok = off < sMeta[ring * kPagesPerTile + pi];
+        uint16_t sc[Cfg::NBT];
+        load_scales<Cfg::NBT>(slot + sc_off, sc);
+        // the buffer was last read by the QK of tile nk - 2
+        if (nk >= 2 && !mbar_wait_bounded(&bar_qk_done[kb], ((nk >> 1) - 1) & 1)) { ok = false; break; }
+        if (tk.i == 0) {
+          // this item's q rows; the previous tile's QK must have read the old ones
+          if (nk >= 1 && !mbar_wait_bounded(&bar_qk_done[(nk - 1) & 1], ((nk - 1) >> 1) & 1)) {
+            ok = false;
+            break;
+          }
+#pragma unroll
+          for (int j = 0; j < QPT; ++j) {
+            const int idx = dw + j * kDwThreads;
+            if (idx < QPIECES) {
+              const int h = idx / (D / 8), c8 = idx % (D / 8);
+              *reinterpret_cast<uint4*>(sQ + (h % 8) * 16 + (h / 8) * Cfg::RS + c8 * 128) = qreg[j];
+            }
+          }
+          fence_proxy_async_smem();
+        }
+        if (tk.i == tk.ntiles - 1) {  // the next item's q rows travel while this tile is dequantized
+          TileIter nx = tk;
+          tile_next(nx, sTab, p, groups, C, n_items);
+          if (nx.live) load_q(nx);
+        }
+        // the validity slot kb was last read by the softmax of tile nk - 2
+        if (nk >= 2 && !mbar_wait_bounded(&bar_p_full[kb], ((nk >> 1) - 1) & 1)) { ok = false; break; }
+        if (part == 0) sValid[kb * kTile + tt] = v_ok ? 1 : 0;  // published to the softmax warps with k_full
 #pragma unroll
         for (int k2 = 0; k2 < Cfg::NCH_T / 2; ++k2) {  // 32 codes -> 16 TMEM columns per tcgen05.st
           uint32_t w[16];
@@ -426,7 +481,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const KParams p,
             const int k = 2 * k2 + h;
             if (v_ok) {
               uint32_t ww[8];
-              dequant16<KIND>(*chunk_addr(sb, 0, k), scl[k >> 1], ww);
+              dequant16<KIND>(*chunk_addr(slot, k), sc[k >> 1], ww);
 #pragma unroll
               for (int e = 0; e < 8; ++e) w[8 * h + e] = ww[e];
             } else {
@@ -439,17 +494,33 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const KParams p,
         asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(&bar_k_full[kb])) : "memory");
+        if (lane == 0) {
+          asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(&bar_k_full[kb])) : "memory");
+          asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(&bar_empty[ring])) : "memory");
+        }
+        tile_next(tk, sTab, p, groups, C, n_items);
+        ++nk;
+        if (nk == 1 && tk.live) continue;  // K runs one tile ahead of V
       }
-      // ---- V tile into shared memory, once the previous PV is complete
-      if (gtile >= 1 && !mbar_wait_bounded(&bar_pv_done[(gtile - 1) & 1], ((gtile - 1) >> 1) & 1)) { ok = false; break; }
+      // ================================================================== V of tile nv -> shared memory
       {
-        const uint16_t* vs = scl + Cfg::SC_KV / 2;
+        const int ring = Cfg::STAGES + nv % Cfg::STAGES;
+        if (!mbar_wait_bounded(&bar_full[ring], (nv / Cfg::STAGES) & 1)) { ok = false; break; }
+        const uint8_t* slot = sVr + (nv % Cfg::STAGES) * Cfg::SLOT_BYTES;
+        const bool v_ok = off < sMeta[ring * kPagesPerTile + pi];
+        uint16_t sc[Cfg::NBT];
+        load_scales<Cfg::NBT>(slot + sc_off, sc);
+        // the previous PV must have read this thread's rows of the V tile (with two O^T slices, part 0
+        // writes exactly the dims of slice 0)
+        if (nv >= 1) {
+          uint64_t* vbar = (Cfg::O_CHUNKS == 2 && part == 0) ? &bar_pv_lo[(nv - 1) & 1] : &bar_pv_done[(nv - 1) & 1];
+          if (!mbar_wait_bounded(vbar, ((nv - 1) >> 1) & 1)) { ok = false; break; }
+        }
 #pragma unroll
         for (int k = 0; k < Cfg::NCH_T; ++k) {
           uint32_t w[8];
           if (v_ok) {
-            dequant16<KIND>(*chunk_addr(sb, 1, k), vs[k >> 1], w);
+            dequant16<KIND>(*chunk_addr(slot, k), sc[k >> 1], w);
           } else {
 #pragma unroll
             for (int e = 0; e < 8; ++e) w[e] = 0u;
@@ -462,11 +533,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const KParams p,
         __syncwarp();
         if (lane == 0) {
           asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar_v_full)) : "memory");
-          asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(&bar_empty[st])) : "memory");
+          asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(&bar_empty[ring])) : "memory");
         }
+        ++nv;
       }
-      tile_next(tc, sTab, p, groups, C, n_items);
-      ++gtile;
     }
   } else if (warp == kMmaWarp) {
     // ===================================================================== MMA issue (lane 0)
@@ -474,7 +544,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const KParams p,
     // V tile np and P tile np.  Whichever is ready is issued first; lane 0 polls, the warp follows.
     const uint32_t idesc_qk = mma_idesc(false, false);
     const uint32_t idesc_pv = mma_idesc(true, true);
-    const uint32_t aV = smem_u32(sV), aQ = smem_u32(sQ), aP = smem_u32(sP);
+    // descriptors of the first K-step; later steps add their byte offset >> 4 to the address field
+    const uint64_t dQ = smem_desc(smem_u32(sQ), 128, Cfg::RS);
+    const uint64_t dV = smem_desc(smem_u32(sV), Cfg::RS, 128);
+    const uint64_t dP0 = smem_desc(smem_u32(sP), 128, 2048);
     TileIter tq, tp;  // next tile to QK; next tile to PV
     tile_first(tq, sTab, p, groups, C, n_items);
     tp = tq;
@@ -482,6 +555,33 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const KParams p,
     uint64_t idle_since = 0;
     while (tp.live) {
       bool progressed = false;
+      // PV first: the dequant warps wait for it before they rewrite the V tile
+      if (np < nq) {
+        const int b = np & 1;
+        int ready = 0;
+        if (lane == 0)
+          ready = mbar_test_wait(bar_v_full, np & 1) && mbar_test_wait(&bar_p_full[b], (np >> 1) & 1);
+        if (__shfl_sync(0xffffffffu, ready, 0)) {
+          tc_fence_after();
+          if (lane == 0) {
+            const uint32_t o = tO + item_obuf(tp.item) * 32;
+            const uint64_t dP = dP0 + static_cast<uint64_t>((b * Cfg::P_BYTES) >> 4);
+#pragma unroll
+            for (int oc = 0; oc < Cfg::O_CHUNKS; ++oc) {
+#pragma unroll
+              for (int ks = 0; ks < kTile / 16; ++ks)
+                mma_bf16(o + oc * kN, dV + static_cast<uint64_t>((oc * 16 * 128 + ks * 2 * Cfg::RS) >> 4),
+                         dP + static_cast<uint64_t>((ks * 2 * 128) >> 4), idesc_pv, (tp.i > 0 || ks > 0) ? 1u : 0u);
+              if (oc == 0 && Cfg::O_CHUNKS == 2) mma_commit(&bar_pv_lo[b]);
+            }
+            mma_commit(&bar_pv_done[b]);
+          }
+          __syncwarp();
+          ++np;
+          tile_next(tp, sTab, p, groups, C, n_items);
+          progressed = true;
+        }
+      }
       if (tq.live && nq < np + 2) {
         const int b = nq & 1;
         int ready = 0;
@@ -491,38 +591,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const KParams p,
         if (__shfl_sync(0xffffffffu, ready, 0)) {
           tc_fence_after();
           if (lane == 0) {
+            const uint32_t ka = tK + b * Cfg::KCOLS;
 #pragma unroll
             for (int ks = 0; ks < D / 16; ++ks)
-              mma_bf16_tmem_a(tS + b * kN, tK + b * Cfg::KCOLS + ks * 8, smem_desc(aQ + ks * 256, 128, Cfg::RS),
-                              idesc_qk, ks > 0);
+              mma_bf16_tmem_a(tS + b * kN, ka + ks * 8, dQ + static_cast<uint64_t>((ks * 256) >> 4), idesc_qk, ks > 0);
             mma_commit(&bar_qk_done[b]);
           }
           __syncwarp();
           ++nq;
           tile_next(tq, sTab, p, groups, C, n_items);
-          progressed = true;
-        }
-      }
-      if (np < nq) {
-        const int b = np & 1;
-        int ready = 0;
-        if (lane == 0)
-          ready = mbar_test_wait(bar_v_full, np & 1) && mbar_test_wait(&bar_p_full[b], (np >> 1) & 1);
-        if (__shfl_sync(0xffffffffu, ready, 0)) {
-          tc_fence_after();
-          if (lane == 0) {
-#pragma unroll
-            for (int oc = 0; oc < Cfg::O_CHUNKS; ++oc)
-#pragma unroll
-              for (int ks = 0; ks < kTile / 16; ++ks)
-                mma_bf16(tO + oc * kN, smem_desc(aV + oc * 16 * 128 + ks * 2 * Cfg::RS, Cfg::RS, 128),
-                         smem_desc(aP + b * Cfg::P_BYTES + ks * 2 * 128, 128, 2048), idesc_pv,
-                         (tp.i > 0 || ks > 0) ? 1u : 0u);
-            mma_commit(&bar_pv_done[b]);
-          }
-          __syncwarp();
-          ++np;
-          tile_next(tp, sTab, p, groups, C, n_items);
           progressed = true;
         }
       }
@@ -539,12 +616,34 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const KParams p,
     if (nq > np) (void)mbar_wait_bounded(&bar_qk_done[(nq - 1) & 1], ((nq - 1) >> 1) & 1);
   } else {
     // ===================================================================== softmax warps
+    // O^T of an item is read out of TMEM (its "flush") only after the next item's first P has been
+    // handed to the MMA thread: the two items use different O accumulators, so the readout overlaps
+    // the next item's first PV instead of stalling the pipeline.
     const int tt = tid;  // token slot / O^T row / TMEM lane
+    int32_t pend_item = -1;  // item whose O^T is still in TMEM
+    uint32_t pend_tile = 0;  // its last tile (CTA tile count), whose PV completes it
+    auto flush_o = [&]() -> bool {
+      if (!mbar_wait_bounded(&bar_pv_done[pend_tile & 1], (pend_tile >> 1) & 1)) return false;
+      tc_fence_after();
+      const uint32_t ob = tO + item_obuf(pend_item) * 32;
+#pragma unroll
+      for (int oc = 0; oc < Cfg::O_CHUNKS; ++oc) {
+        float o[16];
+        tmem_ld16(ob + oc * kN + lane_base, o);
+        const int d = oc * 128 + tt;
+#pragma unroll
+        for (int h = 0; h < GN; ++h) p.part_acc[(static_cast<int64_t>(pend_item) * GN + h) * D + d] = o[h];
+      }
+      tc_fence_before();  // the reads are ordered before this warp's later arrivals
+      pend_item = -1;
+      return true;
+    };
     for (int32_t item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
       const ItemPos ip = locate(sTab, p, groups, C, item);
       const int32_t pg0 = ip.split * C;
       const int32_t pg1 = min(pg0 + C, seq_pages(p, ip.b));
       const int32_t ntiles = (pg1 - pg0 + kPagesPerTile - 1) / kPagesPerTile;
+      const uint32_t ob = tO + item_obuf(item) * 32;
       float m_used[GN], l_t[GN];
 #pragma unroll
       for (int h = 0; h < GN; ++h) {
@@ -618,16 +717,16 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const KParams p,
         }
         // P buffer b is free once the PV two tiles back has read it
         if (gtile >= 2 && !mbar_wait_bounded(&bar_pv_done[b], ((gtile >> 1) - 1) & 1)) { ok = false; break; }
-        if (rescale && o_live) {  // O must hold every earlier PV before it is scaled
+        if (rescale && o_live) {  // O must hold every earlier PV of this item before it is scaled
           if (!mbar_wait_bounded(&bar_pv_done[(gtile - 1) & 1], ((gtile - 1) >> 1) & 1)) { ok = false; break; }
           tc_fence_after();
 #pragma unroll
           for (int oc = 0; oc < Cfg::O_CHUNKS; ++oc) {
             float o[16];
-            tmem_ld16(tO + oc * kN + lane_base, o);
+            tmem_ld16(ob + oc * kN + lane_base, o);
 #pragma unroll
             for (int h = 0; h < GN; ++h) o[h] *= alpha[h];
-            tmem_st16(tO + oc * kN + lane_base, o);
+            tmem_st16(ob + oc * kN + lane_base, o);
           }
         }
         uint8_t* pb = sP + b * Cfg::P_BYTES;
@@ -640,19 +739,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const KParams p,
         tc_fence_before();
         __syncwarp();
         if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(&bar_p_full[b])) : "memory");
+        // the previous item's O^T, now that this item's first PV can run into the other accumulator
+        if (pend_item >= 0 && !flush_o()) { ok = false; break; }
       }
       if (!ok) break;
-      // ---- item epilogue: O^T rows -> partial accumulators; (m, l) per head
-      if (!mbar_wait_bounded(&bar_pv_done[(gtile - 1) & 1], ((gtile - 1) >> 1) & 1)) { ok = false; break; }
-      tc_fence_after();
-#pragma unroll
-      for (int oc = 0; oc < Cfg::O_CHUNKS; ++oc) {
-        float o[16];
-        tmem_ld16(tO + oc * kN + lane_base, o);
-        const int d = oc * 128 + tt;
-#pragma unroll
-        for (int h = 0; h < GN; ++h) p.part_acc[(static_cast<int64_t>(item) * GN + h) * D + d] = o[h];
-      }
+      // ---- item end: (m, l) per head now; O^T at the next item's first tile (or after the last item)
 #pragma unroll
       for (int h = 0; h < GN; ++h) {
         float v = l_t[h];
@@ -661,19 +752,21 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const KParams p,
         if (lane == 0) sRed[warp * kN + h] = v;
       }
       named_sync(1, kSmWarps * 32);
-      if (tt == 0) {  // m_used is identical in every softmax thread
+      if (tt < GN) {  // m_used is identical in every softmax thread; thread h writes head h
+        float lsum = 0.0f, mh = -INFINITY;
 #pragma unroll
-        for (int h = 0; h < GN; ++h) {
-          float lsum = 0.0f;
+        for (int w = 0; w < kSmWarps; ++w) lsum += sRed[w * kN + tt];
 #pragma unroll
-          for (int w = 0; w < kSmWarps; ++w) lsum += sRed[w * kN + h];
-          p.part_ml[(static_cast<int64_t>(item) * GN + h) * 2 + 0] = m_used[h];
-          p.part_ml[(static_cast<int64_t>(item) * GN + h) * 2 + 1] = lsum;
-        }
+        for (int h = 0; h < GN; ++h)
+          if (h == tt) mh = m_used[h];
+        p.part_ml[(static_cast<int64_t>(item) * GN + tt) * 2 + 0] = mh;
+        p.part_ml[(static_cast<int64_t>(item) * GN + tt) * 2 + 1] = lsum;
       }
-      tc_fence_before();
       named_sync(1, kSmWarps * 32);
+      pend_item = item;
+      pend_tile = gtile - 1;
     }
+    if (ok && pend_item >= 0 && !flush_o()) ok = false;
   }
   if (!ok) set_status(p.status, kStatusTimeout);
   tc_fence_before();
@@ -701,7 +794,7 @@ EncodeTiledFn tensor_map_encoder() {
 }
 
 // 5-D view of the code pool [page][kv][head][token][D] as (128-byte slice offset, slice, head*16 + token,
-// kv, page); a box is one slice of the 16 rows of one head, for K and V: 4 KB, 128-byte swizzled.
+// kv, page); a box is one slice of the 16 rows of one head, of K or of V: 2 KB, 128-byte swizzled.
 template <int D>
 bool encode_code_map(CUtensorMap* map, const DecodeArgs& a) {
   const EncodeTiledFn enc = tensor_map_encoder();
@@ -710,7 +803,7 @@ bool encode_code_map(CUtensorMap* map, const DecodeArgs& a) {
   const cuuint64_t pages = static_cast<cuuint64_t>(std::max<int64_t>(a.num_pages, 1));  // no copy reads past it
   const cuuint64_t dims[5] = {128, D / 128, H * kPage, 2, pages};
   const cuuint64_t strides[4] = {128, D, H * kPage * D, 2 * H * kPage * D};
-  const cuuint32_t box[5] = {128, 1, kPage, 2, 1};
+  const cuuint32_t box[5] = {128, 1, kPage, 1, 1};
   const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
   return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 5, const_cast<uint8_t*>(a.codes), dims, strides, box, estr,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
