@@ -13,6 +13,7 @@ host cores, on a bounded sample of the same workload, and prints the same line w
 ``"impl": "reference"``.
 """
 import argparse
+import hashlib
 import json
 import os
 import statistics
@@ -269,7 +270,7 @@ def run_ours(args, world, rank):
                      "achieved": round(dec_gbs, 1), "peak": hbm, "unit": "GB/s",
                      "frac": round(dec_gbs / hbm, 4) if hbm else None,
                      "peak_source": "MEASURED_PEAKS.json hbm_gbs (of measured)" if hbm else "fallback 6800",
-                     "traffic": None},
+                     "traffic": recorded_traffic(args)},
         "clocks": clk,
         "e2e": e2e,
         "gpu_launches": launches_per_step * K,
@@ -324,6 +325,35 @@ def run_e2e(args, case, L, codes, scales, sk, sv, ss, ws, flush, world):
                                                                                hv.numel() * hv.element_size())
     d2h = hout.numel() * hout.element_size()
     return {"step_s": tot / K / 1e3, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+
+
+def csrc_sha256():
+    """sha256 over the library's CUDA sources, in the order the traffic record was hashed."""
+    h = hashlib.sha256()
+    d = os.path.join(os.path.dirname(os.path.abspath(__file__)), "block_quantized_bit_gb300", "csrc")
+    for f in sorted(os.listdir(d)):
+        if f.endswith((".cu", ".cuh", ".h")):
+            h.update(f.encode())
+            with open(os.path.join(d, f), "rb") as fh:
+                h.update(fh.read())
+    return h.hexdigest()
+
+
+def recorded_traffic(args):
+    """DRAM bytes per decode call (split kernel + merge) from the committed ncu record, or None when
+    there is no record for this workload or the library source changed since it was taken."""
+    path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "profiles", "dram_traffic.json")
+    try:
+        with open(path) as fh:
+            rec = json.load(fh)
+    except (OSError, ValueError):
+        return None
+    sha = csrc_sha256()
+    for e in rec.get("entries", []):
+        if (e.get("workload") == args.workload and e.get("kind") == args.kind and e.get("path", 0) == args.path
+                and e.get("csrc_sha256") == sha and args.batch is None and args.ctx is None):
+            return int(e["dram_read_bytes"]) + int(e["dram_write_bytes"])
+    return None
 
 
 def load_peaks():
