@@ -22,6 +22,8 @@
 //   warps 4-11  dequant: each thread owns half of a token row.  It reads its codes from the swizzled
 //               staging rows (bank-conflict free: the 16-byte chunk index is XORed with token % 8),
 //               dequantizes them exactly as on the CUDA-core path, K into tensor memory, V into shared.
+//               Its loops are deliberately not fully unrolled: with five roles sharing each SM
+//               sub-partition, instruction-cache misses cost more than the loop overhead.
 //   warp 12     allocates TMEM; one thread issues every tcgen05.mma / tcgen05.commit, taking QK of the
 //               next tile and PV of the oldest tile in whichever order their inputs become ready.
 //   warps 0-3   softmax: TMEM lane = token; fp32 online softmax in the exp2 domain with lazy
@@ -445,8 +447,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const KParams p,
         if (!mbar_wait_bounded(&bar_full[ring], (nk / Cfg::STAGES) & 1)) { ok = false; break; }
         const uint8_t* slot = sKr + ring * Cfg::SLOT_BYTES;
         const bool v_ok = off < sMeta[ring * kPagesPerTile + pi];
-        uint16_t sc[Cfg::NBT];
-        load_scales<Cfg::NBT>(slot + sc_off, sc);
+        const uint16_t* sc = reinterpret_cast<const uint16_t*>(slot + sc_off);
         // the buffer was last read by the QK of tile nk - 2
         if (nk >= 2 && !mbar_wait_bounded(&bar_qk_done[kb], ((nk >> 1) - 1) & 1)) { ok = false; break; }
         if (tk.i == 0) {
@@ -473,15 +474,16 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const KParams p,
         // the validity slot kb was last read by the softmax of tile nk - 2
         if (nk >= 2 && !mbar_wait_bounded(&bar_p_full[kb], ((nk >> 1) - 1) & 1)) { ok = false; break; }
         if (part == 0) sValid[kb * kTile + tt] = v_ok ? 1 : 0;  // published to the softmax warps with k_full
-#pragma unroll
-        for (int k2 = 0; k2 < Cfg::NCH_T / 2; ++k2) {  // 32 codes -> 16 TMEM columns per tcgen05.st
+#pragma unroll 1
+        for (int k2 = 0; k2 < Cfg::NCH_T / 2; ++k2) {  // 32 codes (one scale) -> 16 TMEM columns per tcgen05.st
           uint32_t w[16];
+          const uint16_t s_k = sc[k2];
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
             const int k = 2 * k2 + h;
             if (v_ok) {
               uint32_t ww[8];
-              dequant16<KIND>(*chunk_addr(slot, k), sc[k >> 1], ww);
+              dequant16<KIND>(*chunk_addr(slot, k), s_k, ww);
 #pragma unroll
               for (int e = 0; e < 8; ++e) w[8 * h + e] = ww[e];
             } else {
@@ -508,15 +510,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const KParams p,
         if (!mbar_wait_bounded(&bar_full[ring], (nv / Cfg::STAGES) & 1)) { ok = false; break; }
         const uint8_t* slot = sVr + (nv % Cfg::STAGES) * Cfg::SLOT_BYTES;
         const bool v_ok = off < sMeta[ring * kPagesPerTile + pi];
-        uint16_t sc[Cfg::NBT];
-        load_scales<Cfg::NBT>(slot + sc_off, sc);
+        const uint16_t* sc = reinterpret_cast<const uint16_t*>(slot + sc_off);
         // the previous PV must have read this thread's rows of the V tile (with two O^T slices, part 0
         // writes exactly the dims of slice 0)
         if (nv >= 1) {
           uint64_t* vbar = (Cfg::O_CHUNKS == 2 && part == 0) ? &bar_pv_lo[(nv - 1) & 1] : &bar_pv_done[(nv - 1) & 1];
           if (!mbar_wait_bounded(vbar, ((nv - 1) >> 1) & 1)) { ok = false; break; }
         }
-#pragma unroll
+#pragma unroll 2
         for (int k = 0; k < Cfg::NCH_T; ++k) {
           uint32_t w[8];
           if (v_ok) {
