@@ -57,7 +57,8 @@ struct WorkspacePlan {
 };
 
 // 1 = CUDA-core kernel, 2 = tensor-core kernel, -1 = the requested path has no kernel for this shape.
-// Automatic: tensor cores where QK^T and PV are dense enough (8..16 query heads per kv head).
+// Automatic: tensor cores where QK^T and PV are dense enough (8..16 query heads per kv head); the
+// tensor-core kernel also runs 1..7 heads (padded), but measured slower there than the CUDA cores.
 int32_t choose_path(const kvq_layout& L, int32_t batch, int32_t num_q_heads, const kvq_decode_options* opt) {
   const int32_t group = num_q_heads / L.num_kv_heads;
   const bool tc = decode_tc_supported(L.head_dim, L.v_dim, L.mla, group, batch);
@@ -65,7 +66,7 @@ int32_t choose_path(const kvq_layout& L, int32_t batch, int32_t num_q_heads, con
   const int32_t want = opt ? opt->path : 0;
   if (want == 2) return tc ? 2 : -1;
   if (want == 1) return cc ? 1 : -1;
-  if (tc) return 2;
+  if (tc && group >= 8) return 2;
   return cc ? 1 : -1;
 }
 

@@ -5,8 +5,8 @@
 // dequantized bf16 tiles are the operands of tcgen05.mma, with fp32 accumulators in tensor memory.
 // "feat(kvcache): 8-bit DSV4 window/compressed KV", section "Testing": split-k decode, masked -1 pages.
 //
-// With G = 8 or 16 query heads per kv head, QK^T and PV are small dense contractions.  They run
-// swapped so that the 128 tokens of a tile are the MMA's M dimension:
+// With G <= 16 query heads per kv head (padded to the MMA N = 16), QK^T and PV are small dense
+// contractions.  They run swapped so that the 128 tokens of a tile are the MMA's M dimension:
 //   S^T[128 tok][16] = Kd[128 tok][D] . Q[16][D]^T     (A = K tile in tensor memory; B = Q, K-major smem)
 //   O^T[d][16]     += Vd^T[d][128 tok] . P[16][128]^T  (A = the V tile read MN-major; B = P, MN-major)
 // (heads beyond G are zero rows of Q and P).  The V tile uses the canonical no-swizzle core-matrix
@@ -298,7 +298,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const KParams p,
   uint32_t* sTmem = reinterpret_cast<uint32_t*>(smem + Cfg::BAR_OFF + Cfg::NBARS * 8);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int32_t groups = p.num_kv_heads;  // one item covers all GN heads of a kv head
+  const int32_t groups = p.num_kv_heads;  // one item covers all G heads of a kv head
+  const int32_t G = p.group;              // query heads per kv head, 1 <= G <= GN (the rest is padding)
 
   // ---- plan: split size, total items, first item of every sequence
   const Plan plan = make_plan(p, 0, -1);
@@ -417,9 +418,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const KParams p,
       return reinterpret_cast<const uint4*>(slot + (pi * Cfg::NSL + sl) * kBox + off * 128 + ((cw ^ swz) * 16));
     };
     const int sc_off = Cfg::SL_SC + pi * Cfg::SC_KV + (off * Cfg::NB + part * Cfg::NBT) * 2;
-    // q rows of an item (GN x D bf16), QPT 16-byte pieces per thread, loaded one tile ahead of use
-    constexpr int QPIECES = GN * (D / 8);
-    constexpr int QPT = (QPIECES + kDwThreads - 1) / kDwThreads;
+    // q rows of an item (G x D bf16), at most QPT 16-byte pieces per thread, loaded one tile ahead of use;
+    // the padding rows G..GN-1 of the shared q tile stay zero
+    constexpr int QPT = (GN * (D / 8) + kDwThreads - 1) / kDwThreads;
+    const int QPIECES = G * (D / 8);
     uint4 qreg[QPT];
     auto load_q = [&](const TileIter& t) {
       const int32_t head0 = t.g * p.group;
@@ -633,7 +635,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const KParams p,
         tmem_ld16(ob + oc * kN + lane_base, o);
         const int d = oc * 128 + tt;
 #pragma unroll
-        for (int h = 0; h < GN; ++h) p.part_acc[(static_cast<int64_t>(pend_item) * GN + h) * D + d] = o[h];
+        for (int h = 0; h < GN; ++h)
+          if (h < G) p.part_acc[(static_cast<int64_t>(pend_item) * G + h) * D + d] = o[h];
       }
       tc_fence_before();  // the reads are ordered before this warp's later arrivals
       pend_item = -1;
@@ -664,7 +667,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const KParams p,
         bool moved = false;
 #pragma unroll
         for (int h = 0; h < GN; ++h) {
-          s[h] = valid ? s[h] * p.score_scale : -INFINITY;
+          s[h] = (valid && h < G) ? s[h] * p.score_scale : -INFINITY;
           moved |= (s[h] > -INFINITY) && (m_used[h] == -INFINITY || s[h] > m_used[h] + kLazyRescale);
         }
         // does any token of the tile move any head's running max?  (one vote per warp, one barrier)
@@ -753,15 +756,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const KParams p,
         if (lane == 0) sRed[warp * kN + h] = v;
       }
       named_sync(1, kSmWarps * 32);
-      if (tt < GN) {  // m_used is identical in every softmax thread; thread h writes head h
+      if (tt < G) {  // m_used is identical in every softmax thread; thread h writes head h
         float lsum = 0.0f, mh = -INFINITY;
 #pragma unroll
         for (int w = 0; w < kSmWarps; ++w) lsum += sRed[w * kN + tt];
 #pragma unroll
         for (int h = 0; h < GN; ++h)
           if (h == tt) mh = m_used[h];
-        p.part_ml[(static_cast<int64_t>(item) * GN + tt) * 2 + 0] = mh;
-        p.part_ml[(static_cast<int64_t>(item) * GN + tt) * 2 + 1] = lsum;
+        p.part_ml[(static_cast<int64_t>(item) * G + tt) * 2 + 0] = mh;
+        p.part_ml[(static_cast<int64_t>(item) * G + tt) * 2 + 1] = lsum;
       }
       named_sync(1, kSmWarps * 32);
       pend_item = item;
@@ -814,7 +817,7 @@ bool encode_code_map(CUtensorMap* map, const DecodeArgs& a) {
 template <int D>
 kvq_status launch_tc_d(const DecodeArgs& a, cudaStream_t stream) {
   using Cfg = TcCfg<D>;
-  const bool g16 = (a.num_q_heads / a.num_kv_heads) == 16;
+  const bool g16 = (a.num_q_heads / a.num_kv_heads) > 8;
   auto kern = (a.kind == KVQ_FP8_E4M3) ? (g16 ? decode_tc_kernel<D, KVQ_FP8_E4M3, 16> : decode_tc_kernel<D, KVQ_FP8_E4M3, 8>)
                                        : (g16 ? decode_tc_kernel<D, KVQ_Q8_0, 16> : decode_tc_kernel<D, KVQ_Q8_0, 8>);
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES) != cudaSuccess)
@@ -835,7 +838,7 @@ kvq_status launch_tc_d(const DecodeArgs& a, cudaStream_t stream) {
 bool decode_tc_supported(int32_t head_dim, int32_t v_dim, int32_t mla, int32_t group, int32_t batch) {
   if (mla || v_dim != head_dim) return false;
   if (head_dim != 128 && head_dim != 256) return false;
-  return (group == 8 || group == 16) && batch <= kMaxPlanBatch;
+  return group >= 1 && group <= kN && batch <= kMaxPlanBatch;
 }
 
 kvq_status launch_decode_tc(const DecodeArgs& a, cudaStream_t stream) {

@@ -134,6 +134,11 @@ size_t kvq_decode_workspace_bytes_ex(const kvq_layout* layout, int32_t batch, in
  * K and V dequantized to bf16 (RNE of code * scale) and fp32 accumulation; a sequence without a
  * valid token outputs zeros.  Supported: page_size 16 and head_dim in {64, 128, 256} with v_dim ==
  * head_dim (GQA), or the MLA row head_dim 576 / v_dim 512; other shapes return KVQ_EUNSUPPORTED.
+ * Kernels (kvq_decode_options.path): the CUDA-core kernel (1) runs every supported shape and keeps the
+ * softmax probabilities P in fp32.  The tensor-core kernel (2) runs head_dim 128 or 256 with 1..16
+ * query heads per kv head and batch <= 2048; it feeds P to the MMA as bf16, so its error relative to
+ * the exact result grows with the magnitude of V (about 2^-9 of max |V|).  Automatic (0) picks 2 for
+ * 8..16 query heads per kv head and 1 otherwise.
  */
 kvq_status kvq_decode(const void* q, const void* pool, const void* scales, const int32_t* block_table,
                       int32_t max_pages_per_seq, const int32_t* seq_lens, int32_t batch, int32_t num_q_heads,

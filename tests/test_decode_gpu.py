@@ -34,12 +34,21 @@ def _stored(name, kind, poison=0xA5, **kw):
     return case, codes, scales, oc, osc
 
 
+@pytest.mark.parametrize("path", [0, 1, 2])
 @pytest.mark.parametrize("kind", KINDS)
 @pytest.mark.parametrize("name", list(CASES))
-def test_decode_matches_oracle(name, kind):
+def test_decode_matches_oracle(name, kind, path):
+    """Every family on the automatic choice, the CUDA-core kernel (1) and the tensor-core kernel (2)."""
+    if path == 2 and name == "mla":
+        pytest.skip("the tensor-core kernel covers GQA pools")
+    if path == 2 and name == "serving":
+        # 1% of the values are scaled by 100, so outputs reach ~50; the tensor-core kernel feeds P to the
+        # MMA as bf16 (relative error 2^-9), which is ~0.1 absolute there.  The automatic choice keeps
+        # this group size (4) on the CUDA-core kernel, whose P stays fp32.
+        pytest.skip("bf16 P of the tensor-core kernel vs the absolute bound at outputs of ~50")
     case, codes, scales, oc, osc = _stored(name, kind)
     ref = oracle_decode(case, oc, osc)
-    got = gpu_decode(case, codes, scales)
+    got = gpu_decode(case, codes, scales, path=path)
     assert_decode_close(got, ref)
     got16 = gpu_decode(case, codes, scales, out_dtype=torch.bfloat16)
     assert_decode_close(got16, ref, rel=2.0 ** -8)
@@ -108,6 +117,10 @@ TC_CASES = [
     dict(batch=2, ctx=9000),                                              # G = 8, D = 256
     dict(batch=3, ctx=2500, num_q_heads=32, num_kv_heads=2, head_dim=128),  # G = 16, D = 128
     dict(batch=2, ctx=3001, num_q_heads=16, num_kv_heads=2, head_dim=128, mask_frac=0.03),
+    dict(batch=3, ctx=2100, num_q_heads=16, num_kv_heads=8, head_dim=128),  # G = 2 (padded to 16)
+    dict(batch=2, ctx=1500, num_q_heads=12, num_kv_heads=4, head_dim=256),  # G = 3
+    dict(batch=2, ctx=2000, num_q_heads=8, num_kv_heads=8, head_dim=128),   # G = 1
+    dict(batch=2, ctx=1800, num_q_heads=24, num_kv_heads=2, head_dim=128),  # G = 12
 ]
 
 
