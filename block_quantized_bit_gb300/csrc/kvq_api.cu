@@ -43,6 +43,15 @@ kvq_status check_layout(const kvq_layout* L) {
 
 bool kind_ok(int kind) { return kind == KVQ_FP8_E4M3 || kind == KVQ_Q8_0; }
 
+// SMs of the current device (the MLA tensor-core plan targets one work item per SM).
+int32_t sm_count() {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+      sms <= 0)
+    return kTargetItems;
+  return sms;
+}
+
 size_t elems_of(const kvq_layout& L) {
   return static_cast<size_t>(L.num_pages) * n_kv_of(L) * L.num_kv_heads * L.page_size * L.head_dim;
 }
@@ -50,6 +59,7 @@ size_t elems_of(const kvq_layout& L) {
 struct WorkspacePlan {
   int32_t path;
   int32_t split_align;
+  int32_t target_items;
   int32_t heads_per_item;
   int32_t query_groups;
   int64_t max_items;
@@ -57,16 +67,18 @@ struct WorkspacePlan {
 };
 
 // 1 = CUDA-core kernel, 2 = tensor-core kernel, -1 = the requested path has no kernel for this shape.
-// Automatic: tensor cores where QK^T and PV are dense enough (8..16 query heads per kv head); the
-// tensor-core kernel also runs 1..7 heads (padded), but measured slower there than the CUDA cores.
+// Automatic: tensor cores where QK^T and PV are dense enough -- 8..16 query heads per kv head, or an MLA
+// pool read by a multiple of 64 query heads; the GQA tensor-core kernel also runs 1..7 heads (padded),
+// but measured slower there than the CUDA cores.
 int32_t choose_path(const kvq_layout& L, int32_t batch, int32_t num_q_heads, const kvq_decode_options* opt) {
   const int32_t group = num_q_heads / L.num_kv_heads;
-  const bool tc = decode_tc_supported(L.head_dim, L.v_dim, L.mla, group, batch);
+  const bool tc = L.mla ? decode_mla_tc_supported(L.head_dim, L.v_dim, L.mla, group, batch)
+                        : decode_tc_supported(L.head_dim, L.v_dim, L.mla, group, batch);
   const bool cc = decode_cc_supported(L.head_dim, L.v_dim, L.mla);
   const int32_t want = opt ? opt->path : 0;
   if (want == 2) return tc ? 2 : -1;
   if (want == 1) return cc ? 1 : -1;
-  if (tc && group >= 8) return 2;
+  if (tc && (group >= 8 || L.mla)) return 2;
   return cc ? 1 : -1;
 }
 
@@ -79,10 +91,14 @@ bool plan_workspace(const kvq_layout& L, int32_t batch, int32_t num_q_heads, int
   if (pps < 0) return false;
   const int32_t path = choose_path(L, batch, num_q_heads, opt);
   w->path = path;
-  w->heads_per_item = (path == 2) ? group : cc_heads_per_item(group, L.head_dim, L.mla);
+  if (path == 2 && L.mla) w->heads_per_item = decode_mla_tc_heads_per_item(group);
+  else w->heads_per_item = (path == 2) ? group : cc_heads_per_item(group, L.head_dim, L.mla);
   w->split_align = (path == 2) ? 8 : 1;
+  // the MLA tensor-core kernel's items are expensive to start and finish (64 query rows of 576,
+  // 64 x 512 partial outputs): about one item per SM instead of eight
+  w->target_items = (path == 2 && L.mla) ? sm_count() : kTargetItems;
   w->query_groups = L.num_kv_heads * (group / w->heads_per_item);
-  w->max_items = max_work_items(batch, w->query_groups, max_pages, pps);
+  w->max_items = max_work_items(batch, w->query_groups, max_pages, pps, w->target_items);
   const size_t acc = static_cast<size_t>(w->max_items) * w->heads_per_item * L.v_dim * sizeof(float);
   const size_t ml = static_cast<size_t>(w->max_items) * w->heads_per_item * 2 * sizeof(float);
   w->acc_offset = kWorkspaceHeader;
@@ -93,12 +109,13 @@ bool plan_workspace(const kvq_layout& L, int32_t batch, int32_t num_q_heads, int
 
 }  // namespace
 
-int64_t max_work_items(int32_t batch, int32_t query_groups, int32_t max_pages, int32_t pages_per_split) {
+int64_t max_work_items(int32_t batch, int32_t query_groups, int32_t max_pages, int32_t pages_per_split,
+                       int32_t target_items) {
   const int64_t per_seq = static_cast<int64_t>(query_groups);
   if (pages_per_split > 0)
     return static_cast<int64_t>(batch) * per_seq * ((max_pages + pages_per_split - 1) / pages_per_split);
   const int64_t upper = static_cast<int64_t>(batch) * per_seq * ((max_pages + kMinPagesPerSplit - 1) / kMinPagesPerSplit);
-  return std::min<int64_t>(upper, kTargetItems + static_cast<int64_t>(batch) * per_seq);
+  return std::min<int64_t>(upper, static_cast<int64_t>(target_items) + static_cast<int64_t>(batch) * per_seq);
 }
 
 }  // namespace kvq
@@ -243,9 +260,11 @@ kvq_status kvq_decode_ex(const void* q, const void* pool, const void* scales, co
   a.max_items = w.max_items;
   a.heads_per_item = w.heads_per_item;
   a.split_align = w.split_align;
+  a.target_items = w.target_items;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (cudaMemsetAsync(ws, 0, sizeof(uint32_t), s) != cudaSuccess) return KVQ_ECUDA;
-  st = (w.path == 2) ? launch_decode_tc(a, s) : launch_decode_cc(a, s);
+  if (w.path == 2) st = a.mla ? launch_decode_mla_tc(a, s) : launch_decode_tc(a, s);
+  else st = launch_decode_cc(a, s);
   if (st != KVQ_OK) return st;
   return launch_merge(a, w.query_groups, s);
 }

@@ -35,6 +35,7 @@ struct DecodeArgs {
   int64_t max_items;
   int32_t heads_per_item;  // query heads one work item covers (a tile of the group)
   int32_t split_align;     // automatic split sizes are a multiple of this many pages
+  int32_t target_items;    // automatic split sizes aim at about this many work items
 };
 
 // Tokens per page the decode kernels support, and the workspace's leading status block.
@@ -42,13 +43,14 @@ constexpr int kPageTokens = 16;
 constexpr size_t kWorkspaceHeader = 256;
 
 // Work-item planning constants shared by the host (workspace bound) and the kernels.
-constexpr int kTargetItems = 1216;  // 8 items per SM on a 152-SM GB300
+constexpr int kTargetItems = 1216;  // 8 items per SM on a 152-SM GB300 (kernels with cheap items)
 constexpr int kMinPagesPerSplit = 4;
 
 // Heads of one query group that a CUDA-core work item covers.
 int32_t cc_heads_per_item(int32_t group, int32_t head_dim, int32_t mla);
 // Upper bound on work items for the given sizes (used for workspace sizing and the grid).
-int64_t max_work_items(int32_t batch, int32_t query_groups, int32_t max_pages, int32_t pages_per_split);
+int64_t max_work_items(int32_t batch, int32_t query_groups, int32_t max_pages, int32_t pages_per_split,
+                       int32_t target_items);
 
 kvq_status launch_store(void* pool, void* scales, const void* k, const void* v, const int64_t* slot_mapping,
                         int64_t num_tokens, const kvq_layout& L, kvq_kind kind, cudaStream_t stream);
@@ -59,6 +61,9 @@ kvq_status launch_dequant_probe(kvq_kind kind, const uint8_t* codes, const uint1
                                 int64_t n, cudaStream_t stream);
 bool decode_cc_supported(int32_t head_dim, int32_t v_dim, int32_t mla);
 bool decode_tc_supported(int32_t head_dim, int32_t v_dim, int32_t mla, int32_t group, int32_t batch);
+bool decode_mla_tc_supported(int32_t head_dim, int32_t v_dim, int32_t mla, int32_t group, int32_t batch);
+int32_t decode_mla_tc_heads_per_item(int32_t group);
+kvq_status launch_decode_mla_tc(const DecodeArgs& a, cudaStream_t stream);
 kvq_status launch_decode_tc(const DecodeArgs& a, cudaStream_t stream);
 kvq_status launch_decode_cc(const DecodeArgs& a, cudaStream_t stream);
 kvq_status launch_merge(const DecodeArgs& a, int32_t query_groups, cudaStream_t stream);

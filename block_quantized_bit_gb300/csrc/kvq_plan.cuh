@@ -3,7 +3,8 @@
 // A decode work item is (sequence b, query group, split): a query group is a kv head together with a
 // tile of the query heads that read it, and a split is a run of C consecutive pages of the sequence.
 // C = pages_per_split when the caller fixes it; otherwise C = max(4, ceil(sum_b pages_b * groups /
-// 1216)) rounded up to `split_align` pages.  Every CTA derives the same plan from seq_lens on the
+// target)) rounded up to `split_align` pages, target = 1216 (8 items per SM) unless the kernel asks
+// for fewer, larger items.  Every CTA derives the same plan from seq_lens on the
 // device, so no planning launch and no host read-back are needed.
 #pragma once
 
@@ -38,6 +39,7 @@ struct KParams {
   int32_t group;          // Hq / Hkv
   int32_t head_tiles;     // group / heads_per_item
   int32_t pages_per_split;
+  int32_t target_items;   // automatic split sizes aim at about this many items
   float score_scale;      // sm_scale * log2(e)
 };
 
@@ -76,7 +78,7 @@ __device__ Plan make_plan(const KParams& p, int32_t want_item, int32_t want_b) {
   tot *= groups;
   int32_t C = p.pages_per_split;
   if (C <= 0) {
-    long long c = (tot + kTargetItems - 1) / kTargetItems;
+    long long c = (tot + p.target_items - 1) / p.target_items;
     C = static_cast<int32_t>(c > kMinPagesPerSplit ? c : static_cast<long long>(kMinPagesPerSplit));
     C = (C + p.split_align - 1) / p.split_align * p.split_align;
   }
@@ -143,6 +145,7 @@ inline KParams make_kparams(const DecodeArgs& a) {
   p.pages_per_split = a.pages_per_split;
   p.score_scale = a.sm_scale * kLog2e;
   p.split_align = a.split_align;
+  p.target_items = a.target_items > 0 ? a.target_items : kTargetItems;
   return p;
 }
 

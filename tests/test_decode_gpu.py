@@ -39,8 +39,6 @@ def _stored(name, kind, poison=0xA5, **kw):
 @pytest.mark.parametrize("name", list(CASES))
 def test_decode_matches_oracle(name, kind, path):
     """Every family on the automatic choice, the CUDA-core kernel (1) and the tensor-core kernel (2)."""
-    if path == 2 and name == "mla":
-        pytest.skip("the tensor-core kernel covers GQA pools")
     if path == 2 and name == "serving":
         # 1% of the values are scaled by 100, so outputs reach ~50; the tensor-core kernel feeds P to the
         # MMA as bf16 (relative error 2^-9), which is ~0.1 absolute there.  The automatic choice keeps
@@ -157,3 +155,40 @@ def test_tensor_core_decode_nan_poisoned_tails_and_empty_sequences():
     ref = oracle_decode(case, oc, osc)
     assert not got[1].any() and not got[2].any()
     assert_decode_close(got, ref)
+
+
+# ------------------------------------------------------------------ MLA on the tensor cores
+MLA_TC_CASES = [
+    dict(batch=1, ctx=1037, num_q_heads=128),   # two head groups of 64, ragged last tile
+    dict(batch=3, ctx=2300),                    # 16 heads: one padded head group; several splits
+    dict(batch=2, ctx=700, num_q_heads=64),     # a single full head group
+    dict(batch=1, ctx=1500, num_q_heads=192),   # three head groups
+]
+
+
+@pytest.mark.parametrize("kind", KINDS)
+@pytest.mark.parametrize("ci", range(len(MLA_TC_CASES)))
+def test_mla_tensor_core_decode_matches_oracle(ci, kind):
+    case, codes, scales, oc, osc = _stored("mla", kind, **MLA_TC_CASES[ci])
+    ref = oracle_decode(case, oc, osc)
+    got = gpu_decode(case, codes, scales, path=2)
+    assert_decode_close(got, ref)
+
+
+@pytest.mark.parametrize("pps", [8, 12, 40])
+def test_mla_tensor_core_masked_pages_ragged_lengths_and_split_sizes(pps):
+    """Masked (-1) pages, sequences shorter than their stored rows (ragged tails, one shorter than a
+    tile) and split sizes that are not whole tiles, against the oracle and the CUDA-core kernel."""
+    case, codes, scales, oc, osc = _stored("mla", "fp8_e4m3", batch=3, ctx=2300, num_q_heads=128)
+    sl = case.seq_lens.clone()
+    sl[1], sl[2] = 1507, 129
+    case.seq_lens = sl
+    bt = case.block_table.clone()
+    g = torch.Generator().manual_seed(7)
+    bt[torch.rand(bt.shape, generator=g) < 0.03] = -1
+    case.block_table = bt
+    ref = oracle_decode(case, oc, osc)
+    tc = gpu_decode(case, codes, scales, path=2, pages_per_split=pps)
+    assert_decode_close(tc, ref)
+    cc = gpu_decode(case, codes, scales, path=1, pages_per_split=pps)
+    np.testing.assert_allclose(tc, cc, rtol=0, atol=5e-3)
