@@ -76,7 +76,8 @@ constexpr int RED_OFF = SC_OFF + 2 * kScTile;             // softmax cross-warp 
 constexpr int M_OFF = RED_OFF + kSmWarps * kHG * 4;       // running max per head [64]
 constexpr int A_OFF = M_OFF + kHG * 4;                    // rescale factor per head [64]
 constexpr int FLAG_OFF = A_OFF + kHG * 4;                 // 4 votes
-constexpr int META_OFF = FLAG_OFF + 16;                   // [kRing][8] valid tokens per page
+constexpr int VAL_OFF = FLAG_OFF + 16;                    // [2][128] token validity by tile parity
+constexpr int META_OFF = VAL_OFF + 2 * kTile;             // [kRing][8] valid tokens per page
 constexpr int TAB_OFF = META_OFF + kRing * kPagesPerTile * 4;
 constexpr int NBARS = 18 + 2 * kRing;
 constexpr int BAR_OFF = TAB_OFF + kMaxBatch * 4;
@@ -248,6 +249,7 @@ __global__ void __launch_bounds__(mla::kThreads, 1) decode_mla_kernel(const KPar
   float* sA = reinterpret_cast<float*>(smem + A_OFF);
   int32_t* sFlag = reinterpret_cast<int32_t*>(smem + FLAG_OFF);
   int32_t* sMeta = reinterpret_cast<int32_t*>(smem + META_OFF);
+  uint8_t* sValid = smem + VAL_OFF;
   int32_t* sTab = reinterpret_cast<int32_t*>(smem + TAB_OFF);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + BAR_OFF);
   // Each barrier completes once per use of its buffer, so a waiter names an unambiguous phase.
@@ -258,7 +260,7 @@ __global__ void __launch_bounds__(mla::kThreads, 1) decode_mla_kernel(const KPar
   uint64_t* bar_v_full = bars + 8;     // [2] V^T buffer v written (V warps)
   uint64_t* bar_v_free = bars + 10;    // [2] the PV reading V^T buffer v completed (commit)
   uint64_t* bar_pv_done = bars + 12;   // [2] every PV of tile parity b completed (commit)
-  uint64_t* bar_sc_free = bars + 14;   // [2] scale buffer b read (K warps)
+  uint64_t* bar_sc_free = bars + 14;   // [2] scale buffer b read and token validity b written (K warps)
   uint64_t* bar_full = bars + 18;              // [kRing] ring slot landed (producer arrival + bytes)
   uint64_t* bar_empty = bars + 18 + kRing;     // [kRing] ring slot read (K warps)
   uint32_t* sTmem = reinterpret_cast<uint32_t*>(smem + BAR_OFF + NBARS * 8);
@@ -391,7 +393,12 @@ __global__ void __launch_bounds__(mla::kThreads, 1) decode_mla_kernel(const KPar
         const uint32_t u = n * kSlabs + j;  // ring use = K slot use
         const int rs = u % kRing, ks = u & 1;
         if (!mbar_wait_bounded(&bar_full[rs], (u / kRing) & 1)) { ok = false; break; }
-        if (j == 0) v_ok = off < sMeta[rs * kPagesPerTile + pi];
+        if (j == 0) {
+          v_ok = off < sMeta[rs * kPagesPerTile + pi];
+          // the validity slot of this tile parity was last read by the softmax of tile n - 2
+          if (n >= 2 && !mbar_wait_bounded(&bar_p_full[n & 1], ((n >> 1) - 1) & 1)) { ok = false; break; }
+          sValid[(n & 1) * kTile + tt] = v_ok ? 1 : 0;  // published with sc_free after the last slab
+        }
         if (u >= 2 && !mbar_wait_bounded(&bar_k_free[ks], ((u >> 1) - 1) & 1)) { ok = false; break; }
         const uint8_t* slot = sRing + rs * kSlab + pi * kBox + off * 128;
         const int c0 = (j < 4) ? 0 : 4;  // the rope slab keeps its upper half only (d = 512..575)
@@ -578,7 +585,6 @@ __global__ void __launch_bounds__(mla::kThreads, 1) decode_mla_kernel(const KPar
   } else {
     // ===================================================================== softmax warps
     const int tt = tid;  // token slot / TMEM lane; in the epilogue, the dim within an O^T block
-    const int pi = tt / kPage, off = tt % kPage;
     uint32_t n = 0;  // tiles
     for (int32_t item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
       MlaIter t;
@@ -591,9 +597,12 @@ __global__ void __launch_bounds__(mla::kThreads, 1) decode_mla_kernel(const KPar
       bool o_live = false;
       for (; t.i < t.ntiles && ok; ++t.i, ++n) {
         const int b = n & 1;
-        const bool valid = mla_phys(p, t, pi, off) >= 0;
         if (!mbar_wait_bounded(&bar_qk_done[b], (n >> 1) & 1)) { ok = false; break; }
+        // token validity was written before sc_free of this tile completed (already complete: the K warps
+        // arrive on it after the last slab, which this QK read)
+        if (!mbar_wait_bounded(&bar_sc_free[b], (n >> 1) & 1)) { ok = false; break; }
         mla_fence_after();
+        const bool valid = sValid[b * kTile + tt] != 0;
         const uint32_t s_base = tS + b * 64 + lane_base;
         // does any score of the tile move its head's running max?  (one vote per warp, one barrier)
         bool moved = false;
