@@ -63,7 +63,7 @@ struct WorkspacePlan {
   int32_t heads_per_item;
   int32_t query_groups;
   int64_t max_items;
-  size_t acc_offset, ml_offset, total;
+  size_t acc_offset, ml_offset, tab_offset, total;
 };
 
 // 1 = CUDA-core kernel, 2 = tensor-core kernel, -1 = the requested path has no kernel for this shape.
@@ -94,16 +94,19 @@ bool plan_workspace(const kvq_layout& L, int32_t batch, int32_t num_q_heads, int
   if (path == 2 && L.mla) w->heads_per_item = decode_mla_tc_heads_per_item(group);
   else w->heads_per_item = (path == 2) ? group : cc_heads_per_item(group, L.head_dim, L.mla);
   w->split_align = (path == 2) ? 8 : 1;
-  // the MLA tensor-core kernel's items are expensive to start and finish (64 query rows of 576,
-  // 64 x 512 partial outputs): about one item per SM instead of eight
-  w->target_items = (path == 2 && L.mla) ? sm_count() : kTargetItems;
+  // Tensor-core items are expensive to start and finish (a pipeline fill, a q tile, an O readout, and
+  // partials the merge must read): the GQA kernel aims at about two items per SM, the MLA kernel
+  // (64 query rows of 576, 64 x 512 partial outputs) at one, instead of eight.
+  w->target_items = (path == 2) ? (L.mla ? sm_count() : 2 * sm_count()) : kTargetItems;
   w->query_groups = L.num_kv_heads * (group / w->heads_per_item);
   w->max_items = max_work_items(batch, w->query_groups, max_pages, pps, w->target_items);
   const size_t acc = static_cast<size_t>(w->max_items) * w->heads_per_item * L.v_dim * sizeof(float);
   const size_t ml = static_cast<size_t>(w->max_items) * w->heads_per_item * 2 * sizeof(float);
   w->acc_offset = kWorkspaceHeader;
   w->ml_offset = w->acc_offset + ((acc + 255) / 256) * 256;
-  w->total = w->ml_offset + ((ml + 255) / 256) * 256;
+  w->tab_offset = w->ml_offset + ((ml + 255) / 256) * 256;
+  const size_t tab = static_cast<size_t>(batch) * 2 * sizeof(int32_t);
+  w->total = w->tab_offset + ((tab + 255) / 256) * 256;
   return true;
 }
 
@@ -257,6 +260,7 @@ kvq_status kvq_decode_ex(const void* q, const void* pool, const void* scales, co
   a.status = reinterpret_cast<uint32_t*>(ws);
   a.part_acc = reinterpret_cast<float*>(ws + w.acc_offset);
   a.part_ml = reinterpret_cast<float*>(ws + w.ml_offset);
+  a.plan_tab = reinterpret_cast<int32_t*>(ws + w.tab_offset);
   a.max_items = w.max_items;
   a.heads_per_item = w.heads_per_item;
   a.split_align = w.split_align;

@@ -399,89 +399,69 @@ __global__ void __launch_bounds__(WARPS * 32, MINB) decode_cc_kernel(KParams p) 
 // 8 float4 columns x 32 split groups: every thread accumulates its columns over the splits
 // s = group, group + 32, ... with weights exp2(m_s - M), and the groups are summed in shared memory.
 constexpr int kMergeThreads = 256;
-constexpr int kMergeCols = 8;                    // float4 columns = 32 dims per CTA
-constexpr int kMergeGroups = kMergeThreads / kMergeCols;
+constexpr int kMergeWarps = kMergeThreads / 32;
 
+// One CTA per (sequence, query group, head of the item, 32-dim slice of v): the log-sum-exp merge of
+// the sequence's split partials, out = sum_s 2^(m_s - M) acc_s / sum_s 2^(m_s - M) l_s, M = max_s m_s.
+// Warp w takes the splits s = w, w + 8, ...; lane = dim.  The decode kernel's CTA 0 left each
+// sequence's first item and split count in plan_tab, so no plan is recomputed here.
 template <typename OutT>
 __global__ void __launch_bounds__(kMergeThreads) merge_kernel(KParams p, OutT* __restrict__ out, int32_t heads_per_item,
-                                                              int32_t DV) {
-  __shared__ float s_red[kMergeThreads];
-  __shared__ float4 s_acc[kMergeGroups][kMergeCols];
-  const int32_t groups = p.num_kv_heads * p.head_tiles;
+                                                              int32_t DV, int32_t units_per_seq) {
+  __shared__ float s_m[kMergeWarps];
+  __shared__ float s_a[kMergeWarps][32];
+  __shared__ float s_l[kMergeWarps];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int32_t b = blockIdx.x / units_per_seq;
+  const int32_t u = blockIdx.x - b * units_per_seq;
   const int32_t slices = DV / 32;
-  int32_t rest = blockIdx.x;
-  const int32_t slice = rest % slices;
-  rest /= slices;
-  const int32_t h = rest % heads_per_item;
-  rest /= heads_per_item;
-  const int32_t qg = rest % groups;
-  const int32_t b = rest / groups;
-  const Plan plan = make_plan(p, -1, b);
+  const int32_t slice = u % slices;
+  const int32_t h = (u / slices) % heads_per_item;
+  const int32_t qg = u / (slices * heads_per_item);
   const int32_t g = qg / p.head_tiles, ht = qg - g * p.head_tiles;
   const int32_t head = g * p.group + ht * heads_per_item + h;
-  int32_t ns = plan.nsplit;
-  const int64_t first = static_cast<int64_t>(plan.base) + static_cast<int64_t>(qg) * ns;
-  if (first + ns > p.max_items) {  // cannot happen when the workspace bound holds; never read past it
-    if (threadIdx.x == 0) set_status(p.status, kStatusBadPage);
+  int32_t ns = p.plan_tab[2 * b + 1];
+  const int64_t first = static_cast<int64_t>(p.plan_tab[2 * b]) + static_cast<int64_t>(qg) * ns;
+  if (ns < 0 || first < 0 || first + ns > p.max_items) {  // cannot happen when the workspace bound holds
+    if (tid == 0) set_status(p.status, kStatusBadPage);
     ns = 0;
   }
-  const int tid = threadIdx.x;
-  // global max of the split maxima
   float M = -INFINITY;
   for (int32_t s = tid; s < ns; s += kMergeThreads) M = fmaxf(M, p.part_ml[((first + s) * heads_per_item + h) * 2]);
-  s_red[tid] = M;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  if (lane == 0) s_m[warp] = M;
   __syncthreads();
-  for (int o = kMergeThreads / 2; o > 0; o >>= 1) {
-    if (tid < o) s_red[tid] = fmaxf(s_red[tid], s_red[tid + o]);
-    __syncthreads();
-  }
-  M = s_red[0];
-  __syncthreads();
-  const int col = tid % kMergeCols, grp = tid / kMergeCols;
-  const int d = slice * 32 + col * 4;
-  float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-  float lsum = 0.0f;
+#pragma unroll
+  for (int w = 0; w < kMergeWarps; ++w) M = fmaxf(M, s_m[w]);
+  float a = 0.0f, l = 0.0f;
   if (M != -INFINITY) {
+    const float* acc = p.part_acc + slice * 32 + lane;
 #pragma unroll 4
-    for (int32_t s = grp; s < ns; s += kMergeGroups) {
+    for (int32_t s = warp; s < ns; s += kMergeWarps) {
       const int64_t it = (first + s) * heads_per_item + h;
       const float2 ml = *reinterpret_cast<const float2*>(p.part_ml + it * 2);
       const float w = (ml.x == -INFINITY) ? 0.0f : exp2f(ml.x - M);
-      const float4 v = *reinterpret_cast<const float4*>(p.part_acc + it * DV + d);
-      a.x = fmaf(v.x, w, a.x);
-      a.y = fmaf(v.y, w, a.y);
-      a.z = fmaf(v.z, w, a.z);
-      a.w = fmaf(v.w, w, a.w);
-      lsum = fmaf(ml.y, w, lsum);
+      a = fmaf(acc[it * DV], w, a);
+      l = fmaf(ml.y, w, l);
     }
   }
-  s_acc[grp][col] = a;
-  s_red[tid] = (col == 0) ? lsum : 0.0f;
+  s_a[warp][lane] = a;
+  if (lane == 0) s_l[warp] = l;
   __syncthreads();
-  for (int o = kMergeThreads / 2; o > 0; o >>= 1) {
-    if (tid < o) s_red[tid] += s_red[tid + o];
-    __syncthreads();
-  }
-  const float L = s_red[0];
-  if (tid < kMergeCols) {
-    float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int gi = 0; gi < kMergeGroups; ++gi) {
-      const float4 v = s_acc[gi][tid];
-      t.x += v.x;
-      t.y += v.y;
-      t.z += v.z;
-      t.w += v.w;
-    }
-    const float inv = (L > 0.0f) ? 1.0f / L : 0.0f;
-    const float o4[4] = {t.x * inv, t.y * inv, t.z * inv, t.w * inv};
-    const int64_t dst = (static_cast<int64_t>(b) * p.num_q_heads + head) * DV + slice * 32 + tid * 4;
+  if (warp == 0) {
+    float at = 0.0f, lt = 0.0f;
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      if constexpr (sizeof(OutT) == 2)
-        out[dst + e] = __float2bfloat16_rn(o4[e]);
-      else
-        out[dst + e] = o4[e];
+    for (int w = 0; w < kMergeWarps; ++w) {
+      at += s_a[w][lane];
+      lt += s_l[w];
     }
+    const float o = (lt > 0.0f) ? at / lt : 0.0f;
+    const int64_t dst = (static_cast<int64_t>(b) * p.num_q_heads + head) * DV + slice * 32 + lane;
+    if constexpr (sizeof(OutT) == 2)
+      out[dst] = __float2bfloat16_rn(o);
+    else
+      out[dst] = o;
   }
 }
 
@@ -556,14 +536,15 @@ kvq_status launch_decode_cc(const DecodeArgs& a, cudaStream_t stream) {
 
 kvq_status launch_merge(const DecodeArgs& a, int32_t query_groups, cudaStream_t stream) {
   const KParams p = make_kparams(a);
-  const int64_t grid = static_cast<int64_t>(a.batch) * query_groups * a.heads_per_item * (a.v_dim / 32);
+  const int32_t units = query_groups * a.heads_per_item * (a.v_dim / 32);
+  const int64_t grid = static_cast<int64_t>(a.batch) * units;
   if (grid == 0) return KVQ_OK;
   if (a.out_dtype == KVQ_OUT_BF16)
     merge_kernel<__nv_bfloat16><<<static_cast<unsigned>(grid), kMergeThreads, 0, stream>>>(
-        p, static_cast<__nv_bfloat16*>(a.out), a.heads_per_item, a.v_dim);
+        p, static_cast<__nv_bfloat16*>(a.out), a.heads_per_item, a.v_dim, units);
   else
-    merge_kernel<float><<<static_cast<unsigned>(grid), kMergeThreads, 0, stream>>>(p, static_cast<float*>(a.out),
-                                                                                 a.heads_per_item, a.v_dim);
+    merge_kernel<float><<<static_cast<unsigned>(grid), kMergeThreads, 0, stream>>>(
+        p, static_cast<float*>(a.out), a.heads_per_item, a.v_dim, units);
   return cudaGetLastError() == cudaSuccess ? KVQ_OK : KVQ_ECUDA;
 }
 

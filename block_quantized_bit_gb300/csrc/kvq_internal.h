@@ -32,6 +32,7 @@ struct DecodeArgs {
   uint32_t* status;
   float* part_acc;   // [max_items][heads_per_item][v_dim]
   float* part_ml;    // [max_items][heads_per_item][2]
+  int32_t* plan_tab; // [batch][2]: first item and split count of each sequence (written by the decode)
   int64_t max_items;
   int32_t heads_per_item;  // query heads one work item covers (a tile of the group)
   int32_t split_align;     // automatic split sizes are a multiple of this many pages

@@ -29,6 +29,7 @@ struct KParams {
   const int32_t* seq_lens;
   float* part_acc;
   float* part_ml;
+  int32_t* plan_tab;      // [batch][2] first item, splits per query group; CTA 0 of the decode writes it
   uint32_t* status;
   int64_t num_pages;      // pages in the pool: larger block-table entries are treated as masked
   int64_t max_items;      // work items the workspace holds
@@ -101,6 +102,10 @@ __device__ Plan make_plan(const KParams& p, int32_t want_item, int32_t want_b) {
   for (int32_t b = b0; b < b1; ++b) {
     const int32_t ns = (seq_pages(p, b) + C - 1) / C;
     const int32_t n = groups * ns;
+    if (blockIdx.x == 0 && p.plan_tab) {  // for the merge, which then needs no plan of its own
+      p.plan_tab[2 * b] = run;
+      p.plan_tab[2 * b + 1] = ns;
+    }
     const bool hit = (want_b >= 0) ? (b == want_b) : (want_item >= run && want_item < run + n);
     if (hit) {
       s_plan.C = C;
@@ -133,6 +138,7 @@ inline KParams make_kparams(const DecodeArgs& a) {
   p.seq_lens = a.seq_lens;
   p.part_acc = a.part_acc;
   p.part_ml = a.part_ml;
+  p.plan_tab = a.plan_tab;
   p.status = a.status;
   p.num_pages = a.num_pages;
   p.max_items = a.max_items;
