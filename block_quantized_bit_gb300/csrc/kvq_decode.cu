@@ -5,8 +5,8 @@
 // "feat(kvcache): 8-bit DSV4 window/compressed KV", section "Testing": the split-k decode kernel and
 // masked (-1) columns; section "What this adds": an MLA latent row serves as both K and V.
 //
-// Work decomposition (computed identically by every CTA and by the merge kernel from seq_lens, so no
-// planning launch and no host read-back is needed):
+// Work decomposition (computed identically by every CTA from seq_lens, so no planning launch and no
+// host read-back is needed; CTA 0 also leaves each sequence's first item and split count for the merge):
 //   query group qg = (kv head g, head tile ht): `heads_per_item` query heads that share kv head g;
 //   pages of sequence b are cut into splits of C pages; one work item = (b, qg, split);
 //   C = pages_per_split, or max(4, ceil(sum_b pages_b * groups / 1216)) when automatic.
