@@ -7,8 +7,9 @@
 //
 // Mapping: one lane owns one 32-element block (four 16-byte loads, 64 contiguous bytes).  The input
 // is walked as a flat stream of blocks, K first then V; a warp covers 2 KiB of contiguous input per
-// sweep and each lane keeps UNROLL blocks in flight.  The lane computes amax, the fp16 scale, the 32
-// codes (two 16-byte stores) and the scale without any cross-lane traffic.
+// sweep.  The grid is persistent (four CTAs per SM) and every lane loads its next block while it
+// quantizes the current one.  The lane computes amax, the fp16 scale, the 32 codes (two 16-byte
+// stores) and the scale without any cross-lane traffic.
 //
 // Division.  The codes must be those of the IEEE fp32 quotient x / s.  Per block the lane takes
 // r = RN(1/s) (IEEE reciprocal) once; per element it forms q0 = x*r, the exact remainder
@@ -28,7 +29,7 @@ namespace kvq {
 namespace {
 
 constexpr int kStoreThreads = 256;
-constexpr int kStoreUnroll = 4;
+constexpr int kStoreCtasPerSm = 4;  // resident CTAs per SM (64 registers per thread)
 
 // Unsigned division by a run-time constant d >= 1 via a multiply-high (Granlund & Montgomery,
 // "Division by invariant integers using multiplication", PLDI 1994): q = (umulhi(n, m) + n) >> s,
@@ -81,79 +82,75 @@ struct StoreArgs {
   int64_t num_slots;
 };
 
-template <int KIND, int UNROLL>
-__global__ void __launch_bounds__(kStoreThreads) store_kernel(StoreArgs a) {
-  const int32_t stride = gridDim.x * kStoreThreads;
-  for (int32_t base = blockIdx.x * kStoreThreads + threadIdx.x; base < a.total; base += stride * UNROLL) {
-    uint4 x[UNROLL][4];
+// Load one 32-element block (64 contiguous bytes: four 16-byte pieces) of the flat K-then-V stream.
+__device__ __forceinline__ void load_block(const StoreArgs& a, int32_t blk, uint4 (&x)[4]) {
+  const int kv = blk >= a.blocks_per_kv;
+  const int32_t local = blk - (kv ? a.blocks_per_kv : 0);
+  const uint4* src = (kv ? a.v : a.k) + static_cast<int64_t>(local) * 4;
 #pragma unroll
-    for (int u = 0; u < UNROLL; ++u) {
-      const int32_t blk = base + u * stride;
-      if (blk < a.total) {
-        const int kv = blk >= a.blocks_per_kv;
-        const int32_t local = blk - (kv ? a.blocks_per_kv : 0);
-        const uint4* src = (kv ? a.v : a.k) + static_cast<int64_t>(local) * 4;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) x[u][i] = __ldcs(src + i);
-      }
-    }
-#pragma unroll
-    for (int u = 0; u < UNROLL; ++u) {
-      const int32_t blk = base + u * stride;
-      if (blk >= a.total) continue;
-      const int kv = blk >= a.blocks_per_kv;
-      const uint32_t local = static_cast<uint32_t>(blk - (kv ? a.blocks_per_kv : 0));
-      const uint32_t t = fdiv(local, a.row_blocks);
-      const uint32_t in_row = local - t * a.row_blocks.d;
-      const uint32_t h = fdiv(in_row, a.nb);
-      const uint32_t j = in_row - h * a.nb.d;
-      const int64_t slot = __ldg(a.slot_mapping + t);
-      if (slot < 0 || slot >= a.num_slots) continue;  // -1 skips; out-of-range slots are never written
-      int64_t page, off;
-      if (a.page_shift >= 0) {
-        page = slot >> a.page_shift;
-        off = slot & (a.P - 1);
-      } else {
-        page = slot / a.P;
-        off = slot - page * a.P;
-      }
-      const int64_t dst_row = ((page * a.n_kv + kv) * a.Hkv + h) * a.P + off;
+  for (int i = 0; i < 4; ++i) x[i] = __ldcs(src + i);
+}
 
-      float f[32];
-      float amax = 0.0f;
+// amax, fp16 scale, codes and scatter of one block whose bf16 values are in x.
+template <int KIND>
+__device__ __forceinline__ void store_block(const StoreArgs& a, int32_t blk, const uint4 (&x)[4]) {
+  const int kv = blk >= a.blocks_per_kv;
+  const uint32_t local = static_cast<uint32_t>(blk - (kv ? a.blocks_per_kv : 0));
+  const uint32_t t = fdiv(local, a.row_blocks);
+  const uint32_t in_row = local - t * a.row_blocks.d;
+  const uint32_t h = fdiv(in_row, a.nb);
+  const uint32_t j = in_row - h * a.nb.d;
+  const int64_t slot = __ldg(a.slot_mapping + t);
+  if (slot < 0 || slot >= a.num_slots) return;  // -1 skips; out-of-range slots are never written
+  int64_t page, off;
+  if (a.page_shift >= 0) {
+    page = slot >> a.page_shift;
+    off = slot & (a.P - 1);
+  } else {
+    page = slot / a.P;
+    off = slot - page * a.P;
+  }
+  const int64_t dst_row = ((page * a.n_kv + kv) * a.Hkv + h) * a.P + off;
+  const uint32_t w[16] = {x[0].x, x[0].y, x[0].z, x[0].w, x[1].x, x[1].y, x[1].z, x[1].w,
+                          x[2].x, x[2].y, x[2].z, x[2].w, x[3].x, x[3].y, x[3].z, x[3].w};
+  // bf16 pair (lo, hi) of word e: lo = w << 16, hi = w & 0xFFFF0000 as fp32 bit patterns
+  float amax = 0.0f;
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const uint32_t w[4] = {x[u][i].x, x[u][i].y, x[u][i].z, x[u][i].w};
+  for (int e = 0; e < 16; ++e)
+    amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(w[e] << 16)), fabsf(__uint_as_float(w[e] & 0xFFFF0000u))));
+  const __half s16 = block_scale<KIND>(amax);
+  const float sf = __half2float(s16);
+  uint32_t o[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+  if (sf != 0.0f) {
+    const float r = __frcp_rn(sf);
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          f[8 * i + 2 * e] = __uint_as_float(w[e] << 16);
-          f[8 * i + 2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u);
-        }
-      }
+    for (int q = 0; q < 8; ++q)  // four elements (two words) per code word
+      o[q] = encode4<KIND>(quotient(__uint_as_float(w[2 * q] << 16), sf, r),
+                           quotient(__uint_as_float(w[2 * q] & 0xFFFF0000u), sf, r),
+                           quotient(__uint_as_float(w[2 * q + 1] << 16), sf, r),
+                           quotient(__uint_as_float(w[2 * q + 1] & 0xFFFF0000u), sf, r));
+  }
+  uint4* dst = reinterpret_cast<uint4*>(a.codes + dst_row * a.D + (static_cast<int64_t>(j) << 5));
+  __stcs(dst, make_uint4(o[0], o[1], o[2], o[3]));
+  __stcs(dst + 1, make_uint4(o[4], o[5], o[6], o[7]));
+  a.scales[dst_row * (a.D >> 5) + j] = (sf != 0.0f) ? s16 : __ushort_as_half(0);
+}
+
+// Persistent grid-stride store: a few CTAs per SM stay resident and every thread loads its next block
+// while it quantizes the current one, so the input stream never waits for a wave of CTAs to finish.
+template <int KIND>
+__global__ void __launch_bounds__(kStoreThreads, kStoreCtasPerSm) store_kernel(StoreArgs a) {
+  const int32_t stride = gridDim.x * kStoreThreads;
+  int32_t blk = blockIdx.x * kStoreThreads + threadIdx.x;
+  if (blk >= a.total) return;
+  uint4 x[4];
+  load_block(a, blk, x);
+  for (; blk < a.total; blk += stride) {
+    uint4 nx[4] = {x[0], x[1], x[2], x[3]};
+    if (blk + stride < a.total) load_block(a, blk + stride, nx);
+    store_block<KIND>(a, blk, x);
 #pragma unroll
-      for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(f[i]));
-      const __half s16 = block_scale<KIND>(amax);
-      const float sf = __half2float(s16);
-      uint4 o0 = make_uint4(0u, 0u, 0u, 0u), o1 = o0;
-      if (sf != 0.0f) {
-        const float r = __frcp_rn(sf);
-        float y[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) y[i] = quotient(f[i], sf, r);
-        o0.x = encode4<KIND>(y[0], y[1], y[2], y[3]);
-        o0.y = encode4<KIND>(y[4], y[5], y[6], y[7]);
-        o0.z = encode4<KIND>(y[8], y[9], y[10], y[11]);
-        o0.w = encode4<KIND>(y[12], y[13], y[14], y[15]);
-        o1.x = encode4<KIND>(y[16], y[17], y[18], y[19]);
-        o1.y = encode4<KIND>(y[20], y[21], y[22], y[23]);
-        o1.z = encode4<KIND>(y[24], y[25], y[26], y[27]);
-        o1.w = encode4<KIND>(y[28], y[29], y[30], y[31]);
-      }
-      uint4* dst = reinterpret_cast<uint4*>(a.codes + dst_row * a.D + (static_cast<int64_t>(j) << 5));
-      __stcs(dst, o0);
-      __stcs(dst + 1, o1);
-      a.scales[dst_row * (a.D >> 5) + j] = (sf != 0.0f) ? s16 : __ushort_as_half(0);
-    }
+    for (int i = 0; i < 4; ++i) x[i] = nx[i];
   }
 }
 
@@ -222,12 +219,12 @@ kvq_status launch_store(void* pool, void* scales, const void* k, const void* v, 
     a.page_shift = page_shift;
     a.P = L.page_size;
     a.num_slots = L.num_pages * L.page_size;
-    int64_t grid = (static_cast<int64_t>(a.total) + kStoreThreads * kStoreUnroll - 1) / (kStoreThreads * kStoreUnroll);
-    grid = std::max<int64_t>(1, std::min<int64_t>(grid, static_cast<int64_t>(sms) * 8));
+    int64_t grid = (static_cast<int64_t>(a.total) + kStoreThreads - 1) / kStoreThreads;
+    grid = std::max<int64_t>(1, std::min<int64_t>(grid, static_cast<int64_t>(sms) * kStoreCtasPerSm));
     if (kind == KVQ_FP8_E4M3)
-      store_kernel<KVQ_FP8_E4M3, kStoreUnroll><<<static_cast<unsigned>(grid), kStoreThreads, 0, stream>>>(a);
+      store_kernel<KVQ_FP8_E4M3><<<static_cast<unsigned>(grid), kStoreThreads, 0, stream>>>(a);
     else
-      store_kernel<KVQ_Q8_0, kStoreUnroll><<<static_cast<unsigned>(grid), kStoreThreads, 0, stream>>>(a);
+      store_kernel<KVQ_Q8_0><<<static_cast<unsigned>(grid), kStoreThreads, 0, stream>>>(a);
     if (cudaGetLastError() != cudaSuccess) return KVQ_ECUDA;
   }
   return KVQ_OK;
