@@ -14,19 +14,20 @@
 // Q, V^T blocks and P use the canonical no-swizzle core-matrix layout (8 rows x 16 bytes per core
 // matrix), so one V^T block written token-major serves as the MN-major A operand.
 //
-// One persistent CTA per SM, 14 warps:
-//   warp 13     producer: per tile, TMA copies of five 128-byte-wide code slabs (d = 0, 128, 256, 384 and
+// One persistent CTA per SM, 26 warps (72 registers each):
+//   warp 25     producer: per tile, TMA copies of five 128-byte-wide code slabs (d = 0, 128, 256, 384 and
 //               448; the last one's upper half is the rope part) into a 3-slot ring, one 2 KB box per
 //               page (128-byte swizzle), and the tile's scales with the first slab.
-//   warps 4-7   K dequant: thread = token; each slab to bf16 in a TMEM slot (two slots).
-//   warps 8-11  V dequant: thread = token; reads its codes of each 128-dim block straight from global
-//               memory (the K pass just brought them into L2), one block ahead in registers, and writes
-//               the bf16 V^T block into one of two shared buffers.
-//   warp 12     MMA issue (one thread): QK slab by slab into S (double-buffered in TMEM), PV block by
+//   warps 8-15  K dequant: thread = (token, half of the slab's dims); each slab to bf16 in a TMEM slot
+//               (two slots).
+//   warps 16-23 V dequant: thread = (token, half of the block's dims); reads its codes of each 128-dim
+//               block straight from global memory (the K pass just brought them into L2), one block
+//               ahead in registers, and writes the bf16 V^T block into one of two shared buffers.
+//   warp 24     MMA issue (one thread): QK slab by slab into S (double-buffered in TMEM), PV block by
 //               block into O; whichever is ready first.
-//   warps 0-3   softmax: thread = token; fp32 online softmax in the exp2 domain with lazy rescaling
-//               (a head's running max moves only when a score exceeds it by 2^8); P to shared memory as
-//               bf16; O rescaled in TMEM when a max moves; the item's partial at its end.
+//   warps 0-7   softmax: thread = (token, 32 of the 64 heads); fp32 online softmax in the exp2 domain
+//               with lazy rescaling (a head's running max moves only when a score exceeds it by 2^8); P
+//               to shared memory as bf16; O rescaled in TMEM when a max moves; the item's partial.
 // TMEM: S[2] 128 columns, O^T 4 x 64, K slots 2 x 64 = 512.  Every wait is bounded (2 s) and reports a
 // timeout in the workspace status word instead of hanging.
 #include <cuda.h>  // CUtensorMap and its enums (the encoder is fetched from the driver at run time)
@@ -60,23 +61,24 @@ constexpr int kMaxBatch = 1024;                    // sequences whose item bases
 constexpr float kLazyRescale = 8.0f;
 constexpr int kTmemCols = 512;
 
-constexpr int kSmWarps = 4;   // 0-3
-constexpr int kKWarp0 = 4;    // 4-7
-constexpr int kVWarp0 = 8;    // 8-11
-constexpr int kMmaWarp = 12;
-constexpr int kProdWarp = 13;
-constexpr int kThreads = 14 * 32;
+constexpr int kSmWarps = 8;   // 0-7: warp w covers TMEM lane quarter w % 4 and heads 32 (w / 4) ..
+constexpr int kKWarp0 = 8;    // 8-15: quarter w % 4, dims 64 ((w - 8) / 4) .. of each slab
+constexpr int kVWarp0 = 16;   // 16-23: quarter w % 4, dims 64 ((w - 16) / 4) .. of each V block
+constexpr int kMmaWarp = 24;
+constexpr int kProdWarp = 25;
+constexpr int kThreads = 26 * 32;  // 72 registers per thread
+constexpr int kHS = kHG / 2;       // query heads per softmax thread
 
 constexpr int RING_OFF = 0;                               // 1024-byte aligned (swizzle atoms)
 constexpr int VT_OFF = RING_OFF + kRing * kSlab;          // 2 x 32 KB
 constexpr int Q_OFF = VT_OFF + 2 * kTile * 128 * 2;       // 72 KB
 constexpr int P_OFF = Q_OFF + kHG * kD * 2;               // 16 KB
 constexpr int SC_OFF = P_OFF + kTile * kHG * 2;           // 2 x 4608
-constexpr int RED_OFF = SC_OFF + 2 * kScTile;             // softmax cross-warp scratch [4][64]
-constexpr int M_OFF = RED_OFF + kSmWarps * kHG * 4;       // running max per head [64]
+constexpr int RED_OFF = SC_OFF + 2 * kScTile;             // softmax cross-warp scratch [8][32]
+constexpr int M_OFF = RED_OFF + kSmWarps * kHS * 4;       // running max per head [64]
 constexpr int A_OFF = M_OFF + kHG * 4;                    // rescale factor per head [64]
-constexpr int FLAG_OFF = A_OFF + kHG * 4;                 // 4 votes
-constexpr int VAL_OFF = FLAG_OFF + 16;                    // [2][128] token validity by tile parity
+constexpr int FLAG_OFF = A_OFF + kHG * 4;                 // one vote per softmax warp
+constexpr int VAL_OFF = FLAG_OFF + kSmWarps * 4;          // [2][128] token validity by tile parity
 constexpr int META_OFF = VAL_OFF + 2 * kTile;             // [kRing][8] valid tokens per page
 constexpr int TAB_OFF = META_OFF + kRing * kPagesPerTile * 4;
 constexpr int NBARS = 18 + 2 * kRing;
@@ -278,18 +280,18 @@ __global__ void __launch_bounds__(mla::kThreads, 1) decode_mla_kernel(const KPar
       run += groups * ((seq_pages(p, b) + C - 1) / C);
     }
     for (int b = 0; b < 2; ++b) {
-      mbar_init(&bar_k_full[b], 4);
+      mbar_init(&bar_k_full[b], 8);
       mbar_init(&bar_k_free[b], 1);
       mbar_init(&bar_qk_done[b], 1);
       mbar_init(&bar_p_full[b], kSmWarps);
-      mbar_init(&bar_v_full[b], 4);
+      mbar_init(&bar_v_full[b], 8);
       mbar_init(&bar_v_free[b], 1);
       mbar_init(&bar_pv_done[b], 1);
-      mbar_init(&bar_sc_free[b], 4);
+      mbar_init(&bar_sc_free[b], 8);
     }
     for (int s = 0; s < kRing; ++s) {
       mbar_init(&bar_full[s], 1);
-      mbar_init(&bar_empty[s], 4);
+      mbar_init(&bar_empty[s], 8);
     }
     fence_mbar_init();
   }
@@ -365,9 +367,11 @@ __global__ void __launch_bounds__(mla::kThreads, 1) decode_mla_kernel(const KPar
       const uint32_t u = uses - j;
       (void)mbar_wait_bounded(&bar_full[u % kRing], (u / kRing) & 1);
     }
-  } else if (warp >= kKWarp0 && warp < kKWarp0 + 4) {
+  } else if (warp >= kKWarp0 && warp < kKWarp0 + 8) {
     // ===================================================================== K dequant
-    const int tt = tid - kKWarp0 * 32;  // token slot = TMEM lane
+    const int kt = tid - kKWarp0 * 32;  // 0 .. 255
+    const int tt = kt & (kTile - 1);    // token slot = TMEM lane
+    const int part = kt >> 7;           // which 64 dims of each slab
     const int pi = tt / kPage, off = tt % kPage, swz = off & 7;
     MlaIter t;
     mla_first(t, sTab, p, C, n_items);
@@ -378,7 +382,7 @@ __global__ void __launch_bounds__(mla::kThreads, 1) decode_mla_kernel(const KPar
         if (n >= 1 && !mbar_wait_bounded(&bar_qk_done[(n - 1) & 1], ((n - 1) >> 1) & 1)) { ok = false; break; }
         const __nv_bfloat16* qb = p.q + (static_cast<int64_t>(t.b) * p.num_q_heads + t.hg * HP) * kD;
 #pragma unroll 4
-        for (int idx = tt; idx < kHG * (kD / 8); idx += 128) {
+        for (int idx = kt; idx < kHG * (kD / 8); idx += 256) {
           const int h = idx % kHG, d8 = idx / kHG;
           if (h >= HP) continue;  // padding rows stay zero
           const uint4 v = __ldg(reinterpret_cast<const uint4*>(qb + static_cast<int64_t>(h) * kD + d8 * 8));
@@ -397,13 +401,16 @@ __global__ void __launch_bounds__(mla::kThreads, 1) decode_mla_kernel(const KPar
           v_ok = off < sMeta[rs * kPagesPerTile + pi];
           // the validity slot of this tile parity was last read by the softmax of tile n - 2
           if (n >= 2 && !mbar_wait_bounded(&bar_p_full[n & 1], ((n >> 1) - 1) & 1)) { ok = false; break; }
-          sValid[(n & 1) * kTile + tt] = v_ok ? 1 : 0;  // published with sc_free after the last slab
+          if (part == 0) sValid[(n & 1) * kTile + tt] = v_ok ? 1 : 0;  // published with sc_free (last slab)
         }
         if (u >= 2 && !mbar_wait_bounded(&bar_k_free[ks], ((u >> 1) - 1) & 1)) { ok = false; break; }
         const uint8_t* slot = sRing + rs * kSlab + pi * kBox + off * 128;
-        const int c0 = (j < 4) ? 0 : 4;  // the rope slab keeps its upper half only (d = 512..575)
+        // 32 codes (one scale) -> 16 TMEM columns; a part takes chunk pairs 2 part, 2 part + 1 of a latent
+        // slab, and of the rope slab (whose upper half, d = 512..575, is all that is used) pair 2 + part
+        const int c2a = (j < 4) ? 2 * part : 2 + part;
+        const int c2b = (j < 4) ? 2 * part + 2 : 3 + part;
 #pragma unroll 1
-        for (int c2 = c0 / 2; c2 < 4; ++c2) {  // 32 codes (one scale) -> 16 TMEM columns
+        for (int c2 = c2a; c2 < c2b; ++c2) {
           uint32_t w[16];
           const int blk = (j < 4 ? 4 * j : 14) + c2;  // scale block of these 32 dims
 #pragma unroll
@@ -434,25 +441,28 @@ __global__ void __launch_bounds__(mla::kThreads, 1) decode_mla_kernel(const KPar
       mla_next(t, sTab, p, C, n_items);
       ++n;
     }
-  } else if (warp >= kVWarp0 && warp < kVWarp0 + 4) {
+  } else if (warp >= kVWarp0 && warp < kVWarp0 + 8) {
     // ===================================================================== V dequant
-    const int tt = tid - kVWarp0 * 32;
+    const int vt = tid - kVWarp0 * 32;  // 0 .. 255
+    const int tt = vt & (kTile - 1);
+    const int part = vt >> 7;           // which 64 dims of each V block
     const int pi = tt / kPage, off = tt % kPage;
-    const uint32_t voff = (tt % 8) * 16 + (tt / 8) * kVRS;
+    const uint32_t voff = (tt % 8) * 16 + (tt / 8) * kVRS + part * 8 * 128;
     MlaIter t;
     mla_first(t, sTab, p, C, n_items);
-    // codes and scales of V block c of the tile whose page for this token is `phys` (-1: zeros)
-    uint4 nxt[8];
-    uint2 nxt_s = make_uint2(0, 0);
+    // codes and the two scales of this part of V block c of the tile whose page for this token is
+    // `phys` (-1: zeros)
+    uint4 nxt[4];
+    uint32_t nxt_s = 0;
     auto fetch = [&](int32_t phys, int c) {
       if (phys < 0) return;
       const int64_t row = static_cast<int64_t>(phys) * kPage + off;
-      const uint4* src = reinterpret_cast<const uint4*>(p.codes + row * kD + c * 128);
+      const uint4* src = reinterpret_cast<const uint4*>(p.codes + row * kD + c * 128 + part * 64);
 #pragma unroll
-      for (int k = 0; k < 8; ++k) nxt[k] = __ldg(src + k);
-      // a row's scales start 36 bytes apart: two 4-byte loads (8-byte alignment is not guaranteed)
-      const uint32_t* ss = reinterpret_cast<const uint32_t*>(reinterpret_cast<const uint16_t*>(p.scales) + row * kNB + c * 4);
-      nxt_s = make_uint2(__ldg(ss), __ldg(ss + 1));
+      for (int k = 0; k < 4; ++k) nxt[k] = __ldg(src + k);
+      // a row's scales start 36 bytes apart: a 4-byte load is always aligned
+      nxt_s = __ldg(reinterpret_cast<const uint32_t*>(reinterpret_cast<const uint16_t*>(p.scales) + row * kNB + c * 4 +
+                                                      part * 2));
     };
     int32_t phys = mla_phys(p, t, pi, off);
     fetch(phys, 0);
@@ -463,23 +473,21 @@ __global__ void __launch_bounds__(mla::kThreads, 1) decode_mla_kernel(const KPar
       const int32_t phys_n = mla_phys(p, tn, pi, off);
 #pragma unroll 1
       for (int c = 0; c < kVBlocks; ++c, ++nb) {
-        uint4 cur[8];
+        uint4 cur[4];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) cur[k] = nxt[k];
-        const uint2 cs = nxt_s;
+        for (int k = 0; k < 4; ++k) cur[k] = nxt[k];
+        const uint32_t cs = nxt_s;
         const bool v_ok = phys >= 0;
         if (c + 1 < kVBlocks) fetch(phys, c + 1);
         else fetch(phys_n, 0);
         const int vb = nb & 1;
         if (nb >= 2 && !mbar_wait_bounded(&bar_v_free[vb], ((nb >> 1) - 1) & 1)) { ok = false; break; }
         uint8_t* dst = sVt + vb * (kTile * 128 * 2) + voff;
-        const uint16_t scs[4] = {static_cast<uint16_t>(cs.x), static_cast<uint16_t>(cs.x >> 16),
-                                 static_cast<uint16_t>(cs.y), static_cast<uint16_t>(cs.y >> 16)};
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
+        for (int k = 0; k < 4; ++k) {
           uint32_t w[8];
           if (v_ok) {
-            dequant16<KIND>(cur[k], scs[k >> 1], w);
+            dequant16<KIND>(cur[k], static_cast<uint16_t>((k & 2) ? (cs >> 16) : cs), w);
           } else {
 #pragma unroll
             for (int e = 0; e < 8; ++e) w[e] = 0u;
@@ -584,16 +592,18 @@ __global__ void __launch_bounds__(mla::kThreads, 1) decode_mla_kernel(const KPar
     if (nq > np) (void)mbar_wait_bounded(&bar_qk_done[(nq - 1) & 1], ((nq - 1) >> 1) & 1);
   } else {
     // ===================================================================== softmax warps
-    const int tt = tid;  // token slot / TMEM lane; in the epilogue, the dim within an O^T block
+    // Warp w: TMEM lane quarter w % 4 (its tokens; in the epilogue, dims), heads h0 .. h0 + 31.
+    const int tt = tid & (kTile - 1);
+    const int h0 = (warp >> 2) * kHS;
     uint32_t n = 0;  // tiles
     for (int32_t item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
       MlaIter t;
       t.item = item;
       t.live = true;
       mla_load_item(t, sTab, p, C);
-      float l_t[kHG];
+      float l_t[kHS];
 #pragma unroll
-      for (int h = 0; h < kHG; ++h) l_t[h] = 0.0f;
+      for (int h = 0; h < kHS; ++h) l_t[h] = 0.0f;
       bool o_live = false;
       for (; t.i < t.ntiles && ok; ++t.i, ++n) {
         const int b = n & 1;
@@ -603,55 +613,60 @@ __global__ void __launch_bounds__(mla::kThreads, 1) decode_mla_kernel(const KPar
         if (!mbar_wait_bounded(&bar_sc_free[b], (n >> 1) & 1)) { ok = false; break; }
         mla_fence_after();
         const bool valid = sValid[b * kTile + tt] != 0;
-        const uint32_t s_base = tS + b * 64 + lane_base;
+        const uint32_t s_base = tS + b * 64 + h0 + lane_base;
         // does any score of the tile move its head's running max?  (one vote per warp, one barrier)
         bool moved = false;
 #pragma unroll 1
-        for (int g = 0; g < 4; ++g) {
+        for (int g = 0; g < kHS / 16; ++g) {
           float s[16];
           mla_ld16(s_base + g * 16, s);
 #pragma unroll
           for (int h = 0; h < 16; ++h) {
-            const float m = sM[g * 16 + h];
-            const float x = (valid && g * 16 + h < HP) ? s[h] * p.score_scale : -INFINITY;
+            const int hd = h0 + g * 16 + h;
+            const float m = sM[hd];
+            const float x = (valid && hd < HP) ? s[h] * p.score_scale : -INFINITY;
             moved |= (x > -INFINITY) && (m == -INFINITY || x > m + kLazyRescale);
           }
         }
         const int wv = __any_sync(0xffffffffu, moved);
         if (lane == 0) sFlag[warp] = wv;
         mla_named_sync(1, kSmWarps * 32);
-        const bool any_moved = (sFlag[0] | sFlag[1] | sFlag[2] | sFlag[3]) != 0;
+        int fl = 0;
+#pragma unroll
+        for (int w = 0; w < kSmWarps; ++w) fl |= sFlag[w];
+        const bool any_moved = fl != 0;
         bool rescale = false;
         if (any_moved) {  // uniform branch: exact tile maxima, new running maxima, rescale factors
           mla_named_sync(1, kSmWarps * 32);  // sFlag has been read by every warp
 #pragma unroll 1
-          for (int g = 0; g < 4; ++g) {
+          for (int g = 0; g < kHS / 16; ++g) {
             float s[16];
             mla_ld16(s_base + g * 16, s);
 #pragma unroll
             for (int h = 0; h < 16; ++h) {
-              float mx = (valid && g * 16 + h < HP) ? s[h] * p.score_scale : -INFINITY;
+              float mx = (valid && h0 + g * 16 + h < HP) ? s[h] * p.score_scale : -INFINITY;
 #pragma unroll
               for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-              if (lane == 0) sRed[warp * kHG + g * 16 + h] = mx;
+              if (lane == 0) sRed[warp * kHS + g * 16 + h] = mx;
             }
           }
           mla_named_sync(1, kSmWarps * 32);
-          if (tt < kHG) {
-            float mx = sRed[tt];
+          if (tid < kHG) {  // thread tid updates head tid: the four warps of its half hold its maxima
+            const int half = tid / kHS, idx = tid % kHS;
+            float mx = -INFINITY;
 #pragma unroll
-            for (int w = 1; w < kSmWarps; ++w) mx = fmaxf(mx, sRed[w * kHG + tt]);
-            const float m = sM[tt];
+            for (int w = 0; w < 4; ++w) mx = fmaxf(mx, sRed[(half * 4 + w) * kHS + idx]);
+            const float m = sM[tid];
             float a = 1.0f;
             if (mx > -INFINITY && (m == -INFINITY || mx > m + kLazyRescale)) {
               if (m != -INFINITY) a = exp2f(m - mx);
-              sM[tt] = mx;
+              sM[tid] = mx;
             }
-            sA[tt] = a;
+            sA[tid] = a;
           }
           mla_named_sync(1, kSmWarps * 32);
 #pragma unroll
-          for (int h = 0; h < kHG; ++h) rescale |= sA[h] != 1.0f;
+          for (int h = 0; h < kHS; ++h) rescale |= sA[h0 + h] != 1.0f;
         }
         mla_named_sync(1, kSmWarps * 32);  // sFlag / sRed are rewritten next tile
         // P is single-buffered: the previous tile's PV must be complete before it is rewritten (and
@@ -662,20 +677,20 @@ __global__ void __launch_bounds__(mla::kThreads, 1) decode_mla_kernel(const KPar
 #pragma unroll 1
           for (int c = 0; c < kVBlocks; ++c) {
 #pragma unroll 1
-            for (int g = 0; g < 4; ++g) {
+            for (int g = 0; g < kHS / 16; ++g) {
               float o[16];
-              mla_ld16(tO + c * 64 + g * 16 + lane_base, o);
+              mla_ld16(tO + c * 64 + h0 + g * 16 + lane_base, o);
               uint32_t r[16];
 #pragma unroll
-              for (int h = 0; h < 16; ++h) r[h] = __float_as_uint(o[h] * sA[g * 16 + h]);
-              mla_st16(tO + c * 64 + g * 16 + lane_base, r);
+              for (int h = 0; h < 16; ++h) r[h] = __float_as_uint(o[h] * sA[h0 + g * 16 + h]);
+              mla_st16(tO + c * 64 + h0 + g * 16 + lane_base, r);
             }
           }
           asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
         }
-        // P row of this token (bf16) and the row sums of exactly those bf16 values
+        // P row of this token for heads h0 .. h0 + 31 (bf16) and the row sums of exactly those values
 #pragma unroll
-        for (int g = 0; g < 4; ++g) {
+        for (int g = 0; g < kHS / 16; ++g) {
           float s[16];
           mla_ld16(s_base + g * 16, s);
           uint32_t pw[8];
@@ -684,21 +699,22 @@ __global__ void __launch_bounds__(mla::kThreads, 1) decode_mla_kernel(const KPar
             float pr[2];
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
-              const int h = g * 16 + 2 * h2 + e;
-              const float m = sM[h];
-              const float x = (valid && h < HP) ? s[2 * h2 + e] * p.score_scale : -INFINITY;
+              const int hd = h0 + g * 16 + 2 * h2 + e;
+              const float m = sM[hd];
+              const float x = (valid && hd < HP) ? s[2 * h2 + e] * p.score_scale : -INFINITY;
               pr[e] = (x == -INFINITY || m == -INFINITY) ? 0.0f : exp2f(x - m);
             }
             pw[h2] = pack_bf16x2(pr[0], pr[1]);
             const float2 pb = unpack_bf16x2(pw[h2]);
             const int h = g * 16 + 2 * h2;
-            const float a0 = any_moved ? sA[h] : 1.0f, a1 = any_moved ? sA[h + 1] : 1.0f;
+            const float a0 = any_moved ? sA[h0 + h] : 1.0f, a1 = any_moved ? sA[h0 + h + 1] : 1.0f;
             l_t[h] = fmaf(l_t[h], a0, pb.x);
             l_t[h + 1] = fmaf(l_t[h + 1], a1, pb.y);
           }
-          *reinterpret_cast<uint4*>(sP + (tt % 8) * 16 + (tt / 8) * 128 + (2 * g) * kPS) =
+          const int hg8 = (h0 + g * 16) / 8;  // 8-head group of pw[0..3]
+          *reinterpret_cast<uint4*>(sP + (tt % 8) * 16 + (tt / 8) * 128 + hg8 * kPS) =
               make_uint4(pw[0], pw[1], pw[2], pw[3]);
-          *reinterpret_cast<uint4*>(sP + (tt % 8) * 16 + (tt / 8) * 128 + (2 * g + 1) * kPS) =
+          *reinterpret_cast<uint4*>(sP + (tt % 8) * 16 + (tt / 8) * 128 + (hg8 + 1) * kPS) =
               make_uint4(pw[4], pw[5], pw[6], pw[7]);
         }
         o_live = true;
@@ -715,31 +731,34 @@ __global__ void __launch_bounds__(mla::kThreads, 1) decode_mla_kernel(const KPar
 #pragma unroll 1
       for (int c = 0; c < kVBlocks; ++c) {
 #pragma unroll 1
-        for (int g = 0; g < 4; ++g) {
+        for (int g = 0; g < kHS / 16; ++g) {
           float o[16];
-          mla_ld16(tO + c * 64 + g * 16 + lane_base, o);
+          mla_ld16(tO + c * 64 + h0 + g * 16 + lane_base, o);
 #pragma unroll
-          for (int h = 0; h < 16; ++h)
-            if (g * 16 + h < HP) acc[static_cast<int64_t>(g * 16 + h) * kDV + c * 128 + tt] = o[h];
+          for (int h = 0; h < 16; ++h) {
+            const int hd = h0 + g * 16 + h;
+            if (hd < HP) acc[static_cast<int64_t>(hd) * kDV + c * 128 + tt] = o[h];
+          }
         }
       }
 #pragma unroll
-      for (int h = 0; h < kHG; ++h) {
+      for (int h = 0; h < kHS; ++h) {
         float v = l_t[h];
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-        if (lane == 0) sRed[warp * kHG + h] = v;
+        if (lane == 0) sRed[warp * kHS + h] = v;
       }
       mla_named_sync(1, kSmWarps * 32);
-      if (tt < kHG) {
-        if (tt < HP) {
+      if (tid < kHG) {
+        if (tid < HP) {
+          const int half = tid / kHS, idx = tid % kHS;
           float lsum = 0.0f;
 #pragma unroll
-          for (int w = 0; w < kSmWarps; ++w) lsum += sRed[w * kHG + tt];
-          p.part_ml[(static_cast<int64_t>(item) * HP + tt) * 2 + 0] = sM[tt];
-          p.part_ml[(static_cast<int64_t>(item) * HP + tt) * 2 + 1] = lsum;
+          for (int w = 0; w < 4; ++w) lsum += sRed[(half * 4 + w) * kHS + idx];
+          p.part_ml[(static_cast<int64_t>(item) * HP + tid) * 2 + 0] = sM[tid];
+          p.part_ml[(static_cast<int64_t>(item) * HP + tid) * 2 + 1] = lsum;
         }
-        sM[tt] = -INFINITY;  // the next item starts afresh
+        sM[tid] = -INFINITY;  // the next item starts afresh
       }
       mla_fence_before();
       mla_named_sync(1, kSmWarps * 32);
