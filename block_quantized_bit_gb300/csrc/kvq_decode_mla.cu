@@ -23,8 +23,8 @@
 //   warps 16-23 V dequant: thread = (token, half of the block's dims); reads its codes of each 128-dim
 //               block straight from global memory (the K pass just brought them into L2), one block
 //               ahead in registers, and writes the bf16 V^T block into one of two shared buffers.
-//   warp 24     MMA issue (one thread): QK slab by slab into S (double-buffered in TMEM), PV block by
-//               block into O; whichever is ready first.
+//   warp 24     MMA issue (one elected lane): QK slab by slab into S (double-buffered in TMEM), PV
+//               block by block into O; whichever is ready first.
 //   warps 0-7   softmax: thread = (token, 32 of the 64 heads); fp32 online softmax in the exp2 domain
 //               with lazy rescaling (a head's running max moves only when a score exceeds it by 2^8); P
 //               to shared memory as bf16; O rescaled in TMEM when a max moves; the item's partial.
@@ -111,10 +111,14 @@ __device__ __forceinline__ uint32_t mla_idesc(bool a_mn_major, bool b_mn_major) 
   return d;
 }
 
+// Warp-collective MMA and commit: all 32 lanes of the converged MMA warp call them with the same operands
+// and the lane chosen by elect.sync issues (the descriptors stay in uniform registers, which a probe measured
+// at 15 to 40 clocks per MMA against 56 from a lane-0 branch).  The full mask elects the same lane every
+// time, so a commit tracks every MMA issued before it.
 __device__ __forceinline__ void mla_mma_ss(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
   asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "{\n\t.reg .pred p, e;\n\tsetp.ne.b32 p, %4, 0;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(a), "l"(b), "r"(idesc), "r"(acc)
       : "memory");
 }
@@ -122,15 +126,17 @@ __device__ __forceinline__ void mla_mma_ss(uint32_t d_tmem, uint64_t a, uint64_t
 __device__ __forceinline__ void mla_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc,
                                            uint32_t acc) {
   asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "{\n\t.reg .pred p, e;\n\tsetp.ne.b32 p, %4, 0;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
       "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc)
       : "memory");
 }
 
 __device__ __forceinline__ void mla_commit(uint64_t* bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
-               : "memory");
+  asm volatile(
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(smem_u32(bar))
+      : "memory");
 }
 
 __device__ __forceinline__ void mla_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
@@ -504,7 +510,7 @@ __global__ void __launch_bounds__(mla::kThreads, 1) decode_mla_kernel(const KPar
       phys = phys_n;
     }
   } else if (warp == kMmaWarp) {
-    // ===================================================================== MMA issue (lane 0)
+    // ===================================================================== MMA issue (elected lane)
     const uint32_t idesc_qk = mla_idesc(false, false);
     const uint32_t idesc_pv = mla_idesc(true, true);
     const uint64_t dQ = mla_desc(smem_u32(sQ), 128, kQS);
@@ -527,15 +533,13 @@ __global__ void __launch_bounds__(mla::kThreads, 1) decode_mla_kernel(const KPar
                   mbar_test_wait(&bar_v_full[vb], (nb >> 1) & 1);
         if (__shfl_sync(0xffffffffu, ready, 0)) {
           mla_fence_after();
-          if (lane == 0) {
-            const uint64_t dV = dV0 + static_cast<uint64_t>((vb * kTile * 128 * 2) >> 4);
+          const uint64_t dV = dV0 + static_cast<uint64_t>((vb * kTile * 128 * 2) >> 4);
 #pragma unroll
-            for (int ks = 0; ks < kTile / 16; ++ks)
-              mla_mma_ss(tO + cp * 64, dV + static_cast<uint64_t>((ks * 2 * kVRS) >> 4),
-                         dP + static_cast<uint64_t>((ks * 2 * 128) >> 4), idesc_pv, (tp.i > 0 || ks > 0) ? 1u : 0u);
-            mla_commit(&bar_v_free[vb]);
-            if (cp == kVBlocks - 1) mla_commit(&bar_pv_done[np & 1]);
-          }
+          for (int ks = 0; ks < kTile / 16; ++ks)
+            mla_mma_ss(tO + cp * 64, dV + static_cast<uint64_t>((ks * 2 * kVRS) >> 4),
+                       dP + static_cast<uint64_t>((ks * 2 * 128) >> 4), idesc_pv, (tp.i > 0 || ks > 0) ? 1u : 0u);
+          mla_commit(&bar_v_free[vb]);
+          if (cp == kVBlocks - 1) mla_commit(&bar_pv_done[np & 1]);
           __syncwarp();
           if (++cp == kVBlocks) {
             cp = 0;
@@ -554,22 +558,20 @@ __global__ void __launch_bounds__(mla::kThreads, 1) decode_mla_kernel(const KPar
                   (jq > 0 || nq < 2 || mbar_test_wait(&bar_p_full[nq & 1], ((nq >> 1) - 1) & 1));
         if (__shfl_sync(0xffffffffu, ready, 0)) {
           mla_fence_after();
-          if (lane == 0) {
-            const uint32_t d_s = tS + (nq & 1) * 64;
-            const uint32_t a0 = tK + ks * 64;
-            if (jq < 4) {
+          const uint32_t d_s = tS + (nq & 1) * 64;
+          const uint32_t a0 = tK + ks * 64;
+          if (jq < 4) {
 #pragma unroll
-              for (int k = 0; k < 8; ++k)
-                mla_mma_ts(d_s, a0 + k * 8, dQ + static_cast<uint64_t>(((16 * jq + 2 * k) * 128) >> 4), idesc_qk,
-                           (jq > 0 || k > 0) ? 1u : 0u);
-            } else {
+            for (int k = 0; k < 8; ++k)
+              mla_mma_ts(d_s, a0 + k * 8, dQ + static_cast<uint64_t>(((16 * jq + 2 * k) * 128) >> 4), idesc_qk,
+                         (jq > 0 || k > 0) ? 1u : 0u);
+          } else {
 #pragma unroll
-              for (int k = 4; k < 8; ++k)  // dims 512..575 sit in the upper half of the slot
-                mla_mma_ts(d_s, a0 + k * 8, dQ + static_cast<uint64_t>(((64 + 2 * (k - 4)) * 128) >> 4), idesc_qk, 1u);
-            }
-            mla_commit(&bar_k_free[ks]);
-            if (jq == kSlabs - 1) mla_commit(&bar_qk_done[nq & 1]);
+            for (int k = 4; k < 8; ++k)  // dims 512..575 sit in the upper half of the slot
+              mla_mma_ts(d_s, a0 + k * 8, dQ + static_cast<uint64_t>(((64 + 2 * (k - 4)) * 128) >> 4), idesc_qk, 1u);
           }
+          mla_commit(&bar_k_free[ks]);
+          if (jq == kSlabs - 1) mla_commit(&bar_qk_done[nq & 1]);
           __syncwarp();
           if (++jq == kSlabs) {
             jq = 0;

@@ -14,11 +14,12 @@
 // descriptor LBO = RS (token groups) and SBO = 128 (8-dim groups); Q uses the same form, K-major.
 // The K tile lives in tensor memory (lane = token, two bf16 per column), double-buffered.
 //
-// One persistent CTA per SM, 14 warps (at most 4 per SM sub-partition):
-//   warp 13     producer: one lane per page of a tile reads the block table and issues TMA copies of
-//               the page's codes (a 5-D tensor map over the pool, one 4 KB box = 16 tokens x 128 code
-//               bytes of K and of V, stored with the 128-byte swizzle) and 1-D bulk copies of its K and V
-//               scales into a multi-stage staging ring; the tile's valid-token counts go with it.
+// One persistent CTA per SM, 15 warps (at most 4 per SM sub-partition):
+//   warps 13-14 producers, one for K and one for V: one lane per page of a tile reads the block table
+//               and issues TMA copies of the page's codes (a 5-D tensor map over the pool, one 2 KB box
+//               = 16 tokens x 128 code bytes, stored with the 128-byte swizzle) and a 1-D bulk copy of
+//               its scales into that producer's multi-stage staging ring; the tile's valid-token counts
+//               go with it.
 //   warps 4-11  dequant: each thread owns half of a token row.  It reads its codes from the swizzled
 //               staging rows (bank-conflict free: the 16-byte chunk index is XORed with token % 8),
 //               dequantizes them exactly as on the CUDA-core path, K into tensor memory, V into shared.
@@ -116,6 +117,18 @@ __device__ __forceinline__ void tmem_st16u(uint32_t taddr, const uint32_t (&r)[1
       "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
       "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
       : "memory");
+}
+
+// This thread's NBT (<= 4) block scales of a staged row, in one load: 16 bits each, lowest first.  A
+// 2-byte load per scale would hit each bank four times (the token rows are 16 bytes apart).
+template <int NBT>
+__device__ __forceinline__ uint64_t load_scales(const uint8_t* p) {
+  static_assert(NBT == 2 || NBT == 4, "scale blocks per dequant thread");
+  if (NBT == 4) {
+    const uint2 v = *reinterpret_cast<const uint2*>(p);
+    return static_cast<uint64_t>(v.x) | (static_cast<uint64_t>(v.y) << 32);
+  }
+  return *reinterpret_cast<const uint32_t*>(p);
 }
 
 __device__ __forceinline__ void mma_bf16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc,
@@ -449,7 +462,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const KParams p,
         if (!mbar_wait_bounded(&bar_full[ring], (nk / Cfg::STAGES) & 1)) { ok = false; break; }
         const uint8_t* slot = sKr + ring * Cfg::SLOT_BYTES;
         const bool v_ok = off < sMeta[ring * kPagesPerTile + pi];
-        const uint16_t* sc = reinterpret_cast<const uint16_t*>(slot + sc_off);
+        const uint64_t scw = load_scales<Cfg::NBT>(slot + sc_off);
         // the buffer was last read by the QK of tile nk - 2
         if (nk >= 2 && !mbar_wait_bounded(&bar_qk_done[kb], ((nk >> 1) - 1) & 1)) { ok = false; break; }
         if (tk.i == 0) {
@@ -479,7 +492,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const KParams p,
 #pragma unroll 1
         for (int k2 = 0; k2 < Cfg::NCH_T / 2; ++k2) {  // 32 codes (one scale) -> 16 TMEM columns per tcgen05.st
           uint32_t w[16];
-          const uint16_t s_k = sc[k2];
+          const uint16_t s_k = static_cast<uint16_t>(scw >> (16 * k2));
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
             const int k = 2 * k2 + h;
@@ -512,7 +525,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const KParams p,
         if (!mbar_wait_bounded(&bar_full[ring], (nv / Cfg::STAGES) & 1)) { ok = false; break; }
         const uint8_t* slot = sVr + (nv % Cfg::STAGES) * Cfg::SLOT_BYTES;
         const bool v_ok = off < sMeta[ring * kPagesPerTile + pi];
-        const uint16_t* sc = reinterpret_cast<const uint16_t*>(slot + sc_off);
+        const uint64_t scw = load_scales<Cfg::NBT>(slot + sc_off);
         // the previous PV must have read this thread's rows of the V tile (with two O^T slices, part 0
         // writes exactly the dims of slice 0)
         if (nv >= 1) {
@@ -523,7 +536,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const KParams p,
         for (int k = 0; k < Cfg::NCH_T; ++k) {
           uint32_t w[8];
           if (v_ok) {
-            dequant16<KIND>(*chunk_addr(slot, k), sc[k >> 1], w);
+            dequant16<KIND>(*chunk_addr(slot, k), static_cast<uint16_t>(scw >> (16 * (k >> 1))), w);
           } else {
 #pragma unroll
             for (int e = 0; e < 8; ++e) w[e] = 0u;
