@@ -63,7 +63,7 @@ struct WorkspacePlan {
   int32_t heads_per_item;
   int32_t query_groups;
   int64_t max_items;
-  size_t acc_offset, ml_offset, tab_offset, total;
+  size_t cnt_offset, acc_offset, ml_offset, tab_offset, total;
 };
 
 // 1 = CUDA-core kernel, 2 = tensor-core kernel, -1 = the requested path has no kernel for this shape.
@@ -102,7 +102,10 @@ bool plan_workspace(const kvq_layout& L, int32_t batch, int32_t num_q_heads, int
   w->max_items = max_work_items(batch, w->query_groups, max_pages, pps, w->target_items);
   const size_t acc = static_cast<size_t>(w->max_items) * w->heads_per_item * L.v_dim * sizeof(float);
   const size_t ml = static_cast<size_t>(w->max_items) * w->heads_per_item * 2 * sizeof(float);
-  w->acc_offset = kWorkspaceHeader;
+  // split counters of the fused merge (CUDA-core path) follow the header: one memset clears both
+  const size_t cnt = static_cast<size_t>(batch) * w->query_groups * sizeof(int32_t);
+  w->cnt_offset = kWorkspaceHeader;
+  w->acc_offset = w->cnt_offset + ((cnt + 255) / 256) * 256;
   w->ml_offset = w->acc_offset + ((acc + 255) / 256) * 256;
   w->tab_offset = w->ml_offset + ((ml + 255) / 256) * 256;
   const size_t tab = static_cast<size_t>(batch) * 2 * sizeof(int32_t);
@@ -261,14 +264,17 @@ kvq_status kvq_decode_ex(const void* q, const void* pool, const void* scales, co
   a.part_acc = reinterpret_cast<float*>(ws + w.acc_offset);
   a.part_ml = reinterpret_cast<float*>(ws + w.ml_offset);
   a.plan_tab = reinterpret_cast<int32_t*>(ws + w.tab_offset);
+  a.split_cnt = (w.path == 1) ? reinterpret_cast<int32_t*>(ws + w.cnt_offset) : nullptr;
   a.max_items = w.max_items;
   a.heads_per_item = w.heads_per_item;
   a.split_align = w.split_align;
   a.target_items = w.target_items;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (cudaMemsetAsync(ws, 0, sizeof(uint32_t), s) != cudaSuccess) return KVQ_ECUDA;
+  // status word and split counters (the counters only on the CUDA-core path, which merges in-kernel)
+  const size_t clear = (w.path == 1) ? w.acc_offset : sizeof(uint32_t);
+  if (cudaMemsetAsync(ws, 0, clear, s) != cudaSuccess) return KVQ_ECUDA;
   if (w.path == 2) st = a.mla ? launch_decode_mla_tc(a, s) : launch_decode_tc(a, s);
-  else st = launch_decode_cc(a, s);
+  else return launch_decode_cc(a, s);
   if (st != KVQ_OK) return st;
   return launch_merge(a, w.query_groups, s);
 }

@@ -14,7 +14,10 @@
 // STAGES-deep pipeline of 1-D bulk copies (codes and scales of the page's K and V chunks into shared
 // memory, completion on an mbarrier).  Lanes read 16-byte code chunks, dequantize to bf16-exact fp32,
 // and run the fp32 online softmax in the exp2 domain; the CTA combines its warps and writes one
-// (m, l, acc) partial per query head.  The merge kernel combines the partials of a (b, qg).
+// (m, l, acc) partial per query head.  The CTA that finishes the last split of a (b, qg) merges the
+// group's partials itself (a split counter in the workspace), so this path needs no merge launch; a
+// group with one split writes its output directly.  The merge kernel below combines the partials of
+// the tensor-core kernels.
 #include <math.h>
 
 #include <algorithm>
@@ -102,6 +105,14 @@ __device__ __forceinline__ float reduce_heads(float (&v)[GT], int lane) {
 #pragma unroll
   for (int o = LPT >> (LG + 1); o >= 1; o >>= 1) r += __shfl_xor_sync(0xffffffffu, r, o);
   return r;
+}
+
+// One element of the decode output, bf16 (round to nearest-even) or fp32.
+__device__ __forceinline__ void store_out(const KParams& p, int64_t idx, float v) {
+  if (p.out_f32)
+    static_cast<float*>(p.out)[idx] = v;
+  else
+    static_cast<__nv_bfloat16*>(p.out)[idx] = __float2bfloat16_rn(v);
 }
 
 template <int D, int DV, int GT, int KIND, bool MLA, int WARPS, int STAGES, int MINB>
@@ -370,6 +381,7 @@ __global__ void __launch_bounds__(WARPS * 32, MINB) decode_cc_kernel(KParams p) 
   }
   __syncthreads();
   const int64_t item = blockIdx.x;
+  const bool only_split = (plan.nsplit == 1) && (p.split_cnt != nullptr);
   for (int idx = tid; idx < GT * DV; idx += WARPS * 32) {
     const int h = idx / DV, d = idx - h * DV;
     float M = -INFINITY;
@@ -386,11 +398,89 @@ __global__ void __launch_bounds__(WARPS * 32, MINB) decode_cc_kernel(KParams p) 
         lsum = fmaf(cl[w * GT + h], wgt, lsum);
       }
     }
+    if (only_split) {  // the group's only split: its normalised output, no partial
+      store_out(p, (static_cast<int64_t>(b) * p.num_q_heads + head0 + h) * DV + d, lsum > 0.0f ? a / lsum : 0.0f);
+      continue;
+    }
     p.part_acc[(item * GT + h) * DV + d] = a;
     if (d == 0) {
       p.part_ml[(item * GT + h) * 2 + 0] = M;
       p.part_ml[(item * GT + h) * 2 + 1] = lsum;
     }
+  }
+  if (only_split || p.split_cnt == nullptr) return;
+
+  // ---- fused merge: the CTA that finishes the last split of its (b, query group) merges the group.
+  // Every CTA publishes its partial (fence) before it counts itself in; the last one fences again
+  // before reading the others' partials, which it reads from L2 (ld.cg: its L1 may hold stale lines).
+  __shared__ int s_last;
+  __threadfence();
+  __syncthreads();
+  const int32_t groups = p.num_kv_heads * p.head_tiles;
+  if (tid == 0) s_last = atomicAdd(p.split_cnt + static_cast<int64_t>(b) * groups + qg, 1) == plan.nsplit - 1;
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  const int64_t first = static_cast<int64_t>(plan.base) + static_cast<int64_t>(qg) * plan.nsplit;
+  const int32_t ns = plan.nsplit;
+  // (1) M_h = max_s m_s,h.  The (split, head) pairs are contiguous and the stride is a multiple of GT,
+  // so every thread sees one head only: tid % GT.
+  float* sM = reinterpret_cast<float*>(smem);  // [WARPS][GT]
+  float* sL = sM + WARPS * GT;                  // [WARPS][GT]
+  float* sA = sL + WARPS * GT;                  // [WARPS][GT][DV]
+  {
+    float mt = -INFINITY;
+    for (int32_t i = tid; i < ns * GT; i += WARPS * 32) mt = fmaxf(mt, __ldcg(p.part_ml + (first * GT + i) * 2));
+#pragma unroll
+    for (int o = 16; o >= GT; o >>= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, o));
+    if (lane < GT) sM[warp * GT + lane] = mt;
+  }
+  __syncthreads();
+  float Mh[GT];
+#pragma unroll
+  for (int h = 0; h < GT; ++h) {
+    Mh[h] = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < WARPS; ++w) Mh[h] = fmaxf(Mh[h], sM[w * GT + h]);
+  }
+  // (2) warp w sums the splits s = w, w + WARPS, ...; lane = dim (mod 32)
+  constexpr int DPL = DV / 32;  // dims per lane
+  float am[GT][DPL], lw[GT];
+#pragma unroll
+  for (int h = 0; h < GT; ++h) {
+    lw[h] = 0.0f;
+#pragma unroll
+    for (int j = 0; j < DPL; ++j) am[h][j] = 0.0f;
+  }
+#pragma unroll 2
+  for (int32_t sp = warp; sp < ns; sp += WARPS) {
+#pragma unroll
+    for (int h = 0; h < GT; ++h) {
+      const int64_t it = (first + sp) * GT + h;
+      const float2 ml = __ldcg(reinterpret_cast<const float2*>(p.part_ml + it * 2));
+      const float wgt = (ml.x == -INFINITY) ? 0.0f : exp2f(ml.x - Mh[h]);
+      lw[h] = fmaf(ml.y, wgt, lw[h]);
+#pragma unroll
+      for (int j = 0; j < DPL; ++j) am[h][j] = fmaf(__ldcg(p.part_acc + it * DV + lane + 32 * j), wgt, am[h][j]);
+    }
+  }
+#pragma unroll
+  for (int h = 0; h < GT; ++h) {
+    if (lane == 0) sL[warp * GT + h] = lw[h];
+#pragma unroll
+    for (int j = 0; j < DPL; ++j) sA[(warp * GT + h) * DV + lane + 32 * j] = am[h][j];
+  }
+  __syncthreads();
+  // (3) sum over the warps, normalise
+  for (int idx = tid; idx < GT * DV; idx += WARPS * 32) {
+    const int h = idx / DV, d = idx - h * DV;
+    float at = 0.0f, lt = 0.0f;
+#pragma unroll
+    for (int w = 0; w < WARPS; ++w) {
+      at += sA[(w * GT + h) * DV + d];
+      lt += sL[w * GT + h];
+    }
+    store_out(p, (static_cast<int64_t>(b) * p.num_q_heads + head0 + h) * DV + d, lt > 0.0f ? at / lt : 0.0f);
   }
 }
 

@@ -33,6 +33,8 @@ struct DecodeArgs {
   float* part_acc;   // [max_items][heads_per_item][v_dim]
   float* part_ml;    // [max_items][heads_per_item][2]
   int32_t* plan_tab; // [batch][2]: first item and split count of each sequence (written by the decode)
+  int32_t* split_cnt; // [batch][query groups]: splits finished, zeroed per call; set when the decode
+                      // kernel merges its own partials (the last split of a group merges), else null
   int64_t max_items;
   int32_t heads_per_item;  // query heads one work item covers (a tile of the group)
   int32_t split_align;     // automatic split sizes are a multiple of this many pages

@@ -12,8 +12,8 @@
 // address (in host code it is only a host-side shadow symbol), so the first call on each device
 // asks the runtime for the real address with cudaGetSymbolAddress, with that device current, and
 // caches it.  All calls share the one array and it keeps the last call's contents: the status word
-// is cleared on every call (kvq_decode does that), and the split partials are always written before
-// they are read.  Calls whose kernels overlap on the GPU (different streams, or different host
+// and the split counters are cleared on every call (kvq_decode does that), and the split partials are
+// always written before they are read.  Calls whose kernels overlap on the GPU (different streams, or different host
 // threads without ordering) race on the array and give wrong results.
 #include <cuda_runtime.h>
 

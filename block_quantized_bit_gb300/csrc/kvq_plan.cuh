@@ -30,6 +30,9 @@ struct KParams {
   float* part_acc;
   float* part_ml;
   int32_t* plan_tab;      // [batch][2] first item, splits per query group; CTA 0 of the decode writes it
+  int32_t* split_cnt;     // [batch][groups] splits finished (zeroed per call), or null: no fused merge
+  void* out;              // [batch][num_q_heads][v_dim], bf16 or fp32 (out_f32)
+  int32_t out_f32;
   uint32_t* status;
   int64_t num_pages;      // pages in the pool: larger block-table entries are treated as masked
   int64_t max_items;      // work items the workspace holds
@@ -139,6 +142,9 @@ inline KParams make_kparams(const DecodeArgs& a) {
   p.part_acc = a.part_acc;
   p.part_ml = a.part_ml;
   p.plan_tab = a.plan_tab;
+  p.split_cnt = a.split_cnt;
+  p.out = a.out;
+  p.out_f32 = a.out_dtype == KVQ_OUT_F32;
   p.status = a.status;
   p.num_pages = a.num_pages;
   p.max_items = a.max_items;
