@@ -239,7 +239,8 @@ def run_ours(args, world, rank):
     e2e["value"] = world * (store_b + dec_b) / e2e.pop("step_s") / 1e9
     e2e["unit"] = "GB/s"
 
-    launches_per_step = 3  # store kernel, decode split kernel, merge kernel
+    # store kernel + decode kernel (+ merge kernel on the tensor-core path)
+    launches_per_step = 1 + (2 if kvq.kvq_decode_path(L, case.batch, case.num_q_heads, path=args.path) == 2 else 1)
     res = {
         "metric": "quantized-KV decode attention HBM GB/s (% of GB300 peak); kvq_store GB/s",
         "value": round(value, 2),

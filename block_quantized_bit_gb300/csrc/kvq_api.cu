@@ -199,6 +199,16 @@ kvq_status kvq_store(void* pool, void* scales, const void* k, const void* v, con
                       static_cast<cudaStream_t>(stream));
 }
 
+int32_t kvq_decode_path(const kvq_layout* layout, int32_t batch, int32_t num_q_heads,
+                        const kvq_decode_options* options) {
+  if (check_layout(layout) != KVQ_OK) return KVQ_EINVAL;
+  if (batch < 0 || num_q_heads <= 0 || num_q_heads % layout->num_kv_heads != 0) return KVQ_EINVAL;
+  if (options && (options->pages_per_split < 0 || options->path < 0 || options->path > 2)) return KVQ_EINVAL;
+  if (layout->page_size != kPageTokens) return KVQ_EUNSUPPORTED;
+  const int32_t path = choose_path(*layout, batch, num_q_heads, options);
+  return path < 0 ? static_cast<int32_t>(KVQ_EUNSUPPORTED) : path;
+}
+
 size_t kvq_decode_workspace_bytes_ex(const kvq_layout* layout, int32_t batch, int32_t num_q_heads,
                                      int32_t max_pages_per_seq, const kvq_decode_options* options) {
   if (check_layout(layout) != KVQ_OK) return 0;

@@ -27,7 +27,7 @@ STATUS = {0: "KVQ_OK", -1: "KVQ_EINVAL", -2: "KVQ_EKIND", -3: "KVQ_EHEADDIM", -4
           -5: "KVQ_EWORKSPACE", -6: "KVQ_EARCH", -7: "KVQ_ECUDA", -8: "KVQ_EUNSUPPORTED", -9: "KVQ_ETIMEOUT"}
 
 EXPORTS = ["kvq_pool_bytes", "kvq_scale_bytes", "kvq_bytes_per_token", "kvq_num_pages", "kvq_store",
-           "kvq_decode_workspace_bytes", "kvq_decode_workspace_bytes_ex", "kvq_decode", "kvq_decode_ex",
+           "kvq_decode_workspace_bytes", "kvq_decode_workspace_bytes_ex", "kvq_decode_path", "kvq_decode", "kvq_decode_ex",
            "kvq_workspace_status", "kvq_encode_probe", "kvq_quantize_probe", "kvq_dequant_probe", "kvq_strerror",
            "kvq_device_check", "kvq_version", "kvq_decode_noalloc"]
 
@@ -68,6 +68,7 @@ def lib():
             "kvq_store": (i32, [P, P, P, P, P, i64, LP, i32, P]),
             "kvq_decode_workspace_bytes": (sz, [LP, i32, i32, i32]),
             "kvq_decode_workspace_bytes_ex": (sz, [LP, i32, i32, i32, OP]),
+            "kvq_decode_path": (i32, [LP, i32, i32, OP]),
             "kvq_decode": (i32, [P, P, P, P, i32, P, i32, i32, ctypes.c_float, P, i32, P, sz, LP, i32, P]),
             "kvq_decode_ex": (i32, [P, P, P, P, i32, P, i32, i32, ctypes.c_float, P, i32, P, sz, LP, i32, OP, P]),
             "kvq_workspace_status": (i32, [P, P]),
@@ -179,6 +180,12 @@ def kvq_decode_workspace_bytes(layout: Layout, batch: int, num_q_heads: int, max
     o = _opts(pages_per_split, path)
     return lib().kvq_decode_workspace_bytes_ex(ctypes.byref(layout.c()), int(batch), int(num_q_heads),
                                                int(max_pages_per_seq), ctypes.byref(o))
+
+
+def kvq_decode_path(layout: Layout, batch: int, num_q_heads: int, pages_per_split=0, path=0) -> int:
+    """1 (CUDA cores, one launch) or 2 (tensor cores + merge, two launches); negative status if none."""
+    o = _opts(pages_per_split, path)
+    return lib().kvq_decode_path(ctypes.byref(layout.c()), int(batch), int(num_q_heads), ctypes.byref(o))
 
 
 def alloc_workspace(layout: Layout, batch, num_q_heads, max_pages_per_seq, device="cuda", **opts):

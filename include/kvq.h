@@ -134,11 +134,13 @@ size_t kvq_decode_workspace_bytes_ex(const kvq_layout* layout, int32_t batch, in
  * K and V dequantized to bf16 (RNE of code * scale) and fp32 accumulation; a sequence without a
  * valid token outputs zeros.  Supported: page_size 16 and head_dim in {64, 128, 256} with v_dim ==
  * head_dim (GQA), or the MLA row head_dim 576 / v_dim 512; other shapes return KVQ_EUNSUPPORTED.
- * Kernels (kvq_decode_options.path): the CUDA-core kernel (1) runs every supported shape and keeps the
- * softmax probabilities P in fp32.  The tensor-core kernel (2) runs head_dim 128 or 256 with 1..16
- * query heads per kv head and batch <= 2048; it feeds P to the MMA as bf16, so its error relative to
- * the exact result grows with the magnitude of V (about 2^-9 of max |V|).  Automatic (0) picks 2 for
- * 8..16 query heads per kv head and 1 otherwise.
+ * Kernels (kvq_decode_options.path): the CUDA-core kernel (1) runs every supported shape, keeps the
+ * softmax probabilities P in fp32 and merges its split partials itself (one launch).  The tensor-core
+ * kernels (2) run head_dim 128 or 256 with 1..16 query heads per kv head and batch <= 2048, and the
+ * MLA row with at most 64 query heads (or a multiple of 64) and batch <= 1024; a merge kernel follows
+ * them (two launches).  They feed P to the MMA as bf16, so their error relative to the exact result
+ * grows with the magnitude of V (about 2^-9 of max |V|).  Automatic (0) picks 2 for 8..16 query heads
+ * per kv head and for the MLA row, and 1 otherwise; kvq_decode_path tells which.
  */
 kvq_status kvq_decode(const void* q, const void* pool, const void* scales, const int32_t* block_table,
                       int32_t max_pages_per_seq, const int32_t* seq_lens, int32_t batch, int32_t num_q_heads,
@@ -149,6 +151,15 @@ kvq_status kvq_decode_ex(const void* q, const void* pool, const void* scales, co
                          int32_t num_q_heads, float sm_scale, void* out, kvq_out_dtype out_dtype,
                          void* workspace, size_t workspace_bytes, const kvq_layout* layout, kvq_kind kind,
                          const kvq_decode_options* options, void* stream);
+
+/*
+ * The decode kernel kvq_decode_ex would run for these sizes and options: 1 (CUDA cores, one launch) or
+ * 2 (tensor cores, two launches with the merge).  Otherwise a negative kvq_status: KVQ_EINVAL for an
+ * invalid layout, size or option, KVQ_EUNSUPPORTED when no kernel supports the shape.  Host only, no
+ * device call; options may be NULL.
+ */
+int32_t kvq_decode_path(const kvq_layout* layout, int32_t batch, int32_t num_q_heads,
+                        const kvq_decode_options* options);
 
 /*
  * kvq_decode for callers that cannot allocate device memory.  The pages have no counterpart to

@@ -128,6 +128,16 @@ def test_workspace_bound_covers_every_split_choice(lib):
     assert forced > auto > 0
 
 
+def test_decode_path_follows_the_group_size_and_the_options(lib):
+    assert kvq.kvq_decode_path(L(num_kv_heads=8), 8, 16) == 1                         # G = 2: CUDA cores
+    assert kvq.kvq_decode_path(L(num_kv_heads=2, head_dim=256, v_dim=256), 8, 16) == 2  # G = 8: tcgen05
+    assert kvq.kvq_decode_path(L(num_kv_heads=1, head_dim=576, v_dim=512, mla=True), 1, 128) == 2
+    assert kvq.kvq_decode_path(L(num_kv_heads=2, head_dim=256, v_dim=256), 8, 16, path=1) == 1
+    assert kvq.kvq_decode_path(L(num_kv_heads=8, head_dim=64, v_dim=64), 8, 16, path=2) == -8  # unsupported
+    assert kvq.kvq_decode_path(L(), 4, 7) == -1             # Hq % Hkv != 0
+    assert kvq.kvq_decode_path(L(), 4, 8, path=3) == -1
+
+
 def test_strerror_has_a_message_for_every_status(lib):
     for code, name in kvq.STATUS.items():
         msg = kvq.strerror(code)
