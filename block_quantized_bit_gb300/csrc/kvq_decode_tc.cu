@@ -14,19 +14,23 @@
 // descriptor LBO = RS (token groups) and SBO = 128 (8-dim groups); Q uses the same form, K-major.
 // The K tile lives in tensor memory (lane = token, two bf16 per column), double-buffered.
 //
-// One persistent CTA per SM, 15 warps (at most 4 per SM sub-partition):
-//   warps 13-14 producers, one for K and one for V: one lane per page of a tile reads the block table
+// One persistent CTA per SM, 23 warps (80 registers each):
+//   warps 21-22 producers, one for K and one for V: one lane per page of a tile reads the block table
 //               and issues TMA copies of the page's codes (a 5-D tensor map over the pool, one 2 KB box
 //               = 16 tokens x 128 code bytes, stored with the 128-byte swizzle) and a 1-D bulk copy of
 //               its scales into that producer's multi-stage staging ring; the tile's valid-token counts
 //               go with it.
-//   warps 4-11  dequant: each thread owns half of a token row.  It reads its codes from the swizzled
-//               staging rows (bank-conflict free: the 16-byte chunk index is XORed with token % 8),
-//               dequantizes them exactly as on the CUDA-core path, K into tensor memory, V into shared.
-//               Its loops are deliberately not fully unrolled: with five roles sharing each SM
-//               sub-partition, instruction-cache misses cost more than the loop overhead.
-//   warp 12     allocates TMEM; one thread issues every tcgen05.mma / tcgen05.commit, taking QK of the
-//               next tile and PV of the oldest tile in whichever order their inputs become ready.
+//   warps 4-19  dequant: each thread owns a quarter of a token row.  It reads its codes from the
+//               swizzled staging rows (bank-conflict free: the 16-byte chunk index is XORed with
+//               token % 8), dequantizes them exactly as on the CUDA-core path, K into tensor memory, V
+//               into shared.  Its loops are deliberately not fully unrolled: with five roles sharing
+//               each SM sub-partition, instruction-cache misses cost more than the loop overhead.
+//               Sixteen dequant warps (instead of eight) and the elected-lane MMA issue below together
+//               took the long-context decode from 526 to 502 us; either alone gained nothing, because
+//               the other then paced the tile.
+//   warp 20     allocates TMEM and issues every tcgen05.mma / tcgen05.commit (one lane elected by the
+//               converged warp), taking QK of the next tile and PV of the oldest tile in whichever
+//               order their inputs become ready.
 //   warps 0-3   softmax: TMEM lane = token; fp32 online softmax in the exp2 domain with lazy
 //               rescaling: the running max of a head moves only when some token exceeds it by 2^8,
 //               detected by one vote per tile; only then are the exact tile maxima reduced across
@@ -49,10 +53,10 @@ constexpr int kTile = 128;        // tokens per tile (8 pages)
 constexpr int kPagesPerTile = kTile / kPage;
 constexpr int kN = 16;            // MMA N: query heads, padded
 constexpr int kSmWarps = 4;
-constexpr int kDwWarps = 8;
-constexpr int kMmaWarp = kSmWarps + kDwWarps;          // warp 12
+constexpr int kDwWarps = 16;
+constexpr int kMmaWarp = kSmWarps + kDwWarps;          // warp 20
 constexpr int kProdWarp = kMmaWarp + 1;                // warps 13 (K ring) and 14 (V ring)
-constexpr int kThreads = (kProdWarp + 2) * 32;         // 15 warps: at most 4 per sub-partition
+constexpr int kThreads = (kProdWarp + 2) * 32;         // 23 warps
 constexpr int kDwThreads = kDwWarps * 32;
 constexpr int kMaxPlanBatch = 2048;   // sequences whose item bases fit the shared table
 constexpr float kLazyRescale = 8.0f;  // log2 headroom before the running max must move
@@ -123,7 +127,8 @@ __device__ __forceinline__ void tmem_st16u(uint32_t taddr, const uint32_t (&r)[1
 // 2-byte load per scale would hit each bank four times (the token rows are 16 bytes apart).
 template <int NBT>
 __device__ __forceinline__ uint64_t load_scales(const uint8_t* p) {
-  static_assert(NBT == 2 || NBT == 4, "scale blocks per dequant thread");
+  static_assert(NBT == 1 || NBT == 2 || NBT == 4, "scale blocks per dequant thread");
+  if (NBT == 1) return *reinterpret_cast<const uint16_t*>(p);
   if (NBT == 4) {
     const uint2 v = *reinterpret_cast<const uint2*>(p);
     return static_cast<uint64_t>(v.x) | (static_cast<uint64_t>(v.y) << 32);
@@ -131,11 +136,16 @@ __device__ __forceinline__ uint64_t load_scales(const uint8_t* p) {
   return *reinterpret_cast<const uint32_t*>(p);
 }
 
+// The MMA and commit helpers are warp-collective: all 32 lanes of the converged MMA warp call them with the
+// same operands and the lane chosen by elect.sync issues.  The descriptors then stay in uniform registers
+// (a probe measured 15 clocks per MMA with A in tensor memory and 40 with A in shared memory, against 56
+// from a lane-0 branch).  The full mask elects the same lane every time, so a commit tracks every MMA
+// issued before it.
 __device__ __forceinline__ void mma_bf16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc,
                                                 uint32_t acc) {
   asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "{\n\t.reg .pred p, e;\n\tsetp.ne.b32 p, %4, 0;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
       "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc)
       : "memory");
 }
@@ -164,15 +174,17 @@ __device__ __forceinline__ uint32_t mma_idesc(bool a_mn_major, bool b_mn_major) 
 
 __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
   asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "{\n\t.reg .pred p, e;\n\tsetp.ne.b32 p, %4, 0;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(a), "l"(b), "r"(idesc), "r"(acc)
       : "memory");
 }
 
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
-               : "memory");
+  asm volatile(
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(smem_u32(bar))
+      : "memory");
 }
 
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
@@ -526,10 +538,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const KParams p,
         const uint8_t* slot = sVr + (nv % Cfg::STAGES) * Cfg::SLOT_BYTES;
         const bool v_ok = off < sMeta[ring * kPagesPerTile + pi];
         const uint64_t scw = load_scales<Cfg::NBT>(slot + sc_off);
-        // the previous PV must have read this thread's rows of the V tile (with two O^T slices, part 0
-        // writes exactly the dims of slice 0)
+        // the previous PV must have read this thread's rows of the V tile (with two O^T slices, a part
+        // that writes dims of slice 0 only waits for the first half of the PV)
         if (nv >= 1) {
-          uint64_t* vbar = (Cfg::O_CHUNKS == 2 && part == 0) ? &bar_pv_lo[(nv - 1) & 1] : &bar_pv_done[(nv - 1) & 1];
+          const bool lo = Cfg::O_CHUNKS == 2 && part * Cfg::HALF < 128;
+          uint64_t* vbar = lo ? &bar_pv_lo[(nv - 1) & 1] : &bar_pv_done[(nv - 1) & 1];
           if (!mbar_wait_bounded(vbar, ((nv - 1) >> 1) & 1)) { ok = false; break; }
         }
 #pragma unroll 2
@@ -555,9 +568,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const KParams p,
       }
     }
   } else if (warp == kMmaWarp) {
-    // ===================================================================== MMA issue (lane 0)
+    // ===================================================================== MMA issue (elected lane)
     // QK(nq) needs K tile nq in TMEM and S buffer nq&1 read by the softmax of tile nq-2; PV(np) needs
-    // V tile np and P tile np.  Whichever is ready is issued first; lane 0 polls, the warp follows.
+    // V tile np and P tile np.  Whichever is ready is issued first; lane 0 polls,
+    // the converged warp issues (one elected lane).
     const uint32_t idesc_qk = mma_idesc(false, false);
     const uint32_t idesc_pv = mma_idesc(true, true);
     // descriptors of the first K-step; later steps add their byte offset >> 4 to the address field
@@ -579,7 +593,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const KParams p,
           ready = mbar_test_wait(bar_v_full, np & 1) && mbar_test_wait(&bar_p_full[b], (np >> 1) & 1);
         if (__shfl_sync(0xffffffffu, ready, 0)) {
           tc_fence_after();
-          if (lane == 0) {
+          {
             const uint32_t o = tO + item_obuf(tp.item) * 32;
             const uint64_t dP = dP0 + static_cast<uint64_t>((b * Cfg::P_BYTES) >> 4);
 #pragma unroll
@@ -606,7 +620,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const KParams p,
                   (nq < 2 || mbar_test_wait(&bar_p_full[b], ((nq >> 1) - 1) & 1));
         if (__shfl_sync(0xffffffffu, ready, 0)) {
           tc_fence_after();
-          if (lane == 0) {
+          {
             const uint32_t ka = tK + b * Cfg::KCOLS;
 #pragma unroll
             for (int ks = 0; ks < D / 16; ++ks)
