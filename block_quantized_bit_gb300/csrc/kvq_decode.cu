@@ -485,23 +485,24 @@ __global__ void __launch_bounds__(WARPS * 32, MINB) decode_cc_kernel(KParams p) 
 }
 
 // ------------------------------------------------------------------------------------- merge
-// One CTA per (b, query group, head of the group, 32-dim slice of the output).  Its 256 threads are
-// 8 float4 columns x 32 split groups: every thread accumulates its columns over the splits
-// s = group, group + 32, ... with weights exp2(m_s - M), and the groups are summed in shared memory.
 constexpr int kMergeThreads = 256;
 constexpr int kMergeWarps = kMergeThreads / 32;
+constexpr int kMergeSubs = 4;  // splits a warp reads at once: 8 lanes x float4 = the 32 dims of a slice
 
 // One CTA per (sequence, query group, head of the item, 32-dim slice of v): the log-sum-exp merge of
 // the sequence's split partials, out = sum_s 2^(m_s - M) acc_s / sum_s 2^(m_s - M) l_s, M = max_s m_s.
-// Warp w takes the splits s = w, w + 8, ...; lane = dim.  The decode kernel's CTA 0 left each
-// sequence's first item and split count in plan_tab, so no plan is recomputed here.
+// A warp reads four splits at a time (lanes 8j..8j+7 take split j, four dims each), so the CTA has 32
+// splits' loads in flight per round; the sums are reduced across the lane groups and the warps.  The
+// decode kernel's CTA 0 left each sequence's first item and split count in plan_tab, so no plan is
+// recomputed here.
 template <typename OutT>
 __global__ void __launch_bounds__(kMergeThreads) merge_kernel(KParams p, OutT* __restrict__ out, int32_t heads_per_item,
                                                               int32_t DV, int32_t units_per_seq) {
   __shared__ float s_m[kMergeWarps];
-  __shared__ float s_a[kMergeWarps][32];
+  __shared__ __align__(16) float s_a[kMergeWarps][32];
   __shared__ float s_l[kMergeWarps];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int sub = lane >> 3, q = lane & 7;  // split of the four, float4 of the slice
   const int32_t b = blockIdx.x / units_per_seq;
   const int32_t u = blockIdx.x - b * units_per_seq;
   const int32_t slices = DV / 32;
@@ -524,19 +525,32 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(KParams p, OutT* _
   __syncthreads();
 #pragma unroll
   for (int w = 0; w < kMergeWarps; ++w) M = fmaxf(M, s_m[w]);
-  float a = 0.0f, l = 0.0f;
+  float4 a = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+  float l = 0.0f;
   if (M != -INFINITY) {
-    const float* acc = p.part_acc + slice * 32 + lane;
-#pragma unroll 4
-    for (int32_t s = warp; s < ns; s += kMergeWarps) {
+    const float* acc = p.part_acc + slice * 32 + q * 4;
+#pragma unroll 2
+    for (int32_t s = warp * kMergeSubs + sub; s < ns; s += kMergeWarps * kMergeSubs) {
       const int64_t it = (first + s) * heads_per_item + h;
       const float2 ml = *reinterpret_cast<const float2*>(p.part_ml + it * 2);
       const float w = (ml.x == -INFINITY) ? 0.0f : exp2f(ml.x - M);
-      a = fmaf(acc[it * DV], w, a);
+      const float4 v = *reinterpret_cast<const float4*>(acc + it * DV);
+      a.x = fmaf(v.x, w, a.x);
+      a.y = fmaf(v.y, w, a.y);
+      a.z = fmaf(v.z, w, a.z);
+      a.w = fmaf(v.w, w, a.w);
       l = fmaf(ml.y, w, l);
     }
   }
-  s_a[warp][lane] = a;
+#pragma unroll
+  for (int o = 8; o < 32; o <<= 1) {  // over the four lane groups (the same q)
+    a.x += __shfl_xor_sync(0xffffffffu, a.x, o);
+    a.y += __shfl_xor_sync(0xffffffffu, a.y, o);
+    a.z += __shfl_xor_sync(0xffffffffu, a.z, o);
+    a.w += __shfl_xor_sync(0xffffffffu, a.w, o);
+    l += __shfl_xor_sync(0xffffffffu, l, o);
+  }
+  if (lane < 8) *reinterpret_cast<float4*>(&s_a[warp][q * 4]) = a;
   if (lane == 0) s_l[warp] = l;
   __syncthreads();
   if (warp == 0) {
