@@ -26,8 +26,9 @@
 //   warp 24     MMA issue (one elected lane): QK slab by slab into S (double-buffered in TMEM), PV
 //               block by block into O; whichever is ready first.
 //   warps 0-7   softmax: thread = (token, 32 of the 64 heads); fp32 online softmax in the exp2 domain
-//               with lazy rescaling (a head's running max moves only when a score exceeds it by 2^8); P
-//               to shared memory as bf16; O rescaled in TMEM when a max moves; the item's partial.
+//               with lazy rescaling (a head's running max moves only when a score exceeds it by 2^8),
+//               one pass over the scores that forms P with the current maxima (again only if one
+//               moved); P to shared memory as bf16; O rescaled in TMEM when a max moves; the partial.
 // TMEM: S[2] 128 columns, O^T 4 x 64, K slots 2 x 64 = 512.  Every wait is bounded (2 s) and reports a
 // timeout in the workspace status word instead of hanging.
 #include <cuda.h>  // CUtensorMap and its enums (the encoder is fetched from the driver at run time)
@@ -616,20 +617,32 @@ __global__ void __launch_bounds__(mla::kThreads, 1) decode_mla_kernel(const KPar
         mla_fence_after();
         const bool valid = sValid[b * kTile + tt] != 0;
         const uint32_t s_base = tS + b * 64 + h0 + lane_base;
-        // does any score of the tile move its head's running max?  (one vote per warp, one barrier)
-        bool moved = false;
-#pragma unroll 1
-        for (int g = 0; g < kHS / 16; ++g) {
-          float s[16];
-          mla_ld16(s_base + g * 16, s);
+        // One pass over the scores: does any score move its head's running max (one vote per warp, one
+        // barrier)?  P is formed with the current running maxima at the same time; it is final unless a
+        // maximum moves, which the lazy rescale makes rare, and then it is formed again.
+        uint32_t pw[kHS / 2];
+        auto form_p = [&](bool& moved) {
 #pragma unroll
-          for (int h = 0; h < 16; ++h) {
-            const int hd = h0 + g * 16 + h;
-            const float m = sM[hd];
-            const float x = (valid && hd < HP) ? s[h] * p.score_scale : -INFINITY;
-            moved |= (x > -INFINITY) && (m == -INFINITY || x > m + kLazyRescale);
+          for (int g = 0; g < kHS / 16; ++g) {
+            float s[16];
+            mla_ld16(s_base + g * 16, s);
+#pragma unroll
+            for (int h2 = 0; h2 < 8; ++h2) {
+              float pr[2];
+#pragma unroll
+              for (int e = 0; e < 2; ++e) {
+                const int hd = h0 + g * 16 + 2 * h2 + e;
+                const float m = sM[hd];
+                const float x = (valid && hd < HP) ? s[2 * h2 + e] * p.score_scale : -INFINITY;
+                moved |= (x > -INFINITY) && (m == -INFINITY || x > m + kLazyRescale);
+                pr[e] = (x == -INFINITY || m == -INFINITY) ? 0.0f : exp2f(x - m);
+              }
+              pw[g * 8 + h2] = pack_bf16x2(pr[0], pr[1]);
+            }
           }
-        }
+        };
+        bool moved = false;
+        form_p(moved);
         const int wv = __any_sync(0xffffffffu, moved);
         if (lane == 0) sFlag[warp] = wv;
         mla_named_sync(1, kSmWarps * 32);
@@ -669,6 +682,8 @@ __global__ void __launch_bounds__(mla::kThreads, 1) decode_mla_kernel(const KPar
           mla_named_sync(1, kSmWarps * 32);
 #pragma unroll
           for (int h = 0; h < kHS; ++h) rescale |= sA[h0 + h] != 1.0f;
+          bool unused = false;
+          form_p(unused);  // P with the new running maxima
         }
         mla_named_sync(1, kSmWarps * 32);  // sFlag / sRed are rewritten next tile
         // P is single-buffered: the previous tile's PV must be complete before it is rewritten (and
@@ -693,31 +708,19 @@ __global__ void __launch_bounds__(mla::kThreads, 1) decode_mla_kernel(const KPar
         // P row of this token for heads h0 .. h0 + 31 (bf16) and the row sums of exactly those values
 #pragma unroll
         for (int g = 0; g < kHS / 16; ++g) {
-          float s[16];
-          mla_ld16(s_base + g * 16, s);
-          uint32_t pw[8];
 #pragma unroll
           for (int h2 = 0; h2 < 8; ++h2) {
-            float pr[2];
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              const int hd = h0 + g * 16 + 2 * h2 + e;
-              const float m = sM[hd];
-              const float x = (valid && hd < HP) ? s[2 * h2 + e] * p.score_scale : -INFINITY;
-              pr[e] = (x == -INFINITY || m == -INFINITY) ? 0.0f : exp2f(x - m);
-            }
-            pw[h2] = pack_bf16x2(pr[0], pr[1]);
-            const float2 pb = unpack_bf16x2(pw[h2]);
+            const float2 pb = unpack_bf16x2(pw[g * 8 + h2]);
             const int h = g * 16 + 2 * h2;
             const float a0 = any_moved ? sA[h0 + h] : 1.0f, a1 = any_moved ? sA[h0 + h + 1] : 1.0f;
             l_t[h] = fmaf(l_t[h], a0, pb.x);
             l_t[h + 1] = fmaf(l_t[h + 1], a1, pb.y);
           }
-          const int hg8 = (h0 + g * 16) / 8;  // 8-head group of pw[0..3]
+          const int hg8 = (h0 + g * 16) / 8;  // 8-head group of pw[8g .. 8g + 3]
           *reinterpret_cast<uint4*>(sP + (tt % 8) * 16 + (tt / 8) * 128 + hg8 * kPS) =
-              make_uint4(pw[0], pw[1], pw[2], pw[3]);
+              make_uint4(pw[g * 8 + 0], pw[g * 8 + 1], pw[g * 8 + 2], pw[g * 8 + 3]);
           *reinterpret_cast<uint4*>(sP + (tt % 8) * 16 + (tt / 8) * 128 + (hg8 + 1) * kPS) =
-              make_uint4(pw[4], pw[5], pw[6], pw[7]);
+              make_uint4(pw[g * 8 + 4], pw[g * 8 + 5], pw[g * 8 + 6], pw[g * 8 + 7]);
         }
         o_live = true;
         fence_proxy_async_smem();
