@@ -457,6 +457,74 @@ int kvo_decode_bf16(double* out, const uint16_t* q_bits, const uint16_t* pool16,
 }
 
 /* ------------------------------------------------------------------------------------------ */
+/* Sparse (top-K) decode ("Experimental FP8 KV Cache", the SPARSE_MLA_DECODE profile line: each  */
+/* query reads K selected tokens of the latent pool; "feat(kvcache): 8-bit DSV4 window/compressed */
+/* KV", section "Testing": masked -1 columns).  For sequence b the index list holds topk token   */
+/* positions; a column is valid when its position p satisfies 0 <= p < seq_lens[b] and the page  */
+/* block_table[b][p / P] is not -1.  Every valid column is one term (a position listed twice     */
+/* counts twice):                                                                               */
+/*     z_i = sm_scale * sum_d q[b][h][d] * Kd(p_i)[d],   out[b][h] = sum_i softmax(z)_i Vd(p_i)   */
+/* with the dequantized rows of kv head h / (Hq / Hkv); zeros when no column is valid.           */
+/* ------------------------------------------------------------------------------------------ */
+int kvo_decode_sparse(double* out, const uint16_t* q_bits, const uint8_t* codes, const uint16_t* scales,
+                      const int32_t* block_table, int max_pages, const int32_t* seq_lens, const int32_t* indices,
+                      int topk, int B, int Hq, int Hkv, int D, int Dv, int P, int mla, int kind, double sm_scale,
+                      int nthreads)
+{
+    if (Hq % Hkv != 0 || Dv > D || topk < 0) return -1;
+    int n_kv = mla ? 1 : 2;
+    int G = Hq / Hkv;
+    int64_t units = (int64_t)B * Hq;
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 1)
+#else
+    (void)nthreads;
+#endif
+    for (int64_t u = 0; u < units; ++u) {
+        int b = (int)(u / Hq), h = (int)(u % Hq);
+        int g = h / G;
+        const int32_t* idx = indices + (int64_t)b * topk;
+        const uint16_t* qrow = q_bits + ((int64_t)b * Hq + h) * D;
+        double* o = out + ((int64_t)b * Hq + h) * Dv;
+        double* z = (double*)malloc(sizeof(double) * (size_t)(topk > 0 ? topk : 1));
+        int64_t* krow = (int64_t*)malloc(sizeof(int64_t) * (size_t)(topk > 0 ? topk : 1));
+        double zmax = -INFINITY;
+        for (int i = 0; i < topk; ++i) {
+            int32_t p = idx[i];
+            z[i] = -INFINITY;
+            krow[i] = -1;
+            if (p < 0 || p >= seq_lens[b]) continue;
+            int32_t page = block_table[(int64_t)b * max_pages + p / P];
+            if (page < 0) continue;
+            krow[i] = row_index(page, 0, g, p % P, n_kv, Hkv, P);
+            double dot = 0.0;
+            for (int d = 0; d < D; ++d)
+                dot += kvo_bf16_value(qrow[d]) * row_elem(1, kind, codes, scales, NULL, krow[i], D, d);
+            z[i] = sm_scale * dot;
+            if (z[i] > zmax) zmax = z[i];
+        }
+        for (int d = 0; d < Dv; ++d) o[d] = 0.0;
+        if (zmax != -INFINITY) {
+            double denom = 0.0;
+            for (int i = 0; i < topk; ++i) {
+                if (krow[i] < 0) continue;
+                double w = exp(z[i] - zmax);
+                denom += w;
+                int32_t p = idx[i];
+                int32_t page = block_table[(int64_t)b * max_pages + p / P];
+                int64_t r = row_index(page, mla ? 0 : 1, g, p % P, n_kv, Hkv, P);
+                for (int d = 0; d < Dv; ++d) o[d] += w * row_elem(1, kind, codes, scales, NULL, r, D, d);
+            }
+            for (int d = 0; d < Dv; ++d) o[d] /= denom;
+        }
+        free(z);
+        free(krow);
+    }
+    return 0;
+}
+
+/* ------------------------------------------------------------------------------------------ */
 /* Batch helpers for the pins (elementwise maps over arrays).                                   */
 /* ------------------------------------------------------------------------------------------ */
 void kvo_f16_rne_f32_batch(const float* x, uint16_t* out, int64_t n)

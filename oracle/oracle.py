@@ -41,6 +41,8 @@ def lib():
             "kvo_scatter_bf16": (i32, [P, P, P, P, i64, i32, i32, i32, i32, i64]),
             "kvo_decode": (i32, [P, P, P, P, P, i32, P, i32, i32, i32, i32, i32, i32, i32, i32, dbl, i32]),
             "kvo_decode_bf16": (i32, [P, P, P, P, i32, P, i32, i32, i32, i32, i32, i32, i32, dbl, i32]),
+            "kvo_decode_sparse": (i32, [P, P, P, P, P, i32, P, P, i32, i32, i32, i32, i32, i32, i32, i32, i32,
+                                        dbl, i32]),
             "kvo_f16_rne_f32_batch": (None, [P, P, i64]),
             "kvo_bf16_rne_f64_batch": (None, [P, P, i64]),
             "kvo_e4m3_sat_rne_batch": (None, [P, P, i64]),
@@ -216,6 +218,28 @@ def decode(q_bits, codes, scales, block_table, seq_lens, *, num_q_heads, num_kv_
                           _kind(kind), float(sm_scale), int(nthreads))
     if rc != 0:
         raise ValueError("oracle decode rejected its arguments")
+    return out
+
+
+def decode_sparse(q_bits, codes, scales, block_table, seq_lens, indices, *, num_q_heads, num_kv_heads, head_dim,
+                  v_dim, page_size, mla, kind, sm_scale, nthreads=1):
+    """fp64 attention of each sequence's query over the tokens its index list selects ([B, topk] int32
+    positions; -1, positions at or past seq_len and positions on masked pages are skipped; a repeated
+    position counts once per listing); returns out[B, Hq, Dv] float64 (zeros without a valid column)."""
+    q, pq = _c(q_bits, np.uint16)
+    c, pc = _c(codes, np.uint8)
+    s, ps = _c(scales, np.uint16)
+    bt, pbt = _c(block_table, np.int32)
+    sl, psl = _c(seq_lens, np.int32)
+    ix, pix = _c(indices, np.int32)
+    B = sl.size
+    topk = ix.shape[1] if ix.ndim == 2 else 0
+    out = np.zeros((B, num_q_heads, v_dim), np.float64)
+    rc = lib().kvo_decode_sparse(out.ctypes.data_as(ctypes.c_void_p), pq, pc, ps, pbt, bt.shape[1], psl, pix, topk,
+                                 B, num_q_heads, num_kv_heads, head_dim, v_dim, page_size, int(bool(mla)),
+                                 _kind(kind), float(sm_scale), int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle sparse decode rejected its arguments")
     return out
 
 

@@ -522,3 +522,91 @@ def test_unquantized_reference_decode_runs():
                         v_dim=64, page_size=16, mla=False, sm_scale=1.0)
     out = _run(s)
     assert np.all(np.isfinite(ref)) and np.abs(ref - out).max() < 0.1
+
+
+# ===================================================================== sparse (top-K) decode
+def _sparse_indices(s, topk, rng, *, junk=True):
+    """[B, topk] positions: a random selection of each sequence's positions (a few listed twice), with
+    -1 entries and positions past the sequence end mixed in when `junk`."""
+    B = len(s["lens"])
+    ix = np.full((B, topk), -1, np.int32)
+    for b, L in enumerate(s["lens"]):
+        pos = rng.permutation(int(L))[: max(1, topk // 2)]
+        sel = list(pos) + list(pos[:3])                        # three positions listed twice
+        if junk:
+            sel += [-1, int(L), int(L) + 5]                     # masked and out-of-range columns
+        sel = np.array(sel[:topk], np.int32)
+        rng.shuffle(sel)
+        ix[b, :len(sel)] = sel
+    return ix
+
+
+def _run_sparse(s, ix, sm_scale=1.0):
+    return O.decode_sparse(s["q"], s["codes"], s["scales"], s["bt"], s["lens"], ix, num_q_heads=s["Hq"],
+                           num_kv_heads=s["Hkv"], head_dim=s["D"], v_dim=s["Dv"], page_size=s["P"],
+                           mla=s["mla"], kind=s["kind"], sm_scale=sm_scale)
+
+
+def _expected_sparse_scipy(s, ix, sm_scale):
+    """scipy softmax attention over the listed columns, each valid column gathered by its slot."""
+    B, Hq, Hkv, D, Dv, P = len(s["lens"]), s["Hq"], s["Hkv"], s["D"], s["Dv"], s["P"]
+    out = np.zeros((B, Hq, Dv))
+    for b, L in enumerate(s["lens"]):
+        slots = []
+        for p in ix[b]:
+            if 0 <= p < L and s["bt"][b, p // P] >= 0:
+                slots.append(int(s["bt"][b, p // P]) * P + int(p) % P)
+        if not slots:
+            continue
+        for h in range(Hq):
+            g = h // (Hq // Hkv)
+            K = _gather_dequant(s["codes"], s["scales"], s["kind"], slots, 0, g, D)
+            V = K[:, :Dv] if s["mla"] else _gather_dequant(s["codes"], s["scales"], s["kind"], slots, 1, g, D)
+            qv = bf16_to_f32(s["q"][b, h]).astype(np.float64)
+            out[b, h] = scipy.special.softmax(sm_scale * (K @ qv)) @ V[:, :Dv]
+    return out
+
+
+@pytest.mark.parametrize("kind", [FP8, Q8])
+@pytest.mark.parametrize("mla", [False, True])
+def test_sparse_decode_matches_scipy_attention_over_the_listed_columns(kind, mla):
+    """Random selections with repeated positions, -1 columns, positions past the end and a masked page."""
+    D, Dv = (96, 64) if mla else (64, 64)
+    s = _decode_setup(kind, mla=mla, D=D, Dv=Dv, Hkv=1 if mla else 2, mask=[(1, 2)])
+    ix = _sparse_indices(s, 40, np.random.default_rng(5))
+    for sm_scale in (1.0, 0.37):
+        np.testing.assert_allclose(_run_sparse(s, ix, sm_scale), _expected_sparse_scipy(s, ix, sm_scale),
+                                   rtol=1e-12, atol=1e-13)
+
+
+def test_sparse_decode_listing_every_position_equals_the_dense_decode():
+    s = _decode_setup(FP8, mask=[(0, 1)])
+    topk = int(max(s["lens"]))
+    ix = np.full((len(s["lens"]), topk), -1, np.int32)
+    for b, L in enumerate(s["lens"]):
+        ix[b, :L] = np.random.default_rng(b).permutation(int(L))   # order does not matter
+    np.testing.assert_allclose(_run_sparse(s, ix), _run(s), rtol=1e-12, atol=1e-13)
+
+
+def test_sparse_decode_closed_forms():
+    s = _decode_setup(Q8, mla=True, D=96, Dv=64, Hkv=1)
+    B = len(s["lens"])
+    # one listed column: the output is that token's value row
+    ix = np.full((B, 8), -1, np.int32)
+    ix[:, 3] = 5
+    got = _run_sparse(s, ix)
+    for b in range(B):
+        slot = int(s["bt"][b, 0]) * s["P"] + 5
+        row = _gather_dequant(s["codes"], s["scales"], Q8, [slot], 0, 0, 96)[0, :64]
+        for h in range(s["Hq"]):
+            np.testing.assert_allclose(got[b, h], row, rtol=0, atol=1e-15)
+    # no valid column (all -1, or all past the end): zeros
+    none = np.full((B, 8), -1, np.int32)
+    assert not np.any(_run_sparse(s, none))
+    past = np.tile(np.array([[1000, 2000]], np.int32), (B, 1))
+    assert not np.any(_run_sparse(s, past))
+    # listing a position twice equals listing it once with twice the weight: two columns, one doubled
+    two = np.full((B, 3), -1, np.int32)
+    two[:, 0], two[:, 1], two[:, 2] = 2, 9, 9
+    ref = _expected_sparse_scipy(s, two, 1.0)
+    np.testing.assert_allclose(_run_sparse(s, two), ref, rtol=1e-12, atol=1e-13)
