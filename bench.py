@@ -40,6 +40,8 @@ def parse():
     ap.add_argument("--batch", type=int, default=None, help="long_gqa / serving batch override")
     ap.add_argument("--ctx", type=int, default=None, help="long_gqa / mla context override")
     ap.add_argument("--path", type=int, default=0, help="decode path: 0 auto, 1 CUDA cores, 2 tcgen05")
+    ap.add_argument("--topk", type=int, default=0,
+                    help="sparse (top-K) decode: this many index-list columns per sequence (0: dense decode)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--seed", type=int, default=None)
     return ap.parse_args()
@@ -106,7 +108,20 @@ def valid_tokens(case):
     return total
 
 
-def algorithmic_bytes(case):
+def valid_columns(case, ix):
+    """Columns a sparse decode reads: listed positions p < seq_len whose page is not masked."""
+    bt = case.block_table.cpu()
+    lens = case.seq_lens.cpu().tolist()
+    P = case.page_size
+    total = 0
+    for b, L in enumerate(lens):
+        for p in ix[b].cpu().tolist():
+            if 0 <= p < L and int(bt[b, p // P]) >= 0:
+                total += 1
+    return total
+
+
+def algorithmic_bytes(case, ix=None):
     """(store_bytes, decode_bytes) of one step -- the method's own traffic."""
     n_kv = 1 if case.mla else 2
     row_elems = n_kv * case.num_kv_heads * case.head_dim
@@ -115,10 +130,14 @@ def algorithmic_bytes(case):
     else:
         store_rows = int(case.k.shape[0])
     store = store_rows * (row_elems * (2 + 1 + 2 / 32) + 8)
+    out_bytes = case.q.numel() * 2 + case.batch * case.num_q_heads * case.v_dim * 2 + case.batch * 4
+    if ix is not None:  # sparse: the selected rows, the index lists and their block-table lookups
+        toks = valid_columns(case, ix)
+        decode = toks * row_elems * 17 / 16 + out_bytes + ix.numel() * 8
+        return store, decode, store_rows, toks
     toks = valid_tokens(case)
     pages = sum((int(L) + case.page_size - 1) // case.page_size for L in case.seq_lens.cpu().tolist())
-    decode = toks * row_elems * 17 / 16 + case.q.numel() * 2 + case.batch * case.num_q_heads * case.v_dim * 2 \
-        + pages * 4 + case.batch * 4
+    decode = toks * row_elems * 17 / 16 + out_bytes + pages * 4
     return store, decode, store_rows, toks
 
 
@@ -184,14 +203,25 @@ def run_ours(args, world, rank):
     else:  # the store step re-stores the context rows
         sk, sv, ss = case.k, case.v, case.slot_mapping
     out = torch.empty(case.batch, case.num_q_heads, case.v_dim, dtype=torch.bfloat16, device=dev)
-    ws = kvq.alloc_workspace(L, case.batch, case.num_q_heads, case.max_pages, dev, path=args.path)
+    ix = None
+    if args.topk > 0:
+        from block_quantized_bit_gb300 import workloads
+        ix = workloads.sparse_indices(case, args.topk, device=dev)
+        ws = kvq.alloc_sparse_workspace(L, case.batch, case.num_q_heads, args.topk, dev)
+    else:
+        ws = kvq.alloc_workspace(L, case.batch, case.num_q_heads, case.max_pages, dev, path=args.path)
     flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)  # 4x L2
     stream = torch.cuda.current_stream()
 
+    def decode(q, bt, sl, ix_, o):
+        if ix_ is not None:
+            kvq.kvq_decode_sparse(q, codes, scales, bt, sl, ix_, o, ws, L, case.kind, case.sm_scale)
+        else:
+            kvq.kvq_decode(q, codes, scales, bt, sl, o, ws, L, case.kind, case.sm_scale, path=args.path)
+
     def step():
         kvq.kvq_store(codes, scales, sk, sv, ss, L, case.kind)
-        kvq.kvq_decode(case.q, codes, scales, case.block_table, case.seq_lens, out, ws, L, case.kind,
-                       case.sm_scale, path=args.path)
+        decode(case.q, case.block_table, case.seq_lens, ix, out)
 
     for _ in range(args.warmup):
         flush.fill_(1)
@@ -213,8 +243,7 @@ def run_ours(args, world, rank):
         ev[i][0].record(stream)
         kvq.kvq_store(codes, scales, sk, sv, ss, L, case.kind)
         ev[i][1].record(stream)
-        kvq.kvq_decode(case.q, codes, scales, case.block_table, case.seq_lens, out, ws, L, case.kind,
-                       case.sm_scale, path=args.path)
+        decode(case.q, case.block_table, case.seq_lens, ix, out)
         ev[i][2].record(stream)
     torch.cuda.synchronize()
     barrier(world)
@@ -225,7 +254,7 @@ def run_ours(args, world, rank):
     total_ms = max_over_ranks(sum(step_ms), world)
     ms_per_step = total_ms / K
 
-    store_b, dec_b, store_rows, toks = algorithmic_bytes(case)
+    store_b, dec_b, store_rows, toks = algorithmic_bytes(case, ix)
     value = world * (store_b + dec_b) * K / (total_ms / 1e3) / 1e9
     peaks = load_peaks()
     hbm = peaks.get("hbm_gbs")
@@ -235,12 +264,20 @@ def run_ours(args, world, rank):
     store_gbs = store_b / store_avg_s / 1e9
 
     # end to end through the public API: host inputs (pinned) in, host output back, every step
-    e2e = run_e2e(args, case, L, codes, scales, sk, sv, ss, ws, flush, world)
+    e2e = run_e2e(args, case, L, codes, scales, sk, sv, ss, ix, decode, flush, world)
     e2e["value"] = world * (store_b + dec_b) / e2e.pop("step_s") / 1e9
     e2e["unit"] = "GB/s"
 
-    # store kernel + decode kernel (+ merge kernel on the tensor-core path)
-    launches_per_step = 1 + (2 if kvq.kvq_decode_path(L, case.batch, case.num_q_heads, path=args.path) == 2 else 1)
+    # store kernel + decode kernel (+ merge kernel on the tensor-core path; + the gather when sparse, whose
+    # dense decode runs over topk tokens per sequence)
+    if ix is not None:
+        Lc = kvq.Layout(case.batch * max(1, (args.topk + 15) // 16), case.page_size, case.num_kv_heads,
+                        case.head_dim, case.v_dim, case.mla)
+        cpages = max(1, (args.topk + 15) // 16)
+        launches_per_step = 2 + (2 if kvq.kvq_decode_path(Lc, case.batch, case.num_q_heads, cpages) == 2 else 1)
+    else:
+        launches_per_step = 1 + (2 if kvq.kvq_decode_path(L, case.batch, case.num_q_heads, case.max_pages,
+                                                          path=args.path) == 2 else 1)
     res = {
         "metric": "quantized-KV decode attention HBM GB/s (% of GB300 peak); kvq_store GB/s",
         "value": round(value, 2),
@@ -262,7 +299,8 @@ def run_ours(args, world, rank):
         "decode_us": round(dec_avg_s * 1e6, 2),
         "decode_us_per_token": round(dec_avg_s * 1e6 / case.batch, 3),
         "store_us": round(store_avg_s * 1e6, 2),
-        "roofline": {"bound": "hbm", "kernel": "kvq_decode (split kernel + merge)",
+        "roofline": {"bound": "hbm", "kernel": "kvq_decode_sparse (gather + decode)" if ix is not None
+                     else "kvq_decode (split kernel + merge)",
                      "achieved": round(dec_gbs, 1), "peak": hbm, "unit": "GB/s",
                      "frac": round(dec_gbs / hbm, 4) if hbm else None,
                      "peak_source": "MEASURED_PEAKS.json hbm_gbs (of measured)" if hbm else "fallback 6800",
@@ -281,12 +319,12 @@ def workload_config(args, case, store_rows, toks, world):
     return {"workload": args.workload, "kind": args.kind, "batch": case.batch,
             "num_q_heads": case.num_q_heads, "num_kv_heads": case.num_kv_heads,
             "head_dim": case.head_dim, "v_dim": case.v_dim, "page_size": case.page_size,
-            "store_rows": store_rows, "decode_tokens": toks,
+            "store_rows": store_rows, "decode_tokens": toks, **({"topk": args.topk} if args.topk else {}),
             "seq_lens": [int(x) for x in case.seq_lens.cpu().tolist()][:16],
             "l2": "flushed between steps (512 MB write)", "parallelism": "replicas" if world > 1 else "1 gpu"}
 
 
-def run_e2e(args, case, L, codes, scales, sk, sv, ss, ws, flush, world):
+def run_e2e(args, case, L, codes, scales, sk, sv, ss, ix, decode, flush, world):
     from block_quantized_bit_gb300 import kvq
     dev = codes.device
     hk = sk.cpu().pin_memory()
@@ -295,6 +333,8 @@ def run_e2e(args, case, L, codes, scales, sk, sv, ss, ws, flush, world):
     hq = case.q.cpu().pin_memory()
     hbt = case.block_table.cpu().pin_memory()
     hsl = case.seq_lens.cpu().pin_memory()
+    hix = None if ix is None else ix.cpu().pin_memory()
+    dix = None if ix is None else torch.empty_like(ix)
     hout = torch.empty((case.batch, case.num_q_heads, case.v_dim), dtype=torch.bfloat16).pin_memory()
     dk, dv, ds = torch.empty_like(sk), None if sv is None else torch.empty_like(sv), torch.empty_like(ss)
     dq, dbt, dsl = torch.empty_like(case.q), torch.empty_like(case.block_table), torch.empty_like(case.seq_lens)
@@ -309,8 +349,10 @@ def run_e2e(args, case, L, codes, scales, sk, sv, ss, ws, flush, world):
         dq.copy_(hq, non_blocking=True)
         dbt.copy_(hbt, non_blocking=True)
         dsl.copy_(hsl, non_blocking=True)
+        if dix is not None:
+            dix.copy_(hix, non_blocking=True)
         kvq.kvq_store(codes, scales, dk, dv, ds, L, case.kind)
-        kvq.kvq_decode(dq, codes, scales, dbt, dsl, dout, ws, L, case.kind, case.sm_scale, path=args.path)
+        decode(dq, dbt, dsl, dix, dout)
         hout.copy_(dout, non_blocking=True)
 
     for _ in range(max(3, args.warmup)):
@@ -327,8 +369,8 @@ def run_e2e(args, case, L, codes, scales, sk, sv, ss, ws, flush, world):
         torch.cuda.synchronize()
         tot += e0.elapsed_time(e1)
     tot = max_over_ranks(tot, world)
-    h2d = sum(t.numel() * t.element_size() for t in (hk, hs, hq, hbt, hsl)) + (0 if hv is None else
-                                                                               hv.numel() * hv.element_size())
+    h2d = sum(t.numel() * t.element_size() for t in (hk, hs, hq, hbt, hsl) + (() if hix is None else (hix,))) + \
+        (0 if hv is None else hv.numel() * hv.element_size())
     d2h = hout.numel() * hout.element_size()
     return {"step_s": tot / K / 1e3, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
 
@@ -379,7 +421,7 @@ def oracle_sample(case, budget_rows=None, max_seqs=None):
     return n_rows, seqs
 
 
-def oracle_step(case, codes, scales, n_rows, seqs, threads):
+def oracle_step(case, codes, scales, n_rows, seqs, threads, ix=None):
     """One oracle step over the sample: store n_rows rows, decode the chosen sequences.  Returns bytes."""
     import oracle as O
     bits = lambda t: t.contiguous().view(torch.int16).numpy().view(np.uint16)  # noqa: E731
@@ -390,16 +432,28 @@ def oracle_step(case, codes, scales, n_rows, seqs, threads):
     O.store(codes, scales, bits(k), None if v is None else bits(v), s.numpy(), num_kv_heads=case.num_kv_heads,
             head_dim=case.head_dim, page_size=case.page_size, mla=case.mla, kind=case.kind)
     idx = torch.tensor(seqs, dtype=torch.long)
-    O.decode(bits(case.q[idx]), codes, scales, case.block_table[idx].numpy(), case.seq_lens[idx].numpy(),
-             num_q_heads=case.num_q_heads, num_kv_heads=case.num_kv_heads, head_dim=case.head_dim,
-             v_dim=case.v_dim, page_size=case.page_size, mla=case.mla, kind=case.kind, sm_scale=case.sm_scale,
-             nthreads=threads)
+    dims = dict(num_q_heads=case.num_q_heads, num_kv_heads=case.num_kv_heads, head_dim=case.head_dim,
+                v_dim=case.v_dim, page_size=case.page_size, mla=case.mla, kind=case.kind, sm_scale=case.sm_scale,
+                nthreads=threads)
+    if ix is not None:
+        O.decode_sparse(bits(case.q[idx]), codes, scales, case.block_table[idx].numpy(), case.seq_lens[idx].numpy(),
+                        ix[idx].numpy(), **dims)
+    else:
+        O.decode(bits(case.q[idx]), codes, scales, case.block_table[idx].numpy(), case.seq_lens[idx].numpy(), **dims)
     n_kv = 1 if case.mla else 2
     row = n_kv * case.num_kv_heads * case.head_dim
     sub = type(case)(**{**case.__dict__, "seq_lens": case.seq_lens[idx], "block_table": case.block_table[idx],
                         "q": case.q[idx]})
-    toks = valid_tokens(sub)
+    toks = valid_tokens(sub) if ix is None else valid_columns(sub, ix[idx])
     return n_rows * (row * (2 + 1 + 2 / 32) + 8) + toks * row * 17 / 16
+
+
+def sparse_lists(case, args):
+    """The sparse decode's index lists (host), or None for the dense decode."""
+    if args.topk <= 0:
+        return None
+    from block_quantized_bit_gb300 import workloads
+    return workloads.sparse_indices(case, args.topk, device="cpu")
 
 
 def prepare_oracle(case):
@@ -416,18 +470,19 @@ def cpu_baseline(case, args):
     """The oracle, as it stands, on a bounded sample of the same workload (~10-30 s of CPU work)."""
     O, cpu, codes, scales = prepare_oracle(case)
     threads = max(1, O.openmp_threads())
+    ix = sparse_lists(cpu, args)
     # whole workload steps while they fit ~10 s, else a sub-sample (fewer store rows and sequences)
     n_rows, seqs = oracle_sample(cpu)
     t0 = time.perf_counter()
-    nbytes = oracle_step(cpu, codes, scales, n_rows, seqs, threads)
+    nbytes = oracle_step(cpu, codes, scales, n_rows, seqs, threads, ix)
     one = time.perf_counter() - t0
     if one > 15.0:
         n_rows, seqs = oracle_sample(cpu, budget_rows=2048, max_seqs=max(1, int(len(seqs) * 10.0 / one)))
         t0 = time.perf_counter()
-        nbytes = oracle_step(cpu, codes, scales, n_rows, seqs, threads)
+        nbytes = oracle_step(cpu, codes, scales, n_rows, seqs, threads, ix)
     passes = 1
     while time.perf_counter() - t0 < 10.0 and passes < 200:
-        nbytes += oracle_step(cpu, codes, scales, n_rows, seqs, threads)
+        nbytes += oracle_step(cpu, codes, scales, n_rows, seqs, threads, ix)
         passes += 1
     dt = time.perf_counter() - t0
     return {"value": round(nbytes / dt / 1e9, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
@@ -442,13 +497,14 @@ def run_reference(args, world, rank):
     case = make_case(args, "cpu")
     O, cpu, codes, scales = prepare_oracle(case)
     threads = max(1, O.openmp_threads())
+    ix = sparse_lists(cpu, args)
     n_rows, seqs = oracle_sample(cpu, budget_rows=512, max_seqs=1)
     for _ in range(args.warmup):
-        oracle_step(cpu, codes, scales, n_rows, seqs, threads)
+        oracle_step(cpu, codes, scales, n_rows, seqs, threads, ix)
     t0 = time.perf_counter()
     nb = 0.0
     for _ in range(args.steps):
-        nb += oracle_step(cpu, codes, scales, n_rows, seqs, threads)
+        nb += oracle_step(cpu, codes, scales, n_rows, seqs, threads, ix)
     dt = time.perf_counter() - t0
     value = nb / dt / 1e9
     sample = "store of %d rows + fp64 decode of %d of %d sequences (all heads) per step" % (n_rows, len(seqs),
@@ -459,7 +515,7 @@ def run_reference(args, world, rank):
         "value": round(value, 5), "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(dt / args.steps * 1e3, 3), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded; workloads.py)",
-        "config": dict(workload_config(args, case, *algorithmic_bytes(case)[2:], world), sample=sample),
+        "config": dict(workload_config(args, case, *algorithmic_bytes(case, ix)[2:], world), sample=sample),
         "cpu_baseline": {"value": round(value, 5), "unit": "GB/s", "cores": threads, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": round(value, 5), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},

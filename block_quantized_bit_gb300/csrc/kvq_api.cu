@@ -68,9 +68,14 @@ struct WorkspacePlan {
 
 // 1 = CUDA-core kernel, 2 = tensor-core kernel, -1 = the requested path has no kernel for this shape.
 // Automatic: tensor cores where QK^T and PV are dense enough -- 8..16 query heads per kv head, or an MLA
-// pool read by a multiple of 64 query heads; the GQA tensor-core kernel also runs 1..7 heads (padded),
-// but measured slower there than the CUDA cores.
-int32_t choose_path(const kvq_layout& L, int32_t batch, int32_t num_q_heads, const kvq_decode_options* opt) {
+// pool read by a multiple of 64 query heads whose block tables can hold at least kMlaTcMinTokens tokens
+// in all (the MLA tensor-core kernel costs ~50 us however short the contexts: at batch 1 it measured 54
+// us at 256 and 1024 tokens against 21 and 58 us on the CUDA cores); the GQA tensor-core kernel also
+// runs 1..7 heads (padded), but measured slower there than the CUDA cores.
+constexpr int64_t kMlaTcMinTokens = 1024;
+
+int32_t choose_path(const kvq_layout& L, int32_t batch, int32_t num_q_heads, int32_t max_pages,
+                    const kvq_decode_options* opt) {
   const int32_t group = num_q_heads / L.num_kv_heads;
   const bool tc = L.mla ? decode_mla_tc_supported(L.head_dim, L.v_dim, L.mla, group, batch)
                         : decode_tc_supported(L.head_dim, L.v_dim, L.mla, group, batch);
@@ -78,7 +83,8 @@ int32_t choose_path(const kvq_layout& L, int32_t batch, int32_t num_q_heads, con
   const int32_t want = opt ? opt->path : 0;
   if (want == 2) return tc ? 2 : -1;
   if (want == 1) return cc ? 1 : -1;
-  if (tc && (group >= 8 || L.mla)) return 2;
+  const bool long_mla = static_cast<int64_t>(batch) * max_pages * kPageTokens >= kMlaTcMinTokens;
+  if (tc && (L.mla ? long_mla : group >= 8)) return 2;
   return cc ? 1 : -1;
 }
 
@@ -89,7 +95,7 @@ bool plan_workspace(const kvq_layout& L, int32_t batch, int32_t num_q_heads, int
   const int32_t group = num_q_heads / L.num_kv_heads;
   const int32_t pps = opt ? opt->pages_per_split : 0;
   if (pps < 0) return false;
-  const int32_t path = choose_path(L, batch, num_q_heads, opt);
+  const int32_t path = choose_path(L, batch, num_q_heads, max_pages, opt);
   w->path = path;
   if (path == 2 && L.mla) w->heads_per_item = decode_mla_tc_heads_per_item(group);
   else w->heads_per_item = (path == 2) ? group : cc_heads_per_item(group, L.head_dim, L.mla);
@@ -127,6 +133,111 @@ int64_t max_work_items(int32_t batch, int32_t query_groups, int32_t max_pages, i
 }  // namespace kvq
 
 using namespace kvq;
+
+namespace {
+
+kvq_status decode_common(const void* q, const void* pool, const void* scales, const int32_t* block_table,
+                         int32_t max_pages_per_seq, const int32_t* seq_lens, int32_t batch, int32_t num_q_heads,
+                         float sm_scale, void* out, kvq_out_dtype out_dtype, void* workspace,
+                         size_t workspace_bytes, const kvq_layout* layout, kvq_kind kind,
+                         const kvq_decode_options* options, void* stream, bool clear_status) {
+  kvq_status st = check_layout(layout);
+  if (st != KVQ_OK) return st;
+  if (!kind_ok(kind)) return KVQ_EKIND;
+  if (out_dtype != KVQ_OUT_BF16 && out_dtype != KVQ_OUT_F32) return KVQ_EINVAL;
+  if (batch < 0 || num_q_heads <= 0 || max_pages_per_seq <= 0) return KVQ_EINVAL;
+  if (num_q_heads % layout->num_kv_heads != 0) return KVQ_EINVAL;
+  if (!(sm_scale == sm_scale) || sm_scale > std::numeric_limits<float>::max() ||
+      sm_scale < -std::numeric_limits<float>::max())
+    return KVQ_EINVAL;
+  if (options && (options->pages_per_split < 0 || options->path < 0 || options->path > 2)) return KVQ_EINVAL;
+  if (layout->page_size != kPageTokens) return KVQ_EUNSUPPORTED;
+  WorkspacePlan w;
+  if (!plan_workspace(*layout, batch, num_q_heads, max_pages_per_seq, options, &w)) return KVQ_EINVAL;
+  if (w.path < 0) return KVQ_EUNSUPPORTED;
+  if (batch == 0) return KVQ_OK;
+  if (!q || !pool || !scales || !block_table || !seq_lens || !out || !workspace) return KVQ_EINVAL;
+  if (workspace_bytes < w.total) return KVQ_EWORKSPACE;
+  if (!aligned(q) || !aligned(pool) || !aligned(scales) || !aligned(out) || !aligned(workspace) ||
+      (reinterpret_cast<uintptr_t>(block_table) % 4) != 0 || (reinterpret_cast<uintptr_t>(seq_lens) % 4) != 0)
+    return KVQ_EALIGN;
+  st = kvq_device_check();
+  if (st != KVQ_OK) return st;
+
+  DecodeArgs a;
+  a.q = q;
+  a.codes = static_cast<const uint8_t*>(pool);
+  a.scales = static_cast<const uint16_t*>(scales);
+  a.block_table = block_table;
+  a.num_pages = layout->num_pages;
+  a.max_pages = max_pages_per_seq;
+  a.seq_lens = seq_lens;
+  a.batch = batch;
+  a.num_q_heads = num_q_heads;
+  a.num_kv_heads = layout->num_kv_heads;
+  a.head_dim = layout->head_dim;
+  a.v_dim = layout->v_dim;
+  a.mla = layout->mla;
+  a.sm_scale = sm_scale;
+  a.out = out;
+  a.out_dtype = out_dtype;
+  a.kind = kind;
+  a.pages_per_split = options ? options->pages_per_split : 0;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  a.status = reinterpret_cast<uint32_t*>(ws);
+  a.part_acc = reinterpret_cast<float*>(ws + w.acc_offset);
+  a.part_ml = reinterpret_cast<float*>(ws + w.ml_offset);
+  a.plan_tab = reinterpret_cast<int32_t*>(ws + w.tab_offset);
+  a.split_cnt = (w.path == 1) ? reinterpret_cast<int32_t*>(ws + w.cnt_offset) : nullptr;
+  a.max_items = w.max_items;
+  a.heads_per_item = w.heads_per_item;
+  a.split_align = w.split_align;
+  a.target_items = w.target_items;
+  a.min_one_split = (w.path == 1) ? 1 : 0;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // status word and split counters (the counters only on the CUDA-core path, which merges in-kernel)
+  // (a caller that already recorded errors in the status word, the sparse decode, keeps it)
+  const size_t clear = (w.path == 1) ? w.acc_offset : sizeof(uint32_t);
+  const size_t from = clear_status ? 0 : kWorkspaceHeader;
+  if (clear > from && cudaMemsetAsync(ws + from, 0, clear - from, s) != cudaSuccess) return KVQ_ECUDA;
+  if (w.path == 2) st = a.mla ? launch_decode_mla_tc(a, s) : launch_decode_tc(a, s);
+  else return launch_decode_cc(a, s);
+  if (st != KVQ_OK) return st;
+  return launch_merge(a, w.query_groups, s);
+}
+
+// Sparse decode: the dense decode's workspace first (its status word at offset 0 is the call's), then
+// the compact pool, its block table and its sequence lengths.  cpages = ceil(topk / 16) pages per
+// sequence hold every column a list can select.
+struct SparsePlan {
+  kvq_layout compact;
+  int32_t cpages;
+  size_t dense_bytes, codes_offset, scales_offset, table_offset, lens_offset, total;
+};
+
+bool plan_sparse(const kvq_layout* layout, int32_t batch, int32_t num_q_heads, int32_t topk, SparsePlan* sp) {
+  if (check_layout(layout) != KVQ_OK) return false;
+  if (batch < 0 || num_q_heads <= 0 || topk < 0 || topk > kMaxSparseTopk) return false;
+  if (num_q_heads % layout->num_kv_heads != 0) return false;
+  sp->cpages = std::max<int32_t>(1, (topk + kPageTokens - 1) / kPageTokens);
+  sp->compact = *layout;
+  sp->compact.num_pages = static_cast<int64_t>(std::max<int32_t>(batch, 1)) * sp->cpages;
+  WorkspacePlan w;
+  if (!plan_workspace(sp->compact, batch, num_q_heads, sp->cpages, nullptr, &w)) return false;
+  auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+  const size_t n_kv = layout->mla ? 1 : 2;
+  const size_t rows = static_cast<size_t>(sp->compact.num_pages) * kPageTokens * n_kv * layout->num_kv_heads;
+  sp->dense_bytes = up(w.total);
+  sp->codes_offset = sp->dense_bytes;
+  sp->scales_offset = sp->codes_offset + up(rows * layout->head_dim);
+  sp->table_offset = sp->scales_offset + up(rows * (layout->head_dim / 32) * sizeof(uint16_t));
+  sp->lens_offset = sp->table_offset + up(static_cast<size_t>(sp->compact.num_pages) * sizeof(int32_t));
+  sp->total = sp->lens_offset + up(static_cast<size_t>(std::max<int32_t>(batch, 1)) * sizeof(int32_t));
+  return true;
+}
+
+}  // namespace
+
 
 extern "C" {
 
@@ -199,13 +310,14 @@ kvq_status kvq_store(void* pool, void* scales, const void* k, const void* v, con
                       static_cast<cudaStream_t>(stream));
 }
 
-int32_t kvq_decode_path(const kvq_layout* layout, int32_t batch, int32_t num_q_heads,
+int32_t kvq_decode_path(const kvq_layout* layout, int32_t batch, int32_t num_q_heads, int32_t max_pages_per_seq,
                         const kvq_decode_options* options) {
   if (check_layout(layout) != KVQ_OK) return KVQ_EINVAL;
   if (batch < 0 || num_q_heads <= 0 || num_q_heads % layout->num_kv_heads != 0) return KVQ_EINVAL;
+  if (max_pages_per_seq <= 0) return KVQ_EINVAL;
   if (options && (options->pages_per_split < 0 || options->path < 0 || options->path > 2)) return KVQ_EINVAL;
   if (layout->page_size != kPageTokens) return KVQ_EUNSUPPORTED;
-  const int32_t path = choose_path(*layout, batch, num_q_heads, options);
+  const int32_t path = choose_path(*layout, batch, num_q_heads, max_pages_per_seq, options);
   return path < 0 ? static_cast<int32_t>(KVQ_EUNSUPPORTED) : path;
 }
 
@@ -227,66 +339,8 @@ kvq_status kvq_decode_ex(const void* q, const void* pool, const void* scales, co
                          float sm_scale, void* out, kvq_out_dtype out_dtype, void* workspace,
                          size_t workspace_bytes, const kvq_layout* layout, kvq_kind kind,
                          const kvq_decode_options* options, void* stream) {
-  kvq_status st = check_layout(layout);
-  if (st != KVQ_OK) return st;
-  if (!kind_ok(kind)) return KVQ_EKIND;
-  if (out_dtype != KVQ_OUT_BF16 && out_dtype != KVQ_OUT_F32) return KVQ_EINVAL;
-  if (batch < 0 || num_q_heads <= 0 || max_pages_per_seq <= 0) return KVQ_EINVAL;
-  if (num_q_heads % layout->num_kv_heads != 0) return KVQ_EINVAL;
-  if (!(sm_scale == sm_scale) || sm_scale > std::numeric_limits<float>::max() ||
-      sm_scale < -std::numeric_limits<float>::max())
-    return KVQ_EINVAL;
-  if (options && (options->pages_per_split < 0 || options->path < 0 || options->path > 2)) return KVQ_EINVAL;
-  if (layout->page_size != kPageTokens) return KVQ_EUNSUPPORTED;
-  WorkspacePlan w;
-  if (!plan_workspace(*layout, batch, num_q_heads, max_pages_per_seq, options, &w)) return KVQ_EINVAL;
-  if (w.path < 0) return KVQ_EUNSUPPORTED;
-  if (batch == 0) return KVQ_OK;
-  if (!q || !pool || !scales || !block_table || !seq_lens || !out || !workspace) return KVQ_EINVAL;
-  if (workspace_bytes < w.total) return KVQ_EWORKSPACE;
-  if (!aligned(q) || !aligned(pool) || !aligned(scales) || !aligned(out) || !aligned(workspace) ||
-      (reinterpret_cast<uintptr_t>(block_table) % 4) != 0 || (reinterpret_cast<uintptr_t>(seq_lens) % 4) != 0)
-    return KVQ_EALIGN;
-  st = kvq_device_check();
-  if (st != KVQ_OK) return st;
-
-  DecodeArgs a;
-  a.q = q;
-  a.codes = static_cast<const uint8_t*>(pool);
-  a.scales = static_cast<const uint16_t*>(scales);
-  a.block_table = block_table;
-  a.num_pages = layout->num_pages;
-  a.max_pages = max_pages_per_seq;
-  a.seq_lens = seq_lens;
-  a.batch = batch;
-  a.num_q_heads = num_q_heads;
-  a.num_kv_heads = layout->num_kv_heads;
-  a.head_dim = layout->head_dim;
-  a.v_dim = layout->v_dim;
-  a.mla = layout->mla;
-  a.sm_scale = sm_scale;
-  a.out = out;
-  a.out_dtype = out_dtype;
-  a.kind = kind;
-  a.pages_per_split = options ? options->pages_per_split : 0;
-  uint8_t* ws = static_cast<uint8_t*>(workspace);
-  a.status = reinterpret_cast<uint32_t*>(ws);
-  a.part_acc = reinterpret_cast<float*>(ws + w.acc_offset);
-  a.part_ml = reinterpret_cast<float*>(ws + w.ml_offset);
-  a.plan_tab = reinterpret_cast<int32_t*>(ws + w.tab_offset);
-  a.split_cnt = (w.path == 1) ? reinterpret_cast<int32_t*>(ws + w.cnt_offset) : nullptr;
-  a.max_items = w.max_items;
-  a.heads_per_item = w.heads_per_item;
-  a.split_align = w.split_align;
-  a.target_items = w.target_items;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  // status word and split counters (the counters only on the CUDA-core path, which merges in-kernel)
-  const size_t clear = (w.path == 1) ? w.acc_offset : sizeof(uint32_t);
-  if (cudaMemsetAsync(ws, 0, clear, s) != cudaSuccess) return KVQ_ECUDA;
-  if (w.path == 2) st = a.mla ? launch_decode_mla_tc(a, s) : launch_decode_tc(a, s);
-  else return launch_decode_cc(a, s);
-  if (st != KVQ_OK) return st;
-  return launch_merge(a, w.query_groups, s);
+  return decode_common(q, pool, scales, block_table, max_pages_per_seq, seq_lens, batch, num_q_heads, sm_scale, out,
+                       out_dtype, workspace, workspace_bytes, layout, kind, options, stream, true);
 }
 
 kvq_status kvq_decode(const void* q, const void* pool, const void* scales, const int32_t* block_table,
@@ -295,6 +349,62 @@ kvq_status kvq_decode(const void* q, const void* pool, const void* scales, const
                       const kvq_layout* layout, kvq_kind kind, void* stream) {
   return kvq_decode_ex(q, pool, scales, block_table, max_pages_per_seq, seq_lens, batch, num_q_heads, sm_scale, out,
                        out_dtype, workspace, workspace_bytes, layout, kind, nullptr, stream);
+}
+
+size_t kvq_decode_sparse_workspace_bytes(const kvq_layout* layout, int32_t batch, int32_t num_q_heads, int32_t topk) {
+  SparsePlan sp;
+  if (!plan_sparse(layout, batch, num_q_heads, topk, &sp)) return 0;
+  return sp.total;
+}
+
+kvq_status kvq_decode_sparse(const void* q, const void* pool, const void* scales, const int32_t* block_table,
+                             int32_t max_pages_per_seq, const int32_t* seq_lens, const int32_t* indices, int32_t topk,
+                             int32_t batch, int32_t num_q_heads, float sm_scale, void* out, kvq_out_dtype out_dtype,
+                             void* workspace, size_t workspace_bytes, const kvq_layout* layout, kvq_kind kind,
+                             void* stream) {
+  kvq_status st = check_layout(layout);
+  if (st != KVQ_OK) return st;
+  if (!kind_ok(kind)) return KVQ_EKIND;
+  if (out_dtype != KVQ_OUT_BF16 && out_dtype != KVQ_OUT_F32) return KVQ_EINVAL;
+  if (max_pages_per_seq <= 0) return KVQ_EINVAL;
+  SparsePlan sp;
+  if (!plan_sparse(layout, batch, num_q_heads, topk, &sp)) return KVQ_EINVAL;
+  if (layout->page_size != kPageTokens || layout->head_dim % 64 != 0) return KVQ_EUNSUPPORTED;
+  if (batch == 0) return KVQ_OK;
+  if (!q || !pool || !scales || !block_table || !seq_lens || (topk > 0 && !indices) || !out || !workspace)
+    return KVQ_EINVAL;
+  if (workspace_bytes < sp.total) return KVQ_EWORKSPACE;
+  if (!aligned(pool) || !aligned(scales) || !aligned(workspace) || (reinterpret_cast<uintptr_t>(block_table) % 4) != 0 ||
+      (reinterpret_cast<uintptr_t>(seq_lens) % 4) != 0 || (reinterpret_cast<uintptr_t>(indices) % 4) != 0)
+    return KVQ_EALIGN;
+  st = kvq_device_check();
+  if (st != KVQ_OK) return st;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(ws, 0, sizeof(uint32_t), s) != cudaSuccess) return KVQ_ECUDA;
+  SparseGatherArgs g;
+  g.codes = static_cast<const uint8_t*>(pool);
+  g.scales = static_cast<const uint16_t*>(scales);
+  g.block_table = block_table;
+  g.seq_lens = seq_lens;
+  g.indices = indices;
+  g.dst_codes = ws + sp.codes_offset;
+  g.dst_scales = reinterpret_cast<uint16_t*>(ws + sp.scales_offset);
+  g.dst_table = reinterpret_cast<int32_t*>(ws + sp.table_offset);
+  g.dst_lens = reinterpret_cast<int32_t*>(ws + sp.lens_offset);
+  g.status = reinterpret_cast<uint32_t*>(ws);
+  g.num_pages = layout->num_pages;
+  g.max_pages = max_pages_per_seq;
+  g.batch = batch;
+  g.topk = topk;
+  g.cpages = sp.cpages;
+  g.n_kv = layout->mla ? 1 : 2;
+  g.Hkv = layout->num_kv_heads;
+  g.D = layout->head_dim;
+  st = launch_sparse_gather(g, s);
+  if (st != KVQ_OK) return st;
+  return decode_common(q, g.dst_codes, g.dst_scales, g.dst_table, sp.cpages, g.dst_lens, batch, num_q_heads, sm_scale,
+                       out, out_dtype, workspace, sp.dense_bytes, &sp.compact, kind, nullptr, stream, false);
 }
 
 kvq_status kvq_workspace_status(const void* workspace, void* stream) {

@@ -39,6 +39,8 @@ struct DecodeArgs {
   int32_t heads_per_item;  // query heads one work item covers (a tile of the group)
   int32_t split_align;     // automatic split sizes are a multiple of this many pages
   int32_t target_items;    // automatic split sizes aim at about this many work items
+  int32_t min_one_split;   // nonzero: every (sequence, group) has at least one split (an empty one when
+                           // the sequence has no page), as the kernel that merges in-kernel needs
 };
 
 // Tokens per page the decode kernels support, and the workspace's leading status block.
@@ -70,5 +72,27 @@ kvq_status launch_decode_mla_tc(const DecodeArgs& a, cudaStream_t stream);
 kvq_status launch_decode_tc(const DecodeArgs& a, cudaStream_t stream);
 kvq_status launch_decode_cc(const DecodeArgs& a, cudaStream_t stream);
 kvq_status launch_merge(const DecodeArgs& a, int32_t query_groups, cudaStream_t stream);
+
+// Sparse decode: the gather of the selected columns into a compact pool (pages b * cpages ..).
+struct SparseGatherArgs {
+  const uint8_t* codes;
+  const uint16_t* scales;
+  const int32_t* block_table;
+  const int32_t* seq_lens;
+  const int32_t* indices;   // [batch][topk]
+  uint8_t* dst_codes;
+  uint16_t* dst_scales;
+  int32_t* dst_table;       // [batch][cpages]
+  int32_t* dst_lens;        // [batch]
+  uint32_t* status;
+  int64_t num_pages;
+  int32_t max_pages;
+  int32_t batch;
+  int32_t topk;
+  int32_t cpages;
+  int32_t n_kv, Hkv, D;
+};
+constexpr int32_t kMaxSparseTopk = 8192;
+kvq_status launch_sparse_gather(const SparseGatherArgs& g, cudaStream_t stream);
 
 }  // namespace kvq

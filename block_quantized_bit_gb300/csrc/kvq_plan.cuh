@@ -44,6 +44,8 @@ struct KParams {
   int32_t head_tiles;     // group / heads_per_item
   int32_t pages_per_split;
   int32_t target_items;   // automatic split sizes aim at about this many items
+  int32_t min_one_split;  // nonzero: a sequence without pages still gets one (empty) split per group, so
+                          // that the kernel which merges in-kernel writes its zero output
   float score_scale;      // sm_scale * log2(e)
 };
 
@@ -88,7 +90,8 @@ __device__ Plan make_plan(const KParams& p, int32_t want_item, int32_t want_b) {
   }
   // 2) items per sequence, exclusive scan over the batch
   int32_t mine = 0;
-  for (int32_t b = b0; b < b1; ++b) mine += groups * ((seq_pages(p, b) + C - 1) / C);
+  auto splits_of = [&](int32_t b) { return max((seq_pages(p, b) + C - 1) / C, p.min_one_split ? 1 : 0); };
+  for (int32_t b = b0; b < b1; ++b) mine += groups * splits_of(b);
   int32_t incl = mine;
   for (int o = 1; o < 32; o <<= 1) {
     const int32_t y = __shfl_up_sync(0xffffffffu, incl, o);
@@ -103,7 +106,7 @@ __device__ Plan make_plan(const KParams& p, int32_t want_item, int32_t want_b) {
   }
   int32_t run = warp_off + incl - mine;  // first item of b0
   for (int32_t b = b0; b < b1; ++b) {
-    const int32_t ns = (seq_pages(p, b) + C - 1) / C;
+    const int32_t ns = splits_of(b);
     const int32_t n = groups * ns;
     if (blockIdx.x == 0 && p.plan_tab) {  // for the merge, which then needs no plan of its own
       p.plan_tab[2 * b] = run;
@@ -158,6 +161,7 @@ inline KParams make_kparams(const DecodeArgs& a) {
   p.score_scale = a.sm_scale * kLog2e;
   p.split_align = a.split_align;
   p.target_items = a.target_items > 0 ? a.target_items : kTargetItems;
+  p.min_one_split = a.min_one_split;
   return p;
 }
 

@@ -27,7 +27,8 @@ STATUS = {0: "KVQ_OK", -1: "KVQ_EINVAL", -2: "KVQ_EKIND", -3: "KVQ_EHEADDIM", -4
           -5: "KVQ_EWORKSPACE", -6: "KVQ_EARCH", -7: "KVQ_ECUDA", -8: "KVQ_EUNSUPPORTED", -9: "KVQ_ETIMEOUT"}
 
 EXPORTS = ["kvq_pool_bytes", "kvq_scale_bytes", "kvq_bytes_per_token", "kvq_num_pages", "kvq_store",
-           "kvq_decode_workspace_bytes", "kvq_decode_workspace_bytes_ex", "kvq_decode_path", "kvq_decode", "kvq_decode_ex",
+           "kvq_decode_workspace_bytes", "kvq_decode_workspace_bytes_ex", "kvq_decode_path",
+           "kvq_decode_sparse_workspace_bytes", "kvq_decode_sparse", "kvq_decode", "kvq_decode_ex",
            "kvq_workspace_status", "kvq_encode_probe", "kvq_quantize_probe", "kvq_dequant_probe", "kvq_strerror",
            "kvq_device_check", "kvq_version", "kvq_decode_noalloc"]
 
@@ -68,7 +69,10 @@ def lib():
             "kvq_store": (i32, [P, P, P, P, P, i64, LP, i32, P]),
             "kvq_decode_workspace_bytes": (sz, [LP, i32, i32, i32]),
             "kvq_decode_workspace_bytes_ex": (sz, [LP, i32, i32, i32, OP]),
-            "kvq_decode_path": (i32, [LP, i32, i32, OP]),
+            "kvq_decode_path": (i32, [LP, i32, i32, i32, OP]),
+            "kvq_decode_sparse_workspace_bytes": (sz, [LP, i32, i32, i32]),
+            "kvq_decode_sparse": (i32, [P, P, P, P, i32, P, P, i32, i32, i32, ctypes.c_float, P, i32, P, sz, LP,
+                                        i32, P]),
             "kvq_decode": (i32, [P, P, P, P, i32, P, i32, i32, ctypes.c_float, P, i32, P, sz, LP, i32, P]),
             "kvq_decode_ex": (i32, [P, P, P, P, i32, P, i32, i32, ctypes.c_float, P, i32, P, sz, LP, i32, OP, P]),
             "kvq_workspace_status": (i32, [P, P]),
@@ -182,10 +186,12 @@ def kvq_decode_workspace_bytes(layout: Layout, batch: int, num_q_heads: int, max
                                                int(max_pages_per_seq), ctypes.byref(o))
 
 
-def kvq_decode_path(layout: Layout, batch: int, num_q_heads: int, pages_per_split=0, path=0) -> int:
+def kvq_decode_path(layout: Layout, batch: int, num_q_heads: int, max_pages_per_seq: int, pages_per_split=0,
+                    path=0) -> int:
     """1 (CUDA cores, one launch) or 2 (tensor cores + merge, two launches); negative status if none."""
     o = _opts(pages_per_split, path)
-    return lib().kvq_decode_path(ctypes.byref(layout.c()), int(batch), int(num_q_heads), ctypes.byref(o))
+    return lib().kvq_decode_path(ctypes.byref(layout.c()), int(batch), int(num_q_heads), int(max_pages_per_seq),
+                                 ctypes.byref(o))
 
 
 def alloc_workspace(layout: Layout, batch, num_q_heads, max_pages_per_seq, device="cuda", **opts):
@@ -226,6 +232,32 @@ def kvq_decode_noalloc(q: torch.Tensor, pool: torch.Tensor, scales: torch.Tensor
                                     _ptr(seq_lens), int(seq_lens.shape[0]), int(q.shape[1]), float(sm_scale),
                                     _ptr(out), od, ctypes.byref(layout.c()), _kind(kind), _stream(stream)),
            "kvq_decode_noalloc")
+
+
+def alloc_sparse_workspace(layout: Layout, batch: int, num_q_heads: int, topk: int, device="cuda"):
+    n = lib().kvq_decode_sparse_workspace_bytes(ctypes.byref(layout.c()), int(batch), int(num_q_heads), int(topk))
+    if n == 0:
+        raise KvqError(-1, "kvq_decode_sparse_workspace_bytes")
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def kvq_decode_sparse(q: torch.Tensor, pool: torch.Tensor, scales: torch.Tensor, block_table: torch.Tensor,
+                      seq_lens: torch.Tensor, indices: torch.Tensor, out: torch.Tensor, workspace: torch.Tensor,
+                      layout: Layout, kind, sm_scale: float = 1.0, stream=None):
+    """Sparse (top-K) decode over the columns ``indices`` ([B, topk] int32, -1 = masked) selects."""
+    if out.dtype == torch.bfloat16:
+        od = KVQ_OUT_BF16
+    elif out.dtype == torch.float32:
+        od = KVQ_OUT_F32
+    else:
+        raise TypeError("out must be bfloat16 or float32")
+    B, Hq = q.shape[0], q.shape[1]
+    topk = indices.shape[1] if indices.dim() == 2 else 0
+    _check(lib().kvq_decode_sparse(_ptr(q), _ptr(pool), _ptr(scales), _ptr(block_table), int(block_table.shape[1]),
+                                   _ptr(seq_lens), _ptr(indices), int(topk), int(B), int(Hq), float(sm_scale),
+                                   _ptr(out), od, _ptr(workspace), int(workspace.numel() * workspace.element_size()),
+                                   ctypes.byref(layout.c()),
+                                   _kind(kind), _stream(stream)), "kvq_decode_sparse")
 
 
 def kvq_workspace_status(workspace: torch.Tensor, stream=None) -> int:

@@ -24,6 +24,8 @@ Five families, named for what they are:
                [256, 131072], pages randomly permuted, 1% of K/V values scaled by 100; each step stores
                one new row per sequence and decodes it.
 
+``sparse_indices`` draws the per-sequence index lists of the sparse (top-K) decode for any family.
+
 Page size is 16 everywhere.  The softmax scale is 1.0 because q is drawn already divided by
 sqrt(head_dim).
 """
@@ -239,6 +241,23 @@ def serving(kind="fp8_e4m3", seed=1005, device="cpu", batch=64, median=4096, sig
     return Case("serving", kind, Hq, Hkv, D, D, PAGE_SIZE, False, num_pages, _bf16(k), _bf16(v),
                 sm_ctx.to(device), _bf16(q), bt.to(device), seq_lens.to(device),
                 new_k=_bf16(k[is_new_d]), new_v=_bf16(v[is_new_d]), new_slots=sm_all[is_new].to(device))
+
+
+def sparse_indices(case, topk, seed=1006, masked_frac=0.01, device=None):
+    """[B, topk] int32 index lists for the sparse (top-K) decode: for each sequence, topk distinct token
+    positions drawn uniformly from [0, seq_len) in random order (all positions, then -1 padding, when the
+    sequence is shorter), with a fraction ``masked_frac`` of the columns set to -1 (masked columns)."""
+    g = _gen("cpu", seed)
+    lens = [int(x) for x in case.seq_lens.cpu()]
+    ix = torch.full((len(lens), topk), -1, dtype=torch.int32)
+    for b, L in enumerate(lens):
+        n = min(topk, L)
+        if n:
+            ix[b, :n] = torch.randperm(L, generator=g)[:n].to(torch.int32)
+        if masked_frac > 0 and topk:
+            drop = torch.rand((topk,), generator=g) < masked_frac
+            ix[b][drop] = -1
+    return ix.to(device if device is not None else case.seq_lens.device)
 
 
 FAMILIES = {"tiny": tiny, "qwen3_1p7b": qwen3_1p7b, "long_gqa": long_gqa, "mla": mla, "serving": serving}

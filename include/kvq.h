@@ -140,7 +140,8 @@ size_t kvq_decode_workspace_bytes_ex(const kvq_layout* layout, int32_t batch, in
  * MLA row with at most 64 query heads (or a multiple of 64) and batch <= 1024; a merge kernel follows
  * them (two launches).  They feed P to the MMA as bf16, so their error relative to the exact result
  * grows with the magnitude of V (about 2^-9 of max |V|).  Automatic (0) picks 2 for 8..16 query heads
- * per kv head and for the MLA row, and 1 otherwise; kvq_decode_path tells which.
+ * per kv head, and for the MLA row when batch * max_pages_per_seq * 16 >= 1024 (the MLA tensor-core
+ * kernel has a fixed cost of ~50 us); 1 otherwise; kvq_decode_path tells which.
  */
 kvq_status kvq_decode(const void* q, const void* pool, const void* scales, const int32_t* block_table,
                       int32_t max_pages_per_seq, const int32_t* seq_lens, int32_t batch, int32_t num_q_heads,
@@ -153,12 +154,36 @@ kvq_status kvq_decode_ex(const void* q, const void* pool, const void* scales, co
                          const kvq_decode_options* options, void* stream);
 
 /*
+ * Sparse (top-K) decode ("Experimental FP8 KV Cache": a query reads the K selected tokens of a long
+ * latent pool; "feat(kvcache): 8-bit DSV4 window/compressed KV", section "Testing": masked -1 columns).
+ *   indices      device int32 [batch][topk]: token positions of sequence b.  A column is valid when its
+ *                position p satisfies 0 <= p < seq_lens[b] and block_table[b][p / 16] is not -1; -1 and
+ *                any other invalid column are skipped; a position listed twice counts twice.
+ *   topk         columns per sequence, 0 .. 8192 (0: every output is zero)
+ * Other arguments as kvq_decode; the workspace comes from kvq_decode_sparse_workspace_bytes.  For every
+ * (b, h) the result is softmax(sm_scale * q.K^T) V over the valid columns (order does not matter), with
+ * K and V dequantized to bf16; no valid column gives zeros.  The library gathers the valid columns of
+ * each sequence into a compact pool in the workspace (a byte copy of codes and scales), then runs the
+ * dense decode over it, so the kernel choice and precision are those of kvq_decode for a sequence of
+ * that many tokens.  Supported: page_size 16 and head_dim a multiple of 64 (every kvq_decode shape).
+ * A block-table entry >= layout->num_pages at a selected position is skipped and makes
+ * kvq_workspace_status report KVQ_EINVAL.
+ */
+size_t kvq_decode_sparse_workspace_bytes(const kvq_layout* layout, int32_t batch, int32_t num_q_heads,
+                                         int32_t topk);
+kvq_status kvq_decode_sparse(const void* q, const void* pool, const void* scales, const int32_t* block_table,
+                             int32_t max_pages_per_seq, const int32_t* seq_lens, const int32_t* indices,
+                             int32_t topk, int32_t batch, int32_t num_q_heads, float sm_scale, void* out,
+                             kvq_out_dtype out_dtype, void* workspace, size_t workspace_bytes,
+                             const kvq_layout* layout, kvq_kind kind, void* stream);
+
+/*
  * The decode kernel kvq_decode_ex would run for these sizes and options: 1 (CUDA cores, one launch) or
  * 2 (tensor cores, two launches with the merge).  Otherwise a negative kvq_status: KVQ_EINVAL for an
  * invalid layout, size or option, KVQ_EUNSUPPORTED when no kernel supports the shape.  Host only, no
  * device call; options may be NULL.
  */
-int32_t kvq_decode_path(const kvq_layout* layout, int32_t batch, int32_t num_q_heads,
+int32_t kvq_decode_path(const kvq_layout* layout, int32_t batch, int32_t num_q_heads, int32_t max_pages_per_seq,
                         const kvq_decode_options* options);
 
 /*

@@ -129,13 +129,18 @@ def test_workspace_bound_covers_every_split_choice(lib):
 
 
 def test_decode_path_follows_the_group_size_and_the_options(lib):
-    assert kvq.kvq_decode_path(L(num_kv_heads=8), 8, 16) == 1                         # G = 2: CUDA cores
-    assert kvq.kvq_decode_path(L(num_kv_heads=2, head_dim=256, v_dim=256), 8, 16) == 2  # G = 8: tcgen05
-    assert kvq.kvq_decode_path(L(num_kv_heads=1, head_dim=576, v_dim=512, mla=True), 1, 128) == 2
-    assert kvq.kvq_decode_path(L(num_kv_heads=2, head_dim=256, v_dim=256), 8, 16, path=1) == 1
-    assert kvq.kvq_decode_path(L(num_kv_heads=8, head_dim=64, v_dim=64), 8, 16, path=2) == -8  # unsupported
-    assert kvq.kvq_decode_path(L(), 4, 7) == -1             # Hq % Hkv != 0
-    assert kvq.kvq_decode_path(L(), 4, 8, path=3) == -1
+    mla = L(num_kv_heads=1, head_dim=576, v_dim=512, mla=True)
+    assert kvq.kvq_decode_path(L(num_kv_heads=8), 8, 16, 1024) == 1                          # G = 2: CUDA cores
+    assert kvq.kvq_decode_path(L(num_kv_heads=2, head_dim=256, v_dim=256), 8, 16, 64) == 2  # G = 8: tcgen05
+    assert kvq.kvq_decode_path(mla, 1, 128, 10240) == 2                                     # long MLA context
+    assert kvq.kvq_decode_path(mla, 1, 128, 16) == 1                                        # 256 tokens at most
+    assert kvq.kvq_decode_path(mla, 4, 128, 16) == 2                                        # 4 x 256 tokens
+    assert kvq.kvq_decode_path(mla, 1, 128, 16, path=2) == 2                                # forced
+    assert kvq.kvq_decode_path(L(num_kv_heads=2, head_dim=256, v_dim=256), 8, 16, 64, path=1) == 1
+    assert kvq.kvq_decode_path(L(num_kv_heads=8, head_dim=64, v_dim=64), 8, 16, 64, path=2) == -8  # unsupported
+    assert kvq.kvq_decode_path(L(), 4, 7, 64) == -1                                         # Hq % Hkv != 0
+    assert kvq.kvq_decode_path(L(), 4, 8, 64, path=3) == -1
+    assert kvq.kvq_decode_path(L(), 4, 8, 0) == -1
 
 
 def test_strerror_has_a_message_for_every_status(lib):

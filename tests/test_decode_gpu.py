@@ -74,13 +74,16 @@ def test_decode_never_reads_nan_bytes_past_a_sequence_end():
     assert_decode_close(got, ref)
 
 
-def test_decode_empty_and_fully_masked_sequences_give_zeros():
+@pytest.mark.parametrize("path", [1, 2])
+def test_decode_empty_and_fully_masked_sequences_give_zeros(path):
+    """Both kernels: the CUDA-core one merges in-kernel, so an empty sequence still needs a (trivial)
+    work item to write its zeros; the tensor-core one leaves that to the merge kernel."""
     case = workloads.long_gqa(kind="q8_0", batch=3, ctx=300, mask_frac=0.0)
     case.block_table[1, :] = -1                      # every page of sequence 1 masked
     case.seq_lens[2] = 0                             # sequence 2 empty
     L, codes, scales = gpu_pool(case)
     gpu_store(case, codes, scales)
-    got = gpu_decode(case, codes, scales)
+    got = gpu_decode(case, codes, scales, path=path)
     oc, osc = oracle_pool(case)
     oracle_store(case, oc, osc)
     ref = oracle_decode(case, oc, osc)

@@ -17,7 +17,7 @@ import pytest
 import torch
 
 import oracle as O
-from block_quantized_bit_gb300 import workloads
+from block_quantized_bit_gb300 import kvq, workloads
 
 from parity import assert_decode_close, bits, gpu_decode, gpu_pool, gpu_store
 
@@ -125,3 +125,38 @@ def test_full_size_store_and_decode_match_the_oracle_on_samples(key, kind):
         assert_decode_close(got[b, heads, :], ref)
     del codes, scales, case
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("kind", ["fp8_e4m3", "q8_0"])
+def test_full_size_sparse_mla_decode_matches_the_oracle(kind):
+    """The pages' sparse configuration: 163840-token latent pool, 128 heads, 256 selected columns (1%
+    masked).  The oracle quantizes only the selected rows, in list order, into a compact pool and
+    attends over all of them (attention does not depend on the order of its columns)."""
+    case = workloads.make("mla", kind=kind, device="cuda")
+    L, codes, scales = gpu_pool(case)
+    gpu_store(case, codes, scales)
+    ix = workloads.sparse_indices(case, 256)
+    out = torch.empty(case.batch, case.num_q_heads, case.v_dim, dtype=torch.float32, device="cuda")
+    ws = kvq.alloc_sparse_workspace(L, case.batch, case.num_q_heads, ix.shape[1])
+    kvq.kvq_decode_sparse(case.q, codes, scales, case.block_table, case.seq_lens, ix, out, ws, L, case.kind,
+                          case.sm_scale)
+    torch.cuda.synchronize()
+    assert kvq.kvq_workspace_status(ws) == 0
+    got = out.cpu().numpy().astype(np.float64)
+    P = case.page_size
+    for b in range(case.batch):
+        off, Lb = _rows_of_sequence(case, b)
+        bt = case.block_table[b].cpu().numpy()
+        cols = [int(p) for p in ix[b].cpu().numpy() if 0 <= p < Lb and bt[p // P] >= 0]
+        n = len(cols)
+        npg = max((n + P - 1) // P, 1)
+        cs, ss = O.pool_shapes(npg, P, 1, case.head_dim, case.mla)
+        oc, osc = np.zeros(cs, np.uint8), np.zeros(ss, np.uint16)
+        O.store(oc, osc, bits(case.k[[off + p for p in cols]]), None, np.arange(n, dtype=np.int64), num_kv_heads=1,
+                head_dim=case.head_dim, page_size=P, mla=True, kind=case.kind)
+        ref = O.decode_sparse(bits(case.q[b:b + 1]), oc, osc, np.arange(npg, dtype=np.int32)[None, :],
+                              np.array([n], np.int32), np.arange(n, dtype=np.int32)[None, :],
+                              num_q_heads=case.num_q_heads, num_kv_heads=1, head_dim=case.head_dim,
+                              v_dim=case.v_dim, page_size=P, mla=True, kind=case.kind, sm_scale=case.sm_scale,
+                              nthreads=0)[0]
+        assert_decode_close(got[b], ref)
