@@ -625,15 +625,17 @@ kvq_status launch_decode_cc(const DecodeArgs& a, cudaStream_t stream) {
     if (gt == 1) return launch_cc_kind<576, 512, 1, true, 2, 1>(a, stream);
     return launch_cc_kind<576, 512, 2, true, 2, 1>(a, stream);
   }
-#define KVQ_CC_CASE(DD, STG, MB)                                                    \
+// (stages, CTAs per SM) per head_dim and heads per item: two heads at D = 128 fit 93 registers, so five
+// CTAs of two stages each stay resident (qwen3_1p7b 58 -> 55 us); four heads need the registers of four.
+#define KVQ_CC_CASE(DD, STG, MB, STG2, MB2)                                         \
   if (a.head_dim == DD) {                                                           \
     if (gt == 1) return launch_cc_kind<DD, DD, 1, false, STG, MB>(a, stream);       \
-    if (gt == 2) return launch_cc_kind<DD, DD, 2, false, STG, MB>(a, stream);       \
+    if (gt == 2) return launch_cc_kind<DD, DD, 2, false, STG2, MB2>(a, stream);     \
     return launch_cc_kind<DD, DD, 4, false, STG, MB>(a, stream);                    \
   }
-  KVQ_CC_CASE(64, 4, 4)
-  KVQ_CC_CASE(128, 3, 4)
-  KVQ_CC_CASE(256, 2, 3)
+  KVQ_CC_CASE(64, 4, 4, 4, 4)
+  KVQ_CC_CASE(128, 3, 4, 2, 5)
+  KVQ_CC_CASE(256, 2, 3, 2, 3)
 #undef KVQ_CC_CASE
   return KVQ_EUNSUPPORTED;
 }
