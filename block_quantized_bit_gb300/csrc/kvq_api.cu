@@ -102,8 +102,13 @@ bool plan_workspace(const kvq_layout& L, int32_t batch, int32_t num_q_heads, int
   w->split_align = (path == 2) ? 8 : 1;
   // Tensor-core items are expensive to start and finish (a pipeline fill, a q tile, an O readout, and
   // partials the merge must read): the GQA kernel aims at about two items per SM, the MLA kernel
-  // (64 query rows of 576, 64 x 512 partial outputs) at one, instead of eight.
-  w->target_items = (path == 2) ? (L.mla ? sm_count() : 2 * sm_count()) : kTargetItems;
+  // (64 query rows of 576, 64 x 512 partial outputs) at one.
+  // CUDA-core items: a little under two waves of the resident CTAs, because each sequence's last split
+  // is partial and rounds the count up (qwen3_1p7b: 1240 items against 2 x 608 slots at the full two
+  // waves).
+  w->target_items = (path == 2) ? (L.mla ? sm_count() : 2 * sm_count())
+                                : std::max<int32_t>(64, 19 * cc_ctas_per_sm(L.head_dim, L.mla, w->heads_per_item) *
+                                                            sm_count() / 10);
   w->query_groups = L.num_kv_heads * (group / w->heads_per_item);
   w->max_items = max_work_items(batch, w->query_groups, max_pages, pps, w->target_items);
   const size_t acc = static_cast<size_t>(w->max_items) * w->heads_per_item * L.v_dim * sizeof(float);

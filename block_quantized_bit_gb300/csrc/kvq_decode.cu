@@ -614,6 +614,14 @@ int32_t cc_heads_per_item(int32_t group, int32_t head_dim, int32_t mla) {
   return gt;
 }
 
+// CTAs per SM that launch_decode_cc's configuration keeps resident (its MINB).
+int32_t cc_ctas_per_sm(int32_t head_dim, int32_t mla, int32_t gt) {
+  if (mla) return 1;
+  if (head_dim == 64) return 4;
+  if (head_dim == 128) return gt == 2 ? 5 : 4;
+  return 3;
+}
+
 bool decode_cc_supported(int32_t head_dim, int32_t v_dim, int32_t mla) {
   if (mla) return head_dim == 576 && v_dim == 512;
   return v_dim == head_dim && (head_dim == 64 || head_dim == 128 || head_dim == 256);
