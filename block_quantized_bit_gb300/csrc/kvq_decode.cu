@@ -9,7 +9,8 @@
 // host read-back is needed; CTA 0 also leaves each sequence's first item and split count for the merge):
 //   query group qg = (kv head g, head tile ht): `heads_per_item` query heads that share kv head g;
 //   pages of sequence b are cut into splits of C pages; one work item = (b, qg, split);
-//   C = pages_per_split, or max(4, ceil(sum_b pages_b * groups / 1216)) when automatic.
+//   C = pages_per_split, or max(4, ceil(sum_b pages_b * groups / target)) when automatic, target a little
+//   under two waves of the resident CTAs (the host's plan).
 // One CTA runs one item.  Each of its warps walks every WARPS-th page of the split with its own
 // STAGES-deep pipeline of 1-D bulk copies (codes and scales of the page's K and V chunks into shared
 // memory, completion on an mbarrier).  Lanes read 16-byte code chunks, dequantize to bf16-exact fp32,

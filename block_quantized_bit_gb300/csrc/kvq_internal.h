@@ -48,7 +48,7 @@ constexpr int kPageTokens = 16;
 constexpr size_t kWorkspaceHeader = 256;
 
 // Work-item planning constants shared by the host (workspace bound) and the kernels.
-constexpr int kTargetItems = 1216;  // 8 items per SM on a 152-SM GB300 (kernels with cheap items)
+constexpr int kTargetItems = 1216;  // items when the host sets no target; also the SM count assumed without a device
 constexpr int kMinPagesPerSplit = 4;
 
 // Heads of one query group that a CUDA-core work item covers.
