@@ -4,8 +4,9 @@
 // tile of the query heads that read it, and a split is a run of C consecutive pages of the sequence.
 // C = pages_per_split when the caller fixes it; otherwise C = max(4, ceil(sum_b pages_b * groups /
 // target)) rounded up to `split_align` pages; the host sets the target per kernel (about two waves of
-// the CUDA-core kernel's resident CTAs, two items per SM for the GQA tensor-core kernel, one for MLA).  Every CTA derives the same plan from seq_lens on the
-// device, so no planning launch and no host read-back are needed.
+// the CUDA-core kernel's resident CTAs, two items per SM for the GQA tensor-core kernel, one for MLA).
+// Every CTA derives the same plan from seq_lens on the device, so no planning launch and no host
+// read-back are needed.
 #pragma once
 
 #include <cuda_runtime.h>
