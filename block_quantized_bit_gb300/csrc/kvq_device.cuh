@@ -178,8 +178,8 @@ __device__ __forceinline__ float dequant_addend(uint16_t s_bits) {
 }
 
 // Exact f16 values of the four codes of a 32-bit word: lo = codes 0-1, hi = codes 2-3.  The 16-bit
-// halves are taken with mov.b32 {l, h} inside the asm, which maps to register halves (no shift or mask
-// instructions): measured 1.6x the throughput of extracting them in C++ for fp8.
+// halves are taken with mov.b32 {l, h} inside the asm, so the conversions read register halves
+// instead of shifted and masked copies.
 template <int KIND>
 __device__ __forceinline__ void codes_to_f16x2(uint32_t word, uint32_t& lo, uint32_t& hi) {
   if (KIND == KVQ_FP8_E4M3) {
