@@ -455,4 +455,14 @@ kvq_status kvq_dequant_probe(kvq_kind kind, const uint8_t* codes, const uint16_t
   return launch_dequant_probe(kind, codes, scales, out, n, static_cast<cudaStream_t>(stream));
 }
 
+kvq_status kvq_wait_probe(void* workspace, void* stream) {
+  if (!workspace) return KVQ_EINVAL;
+  if (!aligned(workspace)) return KVQ_EALIGN;
+  kvq_status st = kvq_device_check();
+  if (st != KVQ_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(workspace, 0, sizeof(uint32_t), s) != cudaSuccess) return KVQ_ECUDA;
+  return launch_wait_probe(static_cast<uint32_t*>(workspace), s);
+}
+
 }  // extern "C"

@@ -663,6 +663,23 @@ kvq_status launch_merge(const DecodeArgs& a, int32_t query_groups, cudaStream_t 
   return cudaGetLastError() == cudaSuccess ? KVQ_OK : KVQ_ECUDA;
 }
 
+// ------------------------------------------------------------------------------------ wait probe
+// One thread initialises an mbarrier expecting one arrival that never comes, and waits on it with
+// mbar_wait_bounded, the wait every decode kernel uses; it gives up after kWaitLimitNs and reports the
+// timeout exactly as a decode kernel would.
+__global__ void wait_probe_kernel(uint32_t* status) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x != 0) return;
+  mbar_init(&bar, 1);
+  fence_mbar_init();
+  if (!mbar_wait_bounded(&bar, 0)) set_status(status, kStatusTimeout);
+}
+
+kvq_status launch_wait_probe(uint32_t* status, cudaStream_t stream) {
+  wait_probe_kernel<<<1, 32, 0, stream>>>(status);
+  return cudaGetLastError() == cudaSuccess ? KVQ_OK : KVQ_ECUDA;
+}
+
 kvq_status launch_dequant_probe(kvq_kind kind, const uint8_t* codes, const uint16_t* scales, uint16_t* out,
                                 int64_t n, cudaStream_t stream) {
   const int64_t nchunks = n / 16;

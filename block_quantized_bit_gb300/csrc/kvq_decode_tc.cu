@@ -259,23 +259,6 @@ __device__ __forceinline__ void tile_load_item(TileIter& t, const int32_t* tab, 
   t.i = 0;
 }
 
-// N consecutive fp16 scales (2 or 4, naturally aligned) in one shared-memory load.
-template <int N>
-__device__ __forceinline__ void load_scales(const uint8_t* src, uint16_t (&sc)[N]) {
-  static_assert(N == 2 || N == 4, "scale vector");
-  if constexpr (N == 4) {
-    const uint2 v = *reinterpret_cast<const uint2*>(src);
-    sc[0] = static_cast<uint16_t>(v.x);
-    sc[1] = static_cast<uint16_t>(v.x >> 16);
-    sc[2] = static_cast<uint16_t>(v.y);
-    sc[3] = static_cast<uint16_t>(v.y >> 16);
-  } else {
-    const uint32_t v = *reinterpret_cast<const uint32_t*>(src);
-    sc[0] = static_cast<uint16_t>(v);
-    sc[1] = static_cast<uint16_t>(v >> 16);
-  }
-}
-
 // Which of the two O accumulators an item uses: items alternate within a CTA.
 __device__ __forceinline__ int item_obuf(int32_t item) { return ((item - static_cast<int32_t>(blockIdx.x)) / gridDim.x) & 1; }
 

@@ -64,6 +64,7 @@ kvq_status launch_quantize_probe(kvq_kind kind, const uint16_t* x, int64_t nx, c
                                  uint8_t* codes, cudaStream_t stream);
 kvq_status launch_dequant_probe(kvq_kind kind, const uint8_t* codes, const uint16_t* scales, uint16_t* out,
                                 int64_t n, cudaStream_t stream);
+kvq_status launch_wait_probe(uint32_t* status, cudaStream_t stream);
 bool decode_cc_supported(int32_t head_dim, int32_t v_dim, int32_t mla);
 int32_t cc_ctas_per_sm(int32_t head_dim, int32_t mla, int32_t heads_per_item);
 bool decode_tc_supported(int32_t head_dim, int32_t v_dim, int32_t mla, int32_t group, int32_t batch);

@@ -30,7 +30,7 @@ EXPORTS = ["kvq_pool_bytes", "kvq_scale_bytes", "kvq_bytes_per_token", "kvq_num_
            "kvq_decode_workspace_bytes", "kvq_decode_workspace_bytes_ex", "kvq_decode_path",
            "kvq_decode_sparse_workspace_bytes", "kvq_decode_sparse", "kvq_decode", "kvq_decode_ex",
            "kvq_workspace_status", "kvq_encode_probe", "kvq_quantize_probe", "kvq_dequant_probe", "kvq_strerror",
-           "kvq_device_check", "kvq_version", "kvq_decode_noalloc"]
+           "kvq_device_check", "kvq_version", "kvq_decode_noalloc", "kvq_wait_probe"]
 
 
 class kvq_layout(ctypes.Structure):
@@ -83,6 +83,7 @@ def lib():
             "kvq_device_check": (i32, []),
             "kvq_version": (ctypes.c_char_p, []),
             "kvq_decode_noalloc": (i32, [P, P, P, P, i32, P, i32, i32, ctypes.c_float, P, i32, LP, i32, P]),
+            "kvq_wait_probe": (i32, [P, P]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -279,6 +280,11 @@ def kvq_quantize_probe(kind, x_bits: torch.Tensor, s_bits: torch.Tensor, codes: 
 def kvq_dequant_probe(kind, codes: torch.Tensor, scales: torch.Tensor, out: torch.Tensor, stream=None):
     _check(lib().kvq_dequant_probe(_kind(kind), _ptr(codes), _ptr(scales), _ptr(out), int(codes.numel()),
                                    _stream(stream)), "kvq_dequant_probe")
+
+
+def kvq_wait_probe(workspace: torch.Tensor, stream=None):
+    """One bounded wait that never completes: afterwards kvq_workspace_status(workspace) is KVQ_ETIMEOUT."""
+    _check(lib().kvq_wait_probe(_ptr(workspace), _stream(stream)), "kvq_wait_probe")
 
 
 def kvq_device_check() -> int:

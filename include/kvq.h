@@ -237,6 +237,14 @@ kvq_status kvq_quantize_probe(kvq_kind kind, const uint16_t* x, int64_t nx, cons
  */
 kvq_status kvq_dequant_probe(kvq_kind kind, const uint8_t* codes, const uint16_t* scales, uint16_t* out,
                              int64_t n, void* stream);
+/*
+ * Bounded-wait probe: one kernel waits, with the decode kernels' own bounded wait, on an mbarrier
+ * that nothing completes.  The wait gives up after the library's limit (2 s) and the kernel records a
+ * timeout in the status word of `workspace` (a device buffer of at least 256 bytes, cleared first), so
+ * that kvq_workspace_status then reports KVQ_ETIMEOUT.  It shows on the GPU that a wait which never
+ * completes ends in an error the host can read and leaves the context usable.
+ */
+kvq_status kvq_wait_probe(void* workspace, void* stream);
 
 /* ---------------------------------------------------------------- misc */
 /* Message for a status code (static string). */
