@@ -525,6 +525,78 @@ int kvo_decode_sparse(double* out, const uint16_t* q_bits, const uint8_t* codes,
 }
 
 /* ------------------------------------------------------------------------------------------ */
+/* Extend (prefill) attention over the quantized pool ("feat(kvcache): 8-bit KV cache (q8_0 /    */
+/* fp8_e4m3) behind --kv-cache-dtype", section "What": the dequant sits inside every attention   */
+/* kernel, prefill included; "feat(kvcache): 8-bit DSV4 window/compressed KV", section           */
+/* "Testing": quantized attention on the prefill kernel).  Sequence b holds seq_lens[b] tokens,  */
+/* the last n_b = q_start[b + 1] - q_start[b] of them new and already stored.  New token i sits  */
+/* at position pos = seq_lens[b] - n_b + i; its query row q[q_start[b] + i][h] attends causally  */
+/* to every position t <= pos whose page is not masked:                                         */
+/*     z_t = sm_scale * sum_d q[row][h][d] * Kd(t)[d],   out[row][h] = sum_t softmax(z)_t Vd(t)  */
+/* with the dequantized rows of kv head h / (Hq / Hkv); zeros when no position is valid.         */
+/* ------------------------------------------------------------------------------------------ */
+int kvo_extend(double* out, const uint16_t* q_bits, const uint8_t* codes, const uint16_t* scales,
+               const int32_t* block_table, int max_pages, const int32_t* seq_lens, const int32_t* q_start,
+               int B, int Hq, int Hkv, int D, int Dv, int P, int mla, int kind, double sm_scale, int nthreads)
+{
+    if (Hq % Hkv != 0 || Dv > D || B < 0) return -1;
+    if (B > 0 && q_start[0] != 0) return -1;
+    for (int b = 0; b < B; ++b) {
+        int n = q_start[b + 1] - q_start[b];
+        if (n < 0 || n > seq_lens[b]) return -1;
+    }
+    int n_kv = mla ? 1 : 2;
+    int G = Hq / Hkv;
+    int64_t total = B > 0 ? q_start[B] : 0;
+    int64_t units = total * Hq;
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 1)
+#else
+    (void)nthreads;
+#endif
+    for (int64_t u = 0; u < units; ++u) {
+        int64_t row = u / Hq;
+        int h = (int)(u % Hq);
+        int g = h / G;
+        int b = 0;
+        while (q_start[b + 1] <= row) ++b;       /* the sequence this query row belongs to */
+        int n = q_start[b + 1] - q_start[b];
+        int pos = seq_lens[b] - n + (int)(row - q_start[b]);
+        const uint16_t* qrow = q_bits + (row * Hq + h) * D;
+        double* o = out + (row * Hq + h) * Dv;
+        double* z = (double*)malloc(sizeof(double) * (size_t)(pos + 1));
+        double zmax = -INFINITY;
+        for (int t = 0; t <= pos; ++t) {
+            int32_t page = block_table[(int64_t)b * max_pages + t / P];
+            z[t] = -INFINITY;
+            if (page < 0) continue;
+            int64_t r = row_index(page, 0, g, t % P, n_kv, Hkv, P);
+            double dot = 0.0;
+            for (int d = 0; d < D; ++d)
+                dot += kvo_bf16_value(qrow[d]) * row_elem(1, kind, codes, scales, NULL, r, D, d);
+            z[t] = sm_scale * dot;
+            if (z[t] > zmax) zmax = z[t];
+        }
+        for (int d = 0; d < Dv; ++d) o[d] = 0.0;
+        if (zmax != -INFINITY) {
+            double denom = 0.0;
+            for (int t = 0; t <= pos; ++t) {
+                if (z[t] == -INFINITY) continue;
+                double w = exp(z[t] - zmax);
+                denom += w;
+                int32_t page = block_table[(int64_t)b * max_pages + t / P];
+                int64_t r = row_index(page, mla ? 0 : 1, g, t % P, n_kv, Hkv, P);
+                for (int d = 0; d < Dv; ++d) o[d] += w * row_elem(1, kind, codes, scales, NULL, r, D, d);
+            }
+            for (int d = 0; d < Dv; ++d) o[d] /= denom;
+        }
+        free(z);
+    }
+    return 0;
+}
+
+/* ------------------------------------------------------------------------------------------ */
 /* Batch helpers for the pins (elementwise maps over arrays).                                   */
 /* ------------------------------------------------------------------------------------------ */
 void kvo_f16_rne_f32_batch(const float* x, uint16_t* out, int64_t n)

@@ -43,6 +43,7 @@ def lib():
             "kvo_decode_bf16": (i32, [P, P, P, P, i32, P, i32, i32, i32, i32, i32, i32, i32, dbl, i32]),
             "kvo_decode_sparse": (i32, [P, P, P, P, P, i32, P, P, i32, i32, i32, i32, i32, i32, i32, i32, i32,
                                         dbl, i32]),
+            "kvo_extend": (i32, [P, P, P, P, P, i32, P, P, i32, i32, i32, i32, i32, i32, i32, i32, dbl, i32]),
             "kvo_f16_rne_f32_batch": (None, [P, P, i64]),
             "kvo_bf16_rne_f64_batch": (None, [P, P, i64]),
             "kvo_e4m3_sat_rne_batch": (None, [P, P, i64]),
@@ -240,6 +241,33 @@ def decode_sparse(q_bits, codes, scales, block_table, seq_lens, indices, *, num_
                                  _kind(kind), float(sm_scale), int(nthreads))
     if rc != 0:
         raise ValueError("oracle sparse decode rejected its arguments")
+    return out
+
+
+def extend(q_bits, codes, scales, block_table, seq_lens, q_start, *, num_q_heads, num_kv_heads, head_dim, v_dim,
+           page_size, mla, kind, sm_scale, nthreads=1):
+    """fp64 causal attention of the new tokens of every sequence ("feat(kvcache): 8-bit KV cache (q8_0 /
+    fp8_e4m3) behind --kv-cache-dtype", section "What": dequant inside the prefill kernel too).  q_bits is
+    [total_q, Hq, D]; q_start[B + 1] (q_start[0] = 0) gives each sequence's rows; the n_b = q_start[b+1] -
+    q_start[b] new tokens are the last n_b of its seq_lens[b] stored tokens, so new token i sits at position
+    seq_lens[b] - n_b + i and attends to the unmasked positions up to and including its own.  Returns
+    out[total_q, Hq, Dv] float64 (zeros where no position is valid)."""
+    q, pq = _c(q_bits, np.uint16)
+    c, pc = _c(codes, np.uint8)
+    s, ps = _c(scales, np.uint16)
+    bt, pbt = _c(block_table, np.int32)
+    sl, psl = _c(seq_lens, np.int32)
+    qs, pqs = _c(q_start, np.int32)
+    B = sl.size
+    if qs.size != B + 1:
+        raise ValueError("q_start needs batch + 1 entries")
+    total = int(qs[-1])
+    out = np.zeros((total, num_q_heads, v_dim), np.float64)
+    rc = lib().kvo_extend(out.ctypes.data_as(ctypes.c_void_p), pq, pc, ps, pbt, bt.shape[1], psl, pqs, B,
+                          num_q_heads, num_kv_heads, head_dim, v_dim, page_size, int(bool(mla)), _kind(kind),
+                          float(sm_scale), int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle extend rejected its arguments")
     return out
 
 

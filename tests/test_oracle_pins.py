@@ -610,3 +610,112 @@ def test_sparse_decode_closed_forms():
     two[:, 0], two[:, 1], two[:, 2] = 2, 9, 9
     ref = _expected_sparse_scipy(s, two, 1.0)
     np.testing.assert_allclose(_run_sparse(s, two), ref, rtol=1e-12, atol=1e-13)
+
+
+# ===================================================================== extend (prefill) attention
+def _extend_q(s, n_new, seed=9):
+    """Query rows [sum(n_new), Hq, D] and q_start for n_new new tokens per sequence."""
+    rng = np.random.default_rng(seed)
+    total = int(sum(n_new))
+    qf = (rng.standard_normal((total, s["Hq"], s["D"])) / math.sqrt(s["D"])).astype(np.float32)
+    q_start = np.concatenate([[0], np.cumsum(n_new)]).astype(np.int32)
+    return bf16_bits(qf), q_start
+
+
+def _run_extend(s, q, q_start, sm_scale=1.0, lens=None):
+    return O.extend(q, s["codes"], s["scales"], s["bt"], s["lens"] if lens is None else lens, q_start,
+                    num_q_heads=s["Hq"], num_kv_heads=s["Hkv"], head_dim=s["D"], v_dim=s["Dv"], page_size=s["P"],
+                    mla=s["mla"], kind=s["kind"], sm_scale=sm_scale)
+
+
+def _expected_extend_scipy(s, q, q_start, sm_scale):
+    """scipy softmax attention of each new token over the positions 0..pos of its sequence, every valid
+    position gathered from the pool by its slot (pos = seq_len - n_new + i)."""
+    Hq, Hkv, D, Dv, P = s["Hq"], s["Hkv"], s["D"], s["Dv"], s["P"]
+    out = np.zeros((q.shape[0], Hq, Dv))
+    for b, L in enumerate(s["lens"]):
+        n = int(q_start[b + 1] - q_start[b])
+        for i in range(n):
+            pos = int(L) - n + i
+            slots = [int(s["bt"][b, t // P]) * P + t % P for t in range(pos + 1) if s["bt"][b, t // P] >= 0]
+            if not slots:
+                continue
+            row = int(q_start[b]) + i
+            for h in range(Hq):
+                g = h // (Hq // Hkv)
+                K = _gather_dequant(s["codes"], s["scales"], s["kind"], slots, 0, g, D)
+                V = K[:, :Dv] if s["mla"] else _gather_dequant(s["codes"], s["scales"], s["kind"], slots, 1, g, D)
+                qv = bf16_to_f32(q[row, h]).astype(np.float64)
+                out[row, h] = scipy.special.softmax(sm_scale * (K @ qv)) @ V[:, :Dv]
+    return out
+
+
+@pytest.mark.parametrize("kind", [FP8, Q8])
+@pytest.mark.parametrize("mla", [False, True])
+def test_extend_matches_scipy_causal_attention(kind, mla):
+    """Every new token against scipy softmax over its causal prefix: a masked page, one sequence wholly new
+    (a first prefill: its token 0 sees only itself), one with a few new tokens after its context."""
+    D, Dv = (96, 64) if mla else (64, 64)
+    s = _decode_setup(kind, mla=mla, D=D, Dv=Dv, Hkv=1 if mla else 2, mask=[(1, 2)])
+    q, q_start = _extend_q(s, [37, 21])
+    for sm_scale in (1.0, 0.37):
+        np.testing.assert_allclose(_run_extend(s, q, q_start, sm_scale), _expected_extend_scipy(s, q, q_start, sm_scale),
+                                   rtol=1e-12, atol=1e-13)
+
+
+def test_extend_one_new_token_per_sequence_equals_the_decode():
+    s = _decode_setup(FP8, mask=[(0, 1)])
+    q_start = np.arange(len(s["lens"]) + 1, dtype=np.int32)
+    q = s["q"].reshape(len(s["lens"]), s["Hq"], s["D"])
+    np.testing.assert_array_equal(_run_extend(s, q, q_start), _run(s))
+
+
+def test_extend_each_new_token_equals_the_decode_of_its_prefix():
+    """Causality: new token i of sequence b gives what a decode of the same query over a sequence cut to
+    pos + 1 tokens gives; no later position contributes."""
+    s = _decode_setup(Q8, mask=[(1, 3)])
+    n_new = [9, 30]
+    q, q_start = _extend_q(s, n_new)
+    got = _run_extend(s, q, q_start)
+    for b, L in enumerate(s["lens"]):
+        for i in range(n_new[b]):
+            pos = int(L) - n_new[b] + i
+            lens = np.array(s["lens"])
+            lens[b] = pos + 1
+            row = int(q_start[b]) + i
+            sd = dict(s, q=np.repeat(q[row][None], len(lens), axis=0))
+            np.testing.assert_array_equal(got[row], _run(sd, lens=lens)[b])
+
+
+def test_extend_closed_forms():
+    """Identical keys: new token i gives the plain mean of the value rows at the unmasked positions 0..pos,
+    so an off-by-one in the causal bound changes the mean; a first-prefill token 0 returns value row 0;
+    a masked page drops out; a sequence with no new token adds no row."""
+    s = _decode_setup(Q8, kfun=lambda k: np.broadcast_to(k[:1], k.shape).copy(), mask=[(1, 1)])
+    n_new = [37, 5]
+    q, q_start = _extend_q(s, n_new)
+    got = _run_extend(s, q, q_start, 3.0)
+    P = s["P"]
+    for b, L in enumerate(s["lens"]):
+        for i in range(n_new[b]):
+            pos = int(L) - n_new[b] + i
+            slots = [int(s["bt"][b, t // P]) * P + t % P for t in range(pos + 1) if s["bt"][b, t // P] >= 0]
+            for h in range(s["Hq"]):
+                g = h // (s["Hq"] // s["Hkv"])
+                V = _gather_dequant(s["codes"], s["scales"], Q8, slots, 1, g, s["D"])
+                np.testing.assert_allclose(got[int(q_start[b]) + i, h], V.mean(axis=0), rtol=1e-12, atol=1e-14)
+    v0 = _gather_dequant(s["codes"], s["scales"], Q8, [int(s["bt"][0, 0]) * P], 1, 0, s["D"])[0]
+    np.testing.assert_array_equal(got[0, 0], v0)
+    # no new token for sequence 0: only sequence 1's rows, unchanged
+    q1, qs1 = q[37:], np.array([0, 0, 5], np.int32)
+    np.testing.assert_array_equal(_run_extend(s, q1, qs1, 3.0), got[37:])
+
+
+def test_extend_rejects_more_new_tokens_than_stored_and_a_bad_q_start():
+    s = _decode_setup(FP8)
+    q, q_start = _extend_q(s, [38, 2])  # sequence 0 holds 37 tokens
+    with pytest.raises(ValueError):
+        _run_extend(s, q, q_start)
+    q, q_start = _extend_q(s, [3, 2])
+    with pytest.raises(ValueError):
+        _run_extend(s, q, q_start + 1)
