@@ -412,6 +412,61 @@ kvq_status kvq_decode_sparse(const void* q, const void* pool, const void* scales
                        out, out_dtype, workspace, sp.dense_bytes, &sp.compact, kind, nullptr, stream, false);
 }
 
+size_t kvq_extend_workspace_bytes(void) { return kWorkspaceHeader; }
+
+kvq_status kvq_extend(const void* q, const void* pool, const void* scales, const int32_t* block_table,
+                      int32_t max_pages_per_seq, const int32_t* seq_lens, const int32_t* q_start, int32_t total_q,
+                      int32_t batch, int32_t num_q_heads, float sm_scale, void* out, kvq_out_dtype out_dtype,
+                      void* workspace, size_t workspace_bytes, const kvq_layout* layout, kvq_kind kind, void* stream) {
+  kvq_status st = check_layout(layout);
+  if (st != KVQ_OK) return st;
+  if (!kind_ok(kind)) return KVQ_EKIND;
+  if (out_dtype != KVQ_OUT_BF16 && out_dtype != KVQ_OUT_F32) return KVQ_EINVAL;
+  if (batch < 0 || total_q < 0 || num_q_heads <= 0 || max_pages_per_seq <= 0) return KVQ_EINVAL;
+  if (num_q_heads % layout->num_kv_heads != 0) return KVQ_EINVAL;
+  if (static_cast<int64_t>(total_q) * (num_q_heads / layout->num_kv_heads) > std::numeric_limits<int32_t>::max() - 128)
+    return KVQ_EINVAL;  // the kernel counts query rows per sequence in 32 bits
+  if (!(sm_scale == sm_scale) || sm_scale > std::numeric_limits<float>::max() ||
+      sm_scale < -std::numeric_limits<float>::max())
+    return KVQ_EINVAL;
+  if (layout->page_size != kPageTokens) return KVQ_EUNSUPPORTED;
+  if (!extend_tc_supported(layout->head_dim, layout->v_dim, layout->mla, num_q_heads / layout->num_kv_heads, batch))
+    return KVQ_EUNSUPPORTED;
+  if (!workspace) return KVQ_EINVAL;
+  if (workspace_bytes < kWorkspaceHeader) return KVQ_EWORKSPACE;
+  if (!aligned(workspace)) return KVQ_EALIGN;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(workspace, 0, sizeof(uint32_t), s) != cudaSuccess) return KVQ_ECUDA;
+  if (batch == 0 || total_q == 0) return KVQ_OK;
+  if (!q || !pool || !scales || !block_table || !seq_lens || !q_start || !out) return KVQ_EINVAL;
+  if (!aligned(q) || !aligned(pool) || !aligned(scales) || !aligned(out) ||
+      (reinterpret_cast<uintptr_t>(block_table) % 4) != 0 || (reinterpret_cast<uintptr_t>(seq_lens) % 4) != 0 ||
+      (reinterpret_cast<uintptr_t>(q_start) % 4) != 0)
+    return KVQ_EALIGN;
+  st = kvq_device_check();
+  if (st != KVQ_OK) return st;
+  ExtendArgs a;
+  a.q = static_cast<const uint16_t*>(q);
+  a.codes = static_cast<const uint8_t*>(pool);
+  a.scales = static_cast<const uint16_t*>(scales);
+  a.block_table = block_table;
+  a.seq_lens = seq_lens;
+  a.q_start = q_start;
+  a.out = out;
+  a.status = static_cast<uint32_t*>(workspace);
+  a.num_pages = layout->num_pages;
+  a.max_pages = max_pages_per_seq;
+  a.batch = batch;
+  a.total_q = total_q;
+  a.num_q_heads = num_q_heads;
+  a.num_kv_heads = layout->num_kv_heads;
+  a.head_dim = layout->head_dim;
+  a.score_scale = sm_scale * 1.4426950408889634f;  // log2(e)
+  a.out_dtype = out_dtype;
+  a.kind = kind;
+  return launch_extend_tc(a, s);
+}
+
 kvq_status kvq_workspace_status(const void* workspace, void* stream) {
   if (!workspace) return KVQ_EINVAL;
   uint32_t word = 0;

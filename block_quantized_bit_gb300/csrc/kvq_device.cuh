@@ -27,6 +27,7 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;  // bounded waits give up after
 // entry pointed past the pool (that page was skipped).
 constexpr uint32_t kStatusTimeout = 0x7100u;
 constexpr uint32_t kStatusBadPage = 0x7200u;
+constexpr uint32_t kStatusBadExtend = 0x7300u;  // q_start inconsistent with seq_lens or total_q
 
 // ------------------------------------------------------------------------------------------ PTX
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {

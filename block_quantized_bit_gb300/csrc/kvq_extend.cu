@@ -1,0 +1,589 @@
+// kvq_extend.cu -- extend (prefill) attention over the 8-bit pool on the tcgen05 tensor cores.
+//
+// "feat(kvcache): 8-bit KV cache (q8_0 / fp8_e4m3) behind --kv-cache-dtype", section "What": the dequant
+// sits inside every attention kernel, prefill included, and K and V are dequantized to bf16 before the dot
+// (the scale runs along the reduction dim).  "feat(kvcache): 8-bit DSV4 window/compressed KV", section
+// "Testing": quantized attention on the prefill kernel, masked -1 pages.
+//
+// The n_b new tokens of sequence b are the last n_b of its seq_len stored tokens; token i sits at position
+// seq_len - n_b + i and attends to the unmasked positions up to and including its own.  The query side is
+// wide, so the contraction takes the flash-attention shape.  A work item is (sequence, kv head g, block of
+// 128 query rows); row r holds new token blk * (128 / G) + r / G and query head g * G + r % G, so the G
+// heads of a kv head share every dequantized K and V tile:
+//   S[128 rows][T keys]  = Q[128][D] . Kd[T][D]^T   (A = Q, B = the K tile; both K-major in shared memory)
+//   O[128 rows][D]      += P[128][T] . Vd[T][D]     (A = P in tensor memory, B = the V tile read MN-major)
+// with fp32 S and O in tensor memory.  Q, K and V use the canonical no-swizzle core-matrix layout
+//   off(t, d) = (t % 8) * 16 + (t / 8) * RS + (d % 8) * 2 + (d / 8) * 128,   RS = D * 16,
+// with t the row (query row or key): K-major descriptors take LBO = 128 and SBO = RS, the MN-major one
+// LBO = RS and SBO = 128.  T = 128 keys per tile at D = 128 and 64 at D = 256 (shared memory).
+//
+// One persistent CTA per SM, 14 warps:
+//   warp 13     producer: TMA copies of a tile's K and V codes (128-byte swizzled boxes of 16 tokens x 128
+//               code bytes) and bulk copies of their scales into a staging ring, with each page's number
+//               of valid tokens.
+//   warps 4-11  dequant: a thread owns 64 codes of one token row, of K and then of V.  K of tile j + 1 is
+//               written before V of tile j, so the next QK never waits for the V tile.
+//   warp 12     allocates tensor memory and issues every MMA (one elected lane): QK of tile j, then PV of
+//               tile j - 1, so the softmax of tile j overlaps the tensor pipe.
+//   warps 0-3   softmax, one query row per thread (= tensor-memory lane): causal and page masks, online
+//               softmax in the exp2 domain with lazy rescaling (the running max moves only when a score
+//               passes it by more than 2^8), P as bf16 into tensor memory.  At an item's end they write the
+//               next item's Q rows, then O / l to the output.
+// Every wait is bounded (2 s) and reports a timeout in the status word instead of hanging.
+#include <cuda.h>
+#include <math.h>
+
+#include <algorithm>
+
+#include "kvq_device.cuh"
+#include "kvq_internal.h"
+#include "kvq_tc.cuh"
+
+namespace kvq {
+namespace {
+
+constexpr int kM = 128;  // query rows per item (the MMA M)
+constexpr int kSmWarps = 4;
+constexpr int kDwWarps = 8;
+constexpr int kMmaWarp = kSmWarps + kDwWarps;   // warp 12
+constexpr int kProdWarp = kMmaWarp + 1;         // warp 13
+constexpr int kThreads = (kProdWarp + 1) * 32;  // 14 warps
+constexpr int kDwThreads = kDwWarps * 32;
+constexpr int kTmemCols = 512;
+constexpr int kBox = kPage * 128;      // one TMA box: 16 tokens x 128 code bytes
+constexpr float kLazyRescale = 8.0f;   // log2 headroom before the running max must move
+
+template <int D>
+struct XCfg {
+  static constexpr int T = (D == 128) ? 128 : 64;  // keys per tile
+  static constexpr int PPT = T / kPage;            // pages per tile
+  static constexpr int RS = D * 16;                // bytes between 8-row groups of a tile
+  static constexpr int KV_TILE = T * D * 2;        // one bf16 K or V tile
+  static constexpr int Q_BYTES = kM * D * 2;
+  static constexpr int PARTS = kDwThreads / T;     // dequant threads per token row
+  static constexpr int SPAN = D / PARTS;           // codes per dequant thread (of K, and of V)
+  static constexpr int NCH = SPAN / 16;            // 16-code chunks per dequant thread
+  static constexpr int NBT = SPAN / 32;            // scale blocks per dequant thread
+  static constexpr int NB = D / 32;
+  static constexpr int NSL = D / 128;              // 128-byte slices of a code row
+  static constexpr int SC_KV = kPage * NB * 2;     // scale bytes of one page of K or of V
+  // one ring slot: codes [kv][page][slice] boxes as TMA wrote them, then scales [kv][page]
+  static constexpr int CODE_BYTES = 2 * PPT * NSL * kBox;
+  static constexpr int SLOT_BYTES = CODE_BYTES + 2 * PPT * SC_KV;
+  static constexpr int STAGES = (D == 128) ? 3 : 2;
+  static constexpr int RING_OFF = 0;  // 1024-byte aligned: swizzle atoms
+  static constexpr int K_OFF = RING_OFF + STAGES * SLOT_BYTES;
+  static constexpr int V_OFF = K_OFF + KV_TILE;
+  static constexpr int Q_OFF = V_OFF + KV_TILE;
+  static constexpr int META_OFF = Q_OFF + Q_BYTES;              // [STAGES][PPT] valid tokens per page
+  static constexpr int TAB_OFF = META_OFF + STAGES * PPT * 4;   // [batch + 1] first item of each sequence
+  static constexpr int NBARS = 2 * STAGES + 10;
+  static constexpr int BAR_OFF = (TAB_OFF + (kMaxExtendBatch + 1) * 4 + 15) / 16 * 16;  // mbarriers: 8-byte aligned
+  static constexpr int SMEM_BYTES = BAR_OFF + NBARS * 8 + 16 + 1024;  // + slack to align the base
+  // tensor-memory columns: O [0, D); S buffer b [D + b T, D + (b + 1) T); P buffer b [384 + b T / 2, ...)
+  static constexpr int S_COL = D;
+  static constexpr int P_COL = 384;
+  static_assert(D == 128 || D == 256, "extend needs head_dim 128 or 256");
+  static_assert(D + 2 * T <= P_COL && P_COL + T <= kTmemCols, "tensor-memory columns");
+  static_assert(PARTS * T == kDwThreads && NCH % 2 == 0 && NBT == 2, "dequant split");
+  static_assert(SLOT_BYTES % 1024 == 0, "slots keep the boxes 1024-byte aligned");
+  static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
+  static_assert(K_OFF % 16 == 0 && V_OFF % 16 == 0 && Q_OFF % 16 == 0 && BAR_OFF % 8 == 0, "alignment");
+};
+
+// kind::f16 instruction descriptor: fp32 accumulate, bf16 A and B, M = 128, the given N; A K-major.
+__device__ __forceinline__ uint32_t x_idesc(int n, bool b_mn_major) {
+  uint32_t d = 0;
+  d |= 1u << 4;   // D: f32
+  d |= 1u << 7;   // A: bf16
+  d |= 1u << 10;  // B: bf16
+  d |= static_cast<uint32_t>(b_mn_major) << 16;
+  d |= static_cast<uint32_t>(n >> 3) << 17;
+  d |= static_cast<uint32_t>(kM >> 4) << 24;
+  return d;
+}
+
+__device__ __forceinline__ void bar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+// The new tokens of sequence b after validation: 0 <= n <= seq_len and q_start[b + 1] <= total_q, else none
+// (the status word then reports the bad sequence).
+__device__ __forceinline__ int32_t new_tokens(const ExtendArgs& a, int32_t b, bool report) {
+  const int32_t q0 = __ldg(a.q_start + b), q1 = __ldg(a.q_start + b + 1);
+  const int32_t n = q1 - q0;
+  if (q0 < 0 || n < 0 || q1 > a.total_q || n > __ldg(a.seq_lens + b)) {
+    if (report) set_status(a.status, kStatusBadExtend);
+    return 0;
+  }
+  return n;
+}
+
+// One work item: sequence b, kv head g, query block blk; its rows' positions end at pos_max.
+struct XItem {
+  int32_t b, g, blk, n, L, q0, pos_max, ntiles;
+};
+
+template <int D>
+__device__ __forceinline__ XItem x_locate(const int32_t* tab, const ExtendArgs& a, int32_t G, int32_t item) {
+  using Cfg = XCfg<D>;
+  int lo = 0, hi = a.batch;  // first b with tab[b] > item
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (tab[mid] <= item) lo = mid + 1;
+    else hi = mid;
+  }
+  XItem it;
+  it.b = lo - 1;
+  it.L = __ldg(a.seq_lens + it.b);
+  it.q0 = __ldg(a.q_start + it.b);
+  it.n = new_tokens(a, it.b, false);
+  const int32_t tb = kM / G;                   // new tokens per block
+  const int32_t nblk = (it.n + tb - 1) / tb;
+  const int32_t k = item - tab[it.b];
+  it.blk = nblk - 1 - k / a.num_kv_heads;      // the last blocks (the most keys) first
+  it.g = k % a.num_kv_heads;
+  const int32_t last_tok = min(it.n, (it.blk + 1) * tb) - 1;
+  it.pos_max = it.L - it.n + last_tok;
+  it.ntiles = it.pos_max / Cfg::T + 1;
+  return it;
+}
+
+// The sequence of (item, tile) pairs a persistent CTA works through.
+template <int D>
+struct XIter {
+  XItem it;
+  int32_t item, i, n_items;
+  bool live;
+  __device__ __forceinline__ void first(const int32_t* tab, const ExtendArgs& a, int32_t G, int32_t total) {
+    n_items = total;
+    item = blockIdx.x;
+    i = 0;
+    live = item < n_items;
+    if (live) it = x_locate<D>(tab, a, G, item);
+  }
+  __device__ __forceinline__ void next(const int32_t* tab, const ExtendArgs& a, int32_t G) {
+    if (!live) return;
+    if (++i < it.ntiles) return;
+    i = 0;
+    item += gridDim.x;
+    live = item < n_items;
+    if (live) it = x_locate<D>(tab, a, G, item);
+  }
+};
+
+// A bounded wait that the whole warp agrees on: no lane runs ahead into a warp-collective tcgen05 instruction
+// while another gave up.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity) {
+  return __all_sync(0xffffffffu, mbar_wait_bounded(bar, parity));
+}
+
+template <int D, int KIND>
+__global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const ExtendArgs a, const __grid_constant__ CUtensorMap tmap) {
+  using Cfg = XCfg<D>;
+  constexpr int T = Cfg::T;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);  // swizzle atoms are 1024 B
+  uint8_t* sRing = smem + Cfg::RING_OFF;
+  uint8_t* sK = smem + Cfg::K_OFF;
+  uint8_t* sV = smem + Cfg::V_OFF;
+  uint8_t* sQ = smem + Cfg::Q_OFF;
+  int32_t* sMeta = reinterpret_cast<int32_t*>(smem + Cfg::META_OFF);
+  int32_t* sTab = reinterpret_cast<int32_t*>(smem + Cfg::TAB_OFF);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Cfg::BAR_OFF);
+  // Every barrier completes once per use of its buffer, so a waiter names an unambiguous phase.
+  uint64_t* bar_full = bars;                      // [STAGES] ring slot landed (producer arrival + bytes)
+  uint64_t* bar_empty = bars + Cfg::STAGES;       // [STAGES] ring slot read by every dequant warp
+  uint64_t* bar_k_full = bars + 2 * Cfg::STAGES;  // K tile written (dequant warps), once per tile
+  uint64_t* bar_v_full = bar_k_full + 1;          // V tile written (dequant warps), once per tile
+  uint64_t* bar_qk_done = bar_k_full + 2;         // [2] QK into S buffer b completed (commit)
+  uint64_t* bar_pv_done = bar_k_full + 4;         // [2] PV that read P buffer b completed (commit)
+  uint64_t* bar_p_full = bar_k_full + 6;          // [2] P buffer b written, S buffer b read (softmax warps)
+  uint64_t* bar_q_full = bar_k_full + 8;          // an item's Q rows written (softmax warps), once per item
+  uint64_t* bar_o_free = bar_k_full + 9;          // an item's O read out (softmax warps), once per item
+  uint32_t* sTmem = reinterpret_cast<uint32_t*>(smem + Cfg::BAR_OFF + Cfg::NBARS * 8);
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int32_t G = a.num_q_heads / a.num_kv_heads;
+
+  // ---- plan: first item of every sequence (items of a sequence: query blocks x kv heads)
+  if (tid == 0) {
+    int32_t run = 0;
+    for (int32_t b = 0; b < a.batch; ++b) {
+      sTab[b] = run;
+      const int32_t n = new_tokens(a, b, blockIdx.x == 0);
+      run += ((n * G + kM - 1) / kM) * a.num_kv_heads;
+    }
+    sTab[a.batch] = run;
+    for (int s = 0; s < Cfg::STAGES; ++s) {
+      mbar_init(&bar_full[s], 1);
+      mbar_init(&bar_empty[s], kDwWarps);
+    }
+    mbar_init(bar_k_full, kDwWarps);
+    mbar_init(bar_v_full, kDwWarps);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&bar_qk_done[b], 1);
+      mbar_init(&bar_pv_done[b], 1);
+      mbar_init(&bar_p_full[b], kSmWarps);
+    }
+    mbar_init(bar_q_full, kSmWarps);
+    mbar_init(bar_o_free, kSmWarps);
+    fence_mbar_init();
+  }
+  if (warp == kMmaWarp) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(sTmem)),
+                 "r"(kTmemCols));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *sTmem;
+  const int32_t n_items = sTab[a.batch];
+  bool ok = true;
+
+  if (warp == kProdWarp) {
+    // ===================================================================== producer
+    // Lane pi (< PPT) owns page pi of a tile: its block-table entry, valid tokens and copies.
+    XIter<D> t;
+    t.first(sTab, a, G, n_items);
+    uint32_t n = 0;  // tiles issued
+    while (ok && t.live) {
+      const int32_t pg = t.i * Cfg::PPT + lane;
+      int32_t phys = -1, nvalid = 0;
+      if (lane < Cfg::PPT && pg < a.max_pages && pg * kPage < t.it.L) {
+        phys = __ldg(a.block_table + static_cast<int64_t>(t.it.b) * a.max_pages + pg);
+        if (phys >= a.num_pages) {  // never dereferenced; reported in the status word
+          set_status(a.status, kStatusBadPage);
+          phys = -1;
+        }
+        if (phys >= 0) nvalid = min(kPage, t.it.L - pg * kPage);
+      }
+      const int sl = n % Cfg::STAGES;
+      const uint32_t use = n / Cfg::STAGES;
+      if (use > 0 && !warp_wait(&bar_empty[sl], (use - 1) & 1)) { ok = false; break; }
+      const uint32_t bytes = __reduce_add_sync(
+          0xffffffffu, phys >= 0 ? static_cast<uint32_t>(2 * (Cfg::NSL * kBox + Cfg::SC_KV)) : 0u);
+      int32_t nv[Cfg::PPT];
+#pragma unroll
+      for (int i = 0; i < Cfg::PPT; ++i) nv[i] = __shfl_sync(0xffffffffu, nvalid, i);
+      if (lane == 0) {
+#pragma unroll
+        for (int i = 0; i < Cfg::PPT; ++i) sMeta[sl * Cfg::PPT + i] = nv[i];
+        mbar_arrive_expect_tx(&bar_full[sl], bytes);  // releases the page counts with the slot
+      }
+      __syncwarp();
+      if (phys >= 0) {
+        uint8_t* slot = sRing + sl * Cfg::SLOT_BYTES;
+#pragma unroll
+        for (int kv = 0; kv < 2; ++kv) {
+#pragma unroll
+          for (int c = 0; c < Cfg::NSL; ++c)
+            tma_load_codes(smem_u32(slot + ((kv * Cfg::PPT + lane) * Cfg::NSL + c) * kBox), &tmap, c,
+                           t.it.g * kPage, kv, phys, &bar_full[sl]);
+          const uint8_t* src = reinterpret_cast<const uint8_t*>(a.scales) +
+                               ((static_cast<int64_t>(phys) * 2 + kv) * a.num_kv_heads + t.it.g) * Cfg::SC_KV;
+          bulk_g2s(slot + Cfg::CODE_BYTES + (kv * Cfg::PPT + lane) * Cfg::SC_KV, src, Cfg::SC_KV, &bar_full[sl]);
+        }
+      }
+      t.next(sTab, a, G);
+      ++n;
+    }
+    // no copy may still be in flight when the CTA exits
+    for (uint32_t j = 1; j <= n && j <= static_cast<uint32_t>(Cfg::STAGES); ++j) {
+      const uint32_t m = n - j;
+      (void)mbar_wait_bounded(&bar_full[m % Cfg::STAGES], (m / Cfg::STAGES) & 1);
+    }
+  } else if (warp >= kSmWarps && warp < kMmaWarp) {
+    // ===================================================================== dequant warps
+    const int dw = tid - kSmWarps * 32;
+    const int tt = dw % T;     // key of the tile (consecutive threads: consecutive keys)
+    const int part = dw / T;   // which SPAN of the row
+    const int pi = tt / kPage, off = tt % kPage;
+    const int swz = off & 7;   // 128-byte swizzle phase of this token's staging rows
+    const uint32_t toff = (tt % 8) * 16 + (tt / 8) * Cfg::RS;
+    // dequantize this thread's codes of K (kv = 0) or V (kv = 1) from a ring slot into a bf16 tile
+    auto write_tile = [&](uint8_t* dst, const uint8_t* slot, int kv, bool v_ok) {
+      const uint8_t* rows = slot + (kv * Cfg::PPT + pi) * Cfg::NSL * kBox + off * 128;
+      const uint32_t sc = *reinterpret_cast<const uint32_t*>(
+          slot + Cfg::CODE_BYTES + (kv * Cfg::PPT + pi) * Cfg::SC_KV + (off * Cfg::NB + part * Cfg::NBT) * 2);
+#pragma unroll
+      for (int k = 0; k < Cfg::NCH; ++k) {
+        uint32_t w[8];
+        if (v_ok) {
+          const int c = part * Cfg::NCH + k;  // 16-code chunk along the row
+          const uint4 codes = *reinterpret_cast<const uint4*>(rows + (c / 8) * kBox + (((c % 8) ^ swz) * 16));
+          dequant16<KIND>(codes, static_cast<uint16_t>(sc >> (16 * (k >> 1))), w);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) w[e] = 0u;
+        }
+        const int d8 = part * (Cfg::SPAN / 8) + 2 * k;
+        *reinterpret_cast<uint4*>(dst + toff + d8 * 128) = make_uint4(w[0], w[1], w[2], w[3]);
+        *reinterpret_cast<uint4*>(dst + toff + (d8 + 1) * 128) = make_uint4(w[4], w[5], w[6], w[7]);
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+    };
+    XIter<D> tk;  // next tile whose K is dequantized
+    tk.first(sTab, a, G, n_items);
+    uint32_t nk = 0, nv = 0;  // tiles whose K / V have been written
+    while (ok && (tk.live || nv < nk)) {
+      if (tk.live) {
+        const int ring = nk % Cfg::STAGES;
+        if (!warp_wait(&bar_full[ring], (nk / Cfg::STAGES) & 1)) { ok = false; break; }
+        const uint8_t* slot = sRing + ring * Cfg::SLOT_BYTES;
+        const bool v_ok = off < sMeta[ring * Cfg::PPT + pi];
+        // the K tile was last read by the QK of tile nk - 1
+        if (nk >= 1 && !warp_wait(&bar_qk_done[(nk - 1) & 1], ((nk - 1) >> 1) & 1)) { ok = false; break; }
+        write_tile(sK, slot, 0, v_ok);
+        if (lane == 0) bar_arrive(bar_k_full);
+        tk.next(sTab, a, G);
+        ++nk;
+        if (nk == 1 && tk.live) continue;  // K runs one tile ahead of V
+      }
+      {
+        const int ring = nv % Cfg::STAGES;  // landed: its K was read above
+        const uint8_t* slot = sRing + ring * Cfg::SLOT_BYTES;
+        const bool v_ok = off < sMeta[ring * Cfg::PPT + pi];
+        // the V tile was last read by the PV of tile nv - 1
+        if (nv >= 1 && !warp_wait(&bar_pv_done[(nv - 1) & 1], ((nv - 1) >> 1) & 1)) { ok = false; break; }
+        write_tile(sV, slot, 1, v_ok);
+        if (lane == 0) {
+          bar_arrive(bar_v_full);
+          bar_arrive(&bar_empty[ring]);
+        }
+        ++nv;
+      }
+    }
+  } else if (warp == kMmaWarp) {
+    // ===================================================================== MMA issue (elected lane)
+    const uint32_t idesc_qk = x_idesc(T, false);
+    const uint32_t idesc_pv = x_idesc(D, true);
+    // descriptors of the first K-step; later steps add their byte offset >> 4 to the address field
+    const uint64_t dQ = smem_desc(smem_u32(sQ), 128, Cfg::RS);
+    const uint64_t dK = smem_desc(smem_u32(sK), 128, Cfg::RS);
+    const uint64_t dV = smem_desc(smem_u32(sV), Cfg::RS, 128);
+    const uint32_t tS = tmem + Cfg::S_COL, tO = tmem, tP = tmem + Cfg::P_COL;
+    uint32_t n = 0, items = 0;  // tiles QK'd; items finished
+    // PV of tile m; the first tile of an item overwrites O, once the previous item's O has been read out
+    auto pv = [&](uint32_t m, bool first) -> bool {
+      const int bp = m & 1;
+      if (!warp_wait(bar_v_full, m & 1)) return false;
+      if (!warp_wait(&bar_p_full[bp], (m >> 1) & 1)) return false;
+      if (first && items >= 1 && !warp_wait(bar_o_free, (items - 1) & 1)) return false;
+      tc_fence_after();
+#pragma unroll
+      for (int ks = 0; ks < T / 16; ++ks)
+        mma_bf16_tmem_a(tO, tP + bp * (T / 2) + ks * 8, dV + static_cast<uint64_t>((ks * 2 * Cfg::RS) >> 4),
+                        idesc_pv, (!first || ks > 0) ? 1u : 0u);
+      mma_commit(&bar_pv_done[bp]);
+      __syncwarp();
+      return true;
+    };
+    for (int32_t item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
+      const XItem it = x_locate<D>(sTab, a, G, item);
+      if (!warp_wait(bar_q_full, items & 1)) { ok = false; break; }
+      for (int32_t i = 0; i < it.ntiles; ++i, ++n) {
+        const int b = n & 1;
+        if (!warp_wait(bar_k_full, n & 1)) { ok = false; break; }
+        // S buffer b was read by the softmax of tile n - 2
+        if (n >= 2 && !warp_wait(&bar_p_full[b], ((n >> 1) - 1) & 1)) { ok = false; break; }
+        tc_fence_after();
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks)
+          mma_bf16(tS + b * T, dQ + static_cast<uint64_t>((ks * 256) >> 4), dK + static_cast<uint64_t>((ks * 256) >> 4),
+                   idesc_qk, ks > 0 ? 1u : 0u);
+        mma_commit(&bar_qk_done[b]);
+        __syncwarp();
+        if (i > 0 && !pv(n - 1, i == 1)) { ok = false; break; }
+      }
+      if (!ok) break;
+      if (!pv(n - 1, it.ntiles == 1)) { ok = false; break; }
+      ++items;
+    }
+    // before tensor memory is freed, every MMA issued must have completed (the last commit implies all)
+    if (n > 0) (void)mbar_wait_bounded(&bar_pv_done[(n - 1) & 1], ((n - 1) >> 1) & 1);
+    if (n > 0) (void)mbar_wait_bounded(&bar_qk_done[(n - 1) & 1], ((n - 1) >> 1) & 1);
+  } else {
+    // ===================================================================== softmax warps
+    const int r = tid;  // query row = tensor-memory lane
+    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    const uint32_t tS = tmem + Cfg::S_COL + lane_base, tO = tmem + lane_base, tP = tmem + Cfg::P_COL + lane_base;
+    const int32_t tb = kM / G;  // new tokens per query block
+    // the item's Q rows into the shared tile (rows past the sequence's new tokens are zero)
+    auto write_q = [&](const XItem& it) {
+      const int32_t tok = it.blk * tb + r / G;
+      const bool valid = tok < it.n;
+      const uint4* src = reinterpret_cast<const uint4*>(
+          a.q + (static_cast<int64_t>(it.q0 + (valid ? tok : 0)) * a.num_q_heads + it.g * G + r % G) * D);
+      uint8_t* dst = sQ + (r % 8) * 16 + (r / 8) * Cfg::RS;
+#pragma unroll 4
+      for (int j = 0; j < D / 8; ++j)
+        *reinterpret_cast<uint4*>(dst + j * 128) = valid ? __ldg(src + j) : make_uint4(0, 0, 0, 0);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) bar_arrive(bar_q_full);
+    };
+    uint32_t n = 0;  // tiles processed
+    if (static_cast<int32_t>(blockIdx.x) < n_items) write_q(x_locate<D>(sTab, a, G, blockIdx.x));
+    for (int32_t item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
+      const XItem it = x_locate<D>(sTab, a, G, item);
+      const int32_t tok = it.blk * tb + r / G;
+      const bool row_ok = tok < it.n;
+      const int32_t pos = row_ok ? it.L - it.n + tok : -1;  // last key position this row sees
+      float m_used = -INFINITY, l = 0.0f;
+      for (int32_t i = 0; i < it.ntiles; ++i, ++n) {
+        const int b = n & 1;
+        // mapped pages of the tile (chunk c of 16 keys is page c of the tile)
+        uint32_t pmask = 0;
+#pragma unroll
+        for (int pi = 0; pi < Cfg::PPT; ++pi) {
+          const int32_t pg = i * Cfg::PPT + pi;
+          if (pg < a.max_pages && pg * kPage < it.L) {
+            const int32_t e = __ldg(a.block_table + static_cast<int64_t>(it.b) * a.max_pages + pg);
+            if (e >= 0 && e < a.num_pages) pmask |= 1u << pi;
+          }
+        }
+        const int32_t lim = pos - i * T;  // keys k <= lim of this tile are causally visible
+        if (!warp_wait(&bar_qk_done[b], (n >> 1) & 1)) { ok = false; break; }
+        tc_fence_after();
+        // pass 1: the row's max over its visible keys (scaled: exp2 domain)
+        float mx = -INFINITY;
+#pragma unroll 1
+        for (int c = 0; c < T / 16; ++c) {
+          float s[16];
+          tmem_ld16(tS + b * T + c * 16, s);
+          const bool pg_ok = (pmask >> c) & 1u;
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+            if (pg_ok && c * 16 + e <= lim) mx = fmaxf(mx, s[e] * a.score_scale);
+        }
+        float alpha = 1.0f;
+        bool resc = false;
+        if (mx > -INFINITY && (m_used == -INFINITY || mx > m_used + kLazyRescale)) {
+          if (m_used != -INFINITY) {
+            alpha = exp2f(m_used - mx);
+            resc = true;
+          }
+          m_used = mx;
+        }
+        // P buffer b is free once the PV two tiles back has read it
+        if (n >= 2 && !warp_wait(&bar_pv_done[b], ((n >> 1) - 1) & 1)) { ok = false; break; }
+        if (__any_sync(0xffffffffu, resc)) {  // (only from the second tile of an item on)
+          // O must hold the PV of the previous tile before it is scaled
+          if (!warp_wait(&bar_pv_done[(n - 1) & 1], ((n - 1) >> 1) & 1)) { ok = false; break; }
+          tc_fence_after();
+#pragma unroll 1
+          for (int c = 0; c < D / 16; ++c) {
+            float o[16];
+            tmem_ld16(tO + c * 16, o);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) o[e] *= alpha;
+            tmem_st16(tO + c * 16, o);
+          }
+          l *= alpha;
+        }
+        // pass 2: P (bf16) into tensor memory, and the row sum of exactly those bf16 values
+#pragma unroll 1
+        for (int c2 = 0; c2 < T / 32; ++c2) {
+          float s[32];
+          tmem_ld16(tS + b * T + c2 * 32, *reinterpret_cast<float(*)[16]>(s));
+          tmem_ld16(tS + b * T + c2 * 32 + 16, *reinterpret_cast<float(*)[16]>(s + 16));
+          uint32_t w[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            float pr[2];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const int j = 2 * e + h;
+              const bool vis = ((pmask >> (2 * c2 + j / 16)) & 1u) && c2 * 32 + j <= lim;
+              pr[h] = vis ? exp2f(fmaf(s[j], a.score_scale, -m_used)) : 0.0f;
+            }
+            w[e] = pack_bf16x2(pr[0], pr[1]);
+            const float2 pb = unpack_bf16x2(w[e]);
+            l += pb.x + pb.y;
+          }
+          tmem_st16u(tP + b * (T / 2) + c2 * 16, w);
+        }
+        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) bar_arrive(&bar_p_full[b]);
+      }
+      if (!ok) break;
+      // the next item's Q rows (every QK of this item has completed: its last S was read above)
+      const int32_t nxt = item + static_cast<int32_t>(gridDim.x);
+      if (nxt < n_items) write_q(x_locate<D>(sTab, a, G, nxt));
+      // O / l of this item, once its last PV has completed
+      if (!warp_wait(&bar_pv_done[(n - 1) & 1], ((n - 1) >> 1) & 1)) { ok = false; break; }
+      tc_fence_after();
+      const float inv = l > 0.0f ? 1.0f / l : 0.0f;
+      const int64_t orow = (static_cast<int64_t>(it.q0 + (row_ok ? tok : 0)) * a.num_q_heads + it.g * G + r % G) * D;
+#pragma unroll 1
+      for (int c = 0; c < D / 16; ++c) {
+        float o[16];
+        tmem_ld16(tO + c * 16, o);
+        if (row_ok) {
+          if (a.out_dtype == KVQ_OUT_F32) {
+            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(a.out) + orow + c * 16);
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4)
+              dst[q4] = make_float4(o[4 * q4] * inv, o[4 * q4 + 1] * inv, o[4 * q4 + 2] * inv, o[4 * q4 + 3] * inv);
+          } else {
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.out) + orow + c * 16);
+#pragma unroll
+            for (int h8 = 0; h8 < 2; ++h8)
+              dst[h8] = make_uint4(pack_bf16x2(o[8 * h8] * inv, o[8 * h8 + 1] * inv),
+                                   pack_bf16x2(o[8 * h8 + 2] * inv, o[8 * h8 + 3] * inv),
+                                   pack_bf16x2(o[8 * h8 + 4] * inv, o[8 * h8 + 5] * inv),
+                                   pack_bf16x2(o[8 * h8 + 6] * inv, o[8 * h8 + 7] * inv));
+          }
+        }
+      }
+      tc_fence_before();  // the reads are ordered before the arrival that lets the next PV overwrite O
+      __syncwarp();
+      if (lane == 0) bar_arrive(bar_o_free);
+    }
+  }
+  if (!ok) set_status(a.status, kStatusTimeout);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == kMmaWarp)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols));
+}
+
+template <int D>
+kvq_status launch_extend_d(const ExtendArgs& a, cudaStream_t stream) {
+  using Cfg = XCfg<D>;
+  auto kern = (a.kind == KVQ_FP8_E4M3) ? extend_tc_kernel<D, KVQ_FP8_E4M3> : extend_tc_kernel<D, KVQ_Q8_0>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES) != cudaSuccess)
+    return KVQ_ECUDA;
+  CUtensorMap map;
+  if (!encode_code_map(&map, a.codes, a.num_pages, a.num_kv_heads, D)) return KVQ_ECUDA;
+  int dev = 0, sms = 152;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int64_t G = a.num_q_heads / a.num_kv_heads;
+  const int64_t bound = ((static_cast<int64_t>(a.total_q) * G + kM - 1) / kM + a.batch) * a.num_kv_heads;
+  const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(bound, sms));
+  kern<<<static_cast<unsigned>(grid), kThreads, Cfg::SMEM_BYTES, stream>>>(a, map);
+  return cudaGetLastError() == cudaSuccess ? KVQ_OK : KVQ_ECUDA;
+}
+
+}  // namespace
+
+bool extend_tc_supported(int32_t head_dim, int32_t v_dim, int32_t mla, int32_t group, int32_t batch) {
+  if (mla || v_dim != head_dim) return false;
+  if (head_dim != 128 && head_dim != 256) return false;
+  return group >= 1 && group <= kM && kM % group == 0 && batch <= kMaxExtendBatch;
+}
+
+kvq_status launch_extend_tc(const ExtendArgs& a, cudaStream_t stream) {
+  if (a.head_dim == 128) return launch_extend_d<128>(a, stream);
+  if (a.head_dim == 256) return launch_extend_d<256>(a, stream);
+  return KVQ_EUNSUPPORTED;
+}
+
+}  // namespace kvq

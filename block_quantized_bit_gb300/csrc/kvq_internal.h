@@ -97,4 +97,28 @@ struct SparseGatherArgs {
 constexpr int32_t kMaxSparseTopk = 8192;
 kvq_status launch_sparse_gather(const SparseGatherArgs& g, cudaStream_t stream);
 
+// Extend (prefill) attention: the new tokens of every sequence attend causally over the pool.
+struct ExtendArgs {
+  const uint16_t* q;          // [total_q][num_q_heads][head_dim] bf16
+  const uint8_t* codes;
+  const uint16_t* scales;
+  const int32_t* block_table; // [batch][max_pages]
+  const int32_t* seq_lens;    // [batch]
+  const int32_t* q_start;     // [batch + 1]
+  void* out;                  // [total_q][num_q_heads][v_dim]
+  uint32_t* status;
+  int64_t num_pages;
+  int32_t max_pages;
+  int32_t batch;
+  int32_t total_q;
+  int32_t num_q_heads;
+  int32_t num_kv_heads;
+  int32_t head_dim;
+  float score_scale;          // sm_scale * log2(e): the kernels work in the exp2 domain
+  kvq_out_dtype out_dtype;
+  kvq_kind kind;
+};
+constexpr int32_t kMaxExtendBatch = 2048;  // sequences whose item bases fit the kernel's shared table
+bool extend_tc_supported(int32_t head_dim, int32_t v_dim, int32_t mla, int32_t group, int32_t batch);
+kvq_status launch_extend_tc(const ExtendArgs& a, cudaStream_t stream);
 }  // namespace kvq

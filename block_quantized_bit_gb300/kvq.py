@@ -30,7 +30,8 @@ EXPORTS = ["kvq_pool_bytes", "kvq_scale_bytes", "kvq_bytes_per_token", "kvq_num_
            "kvq_decode_workspace_bytes", "kvq_decode_workspace_bytes_ex", "kvq_decode_path",
            "kvq_decode_sparse_workspace_bytes", "kvq_decode_sparse", "kvq_decode", "kvq_decode_ex",
            "kvq_workspace_status", "kvq_encode_probe", "kvq_quantize_probe", "kvq_dequant_probe", "kvq_strerror",
-           "kvq_device_check", "kvq_version", "kvq_decode_noalloc", "kvq_wait_probe"]
+           "kvq_device_check", "kvq_version", "kvq_decode_noalloc", "kvq_wait_probe", "kvq_extend_workspace_bytes",
+           "kvq_extend"]
 
 
 class kvq_layout(ctypes.Structure):
@@ -74,6 +75,8 @@ def lib():
             "kvq_decode_sparse": (i32, [P, P, P, P, i32, P, P, i32, i32, i32, ctypes.c_float, P, i32, P, sz, LP,
                                         i32, P]),
             "kvq_decode": (i32, [P, P, P, P, i32, P, i32, i32, ctypes.c_float, P, i32, P, sz, LP, i32, P]),
+            "kvq_extend_workspace_bytes": (sz, []),
+            "kvq_extend": (i32, [P, P, P, P, i32, P, P, i32, i32, i32, ctypes.c_float, P, i32, P, sz, LP, i32, P]),
             "kvq_decode_ex": (i32, [P, P, P, P, i32, P, i32, i32, ctypes.c_float, P, i32, P, sz, LP, i32, OP, P]),
             "kvq_workspace_status": (i32, [P, P]),
             "kvq_encode_probe": (i32, [i32, P, P, i64, P]),
@@ -259,6 +262,29 @@ def kvq_decode_sparse(q: torch.Tensor, pool: torch.Tensor, scales: torch.Tensor,
                                    _ptr(out), od, _ptr(workspace), int(workspace.numel() * workspace.element_size()),
                                    ctypes.byref(layout.c()),
                                    _kind(kind), _stream(stream)), "kvq_decode_sparse")
+
+
+def alloc_extend_workspace(device="cuda"):
+    return torch.empty(lib().kvq_extend_workspace_bytes(), dtype=torch.uint8, device=device)
+
+
+def kvq_extend(q: torch.Tensor, pool: torch.Tensor, scales: torch.Tensor, block_table: torch.Tensor,
+               seq_lens: torch.Tensor, q_start: torch.Tensor, out: torch.Tensor, workspace: torch.Tensor,
+               layout: Layout, kind, sm_scale: float = 1.0, stream=None):
+    """Extend (prefill) attention: the q rows q_start[b] .. q_start[b+1]-1 ([total_q, Hq, D] bf16) are the
+    last new tokens of sequence b and attend causally over the pool; out is [total_q, Hq, Dv]."""
+    if out.dtype == torch.bfloat16:
+        od = KVQ_OUT_BF16
+    elif out.dtype == torch.float32:
+        od = KVQ_OUT_F32
+    else:
+        raise TypeError("out must be bfloat16 or float32")
+    total_q, Hq = q.shape[0], q.shape[1]
+    B = seq_lens.numel()
+    _check(lib().kvq_extend(_ptr(q), _ptr(pool), _ptr(scales), _ptr(block_table), int(block_table.shape[1]),
+                            _ptr(seq_lens), _ptr(q_start), int(total_q), int(B), int(Hq), float(sm_scale), _ptr(out),
+                            od, _ptr(workspace), int(workspace.numel() * workspace.element_size()),
+                            ctypes.byref(layout.c()), _kind(kind), _stream(stream)), "kvq_extend")
 
 
 def kvq_workspace_status(workspace: torch.Tensor, stream=None) -> int:

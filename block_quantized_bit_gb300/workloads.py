@@ -24,7 +24,8 @@ Five families, named for what they are:
                [256, 131072], pages randomly permuted, 1% of K/V values scaled by 100; each step stores
                one new row per sequence and decodes it.
 
-``sparse_indices`` draws the per-sequence index lists of the sparse (top-K) decode for any family.
+``sparse_indices`` draws the per-sequence index lists of the sparse (top-K) decode for any family;
+``extend_inputs`` the queries of an extend (prefill) step whose new tokens are the last ones stored.
 
 Page size is 16 everywhere.  The softmax scale is 1.0 because q is drawn already divided by
 sqrt(head_dim).
@@ -258,6 +259,32 @@ def sparse_indices(case, topk, seed=1006, masked_frac=0.01, device=None):
             drop = torch.rand((topk,), generator=g) < masked_frac
             ix[b][drop] = -1
     return ix.to(device if device is not None else case.seq_lens.device)
+
+
+def extend_inputs(case, n_new, seed=1007, device=None):
+    """Inputs of one extend (prefill) step over a GQA case: the last n_b of each sequence's stored tokens are
+    the step's new tokens (n_new: one count for every sequence, capped at its length, or a list).  Returns
+    (q [total, Hq, D] bf16 ~ N(0,1)/sqrt(D), q_start [B + 1] int32, rows) where rows (int64) indexes the
+    new tokens' K/V rows in case.k / case.v and case.slot_mapping, sequence by sequence."""
+    dev = device if device is not None else case.seq_lens.device
+    lens = [int(x) for x in case.seq_lens.cpu()]
+    if isinstance(n_new, int):
+        n = [min(n_new, L) for L in lens]
+    else:
+        n = [int(x) for x in n_new]
+    if any(x < 0 or x > L for x, L in zip(n, lens)):
+        raise ValueError("0 <= new tokens <= seq_len")
+    q_start = torch.zeros(len(lens) + 1, dtype=torch.int32)
+    q_start[1:] = torch.cumsum(torch.tensor(n, dtype=torch.int64), 0).to(torch.int32)
+    total = int(q_start[-1])
+    g = _gen("cpu", seed)
+    q = _randn((total, case.num_q_heads, case.head_dim), g, "cpu") / math.sqrt(case.head_dim)
+    rows, off = [], 0
+    for L, x in zip(lens, n):
+        rows.append(torch.arange(off + L - x, off + L, dtype=torch.int64))
+        off += L
+    rows = torch.cat(rows) if rows else torch.zeros(0, dtype=torch.int64)
+    return _bf16(q).to(dev), q_start.to(dev), rows.to(dev)
 
 
 FAMILIES = {"tiny": tiny, "qwen3_1p7b": qwen3_1p7b, "long_gqa": long_gqa, "mla": mla, "serving": serving}

@@ -178,6 +178,34 @@ kvq_status kvq_decode_sparse(const void* q, const void* pool, const void* scales
                              const kvq_layout* layout, kvq_kind kind, void* stream);
 
 /*
+ * Extend (prefill) attention ("feat(kvcache): 8-bit KV cache (q8_0 / fp8_e4m3) behind --kv-cache-dtype",
+ * section "What": the dequant sits inside every attention kernel, prefill included; "feat(kvcache): 8-bit
+ * DSV4 window/compressed KV", section "Testing": quantized attention on the prefill kernel).  Store the
+ * step's new K/V rows with kvq_store first: every key, the new ones included, is read from the pool.
+ *   q            [total_q, num_q_heads, head_dim] bf16, device; the rows of sequence b are
+ *                q_start[b] .. q_start[b + 1] - 1
+ *   q_start      [batch + 1] int32, device: q_start[0] = 0, non-decreasing, q_start[batch] = total_q
+ *   seq_lens     stored tokens per sequence, the new ones included: the n_b = q_start[b + 1] - q_start[b]
+ *                new tokens are the last n_b, so new token i sits at position seq_lens[b] - n_b + i
+ *   out          [total_q, num_q_heads, v_dim], bf16 or f32 (out_dtype), device
+ *   workspace    at least kvq_extend_workspace_bytes() (its status word), 16-byte aligned, device
+ * Other arguments as kvq_decode.  Query row (b, i, h) gets softmax(sm_scale * q.K^T) V over the positions
+ * 0 .. seq_lens[b] - n_b + i of sequence b whose pages are not masked (causal), with K and V dequantized to
+ * bf16 and fp32 accumulation; no valid position gives zeros.  Runs on the tensor cores (tcgen05).
+ * Supported: page_size 16, head_dim = v_dim in {128, 256}, not MLA, query heads per kv head dividing
+ * 128, batch <= 2048; otherwise KVQ_EUNSUPPORTED.  q_start and seq_lens are read on the device: a
+ * sequence with n_b < 0, n_b > seq_lens[b] or q_start[b + 1] > total_q is skipped and makes
+ * kvq_workspace_status report KVQ_EINVAL, as does a block-table entry >= layout->num_pages (that page is
+ * skipped).  Asynchronous on `stream`.
+ */
+size_t kvq_extend_workspace_bytes(void);
+kvq_status kvq_extend(const void* q, const void* pool, const void* scales, const int32_t* block_table,
+                      int32_t max_pages_per_seq, const int32_t* seq_lens, const int32_t* q_start, int32_t total_q,
+                      int32_t batch, int32_t num_q_heads, float sm_scale, void* out, kvq_out_dtype out_dtype,
+                      void* workspace, size_t workspace_bytes, const kvq_layout* layout, kvq_kind kind,
+                      void* stream);
+
+/*
  * The decode kernel kvq_decode_ex would run for these sizes and options: 1 (CUDA cores, one launch) or
  * 2 (tensor cores, two launches with the merge).  Otherwise a negative kvq_status: KVQ_EINVAL for an
  * invalid layout, size or option, KVQ_EUNSUPPORTED when no kernel supports the shape.  Host only, no

@@ -8,7 +8,7 @@ import torch
 
 from block_quantized_bit_gb300 import workloads
 
-from parity import (assert_decode_close, gpu_decode, gpu_pool, gpu_store, oracle_decode, oracle_pool,
+from parity import (abs_value_pool, assert_decode_close, gpu_decode, gpu_pool, gpu_store, oracle_decode, oracle_pool,
                     oracle_store)
 
 pytestmark = pytest.mark.gpu
@@ -39,15 +39,17 @@ def _stored(name, kind, poison=0xA5, **kw):
 @pytest.mark.parametrize("name", list(CASES))
 def test_decode_matches_oracle(name, kind, path):
     """Every family on the automatic choice, the CUDA-core kernel (1) and the tensor-core kernel (2)."""
-    if path == 2 and name == "serving":
-        # 1% of the values are scaled by 100, so outputs reach ~50; the tensor-core kernel feeds P to the
-        # MMA as bf16 (relative error 2^-9), which is ~0.1 absolute there.  The automatic choice keeps
-        # this group size (4) on the CUDA-core kernel, whose P stays fp32.
-        pytest.skip("bf16 P of the tensor-core kernel vs the absolute bound at outputs of ~50")
     case, codes, scales, oc, osc = _stored(name, kind)
     ref = oracle_decode(case, oc, osc)
     got = gpu_decode(case, codes, scales, path=path)
-    assert_decode_close(got, ref)
+    if path == 2 and name == "serving":
+        # 1% of the values are scaled by 100.  The tensor-core kernel feeds P to the MMA as bf16 (relative
+        # error 2^-9 each), so its error scales with sum_t p_t |V_t| (the oracle over the pool with absolute
+        # V codes), which the spikes make ~100: the bound gains 2^-8 times that sum.  The automatic choice
+        # keeps this group size (4) on the CUDA-core kernel, whose P stays fp32.
+        assert_decode_close(got, ref, rel=2.0 ** -8, scale=oracle_decode(case, abs_value_pool(oc, kind), osc))
+    else:
+        assert_decode_close(got, ref)
     got16 = gpu_decode(case, codes, scales, out_dtype=torch.bfloat16)
     assert_decode_close(got16, ref, rel=2.0 ** -8)
 

@@ -1,0 +1,143 @@
+"""GPU parity of the extend (prefill) attention, through the C ABI, against the oracle's fp64 causal attention.
+
+Each case stores every row of its sequences (kvq_store on the GPU, the oracle's store on the host, checked
+bit-exact by the store tests) and declares the last n_b stored tokens of sequence b new; the kernel's output
+for every (new token, query head) must meet the decode bound (max abs <= 1.5e-2, mean abs <= 2e-3).  The
+cases span several key tiles and query blocks with ragged tails, D = 128 and 256, 1 to 16 query heads per kv
+head, masked pages, a first prefill (every token new), single new tokens and sequences without new tokens."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from block_quantized_bit_gb300 import kvq, workloads
+
+from parity import (abs_value_pool, assert_decode_close, bits, gpu_pool, gpu_store, layout_of, oracle_pool,
+                    oracle_store)
+
+pytestmark = pytest.mark.gpu
+
+KVQ_EINVAL, KVQ_EUNSUPPORTED = -1, -8
+
+
+def _case(name, kind, **kw):
+    return workloads.make(name, kind=kind, device="cuda", **kw)
+
+
+CASES = {
+    # D = 128, 2 query heads per kv head: 64 new tokens per query block, 128-key tiles
+    "qwen3_small": (lambda kind: _case("qwen3_1p7b", kind, batch=3, ctx_lo=150, ctx_hi=700), [None, 37, 1]),
+    # D = 256, 8 heads per kv head (16 tokens per block), 64-key tiles, masked pages
+    "long_gqa_small": (lambda kind: _case("long_gqa", kind, batch=2, ctx=900, mask_frac=0.05), [300, 900]),
+    # D = 128, 4 heads per kv head, randomly permuted pages, 1% of K/V values x100 (outputs reach ~130)
+    "serving_small": (lambda kind: _case("serving", kind, batch=4, median=300, lo=40, hi=600), [40, 0, 17, 129]),
+    # 1 head per kv head (128 new tokens per block) and 16 heads per kv head (8 per block)
+    "mha": (lambda kind: _case("long_gqa", kind, batch=2, ctx=333, mask_frac=0.0, num_q_heads=8,
+                               num_kv_heads=8, head_dim=128), [333, 130]),
+    "g16": (lambda kind: _case("long_gqa", kind, batch=1, ctx=520, mask_frac=0.02, num_q_heads=32,
+                               num_kv_heads=2, head_dim=128), [200]),
+}
+
+
+def _stored(key, kind):
+    make, n_new = CASES[key]
+    case = make(kind)
+    lens = case.seq_lens.cpu().tolist()
+    n_new = [L if x is None else x for x, L in zip(n_new, lens)]
+    L, codes, scales = gpu_pool(case)
+    gpu_store(case, codes, scales)
+    oc, osc = oracle_pool(case)
+    oracle_store(case, oc, osc)
+    q, q_start, _ = workloads.extend_inputs(case, n_new)
+    return case, L, codes, scales, oc, osc, q, q_start
+
+
+def _gpu_extend(case, L, codes, scales, q, q_start, out_dtype=torch.float32):
+    out = torch.full((q.shape[0], case.num_q_heads, case.v_dim), float("nan"), dtype=out_dtype, device="cuda")
+    ws = kvq.alloc_extend_workspace()
+    ws.fill_(0x5A)
+    kvq.kvq_extend(q, codes, scales, case.block_table, case.seq_lens, q_start, out, ws, L, case.kind, case.sm_scale)
+    torch.cuda.synchronize()
+    return out, ws
+
+
+def _oracle_extend(case, oc, osc, q, q_start):
+    return O.extend(bits(q), oc, osc, case.block_table.cpu().numpy(), case.seq_lens.cpu().numpy(),
+                    q_start.cpu().numpy(), num_q_heads=case.num_q_heads, num_kv_heads=case.num_kv_heads,
+                    head_dim=case.head_dim, v_dim=case.v_dim, page_size=case.page_size, mla=case.mla,
+                    kind=case.kind, sm_scale=case.sm_scale, nthreads=0)
+
+
+# P enters the MMA as bf16 (relative error 2^-9 per probability), so the output error scales with
+# sum_t p_t |V_t|, which the oracle gives over the pool with absolute V codes.  With the x100 spikes of the
+# serving family that sum reaches hundreds while outputs cancel to a few units, so there the bound gains
+# 2^-8 (twice the rounding) times that sum.
+SPIKED = {"serving_small"}
+
+
+@pytest.mark.parametrize("kind", ["fp8_e4m3", "q8_0"])
+@pytest.mark.parametrize("key", list(CASES))
+def test_extend_matches_the_oracle(key, kind):
+    case, L, codes, scales, oc, osc, q, q_start = _stored(key, kind)
+    out, ws = _gpu_extend(case, L, codes, scales, q, q_start)
+    assert kvq.kvq_workspace_status(ws) == 0
+    ref = _oracle_extend(case, oc, osc, q, q_start)
+    got = out.cpu().numpy().astype(np.float64)
+    if key in SPIKED:
+        scale = _oracle_extend(case, abs_value_pool(oc, kind), osc, q, q_start)
+        assert_decode_close(got, ref, rel=2.0 ** -8, scale=scale)
+    else:
+        assert_decode_close(got, ref)
+
+
+def test_extend_bf16_output_is_the_rounded_f32_output():
+    case, L, codes, scales, oc, osc, q, q_start = _stored("qwen3_small", "fp8_e4m3")
+    out32, _ = _gpu_extend(case, L, codes, scales, q, q_start)
+    out16, ws = _gpu_extend(case, L, codes, scales, q, q_start, torch.bfloat16)
+    assert kvq.kvq_workspace_status(ws) == 0
+    assert torch.equal(out16, out32.to(torch.bfloat16))
+
+
+def test_extend_is_deterministic_and_leaves_the_pool_alone():
+    case, L, codes, scales, oc, osc, q, q_start = _stored("long_gqa_small", "q8_0")
+    c0, s0 = codes.clone(), scales.clone()
+    a, _ = _gpu_extend(case, L, codes, scales, q, q_start)
+    b, _ = _gpu_extend(case, L, codes, scales, q, q_start)
+    assert torch.equal(a, b)
+    assert torch.equal(codes, c0) and torch.equal(scales, s0)
+
+
+def test_extend_with_no_new_token_is_a_no_op_and_a_bad_q_start_is_reported():
+    case, L, codes, scales, oc, osc, q, q_start = _stored("qwen3_small", "fp8_e4m3")
+    # no new token anywhere: nothing is written
+    empty_q = q[:0]
+    zeros = torch.zeros_like(q_start)
+    out, ws = _gpu_extend(case, L, codes, scales, empty_q, zeros)
+    assert out.numel() == 0 and kvq.kvq_workspace_status(ws) == 0
+    # sequence 1 claims more new tokens than it stores: it is skipped and reported; the others are exact
+    lens = case.seq_lens.cpu().tolist()
+    bad = torch.tensor([0, 3, 3 + lens[1] + 1, 3 + lens[1] + 2], dtype=torch.int32, device="cuda")
+    qb = torch.randn((int(bad[-1]), case.num_q_heads, case.head_dim), device="cuda").to(torch.bfloat16) / 12
+    out, ws = _gpu_extend(case, L, codes, scales, qb, bad)
+    assert kvq.kvq_workspace_status(ws) == KVQ_EINVAL
+    good = np.r_[0:3, int(bad[2]):int(bad[3])]
+    ok_start = torch.tensor([0, 3, 3, 4], dtype=torch.int32)
+    ref = O.extend(bits(qb[good]), oc, osc, case.block_table.cpu().numpy(), case.seq_lens.cpu().numpy(),
+                   ok_start.numpy(), num_q_heads=case.num_q_heads, num_kv_heads=case.num_kv_heads,
+                   head_dim=case.head_dim, v_dim=case.v_dim, page_size=case.page_size, mla=False, kind=case.kind,
+                   sm_scale=case.sm_scale, nthreads=0)
+    assert_decode_close(out[good].cpu().numpy().astype(np.float64), ref)
+    assert torch.isnan(out[3:int(bad[2])]).all()  # the skipped sequence's rows are untouched
+
+
+def test_extend_rejects_unsupported_shapes():
+    case = workloads.make("mla", kind="fp8_e4m3", device="cuda", ctx=64)
+    L = layout_of(case)
+    codes, scales = kvq.alloc_pool(L, "cuda")
+    q = torch.zeros((1, case.num_q_heads, case.head_dim), dtype=torch.bfloat16, device="cuda")
+    out = torch.zeros((1, case.num_q_heads, case.v_dim), dtype=torch.float32, device="cuda")
+    qs = torch.tensor([0, 1], dtype=torch.int32, device="cuda")
+    with pytest.raises(kvq.KvqError) as e:
+        kvq.kvq_extend(q, codes, scales, case.block_table, case.seq_lens, qs, out, kvq.alloc_extend_workspace(), L,
+                       case.kind)
+    assert e.value.status == KVQ_EUNSUPPORTED

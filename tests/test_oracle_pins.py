@@ -719,3 +719,18 @@ def test_extend_rejects_more_new_tokens_than_stored_and_a_bad_q_start():
     q, q_start = _extend_q(s, [3, 2])
     with pytest.raises(ValueError):
         _run_extend(s, q, q_start + 1)
+
+
+@pytest.mark.parametrize("kind", [FP8, Q8])
+def test_absolute_value_pool_gives_the_weighted_mean_of_abs_v(kind):
+    """The parity tests' error scale sum_t p_t |V_t|: over the pool with absolute V codes the decode is at
+    least |decode| everywhere (triangle inequality), and equals the decode when every V is already >= 0."""
+    from parity import abs_value_pool
+    s = _decode_setup(kind, mask=[(1, 2)])
+    out = _run(s)
+    sa = dict(s, codes=abs_value_pool(s["codes"], kind))
+    scale = _run(sa)
+    assert np.all(scale >= np.abs(out) - 1e-12) and np.any(scale > np.abs(out) + 1e-3)
+    pos = _decode_setup(kind, seed=3)
+    pos["codes"] = abs_value_pool(pos["codes"], kind)
+    np.testing.assert_array_equal(_run(dict(pos, codes=abs_value_pool(pos["codes"], kind))), _run(pos))
