@@ -426,9 +426,7 @@ kvq_status kvq_extend(const void* q, const void* pool, const void* scales, const
   if (num_q_heads % layout->num_kv_heads != 0) return KVQ_EINVAL;
   if (static_cast<int64_t>(total_q) * (num_q_heads / layout->num_kv_heads) > std::numeric_limits<int32_t>::max() - 128)
     return KVQ_EINVAL;  // the kernel counts query rows per sequence in 32 bits
-  if (!(sm_scale == sm_scale) || sm_scale > std::numeric_limits<float>::max() ||
-      sm_scale < -std::numeric_limits<float>::max())
-    return KVQ_EINVAL;
+  if (!(sm_scale > 0.0f) || sm_scale > std::numeric_limits<float>::max()) return KVQ_EINVAL;  // finite, > 0
   if (layout->page_size != kPageTokens) return KVQ_EUNSUPPORTED;
   if (!extend_tc_supported(layout->head_dim, layout->v_dim, layout->mla, num_q_heads / layout->num_kv_heads, batch))
     return KVQ_EUNSUPPORTED;

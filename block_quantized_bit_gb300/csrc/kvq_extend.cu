@@ -17,10 +17,10 @@
 // with t the row (query row or key): K-major descriptors take LBO = 128 and SBO = RS, the MN-major one
 // LBO = RS and SBO = 128.  T = 128 keys per tile at D = 128 and 64 at D = 256 (shared memory).
 //
-// One persistent CTA per SM, 14 warps:
-//   warp 13     producer: TMA copies of a tile's K and V codes (128-byte swizzled boxes of 16 tokens x 128
-//               code bytes) and bulk copies of their scales into a staging ring, with each page's number
-//               of valid tokens.
+// One persistent CTA per SM, 15 warps:
+//   warps 13-14 producers, one for K and one for V: TMA copies of a tile's codes (128-byte swizzled boxes of
+//               16 tokens x 128 code bytes) and bulk copies of their scales into that producer's staging ring,
+//               with each page's number of valid tokens; the block table is read one tile ahead.
 //   warps 4-11  dequant: a thread owns 64 codes of one token row, of K and then of V.  K of tile j + 1 is
 //               written before V of tile j, so the next QK never waits for the V tile.
 //   warp 12     allocates tensor memory and issues every MMA (one elected lane): QK of tile j, then PV of
@@ -34,6 +34,7 @@
 #include <math.h>
 
 #include <algorithm>
+#include <type_traits>
 
 #include "kvq_device.cuh"
 #include "kvq_internal.h"
@@ -46,8 +47,8 @@ constexpr int kM = 128;  // query rows per item (the MMA M)
 constexpr int kSmWarps = 4;
 constexpr int kDwWarps = 8;
 constexpr int kMmaWarp = kSmWarps + kDwWarps;   // warp 12
-constexpr int kProdWarp = kMmaWarp + 1;         // warp 13
-constexpr int kThreads = (kProdWarp + 1) * 32;  // 14 warps
+constexpr int kProdWarp = kMmaWarp + 1;         // warps 13 (K ring) and 14 (V ring)
+constexpr int kThreads = (kProdWarp + 2) * 32;  // 15 warps
 constexpr int kDwThreads = kDwWarps * 32;
 constexpr int kTmemCols = 512;
 constexpr int kBox = kPage * 128;      // one TMA box: 16 tokens x 128 code bytes
@@ -67,17 +68,21 @@ struct XCfg {
   static constexpr int NB = D / 32;
   static constexpr int NSL = D / 128;              // 128-byte slices of a code row
   static constexpr int SC_KV = kPage * NB * 2;     // scale bytes of one page of K or of V
-  // one ring slot: codes [kv][page][slice] boxes as TMA wrote them, then scales [kv][page]
-  static constexpr int CODE_BYTES = 2 * PPT * NSL * kBox;
-  static constexpr int SLOT_BYTES = CODE_BYTES + 2 * PPT * SC_KV;
-  static constexpr int STAGES = (D == 128) ? 3 : 2;
+  // a ring slot (of the K ring or of the V ring): codes [page][slice] boxes as TMA wrote them, then the
+  // scales [page].  The K ring is freed as soon as K is dequantized, the V ring only after the previous PV,
+  // so the two rings run at their own pace and the K ring runs deeper.
+  static constexpr int CODE_BYTES = PPT * NSL * kBox;
+  static constexpr int SLOT_BYTES = CODE_BYTES + PPT * SC_KV;
+  static constexpr int KSTAGES = (D == 128) ? 4 : 3;
+  static constexpr int VSTAGES = (D == 128) ? 3 : 2;
+  static constexpr int NSLOTS = KSTAGES + VSTAGES;  // K ring slots, then V ring slots
   static constexpr int RING_OFF = 0;  // 1024-byte aligned: swizzle atoms
-  static constexpr int K_OFF = RING_OFF + STAGES * SLOT_BYTES;
+  static constexpr int K_OFF = RING_OFF + NSLOTS * SLOT_BYTES;
   static constexpr int V_OFF = K_OFF + KV_TILE;
   static constexpr int Q_OFF = V_OFF + KV_TILE;
-  static constexpr int META_OFF = Q_OFF + Q_BYTES;              // [STAGES][PPT] valid tokens per page
-  static constexpr int TAB_OFF = META_OFF + STAGES * PPT * 4;   // [batch + 1] first item of each sequence
-  static constexpr int NBARS = 2 * STAGES + 10;
+  static constexpr int META_OFF = Q_OFF + Q_BYTES;              // [NSLOTS][PPT] valid tokens per page
+  static constexpr int TAB_OFF = META_OFF + NSLOTS * PPT * 4;   // [batch + 1] first item of each sequence
+  static constexpr int NBARS = 2 * NSLOTS + 10;
   static constexpr int BAR_OFF = (TAB_OFF + (kMaxExtendBatch + 1) * 4 + 15) / 16 * 16;  // mbarriers: 8-byte aligned
   static constexpr int SMEM_BYTES = BAR_OFF + NBARS * 8 + 16 + 1024;  // + slack to align the base
   // tensor-memory columns: O [0, D); S buffer b [D + b T, D + (b + 1) T); P buffer b [384 + b T / 2, ...)
@@ -172,6 +177,51 @@ struct XIter {
   }
 };
 
+// Tensor-memory loads and stores of 32 consecutive columns of this warp's 32 lanes.  A load's registers are
+// valid only after tcgen05.wait::ld; the waits below take them as operands, so no use moves above the wait.
+__device__ __forceinline__ void tmem_ld32_issue(uint32_t taddr, uint32_t* r) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+               : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  tmem_ld32_issue(taddr, r);
+  asm volatile("tcgen05.wait::ld.sync.aligned;" : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31])::"memory");
+}
+
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&r)[64]) {
+  tmem_ld32_issue(taddr, r);
+  tmem_ld32_issue(taddr + 32, r + 32);
+  asm volatile("tcgen05.wait::ld.sync.aligned;" : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31]), "+r"(r[32]), "+r"(r[33]), "+r"(r[34]), "+r"(r[35]), "+r"(r[36]), "+r"(r[37]), "+r"(r[38]), "+r"(r[39]), "+r"(r[40]), "+r"(r[41]), "+r"(r[42]), "+r"(r[43]), "+r"(r[44]), "+r"(r[45]), "+r"(r[46]), "+r"(r[47]), "+r"(r[48]), "+r"(r[49]), "+r"(r[50]), "+r"(r[51]), "+r"(r[52]), "+r"(r[53]), "+r"(r[54]), "+r"(r[55]), "+r"(r[56]), "+r"(r[57]), "+r"(r[58]), "+r"(r[59]), "+r"(r[60]), "+r"(r[61]), "+r"(r[62]), "+r"(r[63])::"memory");
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+               : "memory");
+}
+
+// 2^x by the hardware approximation (relative error far below the bf16 rounding that follows); 2^-inf = 0.
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// 2^x on the FMA pipe, for a share of the probabilities (the MUFU unit alone would pace the softmax):
+// x = j + f with j = round(x) by the 1.5 * 2^23 addition (the sum's low mantissa bits hold j) and f in
+// [-0.5, 0.5]; 2^f by a cubic fitted for relative error on that interval; j added to the exponent field.
+// Relative error at most 1.5e-4 over [-126, 8], far below the bf16 rounding of P that follows.  x is
+// clamped at -126 (the result is then 2^-126, not 0: callers zero masked keys themselves).
+__device__ __forceinline__ float ex2_fma(float x) {
+  x = fmaxf(x, -126.0f);
+  const float t = x + 12582912.0f;
+  const int j = __float_as_int(t) - 0x4B400000;
+  const float f = x - (t - 12582912.0f);
+  const float p = fmaf(fmaf(fmaf(0.0551716685f, f, 0.2426111251f), f, 0.6932609677f), f, 0.9999280572f);
+  return __int_as_float(__float_as_int(p) + (j << 23));
+}
+
 // A bounded wait that the whole warp agrees on: no lane runs ahead into a warp-collective tcgen05 instruction
 // while another gave up.
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity) {
@@ -192,9 +242,9 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const ExtendArgs
   int32_t* sTab = reinterpret_cast<int32_t*>(smem + Cfg::TAB_OFF);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Cfg::BAR_OFF);
   // Every barrier completes once per use of its buffer, so a waiter names an unambiguous phase.
-  uint64_t* bar_full = bars;                      // [STAGES] ring slot landed (producer arrival + bytes)
-  uint64_t* bar_empty = bars + Cfg::STAGES;       // [STAGES] ring slot read by every dequant warp
-  uint64_t* bar_k_full = bars + 2 * Cfg::STAGES;  // K tile written (dequant warps), once per tile
+  uint64_t* bar_full = bars;                      // [NSLOTS] ring slot landed (producer arrival + bytes)
+  uint64_t* bar_empty = bars + Cfg::NSLOTS;       // [NSLOTS] ring slot read by every dequant warp
+  uint64_t* bar_k_full = bars + 2 * Cfg::NSLOTS;  // K tile written (dequant warps), once per tile
   uint64_t* bar_v_full = bar_k_full + 1;          // V tile written (dequant warps), once per tile
   uint64_t* bar_qk_done = bar_k_full + 2;         // [2] QK into S buffer b completed (commit)
   uint64_t* bar_pv_done = bar_k_full + 4;         // [2] PV that read P buffer b completed (commit)
@@ -215,7 +265,7 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const ExtendArgs
       run += ((n * G + kM - 1) / kM) * a.num_kv_heads;
     }
     sTab[a.batch] = run;
-    for (int s = 0; s < Cfg::STAGES; ++s) {
+    for (int s = 0; s < Cfg::NSLOTS; ++s) {
       mbar_init(&bar_full[s], 1);
       mbar_init(&bar_empty[s], kDwWarps);
     }
@@ -242,28 +292,38 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const ExtendArgs
   const int32_t n_items = sTab[a.batch];
   bool ok = true;
 
-  if (warp == kProdWarp) {
-    // ===================================================================== producer
-    // Lane pi (< PPT) owns page pi of a tile: its block-table entry, valid tokens and copies.
+  if (warp >= kProdWarp) {
+    // ===================================================================== producers
+    // Warp 13 fills the K ring, warp 14 the V ring.  Lane pi (< PPT) owns page pi of a tile: its block-table
+    // entry (read one tile ahead), valid tokens and copies.
+    const int kv = warp - kProdWarp;
+    const int stages = kv ? Cfg::VSTAGES : Cfg::KSTAGES;
+    const int base = kv ? Cfg::KSTAGES : 0;
+    auto page_entry = [&](const XIter<D>& ti) -> int32_t {
+      if (!ti.live || lane >= Cfg::PPT) return -1;
+      const int32_t pg = ti.i * Cfg::PPT + lane;
+      if (pg >= a.max_pages || pg * kPage >= ti.it.L) return -1;
+      return __ldg(a.block_table + static_cast<int64_t>(ti.it.b) * a.max_pages + pg);
+    };
     XIter<D> t;
     t.first(sTab, a, G, n_items);
+    int32_t bt = page_entry(t);
     uint32_t n = 0;  // tiles issued
     while (ok && t.live) {
-      const int32_t pg = t.i * Cfg::PPT + lane;
-      int32_t phys = -1, nvalid = 0;
-      if (lane < Cfg::PPT && pg < a.max_pages && pg * kPage < t.it.L) {
-        phys = __ldg(a.block_table + static_cast<int64_t>(t.it.b) * a.max_pages + pg);
-        if (phys >= a.num_pages) {  // never dereferenced; reported in the status word
-          set_status(a.status, kStatusBadPage);
-          phys = -1;
-        }
-        if (phys >= 0) nvalid = min(kPage, t.it.L - pg * kPage);
+      int32_t phys = bt, nvalid = 0;
+      if (phys >= a.num_pages) {  // never dereferenced; reported in the status word
+        set_status(a.status, kStatusBadPage);
+        phys = -1;
       }
-      const int sl = n % Cfg::STAGES;
-      const uint32_t use = n / Cfg::STAGES;
+      if (phys >= 0) nvalid = min(kPage, t.it.L - (t.i * Cfg::PPT + lane) * kPage);
+      XIter<D> nx = t;
+      nx.next(sTab, a, G);
+      bt = page_entry(nx);
+      const int sl = base + static_cast<int>(n % stages);
+      const uint32_t use = n / stages;
       if (use > 0 && !warp_wait(&bar_empty[sl], (use - 1) & 1)) { ok = false; break; }
-      const uint32_t bytes = __reduce_add_sync(
-          0xffffffffu, phys >= 0 ? static_cast<uint32_t>(2 * (Cfg::NSL * kBox + Cfg::SC_KV)) : 0u);
+      const uint32_t bytes =
+          __reduce_add_sync(0xffffffffu, phys >= 0 ? static_cast<uint32_t>(Cfg::NSL * kBox + Cfg::SC_KV) : 0u);
       int32_t nv[Cfg::PPT];
 #pragma unroll
       for (int i = 0; i < Cfg::PPT; ++i) nv[i] = __shfl_sync(0xffffffffu, nvalid, i);
@@ -276,23 +336,20 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const ExtendArgs
       if (phys >= 0) {
         uint8_t* slot = sRing + sl * Cfg::SLOT_BYTES;
 #pragma unroll
-        for (int kv = 0; kv < 2; ++kv) {
-#pragma unroll
-          for (int c = 0; c < Cfg::NSL; ++c)
-            tma_load_codes(smem_u32(slot + ((kv * Cfg::PPT + lane) * Cfg::NSL + c) * kBox), &tmap, c,
-                           t.it.g * kPage, kv, phys, &bar_full[sl]);
-          const uint8_t* src = reinterpret_cast<const uint8_t*>(a.scales) +
-                               ((static_cast<int64_t>(phys) * 2 + kv) * a.num_kv_heads + t.it.g) * Cfg::SC_KV;
-          bulk_g2s(slot + Cfg::CODE_BYTES + (kv * Cfg::PPT + lane) * Cfg::SC_KV, src, Cfg::SC_KV, &bar_full[sl]);
-        }
+        for (int c = 0; c < Cfg::NSL; ++c)
+          tma_load_codes(smem_u32(slot + (lane * Cfg::NSL + c) * kBox), &tmap, c, t.it.g * kPage, kv, phys,
+                         &bar_full[sl]);
+        const uint8_t* src = reinterpret_cast<const uint8_t*>(a.scales) +
+                             ((static_cast<int64_t>(phys) * 2 + kv) * a.num_kv_heads + t.it.g) * Cfg::SC_KV;
+        bulk_g2s(slot + Cfg::CODE_BYTES + lane * Cfg::SC_KV, src, Cfg::SC_KV, &bar_full[sl]);
       }
-      t.next(sTab, a, G);
+      t = nx;
       ++n;
     }
     // no copy may still be in flight when the CTA exits
-    for (uint32_t j = 1; j <= n && j <= static_cast<uint32_t>(Cfg::STAGES); ++j) {
+    for (uint32_t j = 1; j <= n && j <= static_cast<uint32_t>(stages); ++j) {
       const uint32_t m = n - j;
-      (void)mbar_wait_bounded(&bar_full[m % Cfg::STAGES], (m / Cfg::STAGES) & 1);
+      (void)mbar_wait_bounded(&bar_full[base + m % stages], (m / stages) & 1);
     }
   } else if (warp >= kSmWarps && warp < kMmaWarp) {
     // ===================================================================== dequant warps
@@ -302,11 +359,11 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const ExtendArgs
     const int pi = tt / kPage, off = tt % kPage;
     const int swz = off & 7;   // 128-byte swizzle phase of this token's staging rows
     const uint32_t toff = (tt % 8) * 16 + (tt / 8) * Cfg::RS;
-    // dequantize this thread's codes of K (kv = 0) or V (kv = 1) from a ring slot into a bf16 tile
-    auto write_tile = [&](uint8_t* dst, const uint8_t* slot, int kv, bool v_ok) {
-      const uint8_t* rows = slot + (kv * Cfg::PPT + pi) * Cfg::NSL * kBox + off * 128;
+    // dequantize this thread's codes of K or V from a ring slot into a bf16 tile
+    auto write_tile = [&](uint8_t* dst, const uint8_t* slot, bool v_ok) {
+      const uint8_t* rows = slot + pi * Cfg::NSL * kBox + off * 128;
       const uint32_t sc = *reinterpret_cast<const uint32_t*>(
-          slot + Cfg::CODE_BYTES + (kv * Cfg::PPT + pi) * Cfg::SC_KV + (off * Cfg::NB + part * Cfg::NBT) * 2);
+          slot + Cfg::CODE_BYTES + pi * Cfg::SC_KV + (off * Cfg::NB + part * Cfg::NBT) * 2);
 #pragma unroll
       for (int k = 0; k < Cfg::NCH; ++k) {
         uint32_t w[8];
@@ -330,25 +387,29 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const ExtendArgs
     uint32_t nk = 0, nv = 0;  // tiles whose K / V have been written
     while (ok && (tk.live || nv < nk)) {
       if (tk.live) {
-        const int ring = nk % Cfg::STAGES;
-        if (!warp_wait(&bar_full[ring], (nk / Cfg::STAGES) & 1)) { ok = false; break; }
+        const int ring = nk % Cfg::KSTAGES;
+        if (!warp_wait(&bar_full[ring], (nk / Cfg::KSTAGES) & 1)) { ok = false; break; }
         const uint8_t* slot = sRing + ring * Cfg::SLOT_BYTES;
         const bool v_ok = off < sMeta[ring * Cfg::PPT + pi];
         // the K tile was last read by the QK of tile nk - 1
         if (nk >= 1 && !warp_wait(&bar_qk_done[(nk - 1) & 1], ((nk - 1) >> 1) & 1)) { ok = false; break; }
-        write_tile(sK, slot, 0, v_ok);
-        if (lane == 0) bar_arrive(bar_k_full);
+        write_tile(sK, slot, v_ok);
+        if (lane == 0) {
+          bar_arrive(bar_k_full);
+          bar_arrive(&bar_empty[ring]);
+        }
         tk.next(sTab, a, G);
         ++nk;
         if (nk == 1 && tk.live) continue;  // K runs one tile ahead of V
       }
       {
-        const int ring = nv % Cfg::STAGES;  // landed: its K was read above
+        const int ring = Cfg::KSTAGES + nv % Cfg::VSTAGES;
+        if (!warp_wait(&bar_full[ring], (nv / Cfg::VSTAGES) & 1)) { ok = false; break; }
         const uint8_t* slot = sRing + ring * Cfg::SLOT_BYTES;
         const bool v_ok = off < sMeta[ring * Cfg::PPT + pi];
         // the V tile was last read by the PV of tile nv - 1
         if (nv >= 1 && !warp_wait(&bar_pv_done[(nv - 1) & 1], ((nv - 1) >> 1) & 1)) { ok = false; break; }
-        write_tile(sV, slot, 1, v_ok);
+        write_tile(sV, slot, v_ok);
         if (lane == 0) {
           bar_arrive(bar_v_full);
           bar_arrive(&bar_empty[ring]);
@@ -433,37 +494,53 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const ExtendArgs
       const bool row_ok = tok < it.n;
       const int32_t pos = row_ok ? it.L - it.n + tok : -1;  // last key position this row sees
       float m_used = -INFINITY, l = 0.0f;
+      // lane pi (< PPT) holds the block-table entry of page pi of a tile, read one tile ahead of its use
+      auto fetch = [&](int32_t i) -> int32_t {
+        const int32_t pg = i * Cfg::PPT + lane;
+        if (lane >= Cfg::PPT || i >= it.ntiles || pg >= a.max_pages || pg * kPage >= it.L) return -1;
+        return __ldg(a.block_table + static_cast<int64_t>(it.b) * a.max_pages + pg);
+      };
+      int32_t ent = fetch(0);
       for (int32_t i = 0; i < it.ntiles; ++i, ++n) {
         const int b = n & 1;
         // mapped pages of the tile (chunk c of 16 keys is page c of the tile)
-        uint32_t pmask = 0;
-#pragma unroll
-        for (int pi = 0; pi < Cfg::PPT; ++pi) {
-          const int32_t pg = i * Cfg::PPT + pi;
-          if (pg < a.max_pages && pg * kPage < it.L) {
-            const int32_t e = __ldg(a.block_table + static_cast<int64_t>(it.b) * a.max_pages + pg);
-            if (e >= 0 && e < a.num_pages) pmask |= 1u << pi;
-          }
-        }
+        const uint32_t pmask = __ballot_sync(0xffffffffu, ent >= 0 && ent < a.num_pages) & ((1u << Cfg::PPT) - 1u);
+        ent = fetch(i + 1);
         const int32_t lim = pos - i * T;  // keys k <= lim of this tile are causally visible
         if (!warp_wait(&bar_qk_done[b], (n >> 1) & 1)) { ok = false; break; }
         tc_fence_after();
-        // pass 1: the row's max over its visible keys (scaled: exp2 domain)
+        // every row of the warp sees every key of the tile (no causal edge, no masked page): no masking.  The
+        // two variants of each pass are separate straight-line loops behind one warp-uniform branch.
+        const bool full = __all_sync(0xffffffffu, lim >= T - 1) && pmask == (1u << Cfg::PPT) - 1u;
+        // pass 1: the row's max over its visible keys (sm_scale > 0, so scaling commutes with the max)
         float mx = -INFINITY;
+        auto pass1 = [&](auto masked) {
+          float m[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll 1
-        for (int c = 0; c < T / 16; ++c) {
-          float s[16];
-          tmem_ld16(tS + b * T + c * 16, s);
-          const bool pg_ok = (pmask >> c) & 1u;
+          for (int h = 0; h < T / 64; ++h) {
+            uint32_t v[64];
+            tmem_ld64(tS + b * T + h * 64, v);
 #pragma unroll
-          for (int e = 0; e < 16; ++e)
-            if (pg_ok && c * 16 + e <= lim) mx = fmaxf(mx, s[e] * a.score_scale);
-        }
+            for (int e = 0; e < 64; ++e) {
+              float x = __uint_as_float(v[e]);
+              if constexpr (decltype(masked)::value) {
+                const int k = h * 64 + e;
+                const bool vis = (((pmask >> (k / kPage)) & 1u) != 0u) & (k <= lim);
+                x = vis ? x : -INFINITY;
+              }
+              m[e & 3] = fmaxf(m[e & 3], x);
+            }
+          }
+          mx = fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3]));
+        };
+        if (full) pass1(std::false_type{});
+        else pass1(std::true_type{});
+        if (mx > -INFINITY) mx *= a.score_scale;
         float alpha = 1.0f;
         bool resc = false;
         if (mx > -INFINITY && (m_used == -INFINITY || mx > m_used + kLazyRescale)) {
           if (m_used != -INFINITY) {
-            alpha = exp2f(m_used - mx);
+            alpha = ex2(m_used - mx);
             resc = true;
           }
           m_used = mx;
@@ -475,37 +552,47 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const ExtendArgs
           if (!warp_wait(&bar_pv_done[(n - 1) & 1], ((n - 1) >> 1) & 1)) { ok = false; break; }
           tc_fence_after();
 #pragma unroll 1
-          for (int c = 0; c < D / 16; ++c) {
-            float o[16];
-            tmem_ld16(tO + c * 16, o);
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t o[32];
+            tmem_ld32(tO + c * 32, o);
 #pragma unroll
-            for (int e = 0; e < 16; ++e) o[e] *= alpha;
-            tmem_st16(tO + c * 16, o);
+            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+            tmem_st32(tO + c * 32, o);
           }
+          asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
           l *= alpha;
         }
-        // pass 2: P (bf16) into tensor memory, and the row sum of exactly those bf16 values
+        // pass 2: P = 2^(s * scale - m) as bf16 into tensor memory; the row sum in fp32
+        auto pass2 = [&](auto masked) {
+          float ls[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll 1
-        for (int c2 = 0; c2 < T / 32; ++c2) {
-          float s[32];
-          tmem_ld16(tS + b * T + c2 * 32, *reinterpret_cast<float(*)[16]>(s));
-          tmem_ld16(tS + b * T + c2 * 32 + 16, *reinterpret_cast<float(*)[16]>(s + 16));
-          uint32_t w[16];
+          for (int h = 0; h < T / 64; ++h) {
+            uint32_t v[64];
+            tmem_ld64(tS + b * T + h * 64, v);
+            uint32_t w[32];
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            float pr[2];
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              const int j = 2 * e + h;
-              const bool vis = ((pmask >> (2 * c2 + j / 16)) & 1u) && c2 * 32 + j <= lim;
-              pr[h] = vis ? exp2f(fmaf(s[j], a.score_scale, -m_used)) : 0.0f;
+            for (int e = 0; e < 32; ++e) {
+              const float x0 = fmaf(__uint_as_float(v[2 * e]), a.score_scale, -m_used);
+              const float x1 = fmaf(__uint_as_float(v[2 * e + 1]), a.score_scale, -m_used);
+              // every fourth pair on the FMA pipe, the rest on the MUFU unit
+              float p0 = (e & 3) == 3 ? ex2_fma(x0) : ex2(x0);
+              float p1 = (e & 3) == 3 ? ex2_fma(x1) : ex2(x1);
+              if constexpr (decltype(masked)::value) {
+                const int k = h * 64 + 2 * e;  // k and k + 1 share a page
+                const bool pg = ((pmask >> (k / kPage)) & 1u) != 0u;
+                p0 = (pg & (k <= lim)) ? p0 : 0.0f;
+                p1 = (pg & (k + 1 <= lim)) ? p1 : 0.0f;
+              }
+              ls[(2 * e) & 3] += p0;
+              ls[(2 * e + 1) & 3] += p1;
+              w[e] = pack_bf16x2(p0, p1);
             }
-            w[e] = pack_bf16x2(pr[0], pr[1]);
-            const float2 pb = unpack_bf16x2(w[e]);
-            l += pb.x + pb.y;
+            tmem_st32(tP + b * (T / 2) + h * 32, w);
           }
-          tmem_st16u(tP + b * (T / 2) + c2 * 16, w);
-        }
+          l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+        };
+        if (full) pass2(std::false_type{});
+        else pass2(std::true_type{});
         asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
         tc_fence_before();
         __syncwarp();
@@ -521,23 +608,23 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const ExtendArgs
       const float inv = l > 0.0f ? 1.0f / l : 0.0f;
       const int64_t orow = (static_cast<int64_t>(it.q0 + (row_ok ? tok : 0)) * a.num_q_heads + it.g * G + r % G) * D;
 #pragma unroll 1
-      for (int c = 0; c < D / 16; ++c) {
-        float o[16];
-        tmem_ld16(tO + c * 16, o);
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t ov[32];
+        tmem_ld32(tO + c * 32, ov);
         if (row_ok) {
+          float o[32];
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] = __uint_as_float(ov[e]) * inv;
           if (a.out_dtype == KVQ_OUT_F32) {
-            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(a.out) + orow + c * 16);
+            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(a.out) + orow + c * 32);
 #pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4)
-              dst[q4] = make_float4(o[4 * q4] * inv, o[4 * q4 + 1] * inv, o[4 * q4 + 2] * inv, o[4 * q4 + 3] * inv);
+            for (int q4 = 0; q4 < 8; ++q4) dst[q4] = make_float4(o[4 * q4], o[4 * q4 + 1], o[4 * q4 + 2], o[4 * q4 + 3]);
           } else {
-            uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.out) + orow + c * 16);
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.out) + orow + c * 32);
 #pragma unroll
-            for (int h8 = 0; h8 < 2; ++h8)
-              dst[h8] = make_uint4(pack_bf16x2(o[8 * h8] * inv, o[8 * h8 + 1] * inv),
-                                   pack_bf16x2(o[8 * h8 + 2] * inv, o[8 * h8 + 3] * inv),
-                                   pack_bf16x2(o[8 * h8 + 4] * inv, o[8 * h8 + 5] * inv),
-                                   pack_bf16x2(o[8 * h8 + 6] * inv, o[8 * h8 + 7] * inv));
+            for (int h8 = 0; h8 < 4; ++h8)
+              dst[h8] = make_uint4(pack_bf16x2(o[8 * h8], o[8 * h8 + 1]), pack_bf16x2(o[8 * h8 + 2], o[8 * h8 + 3]),
+                                   pack_bf16x2(o[8 * h8 + 4], o[8 * h8 + 5]), pack_bf16x2(o[8 * h8 + 6], o[8 * h8 + 7]));
           }
         }
       }
