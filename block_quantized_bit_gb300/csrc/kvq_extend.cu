@@ -21,14 +21,16 @@
 //   warps 13-14 producers, one for K and one for V: TMA copies of a tile's codes (128-byte swizzled boxes of
 //               16 tokens x 128 code bytes) and bulk copies of their scales into that producer's staging ring,
 //               with each page's number of valid tokens; the block table is read one tile ahead.
-//   warps 4-11  dequant: a thread owns 64 codes of one token row, of K and then of V.  K of tile j + 1 is
+//   warps 8-15  dequant: a thread owns 64 codes of one token row, of K and then of V.  K of tile j + 1 is
 //               written before V of tile j, so the next QK never waits for the V tile.
-//   warp 12     allocates tensor memory and issues every MMA (one elected lane): QK of tile j, then PV of
+//   warp 16     allocates tensor memory and issues every MMA (one elected lane): QK of tile j, then PV of
 //               tile j - 1, so the softmax of tile j overlaps the tensor pipe.
-//   warps 0-3   softmax, one query row per thread (= tensor-memory lane): causal and page masks, online
-//               softmax in the exp2 domain with lazy rescaling (the running max moves only when a score
-//               passes it by more than 2^8), P as bf16 into tensor memory.  At an item's end they write the
-//               next item's Q rows, then O / l to the output.
+//   warps 0-7   softmax: warps q and q + 4 own the 32 query rows of tensor-memory lane quarter q (one row
+//               per thread) and each takes half of a tile's keys and of O's columns; the two exchange
+//               their half-tile maxima through shared memory.  Causal and page masks, online softmax in
+//               the exp2 domain with lazy rescaling (the running max moves only when a score passes it
+//               by more than 2^8), P as bf16 into tensor memory.  At an item's end they write the next
+//               item's Q rows, then O / l to the output.
 // Every wait is bounded (2 s) and reports a timeout in the status word instead of hanging.
 #include <cuda.h>
 #include <math.h>
@@ -44,11 +46,11 @@ namespace kvq {
 namespace {
 
 constexpr int kM = 128;  // query rows per item (the MMA M)
-constexpr int kSmWarps = 4;
+constexpr int kSmWarps = 8;  // two per tensor-memory lane quarter, each on half of a tile's keys
 constexpr int kDwWarps = 8;
-constexpr int kMmaWarp = kSmWarps + kDwWarps;   // warp 12
-constexpr int kProdWarp = kMmaWarp + 1;         // warps 13 (K ring) and 14 (V ring)
-constexpr int kThreads = (kProdWarp + 2) * 32;  // 15 warps
+constexpr int kMmaWarp = kSmWarps + kDwWarps;   // warp 16
+constexpr int kProdWarp = kMmaWarp + 1;         // warps 17 (K ring) and 18 (V ring)
+constexpr int kThreads = (kProdWarp + 2) * 32;  // 19 warps
 constexpr int kDwThreads = kDwWarps * 32;
 constexpr int kTmemCols = 512;
 constexpr int kBox = kPage * 128;      // one TMA box: 16 tokens x 128 code bytes
@@ -73,7 +75,7 @@ struct XCfg {
   // so the two rings run at their own pace and the K ring runs deeper.
   static constexpr int CODE_BYTES = PPT * NSL * kBox;
   static constexpr int SLOT_BYTES = CODE_BYTES + PPT * SC_KV;
-  static constexpr int KSTAGES = (D == 128) ? 4 : 3;
+  static constexpr int KSTAGES = 3;
   static constexpr int VSTAGES = (D == 128) ? 3 : 2;
   static constexpr int NSLOTS = KSTAGES + VSTAGES;  // K ring slots, then V ring slots
   static constexpr int RING_OFF = 0;  // 1024-byte aligned: swizzle atoms
@@ -81,8 +83,10 @@ struct XCfg {
   static constexpr int V_OFF = K_OFF + KV_TILE;
   static constexpr int Q_OFF = V_OFF + KV_TILE;
   static constexpr int META_OFF = Q_OFF + Q_BYTES;              // [NSLOTS][PPT] valid tokens per page
-  static constexpr int TAB_OFF = META_OFF + NSLOTS * PPT * 4;   // [batch + 1] first item of each sequence
-  static constexpr int NBARS = 2 * NSLOTS + 10;
+  static constexpr int RED_OFF = META_OFF + NSLOTS * PPT * 4;   // [2 parities][2 halves][128 rows] row maxima
+  static constexpr int SUM_OFF = RED_OFF + 2 * 2 * kM * 4;      // [2 item parities][2 halves][128 rows] row sums
+  static constexpr int TAB_OFF = SUM_OFF + 2 * 2 * kM * 4;      // [batch + 1] first item of each sequence
+  static constexpr int NBARS = 2 * NSLOTS + 10 + 12;
   static constexpr int BAR_OFF = (TAB_OFF + (kMaxExtendBatch + 1) * 4 + 15) / 16 * 16;  // mbarriers: 8-byte aligned
   static constexpr int SMEM_BYTES = BAR_OFF + NBARS * 8 + 16 + 1024;  // + slack to align the base
   // tensor-memory columns: O [0, D); S buffer b [D + b T, D + (b + 1) T); P buffer b [384 + b T / 2, ...)
@@ -251,6 +255,8 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const ExtendArgs
   uint64_t* bar_p_full = bar_k_full + 6;          // [2] P buffer b written, S buffer b read (softmax warps)
   uint64_t* bar_q_full = bar_k_full + 8;          // an item's Q rows written (softmax warps), once per item
   uint64_t* bar_o_free = bar_k_full + 9;          // an item's O read out (softmax warps), once per item
+  uint64_t* bar_pair = bar_k_full + 10;           // [4 quarters][2 parities] both half-tile maxima written
+  uint64_t* bar_sum = bar_k_full + 18;            // [4 quarters] both half row sums written, once per item
   uint32_t* sTmem = reinterpret_cast<uint32_t*>(smem + Cfg::BAR_OFF + Cfg::NBARS * 8);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -278,6 +284,7 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const ExtendArgs
     }
     mbar_init(bar_q_full, kSmWarps);
     mbar_init(bar_o_free, kSmWarps);
+    for (int i = 0; i < 12; ++i) mbar_init(&bar_pair[i], 2);
     fence_mbar_init();
   }
   if (warp == kMmaWarp) {
@@ -468,11 +475,16 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const ExtendArgs
     if (n > 0) (void)mbar_wait_bounded(&bar_qk_done[(n - 1) & 1], ((n - 1) >> 1) & 1);
   } else {
     // ===================================================================== softmax warps
-    const int r = tid;  // query row = tensor-memory lane
-    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
-    const uint32_t tS = tmem + Cfg::S_COL + lane_base, tO = tmem + lane_base, tP = tmem + Cfg::P_COL + lane_base;
+    const int quarter = warp & 3, hf = warp >> 2;  // lane quarter; which half of the keys and of O
+    const int r = quarter * 32 + lane;             // query row = tensor-memory lane
+    const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+    const uint32_t tS = tmem + Cfg::S_COL + lane_base + hf * (T / 2);
+    const uint32_t tO = tmem + lane_base + hf * (D / 2);
+    const uint32_t tP = tmem + Cfg::P_COL + lane_base + hf * (T / 4);
+    float* sRed = reinterpret_cast<float*>(smem + Cfg::RED_OFF);
+    float* sSum = reinterpret_cast<float*>(smem + Cfg::SUM_OFF);
     const int32_t tb = kM / G;  // new tokens per query block
-    // the item's Q rows into the shared tile (rows past the sequence's new tokens are zero)
+    // this warp's half of the item's Q rows into the shared tile (rows past the new tokens are zero)
     auto write_q = [&](const XItem& it) {
       const int32_t tok = it.blk * tb + r / G;
       const bool valid = tok < it.n;
@@ -480,13 +492,20 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const ExtendArgs
           a.q + (static_cast<int64_t>(it.q0 + (valid ? tok : 0)) * a.num_q_heads + it.g * G + r % G) * D);
       uint8_t* dst = sQ + (r % 8) * 16 + (r / 8) * Cfg::RS;
 #pragma unroll 4
-      for (int j = 0; j < D / 8; ++j)
+      for (int j = hf * (D / 16); j < (hf + 1) * (D / 16); ++j)
         *reinterpret_cast<uint4*>(dst + j * 128) = valid ? __ldg(src + j) : make_uint4(0, 0, 0, 0);
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) bar_arrive(bar_q_full);
     };
-    uint32_t n = 0;  // tiles processed
+    // the two warps of a lane quarter meet on mbarriers (bounded waits: a warp that gave up cannot strand
+    // the other)
+    auto pair_meet = [&](uint64_t* bar, uint32_t parity) -> bool {
+      __syncwarp();
+      if (lane == 0) bar_arrive(bar);
+      return warp_wait(bar, parity);
+    };
+    uint32_t n = 0, items = 0;  // tiles processed; items finished
     if (static_cast<int32_t>(blockIdx.x) < n_items) write_q(x_locate<D>(sTab, a, G, blockIdx.x));
     for (int32_t item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
       const XItem it = x_locate<D>(sTab, a, G, item);
@@ -506,35 +525,42 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const ExtendArgs
         // mapped pages of the tile (chunk c of 16 keys is page c of the tile)
         const uint32_t pmask = __ballot_sync(0xffffffffu, ent >= 0 && ent < a.num_pages) & ((1u << Cfg::PPT) - 1u);
         ent = fetch(i + 1);
-        const int32_t lim = pos - i * T;  // keys k <= lim of this tile are causally visible
+        const int32_t lim = pos - i * T - hf * (T / 2);  // keys k <= lim of this warp's half are visible
+        const uint32_t hmask = pmask >> (hf * Cfg::PPT / 2);  // this half's pages
         if (!warp_wait(&bar_qk_done[b], (n >> 1) & 1)) { ok = false; break; }
         tc_fence_after();
-        // every row of the warp sees every key of the tile (no causal edge, no masked page): no masking.  The
+        // every row of the warp sees every key of its half (no causal edge, no masked page): no masking.  The
         // two variants of each pass are separate straight-line loops behind one warp-uniform branch.
-        const bool full = __all_sync(0xffffffffu, lim >= T - 1) && pmask == (1u << Cfg::PPT) - 1u;
-        // pass 1: the row's max over its visible keys (sm_scale > 0, so scaling commutes with the max)
-        float mx = -INFINITY;
+        const bool full = __all_sync(0xffffffffu, lim >= T / 2 - 1) && (hmask & ((1u << (Cfg::PPT / 2)) - 1u)) ==
+                                                                         (1u << (Cfg::PPT / 2)) - 1u;
+        // pass 1: the row's max over the visible keys of this half (sm_scale > 0: scaling commutes with it)
+        float mh = -INFINITY;
         auto pass1 = [&](auto masked) {
           float m[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll 1
           for (int h = 0; h < T / 64; ++h) {
-            uint32_t v[64];
-            tmem_ld64(tS + b * T + h * 64, v);
+            uint32_t v[32];
+            tmem_ld32(tS + b * T + h * 32, v);
 #pragma unroll
-            for (int e = 0; e < 64; ++e) {
+            for (int e = 0; e < 32; ++e) {
               float x = __uint_as_float(v[e]);
               if constexpr (decltype(masked)::value) {
-                const int k = h * 64 + e;
-                const bool vis = (((pmask >> (k / kPage)) & 1u) != 0u) & (k <= lim);
+                const int k = h * 32 + e;
+                const bool vis = (((hmask >> (k / kPage)) & 1u) != 0u) & (k <= lim);
                 x = vis ? x : -INFINITY;
               }
               m[e & 3] = fmaxf(m[e & 3], x);
             }
           }
-          mx = fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3]));
+          mh = fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3]));
         };
         if (full) pass1(std::false_type{});
         else pass1(std::true_type{});
+        // the row's max over the whole tile: exchange halves with the other warp of the lane quarter
+        // (double-buffered by tile parity, so one barrier per tile suffices)
+        sRed[(b * 2 + hf) * kM + r] = mh;
+        if (!pair_meet(&bar_pair[quarter * 2 + b], (n >> 1) & 1)) { ok = false; break; }
+        float mx = fmaxf(sRed[(b * 2) * kM + r], sRed[(b * 2 + 1) * kM + r]);
         if (mx > -INFINITY) mx *= a.score_scale;
         float alpha = 1.0f;
         bool resc = false;
@@ -548,11 +574,11 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const ExtendArgs
         // P buffer b is free once the PV two tiles back has read it
         if (n >= 2 && !warp_wait(&bar_pv_done[b], ((n >> 1) - 1) & 1)) { ok = false; break; }
         if (__any_sync(0xffffffffu, resc)) {  // (only from the second tile of an item on)
-          // O must hold the PV of the previous tile before it is scaled
+          // O must hold the PV of the previous tile before it is scaled; this warp scales its half of O
           if (!warp_wait(&bar_pv_done[(n - 1) & 1], ((n - 1) >> 1) & 1)) { ok = false; break; }
           tc_fence_after();
 #pragma unroll 1
-          for (int c = 0; c < D / 32; ++c) {
+          for (int c = 0; c < D / 64; ++c) {
             uint32_t o[32];
             tmem_ld32(tO + c * 32, o);
 #pragma unroll
@@ -562,24 +588,24 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const ExtendArgs
           asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
           l *= alpha;
         }
-        // pass 2: P = 2^(s * scale - m) as bf16 into tensor memory; the row sum in fp32
+        // pass 2: P = 2^(s * scale - m) of this half as bf16 into tensor memory; the row sum in fp32
         auto pass2 = [&](auto masked) {
           float ls[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll 1
           for (int h = 0; h < T / 64; ++h) {
-            uint32_t v[64];
-            tmem_ld64(tS + b * T + h * 64, v);
-            uint32_t w[32];
+            uint32_t v[32];
+            tmem_ld32(tS + b * T + h * 32, v);
+            uint32_t w[16];
 #pragma unroll
-            for (int e = 0; e < 32; ++e) {
+            for (int e = 0; e < 16; ++e) {
               const float x0 = fmaf(__uint_as_float(v[2 * e]), a.score_scale, -m_used);
               const float x1 = fmaf(__uint_as_float(v[2 * e + 1]), a.score_scale, -m_used);
               // every fourth pair on the FMA pipe, the rest on the MUFU unit
               float p0 = (e & 3) == 3 ? ex2_fma(x0) : ex2(x0);
               float p1 = (e & 3) == 3 ? ex2_fma(x1) : ex2(x1);
               if constexpr (decltype(masked)::value) {
-                const int k = h * 64 + 2 * e;  // k and k + 1 share a page
-                const bool pg = ((pmask >> (k / kPage)) & 1u) != 0u;
+                const int k = h * 32 + 2 * e;  // k and k + 1 share a page
+                const bool pg = ((hmask >> (k / kPage)) & 1u) != 0u;
                 p0 = (pg & (k <= lim)) ? p0 : 0.0f;
                 p1 = (pg & (k + 1 <= lim)) ? p1 : 0.0f;
               }
@@ -587,7 +613,7 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const ExtendArgs
               ls[(2 * e + 1) & 3] += p1;
               w[e] = pack_bf16x2(p0, p1);
             }
-            tmem_st32(tP + b * (T / 2) + h * 32, w);
+            tmem_st16u(tP + b * (T / 2) + h * 16, w);
           }
           l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
         };
@@ -602,13 +628,20 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const ExtendArgs
       // the next item's Q rows (every QK of this item has completed: its last S was read above)
       const int32_t nxt = item + static_cast<int32_t>(gridDim.x);
       if (nxt < n_items) write_q(x_locate<D>(sTab, a, G, nxt));
-      // O / l of this item, once its last PV has completed
+      // the row sum over both halves (double-buffered by item parity)
+      float* sum = sSum + (items & 1) * 2 * kM;
+      sum[hf * kM + r] = l;
+      if (!pair_meet(&bar_sum[quarter], items & 1)) { ok = false; break; }
+      const float lt = sum[r] + sum[kM + r];
+      ++items;
+      // this warp's half of O / l, once the item's last PV has completed
       if (!warp_wait(&bar_pv_done[(n - 1) & 1], ((n - 1) >> 1) & 1)) { ok = false; break; }
       tc_fence_after();
-      const float inv = l > 0.0f ? 1.0f / l : 0.0f;
-      const int64_t orow = (static_cast<int64_t>(it.q0 + (row_ok ? tok : 0)) * a.num_q_heads + it.g * G + r % G) * D;
+      const float inv = lt > 0.0f ? 1.0f / lt : 0.0f;
+      const int64_t orow =
+          (static_cast<int64_t>(it.q0 + (row_ok ? tok : 0)) * a.num_q_heads + it.g * G + r % G) * D + hf * (D / 2);
 #pragma unroll 1
-      for (int c = 0; c < D / 32; ++c) {
+      for (int c = 0; c < D / 64; ++c) {
         uint32_t ov[32];
         tmem_ld32(tO + c * 32, ov);
         if (row_ok) {
