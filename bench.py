@@ -8,6 +8,11 @@ Metric: algorithmic HBM bytes moved by the step per second (GB/s), i.e. store by
 and fp16 scales out, slot mapping) plus decode bytes (codes and scales of every valid token, q,
 block table, output), divided by the device time of the step.  L2 is flushed between steps.
 
+``--extend N`` measures the extend (prefill) step instead: the store of each sequence's last N rows (the
+step's new tokens) plus the causal attention of those tokens over the pool (kvq_extend, tensor cores),
+reported in TFLOP/s (4 * head_dim * query heads * the keys each new token sees) against the measured bf16
+tensor peak.
+
 ``--impl reference`` times the CPU oracle (the plain C reference of the same computation) on the
 host cores, on a bounded sample of the same workload, and prints the same line with
 ``"impl": "reference"``.
@@ -42,6 +47,8 @@ def parse():
     ap.add_argument("--path", type=int, default=0, help="decode path: 0 auto, 1 CUDA cores, 2 tcgen05")
     ap.add_argument("--topk", type=int, default=0,
                     help="sparse (top-K) decode: this many index-list columns per sequence (0: dense decode)")
+    ap.add_argument("--extend", type=int, default=0,
+                    help="extend (prefill) step: this many new tokens per sequence (0: the decode step)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--seed", type=int, default=None)
     return ap.parse_args()
@@ -522,17 +529,229 @@ def run_reference(args, world, rank):
     }
 
 
+# ------------------------------------------------------------------------------------------ extend
+EXTEND_METRIC = "quantized-KV extend (prefill) attention TFLOP/s (% of GB300 bf16 peak); kvq_store of the new rows"
+
+
+def extend_keys(case, q_start):
+    """Keys the extend reads, summed over new tokens: the unmasked positions up to each token's own."""
+    bt = case.block_table.cpu().numpy()
+    lens = case.seq_lens.cpu().numpy()
+    qs = q_start.cpu().numpy()
+    P = case.page_size
+    total = 0
+    for b, L in enumerate(lens):
+        n = int(qs[b + 1] - qs[b])
+        if n == 0:
+            continue
+        seen = np.cumsum(bt[b, np.arange(L) // P] >= 0)
+        total += int(seen[L - n + np.arange(n)].sum())
+    return total
+
+
+def extend_inputs(case, args):
+    from block_quantized_bit_gb300 import workloads
+    return workloads.extend_inputs(case, args.extend)
+
+
+def run_extend(args, world, rank):
+    from block_quantized_bit_gb300 import kvq
+    dev = torch.device("cuda", torch.cuda.current_device())
+    case = make_case(args, "cuda")
+    L = kvq.Layout(case.num_pages, case.page_size, case.num_kv_heads, case.head_dim, case.v_dim, case.mla)
+    codes, scales = kvq.alloc_pool(L, dev)
+    codes.zero_()
+    scales.zero_()
+    kvq.kvq_store(codes, scales, case.k, case.v, case.slot_mapping, L, case.kind)  # the context (untimed)
+    q, q_start, rows = extend_inputs(case, args)
+    sk, sv, ss = case.k[rows], case.v[rows], case.slot_mapping[rows]  # the step re-stores its new rows
+    out = torch.empty(q.shape[0], case.num_q_heads, case.v_dim, dtype=torch.bfloat16, device=dev)
+    ws = kvq.alloc_extend_workspace(dev)
+    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)  # 4x L2
+    stream = torch.cuda.current_stream()
+
+    def extend(q_, qs_, bt_, sl_, o):
+        kvq.kvq_extend(q_, codes, scales, bt_, sl_, qs_, o, ws, L, case.kind, case.sm_scale)
+
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        kvq.kvq_store(codes, scales, sk, sv, ss, L, case.kind)
+        extend(q, q_start, case.block_table, case.seq_lens, out)
+    torch.cuda.synchronize()
+    st = kvq.kvq_workspace_status(ws)
+    if st != 0:
+        raise RuntimeError("extend reported status %d" % st)
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    for i in range(K):
+        flush.fill_(i & 0xFF)
+        ev[i][0].record(stream)
+        kvq.kvq_store(codes, scales, sk, sv, ss, L, case.kind)
+        ev[i][1].record(stream)
+        extend(q, q_start, case.block_table, case.seq_lens, out)
+        ev[i][2].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    store_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
+    ext_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K)]
+    total_ms = max_over_ranks(sum(store_ms) + sum(ext_ms), world)
+    keys = extend_keys(case, q_start)
+    flops = 4.0 * case.head_dim * case.num_q_heads * keys
+    ext_s = statistics.mean(ext_ms) / 1e3
+    achieved = flops / ext_s / 1e12
+    peaks = load_peaks()
+    peak = peaks.get("bf16_tflops")
+    store_rows = int(rows.numel())
+    row_elems = 2 * case.num_kv_heads * case.head_dim
+    store_b = store_rows * (row_elems * (2 + 1 + 2 / 32) + 8)
+
+    # end to end through the public API: the step's inputs from pinned host memory, its output back
+    hq, hqs = q.cpu().pin_memory(), q_start.cpu().pin_memory()
+    hk, hv, hs = sk.cpu().pin_memory(), sv.cpu().pin_memory(), ss.cpu().pin_memory()
+    hbt, hsl = case.block_table.cpu().pin_memory(), case.seq_lens.cpu().pin_memory()
+    hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    dq, dqs, dk, dv, ds = (torch.empty_like(t) for t in (q, q_start, sk, sv, ss))
+    dbt, dsl = torch.empty_like(case.block_table), torch.empty_like(case.seq_lens)
+    dout = torch.empty_like(out)
+
+    def one():
+        for d, h in ((dq, hq), (dqs, hqs), (dk, hk), (dv, hv), (ds, hs), (dbt, hbt), (dsl, hsl)):
+            d.copy_(h, non_blocking=True)
+        kvq.kvq_store(codes, scales, dk, dv, ds, L, case.kind)
+        extend(dq, dqs, dbt, dsl, dout)
+        hout.copy_(dout, non_blocking=True)
+
+    for _ in range(2):
+        one()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    e0.record(stream)
+    for _ in range(K):
+        one()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_s = max_over_ranks(e0.elapsed_time(e1) / 1e3, world) / K
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hqs, hk, hv, hs, hbt, hsl))
+    res = {
+        "metric": EXTEND_METRIC,
+        "value": round(world * flops * K / (total_ms / 1e3) / 1e12, 2),
+        "unit": "TFLOP/s",
+        "n_gpus": world, "steps": K, "warmup": args.warmup, "ms_per_step": round(total_ms / K, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16",  # K and V dequantized to bf16, P bf16, fp32 accumulation on the tensor cores
+        "data": "synthetic (seeded; workloads.py)",
+        "config": dict(workload_config(args, case, store_rows, keys, world), new_tokens_per_seq=args.extend,
+                       total_new_tokens=int(q.shape[0]), keys_read=keys),
+        "extend_us": round(ext_s * 1e6, 2),
+        "extend_tflops": round(achieved, 1),
+        "store_us": round(statistics.mean(store_ms) * 1e3, 2),
+        "store_gbs": round(store_b / (statistics.mean(store_ms) / 1e3) / 1e9, 1),
+        "roofline": {"bound": "tensor", "kernel": "kvq_extend (extend_tc_kernel)", "achieved": round(achieved, 1),
+                     "peak": peak, "unit": "TFLOP/s", "frac": round(achieved / peak, 4) if peak else None,
+                     "peak_source": "MEASURED_PEAKS.json bf16_tflops (burst; of measured)", "traffic": None},
+        "clocks": clk,
+        "e2e": {"value": round(world * flops / e2e_s / 1e12, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": hout.numel() * hout.element_size()},
+        "gpu_launches": 2 * K,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        res["cpu_baseline"] = extend_cpu_baseline(case, args)
+    return res
+
+
+def extend_oracle_pass(O, cpu, codes, scales, q, q_start, m, threads):
+    """The oracle on the first m new tokens of sequence 0 (their rows stored, their causal attention):
+    returns the FLOPs of that attention."""
+    bits = lambda t: t.contiguous().view(torch.int16).numpy().view(np.uint16)  # noqa: E731
+    n0 = int(q_start[1] - q_start[0])
+    L0 = int(cpu.seq_lens[0])
+    lens = cpu.seq_lens.clone()
+    lens[0] = L0 - n0 + m                          # the sample's last new token is token m - 1
+    qs = torch.zeros_like(q_start)
+    qs[1:] = m
+    rows = torch.arange(L0 - n0, L0 - n0 + m)      # sequence 0's rows come first in the context order
+    O.store(codes, scales, bits(cpu.k[rows]), bits(cpu.v[rows]), cpu.slot_mapping[rows].numpy(),
+            num_kv_heads=cpu.num_kv_heads, head_dim=cpu.head_dim, page_size=cpu.page_size, mla=False, kind=cpu.kind)
+    O.extend(bits(q[:m]), codes, scales, cpu.block_table.numpy(), lens.numpy(), qs.numpy(),
+             num_q_heads=cpu.num_q_heads, num_kv_heads=cpu.num_kv_heads, head_dim=cpu.head_dim, v_dim=cpu.v_dim,
+             page_size=cpu.page_size, mla=False, kind=cpu.kind, sm_scale=cpu.sm_scale, nthreads=threads)
+    sub = type(cpu)(**{**cpu.__dict__, "seq_lens": lens})
+    return 4.0 * cpu.head_dim * cpu.num_q_heads * extend_keys(sub, qs)
+
+
+def extend_oracle_setup(case, args):
+    O, cpu, codes, scales = prepare_oracle(case)
+    ctx = cpu.slot_mapping
+    bits = lambda t: t.contiguous().view(torch.int16).numpy().view(np.uint16)  # noqa: E731
+    O.store(codes, scales, bits(cpu.k), bits(cpu.v), ctx.numpy(), num_kv_heads=cpu.num_kv_heads,
+            head_dim=cpu.head_dim, page_size=cpu.page_size, mla=False, kind=cpu.kind)  # the context, untimed
+    q, q_start, _ = extend_inputs(cpu, args)
+    return O, cpu, codes, scales, q.cpu(), q_start.cpu(), max(1, O.openmp_threads())
+
+
+def extend_cpu_baseline(case, args):
+    """The oracle on a bounded sample of the extend: the first m new tokens of sequence 0 (~10 s)."""
+    O, cpu, codes, scales, q, q_start, threads = extend_oracle_setup(case, args)
+    n0 = int(q_start[1] - q_start[0])
+    m = min(4, n0)
+    t0 = time.perf_counter()
+    extend_oracle_pass(O, cpu, codes, scales, q, q_start, m, threads)
+    one = time.perf_counter() - t0
+    m = max(1, min(n0, int(m * 10.0 / max(one, 1e-3))))
+    t0 = time.perf_counter()
+    fl = extend_oracle_pass(O, cpu, codes, scales, q, q_start, m, threads)
+    dt = time.perf_counter() - t0
+    return {"value": round(fl / dt / 1e12, 6), "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+            "sample": "store + fp64 causal attention of the first %d of %d new tokens of sequence 0 (all heads); "
+                      "%.1f s" % (m, n0, dt)}
+
+
+def run_extend_reference(args, world, rank):
+    if rank != 0:
+        return None
+    case = make_case(args, "cpu")
+    O, cpu, codes, scales, q, q_start, threads = extend_oracle_setup(case, args)
+    m = min(8, int(q_start[1] - q_start[0]))
+    for _ in range(args.warmup):
+        extend_oracle_pass(O, cpu, codes, scales, q, q_start, m, threads)
+    t0 = time.perf_counter()
+    fl = 0.0
+    for _ in range(args.steps):
+        fl += extend_oracle_pass(O, cpu, codes, scales, q, q_start, m, threads)
+    dt = time.perf_counter() - t0
+    value = fl / dt / 1e12
+    sample = "store + fp64 causal attention of the first %d new tokens of sequence 0 (all heads) per step" % m
+    return {
+        "impl": "reference", "metric": EXTEND_METRIC, "value": round(value, 6), "unit": "TFLOP/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded; workloads.py)",
+        "config": dict(workload_config(args, case, int(q.shape[0]), extend_keys(case, q_start), world),
+                       new_tokens_per_seq=args.extend, sample=sample),
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
 def main():
     args = parse()
     world, rank = dist_setup(args)
     if args.impl == "reference":
-        res = run_reference(args, world, rank)
+        res = run_extend_reference(args, world, rank) if args.extend > 0 else run_reference(args, world, rank)
     else:
         if not torch.cuda.is_available():
             raise SystemExit("bench.py needs a CUDA GPU for --impl ours")
         from __graft_entry__ import build
         build()
-        res = run_ours(args, world, rank)
+        res = run_extend(args, world, rank) if args.extend > 0 else run_ours(args, world, rank)
     if rank == 0 and res is not None:
         print(json.dumps(res), flush=True)
     if world > 1:

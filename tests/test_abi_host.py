@@ -121,6 +121,31 @@ def test_decode_argument_errors(lib):
     assert _decode(lib, L(), opts=bad) == -1
 
 
+def _extend(lib, layout, *, hq=8, kind=1, sm_scale=1.0, ws=FAKE, ws_bytes=256, total_q=5, batch=2, out_dtype=0):
+    P = ctypes.c_void_p
+    return lib.kvq_extend(P(FAKE), P(FAKE), P(FAKE), P(FAKE), 10, P(FAKE), P(FAKE), total_q, batch, hq,
+                          ctypes.c_float(sm_scale), P(FAKE), out_dtype, P(ws), ws_bytes, ctypes.byref(layout.c()), kind,
+                          None)
+
+
+def test_extend_argument_errors(lib):
+    """Everything the host can check is checked before the status word is cleared (no device needed)."""
+    assert lib.kvq_extend_workspace_bytes() == 256
+    assert _extend(lib, L(), kind=0) == -2                      # KVQ_EKIND
+    assert _extend(lib, L(), hq=7) == -1                        # not a multiple of the kv heads
+    assert _extend(lib, L(), sm_scale=0.0) == -1                # the softmax scale must be > 0
+    assert _extend(lib, L(), sm_scale=-0.5) == -1
+    assert _extend(lib, L(), sm_scale=float("nan")) == -1
+    assert _extend(lib, L(), total_q=-1) == -1
+    assert _extend(lib, L(), out_dtype=7) == -1
+    assert _extend(lib, L(head_dim=64, v_dim=64)) == -8        # KVQ_EUNSUPPORTED: head_dim 64
+    assert _extend(lib, L(mla=True, num_kv_heads=1, head_dim=576, v_dim=512), hq=16) == -8
+    assert _extend(lib, L(), hq=6) == -8                        # 3 heads per kv head do not divide 128
+    assert _extend(lib, L(page_size=32)) == -8
+    assert _extend(lib, L(), ws_bytes=16) == -5                 # KVQ_EWORKSPACE
+    assert _extend(lib, L(), ws=FAKE + 8) == -4                 # KVQ_EALIGN
+
+
 def test_workspace_bound_covers_every_split_choice(lib):
     lay = L(num_kv_heads=8, head_dim=128, v_dim=128)
     auto = kvq.kvq_decode_workspace_bytes(lay, 8, 16, 1024)
