@@ -9,6 +9,10 @@ C ABI, and the oracle checks samples it can afford one by one.
   query heads of that kv head (a sample of them for the 128-head MLA row); the GPU rows must meet the
   decode bound (max abs <= 1.5e-2, mean abs <= 2e-3).
 
+* Extend: the bench's extend step (the last 2048 stored tokens of each qwen3_1p7b sequence attend causally);
+  for sampled (sequence, new token, kv head) the oracle attends over a compact pool of that sequence's rows
+  of that kv head, cut at the token's position.
+
 Sizes: qwen3_1p7b (batch 8, 1k-16k), long_gqa batch 8 x 262144 and batch 1 x 262144, mla (163840
 tokens, 128 heads), serving (batch 64, lognormal contexts).  The oracle's share is a few million rows,
 so the file runs in a few minutes on the GPU machine's host cores."""
@@ -160,3 +164,35 @@ def test_full_size_sparse_mla_decode_matches_the_oracle(kind):
                               v_dim=case.v_dim, page_size=P, mla=True, kind=case.kind, sm_scale=case.sm_scale,
                               nthreads=0)[0]
         assert_decode_close(got[b], ref)
+
+
+@pytest.mark.parametrize("kind", ["fp8_e4m3", "q8_0"])
+def test_full_size_extend_matches_the_oracle_on_samples(kind):
+    case = workloads.make("qwen3_1p7b", kind=kind, device="cuda")
+    L, codes, scales = gpu_pool(case)
+    gpu_store(case, codes, scales)
+    q, q_start, _ = workloads.extend_inputs(case, 2048)
+    out = torch.empty(q.shape[0], case.num_q_heads, case.v_dim, dtype=torch.float32, device="cuda")
+    ws = kvq.alloc_extend_workspace()
+    kvq.kvq_extend(q, codes, scales, case.block_table, case.seq_lens, q_start, out, ws, L, case.kind, case.sm_scale)
+    torch.cuda.synchronize()
+    assert kvq.kvq_workspace_status(ws) == 0
+    got = out.cpu().numpy().astype(np.float64)
+    qs = q_start.cpu().numpy()
+    lens = case.seq_lens.cpu().numpy()
+    rng = np.random.default_rng(13)
+    G = case.num_q_heads // case.num_kv_heads
+    for b in rng.choice(case.batch, size=3, replace=False):
+        n = int(qs[b + 1] - qs[b])
+        for i in (0, int(rng.integers(n)), n - 1):          # first, a random and the last new token
+            g = int(rng.integers(case.num_kv_heads))
+            heads = list(range(g * G, (g + 1) * G))
+            pos = int(lens[b]) - n + i
+            # the oracle's extend of that one token over the sequence cut at its position, compact pool
+            sub = type(case)(**{**case.__dict__, "seq_lens": case.seq_lens.clone()})
+            sub.seq_lens[b] = pos + 1
+            row = int(qs[b]) + i
+            sub.q = case.q.clone()
+            sub.q[b] = q[row]
+            ref = _oracle_subcase(sub, int(b), g, heads)
+            assert_decode_close(got[row, heads, :], ref)
