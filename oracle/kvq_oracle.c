@@ -14,6 +14,9 @@
  *     clamp to +-127; fp8 codes are clamped to +-448 and rounded to nearest-even in a single
  *     rounding (the one-sided double rounding through fp16 is the bug; kept here only as the
  *     negative control kvo_e4m3_double_round).
+ *   - "Add fp8 KV-cache quantization (--kv-dtype)", section "How it works": the unscaled variant, where
+ *     the store casts bf16 K/V straight to the pool's fp8 type (e4m3 or e5m2, scale 1.0, 1 byte per
+ *     element) and the attention reads the fp8 values back exactly.
  *   - "feat(kvcache): 8-bit DSV4 window/compressed KV", sections "What this adds" (one MLA latent
  *     row per token serves as both K and V, one scale array) and "Testing" (split-K decode,
  *     masked -1 columns, saturation).
@@ -30,6 +33,8 @@
  *   bfloat16:            1 sign, 8 exponent bits (bias 127), 7 fraction bits, subnormal quantum 2^-133.
  *   E4M3 "fn" (OCP 8-bit floating point): 1 sign, 4 exponent bits (bias 7), 3 fraction bits,
  *                        subnormals M * 2^-9, no infinities, 0x7F / 0xFF are NaN, largest finite 448.
+ *   E5M2 (OCP 8-bit floating point): 1 sign, 5 exponent bits (bias 15), 2 fraction bits, subnormals
+ *                        M * 2^-16, exponent 31 is infinity / NaN, largest finite 57344.
  *
  * Arithmetic: every rounding is done explicitly on exact double values.  fp32 steps that the method
  * fixes (amax / Q, x / s) are done in C float, which is IEEE binary32 with round-to-nearest on the
@@ -49,7 +54,14 @@
 #error "the oracle needs float arithmetic evaluated in binary32"
 #endif
 
-enum { KVO_FP8_E4M3 = 1, KVO_Q8_0 = 2 };
+/* Kinds: the block-scaled 8-bit caches, and the unscaled fp8 casts ("Add fp8 KV-cache quantization
+   (--kv-dtype)", section "How it works": the store casts bf16 K/V to the pool's fp8 type, scale 1.0). */
+enum { KVO_FP8_E4M3 = 1, KVO_Q8_0 = 2, KVO_FP8_E4M3_UNSCALED = 3, KVO_FP8_E5M2_UNSCALED = 4 };
+
+static int kind_is_unscaled(int kind)
+{
+    return kind == KVO_FP8_E4M3_UNSCALED || kind == KVO_FP8_E5M2_UNSCALED;
+}
 
 /* ------------------------------------------------------------------------------------------ */
 /* Rounding a non-negative double that is exactly representable to the nearest integer, ties to */
@@ -216,6 +228,52 @@ uint8_t kvo_e4m3_double_round(float y)
 }
 
 /* ------------------------------------------------------------------------------------------ */
+/* E5M2 (OCP 8-bit floating point): 1 sign, 5 exponent bits (bias 15), 2 fraction bits;          */
+/* subnormals M * 2^-16; exponent 31 holds infinity (M = 0) and NaN; largest finite 57344.        */
+/* ------------------------------------------------------------------------------------------ */
+double kvo_e5m2_value(uint8_t c)
+{
+    int sign = (c >> 7) & 1;
+    int E = (c >> 2) & 0x1F;
+    int M = c & 0x3;
+    double v;
+    if (E == 0x1F)
+        v = (M == 0) ? INFINITY : NAN;
+    else if (E == 0)
+        v = ldexp((double)M, -16);
+    else
+        v = ldexp(1.0 + (double)M / 4.0, E - 15);
+    return sign ? -v : v;
+}
+
+/* Nearest-even E5M2 code of a finite value with |y| <= 57344 (callers clamp first). */
+uint8_t kvo_e5m2_rne(double y)
+{
+    uint8_t sign = signbit(y) ? 0x80u : 0u;
+    double a = fabs(y);
+    if (a == 0.0) return sign;
+    int E = floor_log2(a);
+    if (E < -14) E = -14;                /* subnormal binade keeps quantum 2^-16 */
+    double quantum = ldexp(1.0, E - 2);  /* 2 fraction bits */
+    double n = round_half_even(a / quantum);
+    if (n >= 8.0) {
+        E += 1;
+        n = 4.0;
+    }
+    if (n < 4.0) return (uint8_t)(sign | (uint8_t)n); /* subnormal codes 0..3 (E == -14 only) */
+    return (uint8_t)(sign | (uint8_t)((E + 15) << 2) | (uint8_t)(n - 4.0));
+}
+
+/* Clamp to the largest finite value first (a cache holds no infinity), then one nearest-even rounding. */
+uint8_t kvo_e5m2_sat_rne(float y)
+{
+    double d = (double)y;
+    if (d > 57344.0) d = 57344.0;
+    if (d < -57344.0) d = -57344.0;
+    return kvo_e5m2_rne(d);
+}
+
+/* ------------------------------------------------------------------------------------------ */
 /* q8_0 code: round half away from zero (exact), then clamp to [-127, 127].                     */
 /* ------------------------------------------------------------------------------------------ */
 int8_t kvo_q8_rhaz(float y)
@@ -229,7 +287,8 @@ int8_t kvo_q8_rhaz(float y)
 
 double kvo_code_value(int kind, uint8_t c)
 {
-    if (kind == KVO_FP8_E4M3) return kvo_e4m3_value(c);
+    if (kind == KVO_FP8_E4M3 || kind == KVO_FP8_E4M3_UNSCALED) return kvo_e4m3_value(c);
+    if (kind == KVO_FP8_E5M2_UNSCALED) return kvo_e5m2_value(c);
     return (double)(int8_t)c;
 }
 
@@ -314,6 +373,12 @@ double kvo_bytes_per_token(int n_kv, int Hkv, int D)
     return elems + 2.0 * elems / 32.0;
 }
 
+/* Bytes per element of a kind: 17/16 with the block scales, 1 for an unscaled fp8 cast. */
+double kvo_bytes_per_element(int kind)
+{
+    return kind_is_unscaled(kind) ? 1.0 : 17.0 / 16.0;
+}
+
 /*
  * Store: quantize rows k[t][h][:] (and v for GQA) and scatter them to slot slot_mapping[t];
  * slot -1 skips the row and leaves the pool untouched.  Returns 0, or -1 on bad arguments.
@@ -322,7 +387,8 @@ int kvo_store(uint8_t* codes, uint16_t* scales, const uint16_t* k_bits, const ui
               const int64_t* slot_mapping, int64_t T, int Hkv, int D, int P, int mla, int kind,
               int64_t num_pages)
 {
-    if (D % 32 != 0 || (kind != KVO_FP8_E4M3 && kind != KVO_Q8_0)) return -1;
+    if (D % 32 != 0 || kind < KVO_FP8_E4M3 || kind > KVO_FP8_E5M2_UNSCALED) return -1;
+    if (!kind_is_unscaled(kind) && !scales) return -1;
     int n_kv = mla ? 1 : 2;
     int nb = D / 32;
     for (int64_t t = 0; t < T; ++t) {
@@ -336,6 +402,13 @@ int kvo_store(uint8_t* codes, uint16_t* scales, const uint16_t* k_bits, const ui
             for (int h = 0; h < Hkv; ++h) {
                 const uint16_t* row = src + (t * Hkv + h) * (int64_t)D;
                 int64_t r = row_index(page, kv, h, off, n_kv, Hkv, P);
+                if (kind_is_unscaled(kind)) { /* the plain cast: no scale, no block */
+                    for (int d = 0; d < D; ++d) {
+                        float x = bf16_bits_to_float(row[d]);
+                        codes[r * D + d] = (kind == KVO_FP8_E4M3_UNSCALED) ? kvo_e4m3_sat_rne(x) : kvo_e5m2_sat_rne(x);
+                    }
+                    continue;
+                }
                 for (int j = 0; j < nb; ++j)
                     kvo_quantize_block(kind, row + 32 * j, 32, codes + r * D + 32 * j, scales + r * nb + j);
             }
@@ -380,6 +453,7 @@ static double row_elem(int quantized, int kind, const uint8_t* codes, const uint
                        const uint16_t* pool16, int64_t r, int D, int d)
 {
     if (!quantized) return kvo_bf16_value(pool16[r * D + d]);
+    if (kind_is_unscaled(kind)) return kvo_code_value(kind, codes[r * D + d]); /* exact in bf16 */
     int nb = D / 32;
     return kvo_dequant(kind, codes[r * D + d], scales[r * nb + d / 32]);
 }
@@ -619,6 +693,11 @@ void kvo_q8_rhaz_batch(const float* y, int8_t* out, int64_t n)
 {
     for (int64_t i = 0; i < n; ++i) out[i] = kvo_q8_rhaz(y[i]);
 }
+void kvo_e5m2_sat_rne_batch(const float* y, uint8_t* out, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i) out[i] = kvo_e5m2_sat_rne(y[i]);
+}
+
 void kvo_dequant_batch(int kind, const uint8_t* c, const uint16_t* s16, double* out, int64_t n)
 {
     for (int64_t i = 0; i < n; ++i) out[i] = kvo_dequant(kind, c[i], s16[i]);

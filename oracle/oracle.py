@@ -11,7 +11,11 @@ from . import build_oracle
 
 FP8_E4M3 = 1
 Q8_0 = 2
-KIND_BY_NAME = {"fp8_e4m3": FP8_E4M3, "q8_0": Q8_0}
+FP8_E4M3_UNSCALED = 3
+FP8_E5M2_UNSCALED = 4
+KIND_BY_NAME = {"fp8_e4m3": FP8_E4M3, "q8_0": Q8_0, "fp8_e4m3_unscaled": FP8_E4M3_UNSCALED,
+                "fp8_e5m2_unscaled": FP8_E5M2_UNSCALED}
+UNSCALED = (FP8_E4M3_UNSCALED, FP8_E5M2_UNSCALED)
 
 _lib = None
 
@@ -50,6 +54,10 @@ def lib():
             "kvo_e4m3_double_round_batch": (None, [P, P, i64]),
             "kvo_q8_rhaz_batch": (None, [P, P, i64]),
             "kvo_dequant_batch": (None, [i32, P, P, P, i64]),
+            "kvo_e5m2_value": (dbl, [ctypes.c_uint8]),
+            "kvo_e5m2_rne": (ctypes.c_uint8, [dbl]),
+            "kvo_e5m2_sat_rne_batch": (None, [P, P, i64]),
+            "kvo_bytes_per_element": (dbl, [i32]),
             "kvo_has_openmp": (i32, []),
             "kvo_code_of": (ctypes.c_uint8, [i32, ctypes.c_uint16, ctypes.c_uint16]),
             "kvo_code_table": (None, [i32, P, i64, P, i64, P, i32]),
@@ -71,6 +79,11 @@ def _c(a, dtype):
     return a, a.ctypes.data_as(ctypes.c_void_p)
 
 
+def _c_opt(a, dtype):
+    """As _c, or (None, NULL) for None (the scales of an unscaled pool)."""
+    return (None, None) if a is None else _c(a, dtype)
+
+
 # ----------------------------------------------------------------------------- scalar formats
 def f16_value(bits):
     return lib().kvo_f16_value(int(bits))
@@ -89,8 +102,34 @@ def e4m3_rne(y):
     return lib().kvo_e4m3_rne(float(y))
 
 
+def e5m2_value(code):
+    return lib().kvo_e5m2_value(int(code))
+
+
+def e5m2_rne(y):
+    """Nearest-even E5M2 code of a double with |y| <= 57344."""
+    return lib().kvo_e5m2_rne(float(y))
+
+
+def e5m2_sat_rne(y):
+    """Codes of fp32 values clamped to +-57344, then rounded to nearest-even E5M2."""
+    y = np.ascontiguousarray(y, np.float32)
+    out = np.empty(y.shape, np.uint8)
+    lib().kvo_e5m2_sat_rne_batch(y.ctypes.data_as(ctypes.c_void_p), out.ctypes.data_as(ctypes.c_void_p), y.size)
+    return out
+
+
+def bytes_per_element(kind):
+    return lib().kvo_bytes_per_element(_kind(kind))
+
+
 def code_value(kind, code):
-    return e4m3_value(code) if _kind(kind) == FP8_E4M3 else float(np.int8(np.uint8(code)))
+    k = _kind(kind)
+    if k in (FP8_E4M3, FP8_E4M3_UNSCALED):
+        return e4m3_value(code)
+    if k == FP8_E5M2_UNSCALED:
+        return e5m2_value(code)
+    return float(np.int8(np.uint8(code)))
 
 
 # ----------------------------------------------------------------------------- batch maps
@@ -177,9 +216,13 @@ def pool_shapes(num_pages, page_size, num_kv_heads, head_dim, mla):
 
 
 def store(codes, scales, k_bits, v_bits, slot_mapping, *, num_kv_heads, head_dim, page_size, mla, kind):
-    """Quantize-and-scatter into ``codes`` (uint8) / ``scales`` (uint16) in place."""
+    """Quantize-and-scatter into ``codes`` (uint8) / ``scales`` (uint16) in place (the unscaled kinds have no
+    scales: pass None)."""
     assert codes.dtype == np.uint8 and codes.flags.c_contiguous
-    assert scales.dtype == np.uint16 and scales.flags.c_contiguous
+    if scales is None:
+        assert _kind(kind) in UNSCALED, "the block-scaled kinds need a scale array"
+    else:
+        assert scales.dtype == np.uint16 and scales.flags.c_contiguous
     k, pk = _c(k_bits, np.uint16)
     if mla:
         v, pv = None, None
@@ -187,7 +230,8 @@ def store(codes, scales, k_bits, v_bits, slot_mapping, *, num_kv_heads, head_dim
         v, pv = _c(v_bits, np.uint16)
     sm, psm = _c(slot_mapping, np.int64)
     num_pages = codes.shape[0]
-    rc = lib().kvo_store(codes.ctypes.data_as(ctypes.c_void_p), scales.ctypes.data_as(ctypes.c_void_p),
+    rc = lib().kvo_store(codes.ctypes.data_as(ctypes.c_void_p),
+                         None if scales is None else scales.ctypes.data_as(ctypes.c_void_p),
                          pk, pv, psm, sm.size, num_kv_heads, head_dim, page_size, int(bool(mla)),
                          _kind(kind), num_pages)
     if rc != 0:
@@ -209,7 +253,7 @@ def decode(q_bits, codes, scales, block_table, seq_lens, *, num_q_heads, num_kv_
     """fp64 attention over the dequantized pool; returns out[B, Hq, Dv] float64."""
     q, pq = _c(q_bits, np.uint16)
     c, pc = _c(codes, np.uint8)
-    s, ps = _c(scales, np.uint16)
+    s, ps = _c_opt(scales, np.uint16)
     bt, pbt = _c(block_table, np.int32)
     sl, psl = _c(seq_lens, np.int32)
     B = sl.size
@@ -229,7 +273,7 @@ def decode_sparse(q_bits, codes, scales, block_table, seq_lens, indices, *, num_
     position counts once per listing); returns out[B, Hq, Dv] float64 (zeros without a valid column)."""
     q, pq = _c(q_bits, np.uint16)
     c, pc = _c(codes, np.uint8)
-    s, ps = _c(scales, np.uint16)
+    s, ps = _c_opt(scales, np.uint16)
     bt, pbt = _c(block_table, np.int32)
     sl, psl = _c(seq_lens, np.int32)
     ix, pix = _c(indices, np.int32)
@@ -254,7 +298,7 @@ def extend(q_bits, codes, scales, block_table, seq_lens, q_start, *, num_q_heads
     out[total_q, Hq, Dv] float64 (zeros where no position is valid)."""
     q, pq = _c(q_bits, np.uint16)
     c, pc = _c(codes, np.uint8)
-    s, ps = _c(scales, np.uint16)
+    s, ps = _c_opt(scales, np.uint16)
     bt, pbt = _c(block_table, np.int32)
     sl, psl = _c(seq_lens, np.int32)
     qs, pqs = _c(q_start, np.int32)

@@ -368,12 +368,17 @@ def test_store_is_independent_of_row_order():
 def _gather_dequant(codes, scales, kind, slots, kv, h, D):
     """Dequantized rows at the given slots, read by plain indexing of the pool arrays."""
     P = codes.shape[3]
+    unscaled = O.KIND_BY_NAME.get(kind, kind) in O.UNSCALED  # the cast value (no scale), pinned code table
+    table = np.array([O.code_value(kind, c) for c in range(256)]) if unscaled else None
     rows = []
     for s in slots:
         page, off = divmod(int(s), P)
         c = codes[page, kv, h, off]
-        sc = np.repeat(scales[page, kv, h, off], 32)
-        rows.append(O.dequant(kind, c, sc))
+        if unscaled:
+            rows.append(table[c])
+        else:
+            sc = np.repeat(scales[page, kv, h, off], 32)
+            rows.append(O.dequant(kind, c, sc))
     return np.array(rows).reshape(len(slots), D)
 
 
@@ -734,3 +739,58 @@ def test_absolute_value_pool_gives_the_weighted_mean_of_abs_v(kind):
     pos = _decode_setup(kind, seed=3)
     pos["codes"] = abs_value_pool(pos["codes"], kind)
     np.testing.assert_array_equal(_run(dict(pos, codes=abs_value_pool(pos["codes"], kind))), _run(pos))
+
+
+# ===================================================================== unscaled fp8 (e4m3 / e5m2 casts)
+def test_e5m2_value_of_every_code_matches_torch():
+    """The E5M2 decoding written from the format's definition against torch's float8_e5m2 (library routine)."""
+    codes = np.arange(256, dtype=np.uint8)
+    ref = torch.from_numpy(codes).view(torch.float8_e5m2).to(torch.float64).numpy()
+    got = np.array([O.e5m2_value(c) for c in codes])
+    np.testing.assert_array_equal(got, ref)
+    assert O.e5m2_value(0x3C) == 1.0 and O.e5m2_value(0x7B) == 57344.0 and O.e5m2_value(0x01) == 2.0 ** -16
+
+
+def test_e5m2_nearest_even_matches_torch_cast_on_every_bf16_in_range():
+    """Every finite bf16 value with |x| <= 57344: one nearest-even rounding, as torch's float8_e5m2 cast; beyond
+    the largest finite value the cache's cast saturates instead of producing infinity."""
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    x = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16)
+    xf = x.float().numpy()
+    ok = np.isfinite(xf) & (np.abs(xf) <= 57344.0)
+    got = O.e5m2_sat_rne(xf[ok])
+    ref = x[torch.from_numpy(ok)].to(torch.float8_e5m2).view(torch.uint8).numpy()
+    assert np.array_equal(got, ref), int((got != ref).sum())
+    big = xf[np.isfinite(xf) & (np.abs(xf) > 57344.0)]
+    sat = O.e5m2_sat_rne(big)
+    assert np.all(sat == np.where(big > 0, 0x7B, 0xFB))
+
+
+def test_unscaled_store_is_the_plain_cast_and_costs_one_byte_per_element():
+    """The unscaled kinds cast each bf16 value to fp8 with no scale (1 byte per element, twice the bf16
+    token budget: the pages' 27,142 -> 54,284 tokens at equal bytes)."""
+    g = GOLDEN["unscaled_fp8_kv_budget_tokens"]
+    for kind in ("fp8_e4m3_unscaled", "fp8_e5m2_unscaled"):
+        assert O.bytes_per_element(kind) == 1.0
+        assert round(GOLDEN["bytes_per_element_bf16"]["value"] / O.bytes_per_element(kind), 2) == g["ratio"]
+        assert abs(g["fp8_e4m3"] / g["bf16"] - 2.0) < 1e-3
+        s = _decode_setup(kind, mask=[(1, 1)])
+        P = s["P"]
+        for t, slot in enumerate(s["slots"]):
+            if slot < 0:
+                continue
+            page, off = divmod(int(slot), P)
+            for kv, src in ((0, s["k"]), (1, s["v"])):
+                xf = bf16_to_f32(src[t]).reshape(-1)
+                want = (O.e4m3_sat_rne(xf) if kind == "fp8_e4m3_unscaled" else O.e5m2_sat_rne(xf))
+                assert np.array_equal(s["codes"][page, kv, :, off].reshape(-1), want)
+
+
+@pytest.mark.parametrize("kind", ["fp8_e4m3_unscaled", "fp8_e5m2_unscaled"])
+def test_unscaled_decode_and_extend_match_scipy_over_the_cast_values(kind):
+    s = _decode_setup(kind, mask=[(1, 2)])
+    for sm_scale in (1.0, 0.37):
+        np.testing.assert_allclose(_run(s, sm_scale), _expected_scipy(s, sm_scale), rtol=1e-12, atol=1e-13)
+    q, q_start = _extend_q(s, [37, 21])
+    np.testing.assert_allclose(_run_extend(s, q, q_start), _expected_extend_scipy(s, q, q_start, 1.0),
+                               rtol=1e-12, atol=1e-13)
