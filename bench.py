@@ -382,31 +382,38 @@ def run_e2e(args, case, L, codes, scales, sk, sv, ss, ix, decode, flush, world):
     return {"step_s": tot / K / 1e3, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
 
 
-def csrc_sha256():
-    """sha256 over the library's CUDA sources, in the order the traffic record was hashed."""
+# The sources the decode call is built from (host planning, kernels, shared device code): the traffic record
+# stays valid while these are unchanged, whatever else changes in the library.
+DECODE_SOURCES = ("kvq_api.cu", "kvq_decode.cu", "kvq_decode_mla.cu", "kvq_decode_tc.cu", "kvq_device.cuh",
+                  "kvq_internal.h", "kvq_plan.cuh", "kvq_tc.cuh")
+
+
+def sources_sha256(files):
+    """sha256 over the named library sources, each preceded by its name, in the given order."""
     h = hashlib.sha256()
     d = os.path.join(os.path.dirname(os.path.abspath(__file__)), "block_quantized_bit_gb300", "csrc")
-    for f in sorted(os.listdir(d)):
-        if f.endswith((".cu", ".cuh", ".h")):
-            h.update(f.encode())
-            with open(os.path.join(d, f), "rb") as fh:
-                h.update(fh.read())
+    for f in files:
+        h.update(f.encode())
+        with open(os.path.join(d, f), "rb") as fh:
+            h.update(fh.read())
     return h.hexdigest()
 
 
 def recorded_traffic(args):
     """DRAM bytes per decode call (split kernel + merge) from the committed ncu record, or None when
-    there is no record for this workload or the library source changed since it was taken."""
+    there is no record for this workload or the sources it names changed since it was taken."""
     path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "profiles", "dram_traffic.json")
     try:
         with open(path) as fh:
             rec = json.load(fh)
     except (OSError, ValueError):
         return None
-    sha = csrc_sha256()
     for e in rec.get("entries", []):
+        files = e.get("sources")
+        if not files or e.get("sources_sha256") != sources_sha256(files):
+            continue
         if (e.get("workload") == args.workload and e.get("kind") == args.kind and e.get("path", 0) == args.path
-                and e.get("csrc_sha256") == sha and args.batch is None and args.ctx is None):
+                and args.batch is None and args.ctx is None):
             return int(e["dram_read_bytes"]) + int(e["dram_write_bytes"])
     return None
 
