@@ -671,6 +671,54 @@ int kvo_extend(double* out, const uint16_t* q_bits, const uint8_t* codes, const 
 }
 
 /* ------------------------------------------------------------------------------------------ */
+/* The store fused with its producer ("feat(kvcache): 8-bit DSV4 window/compressed KV", section  */
+/* "Why the precision cost is small": the model rounds the latent part of each MLA row (all but  */
+/* the last rope_dim elements) onto the E4M3 grid with one scale per 64 elements immediately     */
+/* before every store; the rope tail stays bf16).  The pages do not print that rounding's scale  */
+/* format; the reading here is an fp32 scale s = amax / 448 (IEEE division), the code            */
+/* E4M3_sat_RNE(x / s) (IEEE division) and the value code * s in fp32, written back as bf16      */
+/* (RNE); an all-zero block stays zero.  The fused store is that rounding followed by kvo_store. */
+/* ------------------------------------------------------------------------------------------ */
+void kvo_act_quant64(const uint16_t* x_bits, int64_t n, uint16_t* out_bits)
+{
+    for (int64_t b0 = 0; b0 < n; b0 += 64) {
+        int64_t len = (n - b0 < 64) ? n - b0 : 64;
+        float amax = 0.0f;
+        for (int64_t i = 0; i < len; ++i) {
+            float a = fabsf(bf16_bits_to_float(x_bits[b0 + i]));
+            if (a > amax) amax = a;
+        }
+        if (amax == 0.0f) {
+            for (int64_t i = 0; i < len; ++i) out_bits[b0 + i] = x_bits[b0 + i]; /* zeros keep their sign */
+            continue;
+        }
+        float s = amax / kvo_qmax_fp8; /* IEEE binary32 */
+        for (int64_t i = 0; i < len; ++i) {
+            float y = bf16_bits_to_float(x_bits[b0 + i]) / s;
+            float v = (float)kvo_e4m3_value(kvo_e4m3_sat_rne(y)) * s; /* exact code value, fp32 product */
+            out_bits[b0 + i] = kvo_bf16_rne((double)v);
+        }
+    }
+}
+
+/* The fused MLA store: each row's first D - rope_dim elements through kvo_act_quant64, the rope tail */
+/* as is, then the block-scaled store.  Returns kvo_store's status, or -1 on bad arguments.           */
+int kvo_store_act_quant(uint8_t* codes, uint16_t* scales, const uint16_t* k_bits, const int64_t* slot_mapping,
+                        int64_t T, int D, int rope_dim, int P, int kind, int64_t num_pages)
+{
+    if (rope_dim < 0 || rope_dim > D || (D - rope_dim) % 64 != 0) return -1;
+    uint16_t* rows = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)(T > 0 ? T * D : 1));
+    if (!rows) return -1;
+    for (int64_t t = 0; t < T; ++t) {
+        kvo_act_quant64(k_bits + t * D, D - rope_dim, rows + t * D);
+        memcpy(rows + t * D + (D - rope_dim), k_bits + t * D + (D - rope_dim), sizeof(uint16_t) * (size_t)rope_dim);
+    }
+    int rc = kvo_store(codes, scales, rows, NULL, slot_mapping, T, 1, D, P, 1, kind, num_pages);
+    free(rows);
+    return rc;
+}
+
+/* ------------------------------------------------------------------------------------------ */
 /* Batch helpers for the pins (elementwise maps over arrays).                                   */
 /* ------------------------------------------------------------------------------------------ */
 void kvo_f16_rne_f32_batch(const float* x, uint16_t* out, int64_t n)

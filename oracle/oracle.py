@@ -58,6 +58,8 @@ def lib():
             "kvo_e5m2_rne": (ctypes.c_uint8, [dbl]),
             "kvo_e5m2_sat_rne_batch": (None, [P, P, i64]),
             "kvo_bytes_per_element": (dbl, [i32]),
+            "kvo_act_quant64": (None, [P, i64, P]),
+            "kvo_store_act_quant": (i32, [P, P, P, P, i64, i32, i32, i32, i32, i64]),
             "kvo_has_openmp": (i32, []),
             "kvo_code_of": (ctypes.c_uint8, [i32, ctypes.c_uint16, ctypes.c_uint16]),
             "kvo_code_table": (None, [i32, P, i64, P, i64, P, i32]),
@@ -246,6 +248,30 @@ def scatter_bf16(pool16, k_bits, v_bits, slot_mapping, *, num_kv_heads, head_dim
                                 head_dim, page_size, int(bool(mla)), pool16.shape[0])
     if rc != 0:
         raise ValueError("oracle scatter rejected its arguments")
+
+
+def act_quant64(x_bits):
+    """The model's rounding of an MLA latent onto the E4M3 grid, one fp32 scale (amax / 448) per 64 elements
+    along the last axis; returns bf16 bit patterns of the same shape."""
+    x, px = _c(x_bits, np.uint16)
+    assert x.shape[-1] % 64 == 0
+    out = np.empty_like(x)
+    rows = x.reshape(-1, x.shape[-1])
+    o = out.reshape(-1, x.shape[-1])
+    for i in range(rows.shape[0]):  # blocks never straddle rows
+        r = np.ascontiguousarray(rows[i])
+        lib().kvo_act_quant64(r.ctypes.data_as(ctypes.c_void_p), r.size, o[i].ctypes.data_as(ctypes.c_void_p))
+    return out
+
+
+def store_act_quant(codes, scales, k_bits, slot_mapping, *, head_dim, rope_dim, page_size, kind):
+    """The MLA store fused with its producer: act_quant64 over each row's latent part, then the store."""
+    k, pk = _c(k_bits, np.uint16)
+    sm, psm = _c(slot_mapping, np.int64)
+    rc = lib().kvo_store_act_quant(codes.ctypes.data_as(ctypes.c_void_p), scales.ctypes.data_as(ctypes.c_void_p), pk,
+                                   psm, sm.size, head_dim, rope_dim, page_size, _kind(kind), codes.shape[0])
+    if rc != 0:
+        raise ValueError("oracle fused store rejected its arguments")
 
 
 def decode(q_bits, codes, scales, block_table, seq_lens, *, num_q_heads, num_kv_heads, head_dim, v_dim,

@@ -794,3 +794,44 @@ def test_unscaled_decode_and_extend_match_scipy_over_the_cast_values(kind):
     q, q_start = _extend_q(s, [37, 21])
     np.testing.assert_allclose(_run_extend(s, q, q_start), _expected_extend_scipy(s, q, q_start, 1.0),
                                rtol=1e-12, atol=1e-13)
+
+
+# ===================================================================== the store fused with its producer
+def test_act_quant64_matches_torch_float8_rounding():
+    """One fp32 scale (amax / 448) per 64 elements, torch's float8_e4m3fn cast of x / s, times s in fp32, to
+    bf16: the same numbers through a library routine (the mla workload generator does the same)."""
+    g = torch.Generator().manual_seed(5)
+    x = torch.randn(32, 512, generator=g) * torch.exp(torch.randn(32, 8, 1, generator=g)).repeat(1, 1, 64).reshape(32, 512)
+    x[3, 64:128] = 0.0                                   # an all-zero block stays zero
+    x[4, 0] = 3.0e38                                     # a huge block: its scale is still finite
+    xb = x.to(torch.bfloat16)
+    blocks = xb.float().reshape(32, 8, 64)
+    s = blocks.abs().amax(-1, keepdim=True) / 448.0
+    s = torch.where(s > 0, s, torch.ones_like(s))
+    ref = ((blocks / s).to(torch.float8_e4m3fn).float() * s).reshape(32, 512).to(torch.bfloat16)
+    got = O.act_quant64(xb.view(torch.int16).numpy().view(np.uint16))
+    assert np.array_equal(got, ref.view(torch.int16).numpy().view(np.uint16))
+
+
+def test_fused_mla_store_rounds_the_latent_and_keeps_the_rope_tail():
+    """The fused store's codes: latent = the store of the act_quant64 rows; rope tail = the plain store of the
+    same bf16 values (those dims are rounded for the first time by the store itself)."""
+    g = torch.Generator().manual_seed(6)
+    T, D, rope, P = 40, 576, 64, 16
+    k = (torch.randn(T, 1, D, generator=g) * 2).to(torch.bfloat16)
+    kb = k.view(torch.int16).numpy().view(np.uint16)
+    slots = np.arange(T, dtype=np.int64)
+    cs, ss = O.pool_shapes(3, P, 1, D, True)
+    fused_c, fused_s = np.zeros(cs, np.uint8), np.zeros(ss, np.uint16)
+    O.store_act_quant(fused_c, fused_s, kb.reshape(T, D), slots, head_dim=D, rope_dim=rope, page_size=P, kind=FP8)
+    lat = O.act_quant64(kb[:, 0, :D - rope])
+    pre = np.concatenate([lat, kb[:, 0, D - rope:]], axis=1)[:, None, :]
+    plain_c, plain_s = np.zeros(cs, np.uint8), np.zeros(ss, np.uint16)
+    O.store(plain_c, plain_s, pre, None, slots, num_kv_heads=1, head_dim=D, page_size=P, mla=True, kind=FP8)
+    assert np.array_equal(fused_c, plain_c) and np.array_equal(fused_s, plain_s)
+    raw_c, raw_s = np.zeros(cs, np.uint8), np.zeros(ss, np.uint16)
+    O.store(raw_c, raw_s, kb, None, slots, num_kv_heads=1, head_dim=D, page_size=P, mla=True, kind=FP8)
+    assert np.array_equal(fused_c[..., D - rope:], raw_c[..., D - rope:])      # rope tail untouched by act_quant
+    assert not np.array_equal(fused_c[..., :D - rope], raw_c[..., :D - rope])  # the latent is not
+    with pytest.raises(ValueError):
+        O.store_act_quant(fused_c, fused_s, kb.reshape(T, D), slots, head_dim=D, rope_dim=32, page_size=P, kind=FP8)
