@@ -146,6 +146,37 @@ def test_extend_argument_errors(lib):
     assert _extend(lib, L(), ws=FAKE + 8) == -4                 # KVQ_EALIGN
 
 
+def _sparse(lib, layout, *, topk=256, hq=8, kind=1, out_dtype=0, ws=FAKE, ws_bytes=None, ix=FAKE, batch=2):
+    P = ctypes.c_void_p
+    if ws_bytes is None:
+        ws_bytes = lib.kvq_decode_sparse_workspace_bytes(ctypes.byref(layout.c()), batch, hq, topk)
+    return lib.kvq_decode_sparse(P(FAKE), P(FAKE), P(FAKE), P(FAKE), 10, P(FAKE), P(ix), topk, batch, hq,
+                                 ctypes.c_float(1.0), P(FAKE), out_dtype, P(ws), ws_bytes, ctypes.byref(layout.c()),
+                                 kind, None)
+
+
+def test_sparse_decode_argument_errors(lib):
+    """Checked on the host before any device call (no GPU needed)."""
+    lay = L()
+    assert lib.kvq_decode_sparse_workspace_bytes(ctypes.byref(lay.c()), 2, 8, 256) > 0
+    assert lib.kvq_decode_sparse_workspace_bytes(ctypes.byref(lay.c()), 2, 8, 8193) == 0   # above the 8192 cap
+    assert lib.kvq_decode_sparse_workspace_bytes(ctypes.byref(lay.c()), 2, 8, -1) == 0
+    assert _sparse(lib, lay, kind=9) == -2                      # KVQ_EKIND
+    assert _sparse(lib, lay, out_dtype=4) == -1
+    assert _sparse(lib, lay, topk=8193, ws_bytes=1 << 30) == -1
+    assert _sparse(lib, lay, hq=7, ws_bytes=1 << 30) == -1      # not a multiple of the kv heads
+    assert _sparse(lib, L(head_dim=96, v_dim=96), ws_bytes=1 << 30) == -8   # head_dim not a multiple of 64
+    assert _sparse(lib, lay, ws_bytes=64) == -5                 # KVQ_EWORKSPACE
+    assert _sparse(lib, lay, ws=FAKE + 8) == -4                 # KVQ_EALIGN
+    assert _sparse(lib, lay, ix=FAKE + 2) == -4
+    assert _sparse(lib, lay, batch=0) == 0
+
+
+def test_wait_probe_argument_errors(lib):
+    assert lib.kvq_wait_probe(None, None) == -1                 # no workspace
+    assert lib.kvq_wait_probe(ctypes.c_void_p(FAKE + 4), None) == -4
+
+
 def test_workspace_bound_covers_every_split_choice(lib):
     lay = L(num_kv_heads=8, head_dim=128, v_dim=128)
     auto = kvq.kvq_decode_workspace_bytes(lay, 8, 16, 1024)
