@@ -203,3 +203,21 @@ def test_strerror_has_a_message_for_every_status(lib):
     for code, name in kvq.STATUS.items():
         msg = kvq.strerror(code)
         assert msg and msg != "unknown status", name
+
+
+def test_the_product_path_has_no_fallback(monkeypatch):
+    """Without the built library every call raises: there is no CPU path to fall back on.  And the product
+    package never imports the oracle."""
+    monkeypatch.setattr(kvq, "LIB_PATH", os.path.join(os.path.dirname(build_lib.LIB), "missing", "libkvq.so"))
+    monkeypatch.setattr(kvq, "_lib", None)
+    with pytest.raises(RuntimeError, match="not built"):
+        kvq.lib()
+    with pytest.raises(RuntimeError, match="not built"):
+        kvq.alloc_extend_workspace("cpu")
+    pkg = os.path.dirname(kvq.__file__)
+    for root, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(root, f), encoding="utf-8").read()
+                assert not re.search(r"^\s*(import|from)\s+oracle\b", text, re.M), f
+                assert "kvq_oracle" not in text, f
