@@ -189,7 +189,8 @@ kvq_status kvq_decode_sparse(const void* q, const void* pool, const void* scales
  *                new tokens are the last n_b, so new token i sits at position seq_lens[b] - n_b + i
  *   out          [total_q, num_q_heads, v_dim], bf16 or f32 (out_dtype), device
  *   workspace    at least kvq_extend_workspace_bytes() (its status word), 16-byte aligned, device
- * Other arguments as kvq_decode.  Query row (b, i, h) gets softmax(sm_scale * q.K^T) V over the positions
+ * sm_scale must be finite and > 0 (else KVQ_EINVAL).  Other arguments as kvq_decode.
+ * Query row (b, i, h) gets softmax(sm_scale * q.K^T) V over the positions
  * 0 .. seq_lens[b] - n_b + i of sequence b whose pages are not masked (causal), with K and V dequantized to
  * bf16 and fp32 accumulation; no valid position gives zeros.  Runs on the tensor cores (tcgen05).
  * Supported: page_size 16, head_dim = v_dim in {128, 256}, not MLA, query heads per kv head dividing
