@@ -255,3 +255,130 @@ kvq_status launch_quantize_probe(kvq_kind kind, const uint16_t* x, int64_t nx, c
 }
 
 }  // namespace kvq
+
+// ------------------------------------------------------------------------ the store fused with act_quant
+// "feat(kvcache): 8-bit DSV4 window/compressed KV", section "Why the precision cost is small": the model
+// rounds each MLA latent row onto the E4M3 grid with one scale per 64 elements immediately before every
+// store (the rope tail stays bf16).  Fused here: one thread takes one 64-element unit of a row, rounds it
+// in registers when it belongs to the latent (fp32 scale amax / 448, code = E4M3 of x / s by IEEE
+// division, value = code * s in fp32, rounded to bf16; an all-zero unit stays as it is), and stores the
+// unit's two 32-element blocks exactly as the plain store does.  One pass over the bf16 rows instead of a
+// rounding pass that reads and writes them and then the store.
+namespace kvq {
+namespace {
+
+struct ActQuantStoreArgs {
+  uint8_t* codes;
+  __half* scales;
+  const uint4* kv;             // bf16 rows [T][D]
+  const int64_t* slot_mapping;
+  int64_t num_tokens;
+  int32_t D, latent, P;        // latent = D - rope_dim: the rounded part (a multiple of 64)
+  int64_t num_slots;
+};
+
+template <int KIND>
+__global__ void __launch_bounds__(256) act_quant_store_kernel(ActQuantStoreArgs a) {
+  const int32_t units = a.D / 64;
+  const int64_t n = a.num_tokens * units;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t u = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; u < n; u += stride) {
+    const int64_t t = u / units;
+    const int32_t c = static_cast<int32_t>(u - t * units);
+    const int64_t slot = __ldg(a.slot_mapping + t);
+    if (slot < 0 || slot >= a.num_slots) continue;  // -1 skips; out-of-range slots are never written
+    float f[64];
+    const uint4* src = a.kv + (t * a.D + c * 64) / 8;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const uint4 x = __ldcs(src + i);
+      const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        f[8 * i + 2 * e] = __uint_as_float(w[e] << 16);
+        f[8 * i + 2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u);
+      }
+    }
+    if (c * 64 < a.latent) {
+      float amax = 0.0f;
+#pragma unroll
+      for (int i = 0; i < 64; ++i) amax = fmaxf(amax, fabsf(f[i]));
+      if (amax != 0.0f) {
+        const float s = __fdiv_rn(amax, kFp8Max);
+#pragma unroll
+        for (int i = 0; i < 64; i += 2) {
+          const uint16_t pair = encode_fp8x2(__fdiv_rn(f[i], s), __fdiv_rn(f[i + 1], s));
+          const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(pair), __NV_E4M3);
+          f[i] = __bfloat162float(__float2bfloat16_rn(__fmul_rn(__half2float(__ushort_as_half(h.x)), s)));
+          f[i + 1] = __bfloat162float(__float2bfloat16_rn(__fmul_rn(__half2float(__ushort_as_half(h.y)), s)));
+        }
+      }
+    }
+    const int64_t page = slot / a.P, off = slot - (slot / a.P) * a.P;
+    const int64_t dst_row = page * a.P + off;  // one latent row per token: n_kv = 1, one kv head
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      const float* g = f + 32 * half;
+      float amax = 0.0f;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(g[i]));
+      const __half s16 = block_scale<KIND>(amax);
+      const float sf = __half2float(s16);
+      uint32_t o[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+      if (sf != 0.0f) {
+        const float r = __frcp_rn(sf);
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          o[q] = encode4<KIND>(quotient(g[4 * q], sf, r), quotient(g[4 * q + 1], sf, r), quotient(g[4 * q + 2], sf, r),
+                               quotient(g[4 * q + 3], sf, r));
+      }
+      const int32_t j = 2 * c + half;  // 32-element block of the row
+      uint4* dst = reinterpret_cast<uint4*>(a.codes + dst_row * a.D + static_cast<int64_t>(j) * 32);
+      __stcs(dst, make_uint4(o[0], o[1], o[2], o[3]));
+      __stcs(dst + 1, make_uint4(o[4], o[5], o[6], o[7]));
+      a.scales[dst_row * (a.D / 32) + j] = (sf != 0.0f) ? s16 : __ushort_as_half(0);
+    }
+  }
+}
+
+}  // namespace
+}  // namespace kvq
+
+extern "C" kvq_status kvq_store_act_quant(void* pool, void* scales, const void* kv, const int64_t* slot_mapping,
+                                          int64_t num_tokens, int32_t rope_dim, const kvq_layout* layout,
+                                          kvq_kind kind, void* stream) {
+  using namespace kvq;
+  if (!layout) return KVQ_EINVAL;
+  if (kind != KVQ_FP8_E4M3 && kind != KVQ_Q8_0) return KVQ_EKIND;
+  if (!layout->mla || layout->num_kv_heads != 1 || layout->num_pages < 0 || layout->page_size <= 0)
+    return KVQ_EINVAL;
+  if (layout->head_dim <= 0 || layout->head_dim % 64 != 0 || rope_dim < 0 || rope_dim % 64 != 0 ||
+      rope_dim > layout->head_dim)
+    return KVQ_EUNSUPPORTED;
+  if (num_tokens < 0) return KVQ_EINVAL;
+  if (num_tokens == 0) return KVQ_OK;
+  if (!pool || !scales || !kv || !slot_mapping) return KVQ_EINVAL;
+  if ((reinterpret_cast<uintptr_t>(pool) | reinterpret_cast<uintptr_t>(scales) | reinterpret_cast<uintptr_t>(kv)) % 16 ||
+      reinterpret_cast<uintptr_t>(slot_mapping) % 8)
+    return KVQ_EALIGN;
+  const kvq_status st = kvq_device_check();
+  if (st != KVQ_OK) return st;
+  ActQuantStoreArgs a;
+  a.codes = static_cast<uint8_t*>(pool);
+  a.scales = static_cast<__half*>(scales);
+  a.kv = static_cast<const uint4*>(kv);
+  a.slot_mapping = slot_mapping;
+  a.num_tokens = num_tokens;
+  a.D = layout->head_dim;
+  a.latent = layout->head_dim - rope_dim;
+  a.P = layout->page_size;
+  a.num_slots = static_cast<int64_t>(layout->num_pages) * layout->page_size;
+  const int64_t units = num_tokens * (layout->head_dim / 64);
+  const int64_t grid = std::max<int64_t>(1, std::min<int64_t>((units + 255) / 256, static_cast<int64_t>(sm_count()) * 8));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (kind == KVQ_FP8_E4M3)
+    act_quant_store_kernel<KVQ_FP8_E4M3><<<static_cast<unsigned>(grid), 256, 0, s>>>(a);
+  else
+    act_quant_store_kernel<KVQ_Q8_0><<<static_cast<unsigned>(grid), 256, 0, s>>>(a);
+  return cudaGetLastError() == cudaSuccess ? KVQ_OK : KVQ_ECUDA;
+}

@@ -31,7 +31,7 @@ EXPORTS = ["kvq_pool_bytes", "kvq_scale_bytes", "kvq_bytes_per_token", "kvq_num_
            "kvq_decode_sparse_workspace_bytes", "kvq_decode_sparse", "kvq_decode", "kvq_decode_ex",
            "kvq_workspace_status", "kvq_encode_probe", "kvq_quantize_probe", "kvq_dequant_probe", "kvq_strerror",
            "kvq_device_check", "kvq_version", "kvq_decode_noalloc", "kvq_wait_probe", "kvq_extend_workspace_bytes",
-           "kvq_extend"]
+           "kvq_extend", "kvq_store_act_quant"]
 
 
 class kvq_layout(ctypes.Structure):
@@ -76,6 +76,7 @@ def lib():
                                         i32, P]),
             "kvq_decode": (i32, [P, P, P, P, i32, P, i32, i32, ctypes.c_float, P, i32, P, sz, LP, i32, P]),
             "kvq_extend_workspace_bytes": (sz, []),
+            "kvq_store_act_quant": (i32, [P, P, P, P, i64, i32, LP, i32, P]),
             "kvq_extend": (i32, [P, P, P, P, i32, P, P, i32, i32, i32, ctypes.c_float, P, i32, P, sz, LP, i32, P]),
             "kvq_decode_ex": (i32, [P, P, P, P, i32, P, i32, i32, ctypes.c_float, P, i32, P, sz, LP, i32, OP, P]),
             "kvq_workspace_status": (i32, [P, P]),
@@ -262,6 +263,14 @@ def kvq_decode_sparse(q: torch.Tensor, pool: torch.Tensor, scales: torch.Tensor,
                                    _ptr(out), od, _ptr(workspace), int(workspace.numel() * workspace.element_size()),
                                    ctypes.byref(layout.c()),
                                    _kind(kind), _stream(stream)), "kvq_decode_sparse")
+
+
+def kvq_store_act_quant(pool: torch.Tensor, scales: torch.Tensor, kv: torch.Tensor, slot_mapping: torch.Tensor,
+                        layout: Layout, kind, rope_dim: int = 64, stream=None):
+    """The MLA store fused with the model's per-64 E4M3 rounding of the latent: kv is bf16 [T, head_dim]."""
+    _check(lib().kvq_store_act_quant(_ptr(pool), _ptr(scales), _ptr(kv), _ptr(slot_mapping), int(kv.shape[0]),
+                                     int(rope_dim), ctypes.byref(layout.c()), _kind(kind), _stream(stream)),
+           "kvq_store_act_quant")
 
 
 def alloc_extend_workspace(device="cuda"):

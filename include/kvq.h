@@ -178,6 +178,23 @@ kvq_status kvq_decode_sparse(const void* q, const void* pool, const void* scales
                              const kvq_layout* layout, kvq_kind kind, void* stream);
 
 /*
+ * The MLA store fused with its producer ("feat(kvcache): 8-bit DSV4 window/compressed KV", section "Why the
+ * precision cost is small": the model rounds each latent row onto the E4M3 grid with one scale per 64
+ * elements right before every store; the rope tail stays bf16).  kv holds bf16 rows [num_tokens, head_dim]
+ * as they leave the producer.  Each row's first head_dim - rope_dim elements are rounded per 64:
+ *   s = fp32(amax / 448);  value = bf16_RNE(E4M3_sat_RNE(x / s) * s)   (IEEE fp32 division and product;
+ *   an all-zero unit stays as it is).
+ * The row, so rounded, is then stored exactly as kvq_store stores it, in one pass.  Requirements:
+ *   - layout->mla = 1 with one kv head;
+ *   - head_dim and rope_dim multiples of 64, with rope_dim <= head_dim (else KVQ_EUNSUPPORTED);
+ *   - 16-byte aligned pool, scales and kv, and an 8-byte aligned slot_mapping.
+ * Slots of -1 are skipped.  Asynchronous on `stream`.
+ */
+kvq_status kvq_store_act_quant(void* pool, void* scales, const void* kv, const int64_t* slot_mapping,
+                               int64_t num_tokens, int32_t rope_dim, const kvq_layout* layout, kvq_kind kind,
+                               void* stream);
+
+/*
  * Extend (prefill) attention ("feat(kvcache): 8-bit KV cache (q8_0 / fp8_e4m3) behind --kv-cache-dtype",
  * section "What": the dequant sits inside every attention kernel, prefill included; "feat(kvcache): 8-bit
  * DSV4 window/compressed KV", section "Testing": quantized attention on the prefill kernel).  Store the

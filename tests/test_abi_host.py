@@ -221,3 +221,19 @@ def test_the_product_path_has_no_fallback(monkeypatch):
                 text = open(os.path.join(root, f), encoding="utf-8").read()
                 assert not re.search(r"^\s*(import|from)\s+oracle\b", text, re.M), f
                 assert "kvq_oracle" not in text, f
+
+
+def test_fused_store_argument_errors(lib):
+    P = ctypes.c_void_p
+    mla = L(num_kv_heads=1, head_dim=576, v_dim=512, mla=True)
+
+    def call(layout=mla, kind=1, rope=64, kv=FAKE, n=4):
+        return lib.kvq_store_act_quant(P(FAKE), P(FAKE), P(kv), P(FAKE), n, rope, ctypes.byref(layout.c()), kind, None)
+
+    assert call(kind=5) == -2                                   # KVQ_EKIND
+    assert call(layout=L()) == -1                               # a GQA pool: not this store
+    assert call(rope=32) == -8                                  # rope_dim not a multiple of 64
+    assert call(layout=L(num_kv_heads=1, head_dim=544, v_dim=512, mla=True)) == -8
+    assert call(n=-1) == -1
+    assert call(n=0) == 0
+    assert call(kv=FAKE + 8) == -4                              # KVQ_EALIGN
