@@ -382,3 +382,93 @@ extern "C" kvq_status kvq_store_act_quant(void* pool, void* scales, const void* 
     act_quant_store_kernel<KVQ_Q8_0><<<static_cast<unsigned>(grid), 256, 0, s>>>(a);
   return cudaGetLastError() == cudaSuccess ? KVQ_OK : KVQ_ECUDA;
 }
+
+// ------------------------------------------------------------------------ store into an unscaled fp8 pool
+// "Add fp8 KV-cache quantization (--kv-dtype)", section "How it works": the store casts the incoming bf16
+// K/V straight to the pool's fp8 type (scale 1.0; e4m3, or e5m2 wired the same way).  One thread casts 16
+// consecutive elements of a row (two 16-byte loads, one 16-byte store); the conversion rounds once to
+// nearest-even and saturates at the largest finite value.
+namespace kvq {
+namespace {
+
+struct UnscaledStoreArgs {
+  uint8_t* codes;
+  const uint4* k;
+  const uint4* v;
+  const int64_t* slot_mapping;
+  int64_t num_tokens;
+  int32_t Hkv, D, n_kv, P;
+  int64_t num_slots;
+};
+
+template <int FMT>  // __NV_E4M3 or __NV_E5M2
+__global__ void __launch_bounds__(256) unscaled_store_kernel(UnscaledStoreArgs a) {
+  const int32_t chunks = a.D / 16;                            // 16-element pieces of a head row
+  const int64_t per_kv = a.num_tokens * a.Hkv * chunks;
+  const int64_t n = per_kv * a.n_kv;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t u = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; u < n; u += stride) {
+    const int kv = u >= per_kv;
+    const int64_t local = u - (kv ? per_kv : 0);              // (token, head, chunk) of K or of V
+    const int64_t t = local / (static_cast<int64_t>(a.Hkv) * chunks);
+    const int32_t rem = static_cast<int32_t>(local - t * a.Hkv * chunks);
+    const int32_t h = rem / chunks, c = rem - h * chunks;
+    const int64_t slot = __ldg(a.slot_mapping + t);
+    if (slot < 0 || slot >= a.num_slots) continue;            // -1 skips; out-of-range slots are never written
+    const uint4* src = (kv ? a.v : a.k) + local * 2;          // 16 bf16 = two 16-byte pieces
+    const uint4 x0 = __ldcs(src), x1 = __ldcs(src + 1);
+    const uint32_t w[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float2 lo = make_float2(__uint_as_float(w[2 * q] << 16), __uint_as_float(w[2 * q] & 0xFFFF0000u));
+      const float2 hi = make_float2(__uint_as_float(w[2 * q + 1] << 16), __uint_as_float(w[2 * q + 1] & 0xFFFF0000u));
+      const uint32_t a2 = __nv_cvt_float2_to_fp8x2(lo, __NV_SATFINITE, static_cast<__nv_fp8_interpretation_t>(FMT));
+      const uint32_t b2 = __nv_cvt_float2_to_fp8x2(hi, __NV_SATFINITE, static_cast<__nv_fp8_interpretation_t>(FMT));
+      o[q] = (a2 & 0xFFFFu) | (b2 << 16);
+    }
+    const int64_t page = slot / a.P, off = slot - (slot / a.P) * a.P;
+    const int64_t dst_row = ((page * a.n_kv + kv) * a.Hkv + h) * a.P + off;
+    __stcs(reinterpret_cast<uint4*>(a.codes + dst_row * a.D + static_cast<int64_t>(c) * 16),
+           make_uint4(o[0], o[1], o[2], o[3]));
+  }
+}
+
+}  // namespace
+}  // namespace kvq
+
+extern "C" kvq_status kvq_store_unscaled(void* pool, const void* k, const void* v, const int64_t* slot_mapping,
+                                         int64_t num_tokens, const kvq_layout* layout, kvq_kind kind, void* stream) {
+  using namespace kvq;
+  if (!layout) return KVQ_EINVAL;
+  if (kind != KVQ_FP8_E4M3_UNSCALED && kind != KVQ_FP8_E5M2_UNSCALED) return KVQ_EKIND;
+  if (layout->num_pages < 0 || layout->page_size <= 0 || layout->num_kv_heads <= 0) return KVQ_EINVAL;
+  if (layout->head_dim <= 0 || layout->head_dim % 32 != 0) return KVQ_EHEADDIM;
+  if (num_tokens < 0) return KVQ_EINVAL;
+  if (num_tokens == 0) return KVQ_OK;
+  if (!pool || !k || !slot_mapping || (layout->mla ? v != nullptr : v == nullptr)) return KVQ_EINVAL;
+  if ((reinterpret_cast<uintptr_t>(pool) | reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v)) % 16 ||
+      reinterpret_cast<uintptr_t>(slot_mapping) % 8)
+    return KVQ_EALIGN;
+  const kvq_status st = kvq_device_check();
+  if (st != KVQ_OK) return st;
+  UnscaledStoreArgs a;
+  a.codes = static_cast<uint8_t*>(pool);
+  a.k = static_cast<const uint4*>(k);
+  a.v = static_cast<const uint4*>(v);
+  a.slot_mapping = slot_mapping;
+  a.num_tokens = num_tokens;
+  a.Hkv = layout->num_kv_heads;
+  a.D = layout->head_dim;
+  a.n_kv = layout->mla ? 1 : 2;
+  a.P = layout->page_size;
+  a.num_slots = static_cast<int64_t>(layout->num_pages) * layout->page_size;
+  const int64_t n = num_tokens * a.Hkv * (a.D / 16) * a.n_kv;
+  const int64_t grid = std::max<int64_t>(1, std::min<int64_t>((n + 255) / 256, static_cast<int64_t>(sm_count()) * 8));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (kind == KVQ_FP8_E4M3_UNSCALED)
+    unscaled_store_kernel<__NV_E4M3><<<static_cast<unsigned>(grid), 256, 0, s>>>(a);
+  else
+    unscaled_store_kernel<__NV_E5M2><<<static_cast<unsigned>(grid), 256, 0, s>>>(a);
+  return cudaGetLastError() == cudaSuccess ? KVQ_OK : KVQ_ECUDA;
+}

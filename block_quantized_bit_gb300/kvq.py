@@ -19,7 +19,10 @@ LIB_PATH = os.path.join(_HERE, "_build", "libkvq.so")
 
 KVQ_FP8_E4M3 = 1
 KVQ_Q8_0 = 2
-KIND = {"fp8_e4m3": KVQ_FP8_E4M3, "q8_0": KVQ_Q8_0}
+KVQ_FP8_E4M3_UNSCALED = 3
+KVQ_FP8_E5M2_UNSCALED = 4
+KIND = {"fp8_e4m3": KVQ_FP8_E4M3, "q8_0": KVQ_Q8_0, "fp8_e4m3_unscaled": KVQ_FP8_E4M3_UNSCALED,
+        "fp8_e5m2_unscaled": KVQ_FP8_E5M2_UNSCALED}
 KVQ_OUT_BF16 = 0
 KVQ_OUT_F32 = 1
 
@@ -31,7 +34,7 @@ EXPORTS = ["kvq_pool_bytes", "kvq_scale_bytes", "kvq_bytes_per_token", "kvq_num_
            "kvq_decode_sparse_workspace_bytes", "kvq_decode_sparse", "kvq_decode", "kvq_decode_ex",
            "kvq_workspace_status", "kvq_encode_probe", "kvq_quantize_probe", "kvq_dequant_probe", "kvq_strerror",
            "kvq_device_check", "kvq_version", "kvq_decode_noalloc", "kvq_wait_probe", "kvq_extend_workspace_bytes",
-           "kvq_extend", "kvq_store_act_quant"]
+           "kvq_extend", "kvq_store_act_quant", "kvq_store_unscaled"]
 
 
 class kvq_layout(ctypes.Structure):
@@ -77,6 +80,7 @@ def lib():
             "kvq_decode": (i32, [P, P, P, P, i32, P, i32, i32, ctypes.c_float, P, i32, P, sz, LP, i32, P]),
             "kvq_extend_workspace_bytes": (sz, []),
             "kvq_store_act_quant": (i32, [P, P, P, P, i64, i32, LP, i32, P]),
+            "kvq_store_unscaled": (i32, [P, P, P, P, i64, LP, i32, P]),
             "kvq_extend": (i32, [P, P, P, P, i32, P, P, i32, i32, i32, ctypes.c_float, P, i32, P, sz, LP, i32, P]),
             "kvq_decode_ex": (i32, [P, P, P, P, i32, P, i32, i32, ctypes.c_float, P, i32, P, sz, LP, i32, OP, P]),
             "kvq_workspace_status": (i32, [P, P]),
@@ -263,6 +267,14 @@ def kvq_decode_sparse(q: torch.Tensor, pool: torch.Tensor, scales: torch.Tensor,
                                    _ptr(out), od, _ptr(workspace), int(workspace.numel() * workspace.element_size()),
                                    ctypes.byref(layout.c()),
                                    _kind(kind), _stream(stream)), "kvq_decode_sparse")
+
+
+def kvq_store_unscaled(pool: torch.Tensor, k: torch.Tensor, v, slot_mapping: torch.Tensor, layout: Layout, kind,
+                       stream=None):
+    """Store into an unscaled fp8 pool (kind "fp8_e4m3_unscaled" or "fp8_e5m2_unscaled"): the plain cast."""
+    _check(lib().kvq_store_unscaled(_ptr(pool), _ptr(k), None if v is None else _ptr(v), _ptr(slot_mapping),
+                                    int(k.shape[0]), ctypes.byref(layout.c()), _kind(kind), _stream(stream)),
+           "kvq_store_unscaled")
 
 
 def kvq_store_act_quant(pool: torch.Tensor, scales: torch.Tensor, kv: torch.Tensor, slot_mapping: torch.Tensor,

@@ -37,8 +37,10 @@ extern "C" {
 
 /* Code format.  Both use one fp16 scale per 32 elements. */
 typedef enum {
-    KVQ_FP8_E4M3 = 1, /* OCP E4M3 "fn" codes, s = amax / 448 */
-    KVQ_Q8_0 = 2      /* int8 codes,          s = amax / 127 */
+    KVQ_FP8_E4M3 = 1,          /* OCP E4M3 "fn" codes, s = amax / 448 */
+    KVQ_Q8_0 = 2,              /* int8 codes,          s = amax / 127 */
+    KVQ_FP8_E4M3_UNSCALED = 3, /* the plain E4M3 cast, no scales, 1 byte per element (kvq_store_unscaled) */
+    KVQ_FP8_E5M2_UNSCALED = 4  /* the plain E5M2 cast, no scales, 1 byte per element (kvq_store_unscaled) */
 } kvq_kind;
 
 /* Element type of kvq_decode's output. */
@@ -176,6 +178,17 @@ kvq_status kvq_decode_sparse(const void* q, const void* pool, const void* scales
                              int32_t topk, int32_t batch, int32_t num_q_heads, float sm_scale, void* out,
                              kvq_out_dtype out_dtype, void* workspace, size_t workspace_bytes,
                              const kvq_layout* layout, kvq_kind kind, void* stream);
+
+/*
+ * Store into an unscaled fp8 pool ("Add fp8 KV-cache quantization (--kv-dtype)", section "How it works": the
+ * store casts the incoming bf16 k/v to the pool's fp8 type, scale 1.0; fp8_e5m2 is wired the same way).
+ * kind is KVQ_FP8_E4M3_UNSCALED or KVQ_FP8_E5M2_UNSCALED; each bf16 element becomes one code by a single
+ * nearest-even rounding that saturates at the largest finite value (448 / 57344), so the pool holds no NaN
+ * or infinity.  The pool has the codes layout of kvq_pool_bytes and no scale array.  Other arguments as
+ * kvq_store.  The other entry points do not accept these kinds yet (KVQ_EKIND).
+ */
+kvq_status kvq_store_unscaled(void* pool, const void* k, const void* v, const int64_t* slot_mapping,
+                              int64_t num_tokens, const kvq_layout* layout, kvq_kind kind, void* stream);
 
 /*
  * The MLA store fused with its producer ("feat(kvcache): 8-bit DSV4 window/compressed KV", section "Why the

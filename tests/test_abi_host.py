@@ -237,3 +237,25 @@ def test_fused_store_argument_errors(lib):
     assert call(n=-1) == -1
     assert call(n=0) == 0
     assert call(kv=FAKE + 8) == -4                              # KVQ_EALIGN
+
+
+def test_unscaled_store_argument_errors(lib):
+    P = ctypes.c_void_p
+
+    def call(layout=None, kind=3, v=FAKE, n=4, k=FAKE):
+        layout = layout or L()
+        return lib.kvq_store_unscaled(P(FAKE), P(k), P(v) if v else None, P(FAKE), n, ctypes.byref(layout.c()), kind,
+                                      None)
+
+    assert call(kind=1) == -2                                   # the block-scaled kinds use kvq_store
+    assert call(kind=5) == -2
+    assert call(layout=L(head_dim=48, v_dim=48)) == -3          # KVQ_EHEADDIM
+    assert call(v=0) == -1                                      # GQA needs v
+    assert call(layout=L(mla=True, num_kv_heads=1, head_dim=576, v_dim=512)) == -1  # MLA must not pass v
+    assert call(n=-1) == -1
+    assert call(n=0) == 0
+    assert call(k=FAKE + 4) == -4                               # KVQ_EALIGN
+    assert call(kind=4) != -2                                   # e5m2 is accepted (fails later: no device here)
+    # the decode does not read unscaled pools yet
+    assert lib.kvq_decode(P(FAKE), P(FAKE), P(FAKE), P(FAKE), 10, P(FAKE), 2, 8, ctypes.c_float(1.0), P(FAKE), 0,
+                          P(FAKE), 1 << 20, ctypes.byref(L().c()), 3, None) == -2
