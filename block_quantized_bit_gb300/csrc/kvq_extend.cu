@@ -17,8 +17,8 @@
 // with t the row (query row or key): K-major descriptors take LBO = 128 and SBO = RS, the MN-major one
 // LBO = RS and SBO = 128.  T = 128 keys per tile at D = 128 and 64 at D = 256 (shared memory).
 //
-// One persistent CTA per SM, 15 warps:
-//   warps 13-14 producers, one for K and one for V: TMA copies of a tile's codes (128-byte swizzled boxes of
+// One persistent CTA per SM, 19 warps:
+//   warps 17-18 producers, one for K and one for V: TMA copies of a tile's codes (128-byte swizzled boxes of
 //               16 tokens x 128 code bytes) and bulk copies of their scales into that producer's staging ring,
 //               with each page's number of valid tokens; the block table is read one tile ahead.
 //   warps 8-15  dequant: a thread owns 64 codes of one token row, of K and then of V.  K of tile j + 1 is
@@ -27,10 +27,12 @@
 //               tile j - 1, so the softmax of tile j overlaps the tensor pipe.
 //   warps 0-7   softmax: warps q and q + 4 own the 32 query rows of tensor-memory lane quarter q (one row
 //               per thread) and each takes half of a tile's keys and of O's columns; the two exchange
-//               their half-tile maxima through shared memory.  Causal and page masks, online softmax in
-//               the exp2 domain with lazy rescaling (the running max moves only when a score passes it
-//               by more than 2^8), P as bf16 into tensor memory.  At an item's end they write the next
-//               item's Q rows, then O / l to the output.
+//               their half-tile maxima and, per item, their row sums through shared memory, meeting on
+//               bounded mbarriers.  Causal and page masks (one warp-uniform branch per tile picks a
+//               straight-line unmasked or masked variant), online softmax in the exp2 domain with lazy
+//               rescaling (the running max moves only when a score passes it by more than 2^8), a quarter
+//               of the exponentials on the FMA pipe, P as bf16 into tensor memory.  At an item's end they
+//               write the next item's Q rows, then O / l to the output.
 // Every wait is bounded (2 s) and reports a timeout in the status word instead of hanging.
 #include <cuda.h>
 #include <math.h>
