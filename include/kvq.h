@@ -183,8 +183,8 @@ kvq_status kvq_decode_sparse(const void* q, const void* pool, const void* scales
  * Store into an unscaled fp8 pool ("Add fp8 KV-cache quantization (--kv-dtype)", section "How it works": the
  * store casts the incoming bf16 k/v to the pool's fp8 type, scale 1.0; fp8_e5m2 is wired the same way).
  * kind is KVQ_FP8_E4M3_UNSCALED or KVQ_FP8_E5M2_UNSCALED; each bf16 element becomes one code by a single
- * nearest-even rounding that saturates at the largest finite value (448 / 57344), so the pool holds no NaN
- * or infinity.  The pool has the codes layout of kvq_pool_bytes and no scale array.  Other arguments as
+ * nearest-even rounding that saturates at the largest finite value (448 / 57344): finite and infinite inputs
+ * give finite codes.  NaN inputs are outside the domain (as for kvq_store) and give NaN codes.  The pool has the codes layout of kvq_pool_bytes and no scale array.  Other arguments as
  * kvq_store.  The other entry points do not accept these kinds yet (KVQ_EKIND).
  */
 kvq_status kvq_store_unscaled(void* pool, const void* k, const void* v, const int64_t* slot_mapping,

@@ -10,8 +10,6 @@ if ROOT not in sys.path:
 
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (sm_103a) and the built CUDA library")
-    config.addinivalue_line("markers", "gpu_pending: a GPU test of a kernel that has not yet run on a GPU; "
-                                       "selected only by -m gpu_pending, and marked gpu once it has passed there")
 
 
 def pytest_collection_modifyitems(config, items):
@@ -24,5 +22,5 @@ def pytest_collection_modifyitems(config, items):
         return
     skip = pytest.mark.skip(reason="no CUDA GPU in this environment")
     for item in items:
-        if "gpu" in item.keywords or "gpu_pending" in item.keywords:
+        if "gpu" in item.keywords:
             item.add_marker(skip)

@@ -519,14 +519,69 @@ def test_decode_gqa_heads_read_their_own_kv_head():
     np.testing.assert_array_equal(out2[:, :4], out[:, 4:])
 
 
-def test_unquantized_reference_decode_runs():
-    s = _decode_setup(FP8)
+def _expected_bf16_scipy(s, sm_scale):
+    """Unquantized attention by scipy over the input bf16 rows themselves, taken by token index (not through
+    any pool): row t of sequence b is visible when its slot is not -1 (its page is not masked)."""
+    B, Hq, Hkv, D, Dv = len(s["lens"]), s["Hq"], s["Hkv"], s["D"], s["Dv"]
+    kf = bf16_to_f32(s["k"]).astype(np.float64)
+    vf = kf if s["mla"] else bf16_to_f32(s["v"]).astype(np.float64)
+    out = np.zeros((B, Hq, Dv))
+    start = 0
+    for b, L in enumerate(s["lens"]):
+        rows = np.arange(start, start + L)[s["slots"][start:start + L] >= 0]
+        start += L
+        for h in range(Hq):
+            g = h // (Hq // Hkv)
+            if len(rows) == 0:
+                continue
+            qv = bf16_to_f32(s["q"][b, h]).astype(np.float64)
+            p = scipy.special.softmax(sm_scale * (kf[rows, g] @ qv))
+            out[b, h] = p @ vf[rows, g, :Dv]
+    return out
+
+
+def _run_bf16(s, sm_scale=1.0, lens=None):
     pool16 = np.zeros(s["codes"].shape, np.uint16)
-    O.scatter_bf16(pool16, s["k"], s["v"], s["slots"], num_kv_heads=2, head_dim=64, page_size=16, mla=False)
-    ref = O.decode_bf16(s["q"], pool16, s["bt"], s["lens"], num_q_heads=8, num_kv_heads=2, head_dim=64,
-                        v_dim=64, page_size=16, mla=False, sm_scale=1.0)
-    out = _run(s)
-    assert np.all(np.isfinite(ref)) and np.abs(ref - out).max() < 0.1
+    O.scatter_bf16(pool16, s["k"], s["v"], s["slots"], num_kv_heads=s["Hkv"], head_dim=s["D"], page_size=s["P"],
+                   mla=s["mla"])
+    return O.decode_bf16(s["q"], pool16, s["bt"], s["lens"] if lens is None else lens, num_q_heads=s["Hq"],
+                         num_kv_heads=s["Hkv"], head_dim=s["D"], v_dim=s["Dv"], page_size=s["P"], mla=s["mla"],
+                         sm_scale=sm_scale)
+
+
+@pytest.mark.parametrize("mla", [False, True])
+def test_unquantized_decode_matches_scipy_attention_over_the_input_rows(mla):
+    """The unquantized reference (bf16 K/V scattered to a 2-byte pool, then exact attention) equals scipy
+    attention over the input rows taken by token index, so a wrong pool index, head or V row in either the
+    scatter or the decode fails it; masked pages, GQA grouping and MLA's shared row included."""
+    D, Dv = (96, 64) if mla else (64, 64)
+    s = _decode_setup(FP8, mla=mla, D=D, Dv=Dv, Hkv=1 if mla else 2, mask=[(1, 2), (0, 0)])
+    for sm_scale in (1.0, 0.37):
+        np.testing.assert_allclose(_run_bf16(s, sm_scale), _expected_bf16_scipy(s, sm_scale), rtol=1e-12,
+                                   atol=1e-13)
+    # no valid token gives zeros, as in the quantized decode
+    out0 = _run_bf16(s, lens=np.array([0, 5], np.int32))
+    assert not out0[0].any()
+
+
+def test_unquantized_decode_of_exactly_representable_rows_equals_the_quantized_decode():
+    """Rows whose values are code * scale exactly (one fp16 power-of-two scale per block, values on the E4M3
+    grid) dequantize to themselves, so the quantized and unquantized references must agree to the last bit."""
+    rng = np.random.default_rng(5)
+
+    def on_grid(x):
+        # E4M3 grid values times 2^-3 (max |x| per block 448 * 2^-3): the block scale amax/448 is 2^-3 exactly
+        # when every block holds a +-448 * 2^-3 element
+        c = torch.from_numpy(x.astype(np.float32)).to(torch.float8_e4m3fn).to(torch.float32).numpy()
+        c = c.reshape(*c.shape[:-1], -1, 32)
+        c[..., 0] = 448.0
+        return (c * 0.125).reshape(x.shape)
+
+    s = _decode_setup(FP8, kfun=lambda k: on_grid(k * 40), lens=(23, 41))
+    s["v"] = bf16_bits(on_grid(rng.standard_normal((sum(s["lens"]), 2, 64)) * 40).astype(np.float32))
+    O.store(s["codes"], s["scales"], s["k"], s["v"], s["slots"], num_kv_heads=2, head_dim=64, page_size=16, mla=False,
+            kind=FP8)
+    assert np.array_equal(_run_bf16(s, 0.05), _run(s, 0.05))
 
 
 # ===================================================================== sparse (top-K) decode

@@ -9,7 +9,7 @@ import torch
 import oracle as O
 from block_quantized_bit_gb300 import kvq
 
-pytestmark = pytest.mark.gpu_pending
+pytestmark = pytest.mark.gpu
 
 
 def _rows(T, D, seed):

@@ -8,7 +8,7 @@ import torch
 import oracle as O
 from block_quantized_bit_gb300 import kvq
 
-pytestmark = pytest.mark.gpu_pending
+pytestmark = pytest.mark.gpu
 
 
 @pytest.mark.parametrize("kind", ["fp8_e4m3_unscaled", "fp8_e5m2_unscaled"])
