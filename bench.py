@@ -1,8 +1,11 @@
 """Benchmark of the 8-bit paged KV cache hot path on GB300: one step = kvq_store + kvq_decode.
 
-Default workload (``qwen3_1p7b``): a Qwen3-1.7B-shaped attention layer -- Hq=16, Hkv=8, head_dim=128,
-page 16 -- storing 8 x 2048 new rows and decoding batch 8 over contexts drawn uniformly from
-[1024, 16384], fp8_e4m3.  Inputs are seeded synthetic tensors (workloads.py).  Prints one JSON line.
+Default workload (``long_gqa``, batch 8 x 262144 tokens): a long-context GQA layer -- Hq=16, Hkv=2,
+head_dim=256, page 16, 0.5% of the block-table entries masked -- whose step re-stores the whole cached
+context (8 x 262144 rows) and decodes batch 8 over it, fp8_e4m3.  ``--workload qwen3_1p7b`` (Hq=16,
+Hkv=8, head_dim=128; 8 x 2048 new rows stored, batch 8 decoded over contexts uniform in [1024, 16384]),
+``mla``, ``serving`` and ``tiny`` select the other shapes.  Inputs are seeded synthetic tensors
+(workloads.py).  Prints one JSON line.
 
 Metric: algorithmic HBM bytes moved by the step per second (GB/s), i.e. store bytes (bf16 in, codes
 and fp16 scales out, slot mapping) plus decode bytes (codes and scales of every valid token, q,
@@ -39,10 +42,10 @@ def parse():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="qwen3_1p7b",
+    ap.add_argument("--workload", default="long_gqa",
                     choices=["qwen3_1p7b", "long_gqa", "mla", "serving", "tiny"])
     ap.add_argument("--kind", default="fp8_e4m3", choices=["fp8_e4m3", "q8_0"])
-    ap.add_argument("--batch", type=int, default=None, help="long_gqa / serving batch override")
+    ap.add_argument("--batch", type=int, default=None, help="long_gqa (default 8) / serving batch override")
     ap.add_argument("--ctx", type=int, default=None, help="long_gqa / mla context override")
     ap.add_argument("--path", type=int, default=0, help="decode path: 0 auto, 1 CUDA cores, 2 tcgen05")
     ap.add_argument("--topk", type=int, default=0,
@@ -91,7 +94,7 @@ def make_case(args, device):
     if args.seed is not None:
         kw["seed"] = args.seed
     if args.workload == "long_gqa":
-        kw.update(batch=args.batch or 1, ctx=args.ctx or 262144)
+        kw.update(batch=args.batch or 8, ctx=args.ctx or 262144)
     elif args.workload == "mla":
         kw.update(ctx=args.ctx or 163840)
     elif args.workload == "serving" and args.batch:
@@ -435,8 +438,15 @@ def oracle_sample(case, budget_rows=None, max_seqs=None):
     return n_rows, seqs
 
 
-def oracle_step(case, codes, scales, n_rows, seqs, threads, ix=None):
-    """One oracle step over the sample: store n_rows rows, decode the chosen sequences.  Returns bytes."""
+def sample_text(n_rows, seqs, batch, tok_cap):
+    cap = "" if tok_cap is None else ", each cut to its first %d tokens" % tok_cap
+    return "store of %d rows + fp64 decode of %d of %d sequences (all heads%s)" % (n_rows, len(seqs), batch, cap)
+
+
+def oracle_step(case, codes, scales, n_rows, seqs, threads, ix=None, tok_cap=None):
+    """One oracle step over the sample: store n_rows rows, decode the chosen sequences (each cut to its first
+    tok_cap tokens when given: a prefix of a sequence is a shorter sequence of the same workload).  Returns
+    bytes."""
     import oracle as O
     bits = lambda t: t.contiguous().view(torch.int16).numpy().view(np.uint16)  # noqa: E731
     if case.new_k is not None:
@@ -446,17 +456,18 @@ def oracle_step(case, codes, scales, n_rows, seqs, threads, ix=None):
     O.store(codes, scales, bits(k), None if v is None else bits(v), s.numpy(), num_kv_heads=case.num_kv_heads,
             head_dim=case.head_dim, page_size=case.page_size, mla=case.mla, kind=case.kind)
     idx = torch.tensor(seqs, dtype=torch.long)
+    lens = case.seq_lens[idx] if tok_cap is None else case.seq_lens[idx].clamp(max=tok_cap)
     dims = dict(num_q_heads=case.num_q_heads, num_kv_heads=case.num_kv_heads, head_dim=case.head_dim,
                 v_dim=case.v_dim, page_size=case.page_size, mla=case.mla, kind=case.kind, sm_scale=case.sm_scale,
                 nthreads=threads)
     if ix is not None:
-        O.decode_sparse(bits(case.q[idx]), codes, scales, case.block_table[idx].numpy(), case.seq_lens[idx].numpy(),
+        O.decode_sparse(bits(case.q[idx]), codes, scales, case.block_table[idx].numpy(), lens.numpy(),
                         ix[idx].numpy(), **dims)
     else:
-        O.decode(bits(case.q[idx]), codes, scales, case.block_table[idx].numpy(), case.seq_lens[idx].numpy(), **dims)
+        O.decode(bits(case.q[idx]), codes, scales, case.block_table[idx].numpy(), lens.numpy(), **dims)
     n_kv = 1 if case.mla else 2
     row = n_kv * case.num_kv_heads * case.head_dim
-    sub = type(case)(**{**case.__dict__, "seq_lens": case.seq_lens[idx], "block_table": case.block_table[idx],
+    sub = type(case)(**{**case.__dict__, "seq_lens": lens, "block_table": case.block_table[idx],
                         "q": case.q[idx]})
     toks = valid_tokens(sub) if ix is None else valid_columns(sub, ix[idx])
     return n_rows * (row * (2 + 1 + 2 / 32) + 8) + toks * row * 17 / 16
@@ -485,23 +496,27 @@ def cpu_baseline(case, args):
     O, cpu, codes, scales = prepare_oracle(case)
     threads = max(1, O.openmp_threads())
     ix = sparse_lists(cpu, args)
-    # whole workload steps while they fit ~10 s, else a sub-sample (fewer store rows and sequences)
+    # whole workload steps while they fit ~10 s, else a sub-sample (fewer store rows and sequences, and
+    # sequences cut to a prefix); a first pass on a small sample sizes it, so that no pass runs for minutes
     n_rows, seqs = oracle_sample(cpu)
-    t0 = time.perf_counter()
-    nbytes = oracle_step(cpu, codes, scales, n_rows, seqs, threads, ix)
-    one = time.perf_counter() - t0
-    if one > 15.0:
-        n_rows, seqs = oracle_sample(cpu, budget_rows=2048, max_seqs=max(1, int(len(seqs) * 10.0 / one)))
+    tok_cap = None
+    big = n_rows * cpu.head_dim * cpu.num_kv_heads > (64 << 20) or valid_tokens(cpu) * cpu.num_q_heads > (1 << 26)
+    if big:
+        n_rows, seqs = oracle_sample(cpu, budget_rows=4096, max_seqs=1)
+        tok_cap = 16384
         t0 = time.perf_counter()
-        nbytes = oracle_step(cpu, codes, scales, n_rows, seqs, threads, ix)
+        oracle_step(cpu, codes, scales, n_rows, seqs, threads, ix, tok_cap)
+        one = time.perf_counter() - t0
+        seqs = list(range(max(1, min(cpu.batch, int(5.0 / max(one, 1e-3))))))
+    t0 = time.perf_counter()
+    nbytes = oracle_step(cpu, codes, scales, n_rows, seqs, threads, ix, tok_cap)
     passes = 1
     while time.perf_counter() - t0 < 10.0 and passes < 200:
-        nbytes += oracle_step(cpu, codes, scales, n_rows, seqs, threads, ix)
+        nbytes += oracle_step(cpu, codes, scales, n_rows, seqs, threads, ix, tok_cap)
         passes += 1
     dt = time.perf_counter() - t0
     return {"value": round(nbytes / dt / 1e9, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
-            "sample": "%d passes of: store of %d rows + fp64 decode of %d of %d sequences (all heads); %.1f s"
-                      % (passes, n_rows, len(seqs), cpu.batch, dt)}
+            "sample": "%d passes of: %s; %.1f s" % (passes, sample_text(n_rows, seqs, cpu.batch, tok_cap), dt)}
 
 
 def run_reference(args, world, rank):
@@ -513,16 +528,16 @@ def run_reference(args, world, rank):
     threads = max(1, O.openmp_threads())
     ix = sparse_lists(cpu, args)
     n_rows, seqs = oracle_sample(cpu, budget_rows=512, max_seqs=1)
+    tok_cap = 8192 if int(cpu.seq_lens[0]) > 8192 else None   # about 0.1-0.5 s per step on 16 cores
     for _ in range(args.warmup):
-        oracle_step(cpu, codes, scales, n_rows, seqs, threads, ix)
+        oracle_step(cpu, codes, scales, n_rows, seqs, threads, ix, tok_cap)
     t0 = time.perf_counter()
     nb = 0.0
     for _ in range(args.steps):
-        nb += oracle_step(cpu, codes, scales, n_rows, seqs, threads, ix)
+        nb += oracle_step(cpu, codes, scales, n_rows, seqs, threads, ix, tok_cap)
     dt = time.perf_counter() - t0
     value = nb / dt / 1e9
-    sample = "store of %d rows + fp64 decode of %d of %d sequences (all heads) per step" % (n_rows, len(seqs),
-                                                                                          cpu.batch)
+    sample = sample_text(n_rows, seqs, cpu.batch, tok_cap) + " per step"
     return {
         "impl": "reference",
         "metric": "quantized-KV decode attention HBM GB/s (% of GB300 peak); kvq_store GB/s",

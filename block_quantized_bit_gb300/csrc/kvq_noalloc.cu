@@ -15,6 +15,9 @@
 // and the split counters are cleared on every call (kvq_decode does that), and the split partials are
 // always written before they are read.  Calls whose kernels overlap on the GPU (different streams, or different host
 // threads without ordering) race on the array and give wrong results.
+//
+// The status word a decode leaves (a timed-out bounded wait, a block-table entry past the pool) lives in
+// that array too, where the caller has no pointer to it; kvq_noalloc_status reads it.
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -64,4 +67,11 @@ extern "C" kvq_status kvq_decode_noalloc(const void* q, const void* pool, const 
   if (st != KVQ_OK) return st;
   return kvq_decode(q, pool, scales, block_table, max_pages_per_seq, seq_lens, batch, num_q_heads, sm_scale, out,
                     out_dtype, scratch, static_cast<size_t>(KVQ_NOALLOC_SCRATCH_BYTES), layout, kind, stream);
+}
+
+extern "C" kvq_status kvq_noalloc_status(void* stream) {
+  void* scratch = nullptr;
+  const kvq_status st = kvq::scratch_address(&scratch);
+  if (st != KVQ_OK) return st;
+  return kvq_workspace_status(scratch, stream);
 }

@@ -33,8 +33,8 @@ EXPORTS = ["kvq_pool_bytes", "kvq_scale_bytes", "kvq_bytes_per_token", "kvq_num_
            "kvq_decode_workspace_bytes", "kvq_decode_workspace_bytes_ex", "kvq_decode_path",
            "kvq_decode_sparse_workspace_bytes", "kvq_decode_sparse", "kvq_decode", "kvq_decode_ex",
            "kvq_workspace_status", "kvq_encode_probe", "kvq_quantize_probe", "kvq_dequant_probe", "kvq_strerror",
-           "kvq_device_check", "kvq_version", "kvq_decode_noalloc", "kvq_wait_probe", "kvq_extend_workspace_bytes",
-           "kvq_extend", "kvq_store_act_quant", "kvq_store_unscaled"]
+           "kvq_device_check", "kvq_version", "kvq_decode_noalloc", "kvq_noalloc_status", "kvq_wait_probe",
+           "kvq_extend_workspace_bytes", "kvq_extend", "kvq_store_act_quant", "kvq_store_unscaled"]
 
 
 class kvq_layout(ctypes.Structure):
@@ -92,6 +92,7 @@ def lib():
             "kvq_version": (ctypes.c_char_p, []),
             "kvq_decode_noalloc": (i32, [P, P, P, P, i32, P, i32, i32, ctypes.c_float, P, i32, LP, i32, P]),
             "kvq_wait_probe": (i32, [P, P]),
+            "kvq_noalloc_status": (i32, [P]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -310,6 +311,11 @@ def kvq_extend(q: torch.Tensor, pool: torch.Tensor, scales: torch.Tensor, block_
 
 def kvq_workspace_status(workspace: torch.Tensor, stream=None) -> int:
     return lib().kvq_workspace_status(_ptr(workspace), _stream(stream))
+
+
+def kvq_noalloc_status(stream=None) -> int:
+    """Status word the last kvq_decode_noalloc left in the library's scratch (0 = KVQ_OK)."""
+    return lib().kvq_noalloc_status(_stream(stream))
 
 
 # ---------------------------------------------------------------------------- probes

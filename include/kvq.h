@@ -19,7 +19,9 @@
  * Conventions for every entry point:
  *   - Pointers named as device pointers must point to device memory of the current device; host
  *     pointers (kvq_layout) are read during the call only.  The caller owns every buffer; the
- *     library allocates nothing and keeps no state between calls.
+ *     library allocates nothing and keeps no state between calls.  The one exception is
+ *     kvq_decode_noalloc (with kvq_noalloc_status), whose scratch is a fixed array in the library's own
+ *     device memory that keeps its contents from one call to the next.
  *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Calls are asynchronous on it.
  *   - Arguments are validated on the host before anything is launched.  A failed validation returns
  *     a negative kvq_status and leaves every buffer untouched.  A launch failure returns KVQ_ECUDA.
@@ -265,6 +267,15 @@ kvq_status kvq_decode_noalloc(const void* q, const void* pool, const void* scale
                               int32_t max_pages_per_seq, const int32_t* seq_lens, int32_t batch,
                               int32_t num_q_heads, float sm_scale, void* out, kvq_out_dtype out_dtype,
                               const kvq_layout* layout, kvq_kind kind, void* stream);
+/*
+ * Status word the last kvq_decode_noalloc left in the library's scratch array, as kvq_workspace_status
+ * reports it for a caller's workspace: KVQ_OK; KVQ_ETIMEOUT if a kernel gave up a bounded wait (the output
+ * of that call is not valid); KVQ_EINVAL if a block-table entry pointed past the pool.  The caller has no
+ * pointer to that array, so this is the only way to read it.  Synchronizes `stream`; call it on the stream
+ * of the decode it checks, before another kvq_decode_noalloc is issued on any stream.  Like the decode,
+ * it has no counterpart on the pages.
+ */
+kvq_status kvq_noalloc_status(void* stream);
 
 /*
  * Status word a decode left in its workspace: KVQ_OK; KVQ_ETIMEOUT if a kernel gave up a bounded

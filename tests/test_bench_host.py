@@ -103,3 +103,24 @@ def test_extend_keys_count_the_causal_unmasked_positions():
     with pytest.raises(ValueError):
         workloads.extend_inputs(case, [301, 0, 0])
     assert np.array_equal(workloads.extend_inputs(case, 5)[1].numpy(), [0, 5, 10, 15])
+
+
+def test_oracle_sample_with_a_token_cap_counts_the_prefix_it_decodes():
+    """The bounded oracle samples cut each decoded sequence to a prefix: the bytes a step reports are those of
+    the stored rows plus the valid (unmasked) tokens of that prefix, and the default workload is the long-context
+    batch-8 layer."""
+    from block_quantized_bit_gb300 import workloads
+    case = workloads.make("long_gqa", kind="fp8_e4m3", device="cpu", batch=2, ctx=3000, mask_frac=0.05)
+    O, cpu, codes, scales = bench.prepare_oracle(case)
+    nb = bench.oracle_step(cpu, codes, scales, 64, [0, 1], 1, tok_cap=1000)
+    bt = case.block_table.numpy()
+    toks = sum(1 for b in range(2) for t in range(1000) if bt[b, t // 16] >= 0)
+    row = 2 * case.num_kv_heads * case.head_dim
+    assert nb == 64 * (row * (2 + 1 + 2 / 32) + 8) + toks * row * 17 / 16
+    import sys as _sys
+    argv, _sys.argv = _sys.argv, ["bench.py"]
+    try:
+        a = bench.parse()
+    finally:
+        _sys.argv = argv
+    assert a.workload == "long_gqa" and a.kind == "fp8_e4m3" and a.batch is None and a.ctx is None
