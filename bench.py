@@ -36,6 +36,32 @@ import numpy as np  # noqa: E402
 import torch  # noqa: E402
 
 
+# Code bytes per element of each kind: the block-scaled kinds add an fp16 scale per 32 elements; the unscaled
+# fp8 casts have none.
+KINDS = {"fp8_e4m3": 17 / 16, "q8_0": 17 / 16, "fp8_e4m3_unscaled": 1.0, "fp8_e5m2_unscaled": 1.0}
+
+
+def unscaled(kind):
+    return KINDS[kind] == 1.0
+
+
+def store_rows_into(kvq, codes, scales, k, v, slots, L, kind):
+    """The step's store: kvq_store (block-scaled) or kvq_store_unscaled (the plain fp8 cast)."""
+    if unscaled(kind):
+        kvq.kvq_store_unscaled(codes, k, v, slots, L, kind)
+    else:
+        kvq.kvq_store(codes, scales, k, v, slots, L, kind)
+
+
+def alloc_pool(kvq, L, kind, dev):
+    codes, scales = kvq.alloc_pool(L, dev)
+    codes.zero_()
+    if unscaled(kind):
+        return codes, None
+    scales.zero_()
+    return codes, scales
+
+
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -44,7 +70,7 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="long_gqa",
                     choices=["qwen3_1p7b", "long_gqa", "mla", "serving", "tiny"])
-    ap.add_argument("--kind", default="fp8_e4m3", choices=["fp8_e4m3", "q8_0"])
+    ap.add_argument("--kind", default="fp8_e4m3", choices=list(KINDS))
     ap.add_argument("--batch", type=int, default=None, help="long_gqa (default 8) / serving batch override")
     ap.add_argument("--ctx", type=int, default=None, help="long_gqa / mla context override")
     ap.add_argument("--path", type=int, default=0, help="decode path: 0 auto, 1 CUDA cores, 2 tcgen05")
@@ -139,15 +165,16 @@ def algorithmic_bytes(case, ix=None):
         store_rows = int(case.new_k.shape[0])
     else:
         store_rows = int(case.k.shape[0])
-    store = store_rows * (row_elems * (2 + 1 + 2 / 32) + 8)
+    bpe = KINDS[case.kind]
+    store = store_rows * (row_elems * (2 + bpe) + 8)
     out_bytes = case.q.numel() * 2 + case.batch * case.num_q_heads * case.v_dim * 2 + case.batch * 4
     if ix is not None:  # sparse: the selected rows, the index lists and their block-table lookups
         toks = valid_columns(case, ix)
-        decode = toks * row_elems * 17 / 16 + out_bytes + ix.numel() * 8
+        decode = toks * row_elems * bpe + out_bytes + ix.numel() * 8
         return store, decode, store_rows, toks
     toks = valid_tokens(case)
     pages = sum((int(L) + case.page_size - 1) // case.page_size for L in case.seq_lens.cpu().tolist())
-    decode = toks * row_elems * 17 / 16 + out_bytes + pages * 4
+    decode = toks * row_elems * bpe + out_bytes + pages * 4
     return store, decode, store_rows, toks
 
 
@@ -203,11 +230,9 @@ def run_ours(args, world, rank):
     dev = torch.device("cuda", torch.cuda.current_device())
     case = make_case(args, "cuda")
     L = kvq.Layout(case.num_pages, case.page_size, case.num_kv_heads, case.head_dim, case.v_dim, case.mla)
-    codes, scales = kvq.alloc_pool(L, dev)
-    codes.zero_()
-    scales.zero_()
+    codes, scales = alloc_pool(kvq, L, case.kind, dev)
     # fill the cached context (untimed)
-    kvq.kvq_store(codes, scales, case.k, case.v, case.slot_mapping, L, case.kind)
+    store_rows_into(kvq, codes, scales, case.k, case.v, case.slot_mapping, L, case.kind)
     if case.new_k is not None:
         sk, sv, ss = case.new_k, case.new_v, case.new_slots
     else:  # the store step re-stores the context rows
@@ -230,7 +255,7 @@ def run_ours(args, world, rank):
             kvq.kvq_decode(q, codes, scales, bt, sl, o, ws, L, case.kind, case.sm_scale, path=args.path)
 
     def step():
-        kvq.kvq_store(codes, scales, sk, sv, ss, L, case.kind)
+        store_rows_into(kvq, codes, scales, sk, sv, ss, L, case.kind)
         decode(case.q, case.block_table, case.seq_lens, ix, out)
 
     for _ in range(args.warmup):
@@ -251,7 +276,7 @@ def run_ours(args, world, rank):
     for i in range(K):
         flush.fill_(i & 0xFF)
         ev[i][0].record(stream)
-        kvq.kvq_store(codes, scales, sk, sv, ss, L, case.kind)
+        store_rows_into(kvq, codes, scales, sk, sv, ss, L, case.kind)
         ev[i][1].record(stream)
         decode(case.q, case.block_table, case.seq_lens, ix, out)
         ev[i][2].record(stream)
@@ -361,7 +386,7 @@ def run_e2e(args, case, L, codes, scales, sk, sv, ss, ix, decode, flush, world):
         dsl.copy_(hsl, non_blocking=True)
         if dix is not None:
             dix.copy_(hix, non_blocking=True)
-        kvq.kvq_store(codes, scales, dk, dv, ds, L, case.kind)
+        store_rows_into(kvq, codes, scales, dk, dv, ds, L, case.kind)
         decode(dq, dbt, dsl, dix, dout)
         hout.copy_(dout, non_blocking=True)
 
@@ -470,7 +495,8 @@ def oracle_step(case, codes, scales, n_rows, seqs, threads, ix=None, tok_cap=Non
     sub = type(case)(**{**case.__dict__, "seq_lens": lens, "block_table": case.block_table[idx],
                         "q": case.q[idx]})
     toks = valid_tokens(sub) if ix is None else valid_columns(sub, ix[idx])
-    return n_rows * (row * (2 + 1 + 2 / 32) + 8) + toks * row * 17 / 16
+    bpe = KINDS[case.kind]
+    return n_rows * (row * (2 + bpe) + 8) + toks * row * bpe
 
 
 def sparse_lists(case, args):
@@ -487,7 +513,7 @@ def prepare_oracle(case):
     build_oracle.build()
     cpu = type(case)(**{k: (v.cpu() if isinstance(v, torch.Tensor) else v) for k, v in case.__dict__.items()})
     codes = np.zeros((cpu.num_pages, 1 if cpu.mla else 2, cpu.num_kv_heads, cpu.page_size, cpu.head_dim), np.uint8)
-    scales = np.zeros(codes.shape[:-1] + (cpu.head_dim // 32,), np.uint16)
+    scales = None if unscaled(cpu.kind) else np.zeros(codes.shape[:-1] + (cpu.head_dim // 32,), np.uint16)
     return O, cpu, codes, scales
 
 
@@ -555,6 +581,28 @@ def run_reference(args, world, rank):
 EXTEND_METRIC = "quantized-KV extend (prefill) attention TFLOP/s (% of GB300 bf16 peak); kvq_store of the new rows"
 
 
+def extend_kernel_name(case):
+    if case.mla:
+        return "kvq_extend (decode kernels over each new token's causal prefix, + merge)"
+    return "kvq_extend (extend_tc_kernel)"
+
+
+def extend_launches(kvq, case, L, total_q):
+    """Kernels one extend step launches: the store, then the GQA extend kernel; for MLA the prefix expansion
+    and, per chunk of 1024 new tokens, the decode (with the merge on the tensor-core path)."""
+    if not case.mla:
+        return 2
+    chunk = min(total_q, 1024)
+    per = 2 if kvq.kvq_decode_path(L, chunk, case.num_q_heads, case.max_pages) == 2 else 1
+    return 2 + per * ((total_q + chunk - 1) // chunk)
+
+
+def extend_flops_per_key(case):
+    """FLOPs of one (new token, visible key) pair over all query heads: QK over the K width plus PV over the V
+    width (4 * D * Hq for GQA; 2 * Hq * (576 + 512) for the MLA latent row)."""
+    return 2.0 * case.num_q_heads * (case.head_dim + case.v_dim)
+
+
 def extend_keys(case, q_start):
     """Keys the extend reads, summed over new tokens: the unmasked positions up to each token's own."""
     bt = case.block_table.cpu().numpy()
@@ -581,14 +629,13 @@ def run_extend(args, world, rank):
     dev = torch.device("cuda", torch.cuda.current_device())
     case = make_case(args, "cuda")
     L = kvq.Layout(case.num_pages, case.page_size, case.num_kv_heads, case.head_dim, case.v_dim, case.mla)
-    codes, scales = kvq.alloc_pool(L, dev)
-    codes.zero_()
-    scales.zero_()
-    kvq.kvq_store(codes, scales, case.k, case.v, case.slot_mapping, L, case.kind)  # the context (untimed)
+    codes, scales = alloc_pool(kvq, L, case.kind, dev)
+    store_rows_into(kvq, codes, scales, case.k, case.v, case.slot_mapping, L, case.kind)  # the context (untimed)
     q, q_start, rows = extend_inputs(case, args)
-    sk, sv, ss = case.k[rows], case.v[rows], case.slot_mapping[rows]  # the step re-stores its new rows
+    sk, ss = case.k[rows], case.slot_mapping[rows]  # the step re-stores its new rows
+    sv = None if case.mla else case.v[rows]
     out = torch.empty(q.shape[0], case.num_q_heads, case.v_dim, dtype=torch.bfloat16, device=dev)
-    ws = kvq.alloc_extend_workspace(dev)
+    ws = kvq.alloc_extend_workspace(dev, L, q.shape[0], case.num_q_heads, case.max_pages)
     flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)  # 4x L2
     stream = torch.cuda.current_stream()
 
@@ -597,7 +644,7 @@ def run_extend(args, world, rank):
 
     for _ in range(args.warmup):
         flush.fill_(1)
-        kvq.kvq_store(codes, scales, sk, sv, ss, L, case.kind)
+        store_rows_into(kvq, codes, scales, sk, sv, ss, L, case.kind)
         extend(q, q_start, case.block_table, case.seq_lens, out)
     torch.cuda.synchronize()
     st = kvq.kvq_workspace_status(ws)
@@ -613,7 +660,7 @@ def run_extend(args, world, rank):
     for i in range(K):
         flush.fill_(i & 0xFF)
         ev[i][0].record(stream)
-        kvq.kvq_store(codes, scales, sk, sv, ss, L, case.kind)
+        store_rows_into(kvq, codes, scales, sk, sv, ss, L, case.kind)
         ev[i][1].record(stream)
         extend(q, q_start, case.block_table, case.seq_lens, out)
         ev[i][2].record(stream)
@@ -624,28 +671,31 @@ def run_extend(args, world, rank):
     ext_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K)]
     total_ms = max_over_ranks(sum(store_ms) + sum(ext_ms), world)
     keys = extend_keys(case, q_start)
-    flops = 4.0 * case.head_dim * case.num_q_heads * keys
+    flops = extend_flops_per_key(case) * keys
     ext_s = statistics.mean(ext_ms) / 1e3
     achieved = flops / ext_s / 1e12
     peaks = load_peaks()
     peak = peaks.get("bf16_tflops")
     store_rows = int(rows.numel())
-    row_elems = 2 * case.num_kv_heads * case.head_dim
-    store_b = store_rows * (row_elems * (2 + 1 + 2 / 32) + 8)
+    row_elems = (1 if case.mla else 2) * case.num_kv_heads * case.head_dim
+    store_b = store_rows * (row_elems * (2 + KINDS[case.kind]) + 8)
 
     # end to end through the public API: the step's inputs from pinned host memory, its output back
     hq, hqs = q.cpu().pin_memory(), q_start.cpu().pin_memory()
-    hk, hv, hs = sk.cpu().pin_memory(), sv.cpu().pin_memory(), ss.cpu().pin_memory()
+    hk, hs = sk.cpu().pin_memory(), ss.cpu().pin_memory()
+    hv = None if sv is None else sv.cpu().pin_memory()
     hbt, hsl = case.block_table.cpu().pin_memory(), case.seq_lens.cpu().pin_memory()
     hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    dq, dqs, dk, dv, ds = (torch.empty_like(t) for t in (q, q_start, sk, sv, ss))
+    dq, dqs, dk, ds = (torch.empty_like(t) for t in (q, q_start, sk, ss))
+    dv = None if sv is None else torch.empty_like(sv)
     dbt, dsl = torch.empty_like(case.block_table), torch.empty_like(case.seq_lens)
     dout = torch.empty_like(out)
+    pairs = [(dq, hq), (dqs, hqs), (dk, hk), (ds, hs), (dbt, hbt), (dsl, hsl)] + ([] if dv is None else [(dv, hv)])
 
     def one():
-        for d, h in ((dq, hq), (dqs, hqs), (dk, hk), (dv, hv), (ds, hs), (dbt, hbt), (dsl, hsl)):
+        for d, h in pairs:
             d.copy_(h, non_blocking=True)
-        kvq.kvq_store(codes, scales, dk, dv, ds, L, case.kind)
+        store_rows_into(kvq, codes, scales, dk, dv, ds, L, case.kind)
         extend(dq, dqs, dbt, dsl, dout)
         hout.copy_(dout, non_blocking=True)
 
@@ -660,7 +710,7 @@ def run_extend(args, world, rank):
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_s = max_over_ranks(e0.elapsed_time(e1) / 1e3, world) / K
-    h2d = sum(t.numel() * t.element_size() for t in (hq, hqs, hk, hv, hs, hbt, hsl))
+    h2d = sum(h.numel() * h.element_size() for _, h in pairs)
     res = {
         "metric": EXTEND_METRIC,
         "value": round(world * flops * K / (total_ms / 1e3) / 1e12, 2),
@@ -675,13 +725,13 @@ def run_extend(args, world, rank):
         "extend_tflops": round(achieved, 1),
         "store_us": round(statistics.mean(store_ms) * 1e3, 2),
         "store_gbs": round(store_b / (statistics.mean(store_ms) / 1e3) / 1e9, 1),
-        "roofline": {"bound": "tensor", "kernel": "kvq_extend (extend_tc_kernel)", "achieved": round(achieved, 1),
+        "roofline": {"bound": "tensor", "kernel": extend_kernel_name(case), "achieved": round(achieved, 1),
                      "peak": peak, "unit": "TFLOP/s", "frac": round(achieved / peak, 4) if peak else None,
                      "peak_source": "MEASURED_PEAKS.json bf16_tflops (burst; of measured)", "traffic": None},
         "clocks": clk,
         "e2e": {"value": round(world * flops / e2e_s / 1e12, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": hout.numel() * hout.element_size()},
-        "gpu_launches": 2 * K,
+        "gpu_launches": extend_launches(kvq, case, L, int(q.shape[0])) * K,
     }
     if rank == 0 and not args.no_cpu_baseline:
         res["cpu_baseline"] = extend_cpu_baseline(case, args)
@@ -699,21 +749,22 @@ def extend_oracle_pass(O, cpu, codes, scales, q, q_start, m, threads):
     qs = torch.zeros_like(q_start)
     qs[1:] = m
     rows = torch.arange(L0 - n0, L0 - n0 + m)      # sequence 0's rows come first in the context order
-    O.store(codes, scales, bits(cpu.k[rows]), bits(cpu.v[rows]), cpu.slot_mapping[rows].numpy(),
-            num_kv_heads=cpu.num_kv_heads, head_dim=cpu.head_dim, page_size=cpu.page_size, mla=False, kind=cpu.kind)
+    O.store(codes, scales, bits(cpu.k[rows]), None if cpu.mla else bits(cpu.v[rows]), cpu.slot_mapping[rows].numpy(),
+            num_kv_heads=cpu.num_kv_heads, head_dim=cpu.head_dim, page_size=cpu.page_size, mla=cpu.mla,
+            kind=cpu.kind)
     O.extend(bits(q[:m]), codes, scales, cpu.block_table.numpy(), lens.numpy(), qs.numpy(),
              num_q_heads=cpu.num_q_heads, num_kv_heads=cpu.num_kv_heads, head_dim=cpu.head_dim, v_dim=cpu.v_dim,
-             page_size=cpu.page_size, mla=False, kind=cpu.kind, sm_scale=cpu.sm_scale, nthreads=threads)
+             page_size=cpu.page_size, mla=cpu.mla, kind=cpu.kind, sm_scale=cpu.sm_scale, nthreads=threads)
     sub = type(cpu)(**{**cpu.__dict__, "seq_lens": lens})
-    return 4.0 * cpu.head_dim * cpu.num_q_heads * extend_keys(sub, qs)
+    return extend_flops_per_key(cpu) * extend_keys(sub, qs)
 
 
 def extend_oracle_setup(case, args):
     O, cpu, codes, scales = prepare_oracle(case)
     ctx = cpu.slot_mapping
     bits = lambda t: t.contiguous().view(torch.int16).numpy().view(np.uint16)  # noqa: E731
-    O.store(codes, scales, bits(cpu.k), bits(cpu.v), ctx.numpy(), num_kv_heads=cpu.num_kv_heads,
-            head_dim=cpu.head_dim, page_size=cpu.page_size, mla=False, kind=cpu.kind)  # the context, untimed
+    O.store(codes, scales, bits(cpu.k), None if cpu.mla else bits(cpu.v), ctx.numpy(), num_kv_heads=cpu.num_kv_heads,
+            head_dim=cpu.head_dim, page_size=cpu.page_size, mla=cpu.mla, kind=cpu.kind)  # the context, untimed
     q, q_start, _ = extend_inputs(cpu, args)
     return O, cpu, codes, scales, q.cpu(), q_start.cpu(), max(1, O.openmp_threads())
 
@@ -740,7 +791,7 @@ def run_extend_reference(args, world, rank):
         return None
     case = make_case(args, "cpu")
     O, cpu, codes, scales, q, q_start, threads = extend_oracle_setup(case, args)
-    m = min(8, int(q_start[1] - q_start[0]))
+    m = min(1 if cpu.mla else 8, int(q_start[1] - q_start[0]))   # a 128-head latent row costs ~16x a GQA one
     for _ in range(args.warmup):
         extend_oracle_pass(O, cpu, codes, scales, q, q_start, m, threads)
     t0 = time.perf_counter()

@@ -43,6 +43,12 @@ kvq_status check_layout(const kvq_layout* L) {
 
 bool kind_ok(int kind) { return kind == KVQ_FP8_E4M3 || kind == KVQ_Q8_0; }
 
+// Kinds the attention entry points read: the block-scaled ones and the unscaled fp8 casts.
+bool kind_read_ok(int kind) { return kind_ok(kind) || kind == KVQ_FP8_E4M3_UNSCALED || kind == KVQ_FP8_E5M2_UNSCALED; }
+
+// The unscaled kinds have no scale array: their scales pointer is ignored (it may be NULL).
+bool has_scales(int kind) { return kind_ok(kind); }
+
 // SMs of the current device (the MLA tensor-core plan targets one work item per SM).
 int32_t sm_count() {
   int dev = 0, sms = 0;
@@ -145,10 +151,12 @@ kvq_status decode_common(const void* q, const void* pool, const void* scales, co
                          int32_t max_pages_per_seq, const int32_t* seq_lens, int32_t batch, int32_t num_q_heads,
                          float sm_scale, void* out, kvq_out_dtype out_dtype, void* workspace,
                          size_t workspace_bytes, const kvq_layout* layout, kvq_kind kind,
-                         const kvq_decode_options* options, void* stream, bool clear_status) {
+                         const kvq_decode_options* options, void* stream, bool clear_status,
+                         const int32_t* bt_row = nullptr) {
   kvq_status st = check_layout(layout);
   if (st != KVQ_OK) return st;
-  if (!kind_ok(kind)) return KVQ_EKIND;
+  if (!kind_read_ok(kind)) return KVQ_EKIND;
+  if (!has_scales(kind)) scales = nullptr;
   if (out_dtype != KVQ_OUT_BF16 && out_dtype != KVQ_OUT_F32) return KVQ_EINVAL;
   if (batch < 0 || num_q_heads <= 0 || max_pages_per_seq <= 0) return KVQ_EINVAL;
   if (num_q_heads % layout->num_kv_heads != 0) return KVQ_EINVAL;
@@ -161,7 +169,8 @@ kvq_status decode_common(const void* q, const void* pool, const void* scales, co
   if (!plan_workspace(*layout, batch, num_q_heads, max_pages_per_seq, options, &w)) return KVQ_EINVAL;
   if (w.path < 0) return KVQ_EUNSUPPORTED;
   if (batch == 0) return KVQ_OK;
-  if (!q || !pool || !scales || !block_table || !seq_lens || !out || !workspace) return KVQ_EINVAL;
+  if (!q || !pool || (has_scales(kind) && !scales) || !block_table || !seq_lens || !out || !workspace)
+    return KVQ_EINVAL;
   if (workspace_bytes < w.total) return KVQ_EWORKSPACE;
   if (!aligned(q) || !aligned(pool) || !aligned(scales) || !aligned(out) || !aligned(workspace) ||
       (reinterpret_cast<uintptr_t>(block_table) % 4) != 0 || (reinterpret_cast<uintptr_t>(seq_lens) % 4) != 0)
@@ -174,6 +183,7 @@ kvq_status decode_common(const void* q, const void* pool, const void* scales, co
   a.codes = static_cast<const uint8_t*>(pool);
   a.scales = static_cast<const uint16_t*>(scales);
   a.block_table = block_table;
+  a.bt_row = bt_row;
   a.num_pages = layout->num_pages;
   a.max_pages = max_pages_per_seq;
   a.seq_lens = seq_lens;
@@ -241,6 +251,73 @@ bool plan_sparse(const kvq_layout* layout, int32_t batch, int32_t num_q_heads, i
   return true;
 }
 
+// MLA extend: every new token is a sequence of its own (its causal prefix, the block-table row of the sequence
+// it belongs to), decoded in chunks of at most kExtendMlaChunk tokens by the MLA decode kernels.  Workspace:
+// the decode workspace of one chunk (its status word at offset 0 is the call's), then the per-token
+// prefix lengths and block-table rows.
+constexpr int32_t kExtendMlaChunk = 1024;
+
+struct ExtendMlaPlan {
+  int32_t chunk;
+  size_t dense_bytes, lens_offset, rows_offset, total;
+};
+
+bool plan_extend_mla(const kvq_layout& L, int32_t total_q, int32_t num_q_heads, int32_t max_pages,
+                     ExtendMlaPlan* ep) {
+  ep->chunk = std::max<int32_t>(1, std::min<int32_t>(total_q, kExtendMlaChunk));
+  WorkspacePlan w;
+  if (!plan_workspace(L, ep->chunk, num_q_heads, max_pages, nullptr, &w) || w.path < 0) return false;
+  auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+  const size_t n = static_cast<size_t>(std::max<int32_t>(total_q, 1)) * sizeof(int32_t);
+  ep->dense_bytes = up(w.total);
+  ep->lens_offset = ep->dense_bytes;
+  ep->rows_offset = ep->lens_offset + up(n);
+  ep->total = ep->rows_offset + up(n);
+  return true;
+}
+
+kvq_status extend_mla(const void* q, const void* pool, const void* scales, const int32_t* block_table,
+                      int32_t max_pages_per_seq, const int32_t* seq_lens, const int32_t* q_start, int32_t total_q,
+                      int32_t batch, int32_t num_q_heads, float sm_scale, void* out, kvq_out_dtype out_dtype,
+                      void* workspace, size_t workspace_bytes, const kvq_layout* layout, kvq_kind kind,
+                      void* stream) {
+  if (!decode_cc_supported(layout->head_dim, layout->v_dim, layout->mla)) return KVQ_EUNSUPPORTED;
+  if (batch > kMaxExtendBatch) return KVQ_EUNSUPPORTED;
+  ExtendMlaPlan ep;
+  if (!plan_extend_mla(*layout, total_q, num_q_heads, max_pages_per_seq, &ep)) return KVQ_EUNSUPPORTED;
+  if (!workspace) return KVQ_EINVAL;
+  if (workspace_bytes < ep.total) return KVQ_EWORKSPACE;
+  if (!aligned(workspace)) return KVQ_EALIGN;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  if (cudaMemsetAsync(ws, 0, sizeof(uint32_t), s) != cudaSuccess) return KVQ_ECUDA;
+  if (batch == 0 || total_q == 0) return KVQ_OK;
+  if (!q || !pool || (has_scales(kind) && !scales) || !block_table || !seq_lens || !q_start || !out)
+    return KVQ_EINVAL;
+  if (!aligned(q) || !aligned(pool) || !aligned(scales) || !aligned(out) ||
+      (reinterpret_cast<uintptr_t>(block_table) % 4) != 0 || (reinterpret_cast<uintptr_t>(seq_lens) % 4) != 0 ||
+      (reinterpret_cast<uintptr_t>(q_start) % 4) != 0)
+    return KVQ_EALIGN;
+  kvq_status st = kvq_device_check();
+  if (st != KVQ_OK) return st;
+  int32_t* vlens = reinterpret_cast<int32_t*>(ws + ep.lens_offset);
+  int32_t* vrow = reinterpret_cast<int32_t*>(ws + ep.rows_offset);
+  // rows no sequence covers (an inconsistent q_start) keep length 0: zeros out
+  if (cudaMemsetAsync(ws + ep.lens_offset, 0, ep.total - ep.lens_offset, s) != cudaSuccess) return KVQ_ECUDA;
+  st = launch_extend_expand(q_start, seq_lens, batch, total_q, vlens, vrow, reinterpret_cast<uint32_t*>(ws), s);
+  if (st != KVQ_OK) return st;
+  const size_t q_row = static_cast<size_t>(num_q_heads) * layout->head_dim * 2;
+  const size_t o_row = static_cast<size_t>(num_q_heads) * layout->v_dim * (out_dtype == KVQ_OUT_F32 ? 4 : 2);
+  for (int32_t c0 = 0; c0 < total_q; c0 += ep.chunk) {
+    const int32_t n = std::min<int32_t>(ep.chunk, total_q - c0);
+    st = decode_common(static_cast<const uint8_t*>(q) + c0 * q_row, pool, scales, block_table, max_pages_per_seq,
+                       vlens + c0, n, num_q_heads, sm_scale, static_cast<uint8_t*>(out) + c0 * o_row, out_dtype,
+                       workspace, ep.dense_bytes, layout, kind, nullptr, stream, false, vrow + c0);
+    if (st != KVQ_OK) return st;
+  }
+  return KVQ_OK;
+}
+
 }  // namespace
 
 
@@ -252,7 +329,9 @@ const char* kvq_strerror(kvq_status s) {
   switch (s) {
     case KVQ_OK: return "ok";
     case KVQ_EINVAL: return "invalid argument";
-    case KVQ_EKIND: return "unknown quantization kind (expected KVQ_FP8_E4M3 or KVQ_Q8_0)";
+    case KVQ_EKIND:
+      return "quantization kind not accepted by this call (the block-scaled stores take KVQ_FP8_E4M3 or KVQ_Q8_0; "
+             "kvq_store_unscaled the unscaled kinds; the attention calls all four)";
     case KVQ_EHEADDIM: return "head_dim and v_dim must be positive multiples of 32 (the quantization block)";
     case KVQ_EALIGN: return "device pointers must be 16-byte aligned";
     case KVQ_EWORKSPACE: return "workspace smaller than kvq_decode_workspace_bytes()";
@@ -285,6 +364,20 @@ int64_t kvq_num_pages(const kvq_layout* layout, size_t budget_bytes) {
   const uint64_t elems_per_page =
       static_cast<uint64_t>(n_kv_of(*layout)) * layout->num_kv_heads * layout->page_size * layout->head_dim;
   const uint64_t bytes_per_page = elems_per_page + elems_per_page / 32 * 2;
+  return static_cast<int64_t>(budget_bytes / bytes_per_page);
+}
+
+double kvq_bytes_per_token_ex(const kvq_layout* layout, kvq_kind kind) {
+  if (check_layout(layout) != KVQ_OK || !kind_read_ok(kind)) return -1.0;
+  if (has_scales(kind)) return kvq_bytes_per_token(layout);
+  return static_cast<double>(n_kv_of(*layout)) * layout->num_kv_heads * layout->head_dim;
+}
+
+int64_t kvq_num_pages_ex(const kvq_layout* layout, kvq_kind kind, size_t budget_bytes) {
+  if (check_layout(layout) != KVQ_OK || !kind_read_ok(kind)) return -1;
+  if (has_scales(kind)) return kvq_num_pages(layout, budget_bytes);
+  const uint64_t bytes_per_page =
+      static_cast<uint64_t>(n_kv_of(*layout)) * layout->num_kv_heads * layout->page_size * layout->head_dim;
   return static_cast<int64_t>(budget_bytes / bytes_per_page);
 }
 
@@ -369,14 +462,16 @@ kvq_status kvq_decode_sparse(const void* q, const void* pool, const void* scales
                              void* stream) {
   kvq_status st = check_layout(layout);
   if (st != KVQ_OK) return st;
-  if (!kind_ok(kind)) return KVQ_EKIND;
+  if (!kind_read_ok(kind)) return KVQ_EKIND;
+  if (!has_scales(kind)) scales = nullptr;
   if (out_dtype != KVQ_OUT_BF16 && out_dtype != KVQ_OUT_F32) return KVQ_EINVAL;
   if (max_pages_per_seq <= 0) return KVQ_EINVAL;
   SparsePlan sp;
   if (!plan_sparse(layout, batch, num_q_heads, topk, &sp)) return KVQ_EINVAL;
   if (layout->page_size != kPageTokens || layout->head_dim % 64 != 0) return KVQ_EUNSUPPORTED;
   if (batch == 0) return KVQ_OK;
-  if (!q || !pool || !scales || !block_table || !seq_lens || (topk > 0 && !indices) || !out || !workspace)
+  if (!q || !pool || (has_scales(kind) && !scales) || !block_table || !seq_lens || (topk > 0 && !indices) || !out ||
+      !workspace)
     return KVQ_EINVAL;
   if (workspace_bytes < sp.total) return KVQ_EWORKSPACE;
   if (!aligned(pool) || !aligned(scales) || !aligned(workspace) || (reinterpret_cast<uintptr_t>(block_table) % 4) != 0 ||
@@ -394,7 +489,7 @@ kvq_status kvq_decode_sparse(const void* q, const void* pool, const void* scales
   g.seq_lens = seq_lens;
   g.indices = indices;
   g.dst_codes = ws + sp.codes_offset;
-  g.dst_scales = reinterpret_cast<uint16_t*>(ws + sp.scales_offset);
+  g.dst_scales = has_scales(kind) ? reinterpret_cast<uint16_t*>(ws + sp.scales_offset) : nullptr;
   g.dst_table = reinterpret_cast<int32_t*>(ws + sp.table_offset);
   g.dst_lens = reinterpret_cast<int32_t*>(ws + sp.lens_offset);
   g.status = reinterpret_cast<uint32_t*>(ws);
@@ -414,13 +509,24 @@ kvq_status kvq_decode_sparse(const void* q, const void* pool, const void* scales
 
 size_t kvq_extend_workspace_bytes(void) { return kWorkspaceHeader; }
 
+size_t kvq_extend_workspace_bytes_ex(const kvq_layout* layout, int32_t total_q, int32_t num_q_heads,
+                                     int32_t max_pages_per_seq) {
+  if (check_layout(layout) != KVQ_OK || total_q < 0 || num_q_heads <= 0 || max_pages_per_seq <= 0) return 0;
+  if (num_q_heads % layout->num_kv_heads != 0) return 0;
+  if (!layout->mla) return kWorkspaceHeader;
+  ExtendMlaPlan ep;
+  if (!plan_extend_mla(*layout, total_q, num_q_heads, max_pages_per_seq, &ep)) return 0;
+  return ep.total;
+}
+
 kvq_status kvq_extend(const void* q, const void* pool, const void* scales, const int32_t* block_table,
                       int32_t max_pages_per_seq, const int32_t* seq_lens, const int32_t* q_start, int32_t total_q,
                       int32_t batch, int32_t num_q_heads, float sm_scale, void* out, kvq_out_dtype out_dtype,
                       void* workspace, size_t workspace_bytes, const kvq_layout* layout, kvq_kind kind, void* stream) {
   kvq_status st = check_layout(layout);
   if (st != KVQ_OK) return st;
-  if (!kind_ok(kind)) return KVQ_EKIND;
+  if (!kind_read_ok(kind)) return KVQ_EKIND;
+  if (!has_scales(kind)) scales = nullptr;
   if (out_dtype != KVQ_OUT_BF16 && out_dtype != KVQ_OUT_F32) return KVQ_EINVAL;
   if (batch < 0 || total_q < 0 || num_q_heads <= 0 || max_pages_per_seq <= 0) return KVQ_EINVAL;
   if (num_q_heads % layout->num_kv_heads != 0) return KVQ_EINVAL;
@@ -428,6 +534,9 @@ kvq_status kvq_extend(const void* q, const void* pool, const void* scales, const
     return KVQ_EINVAL;  // the kernel counts query rows per sequence in 32 bits
   if (!(sm_scale > 0.0f) || sm_scale > std::numeric_limits<float>::max()) return KVQ_EINVAL;  // finite, > 0
   if (layout->page_size != kPageTokens) return KVQ_EUNSUPPORTED;
+  if (layout->mla)
+    return extend_mla(q, pool, scales, block_table, max_pages_per_seq, seq_lens, q_start, total_q, batch, num_q_heads,
+                      sm_scale, out, out_dtype, workspace, workspace_bytes, layout, kind, stream);
   if (!extend_tc_supported(layout->head_dim, layout->v_dim, layout->mla, num_q_heads / layout->num_kv_heads, batch))
     return KVQ_EUNSUPPORTED;
   if (!workspace) return KVQ_EINVAL;
@@ -436,7 +545,8 @@ kvq_status kvq_extend(const void* q, const void* pool, const void* scales, const
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (cudaMemsetAsync(workspace, 0, sizeof(uint32_t), s) != cudaSuccess) return KVQ_ECUDA;
   if (batch == 0 || total_q == 0) return KVQ_OK;
-  if (!q || !pool || !scales || !block_table || !seq_lens || !q_start || !out) return KVQ_EINVAL;
+  if (!q || !pool || (has_scales(kind) && !scales) || !block_table || !seq_lens || !q_start || !out)
+    return KVQ_EINVAL;
   if (!aligned(q) || !aligned(pool) || !aligned(scales) || !aligned(out) ||
       (reinterpret_cast<uintptr_t>(block_table) % 4) != 0 || (reinterpret_cast<uintptr_t>(seq_lens) % 4) != 0 ||
       (reinterpret_cast<uintptr_t>(q_start) % 4) != 0)
@@ -498,14 +608,25 @@ kvq_status kvq_quantize_probe(kvq_kind kind, const uint16_t* x, int64_t nx, cons
 
 kvq_status kvq_dequant_probe(kvq_kind kind, const uint8_t* codes, const uint16_t* scales, uint16_t* out, int64_t n,
                              void* stream) {
-  if (!kind_ok(kind)) return KVQ_EKIND;
+  if (!kind_read_ok(kind)) return KVQ_EKIND;
+  if (!has_scales(kind)) scales = nullptr;
   if (n < 0 || n % 16 != 0) return KVQ_EINVAL;
   if (n == 0) return KVQ_OK;
-  if (!codes || !scales || !out) return KVQ_EINVAL;
+  if (!codes || (has_scales(kind) && !scales) || !out) return KVQ_EINVAL;
   if (!aligned(codes) || !aligned(out)) return KVQ_EALIGN;
   kvq_status st = kvq_device_check();
   if (st != KVQ_OK) return st;
   return launch_dequant_probe(kind, codes, scales, out, n, static_cast<cudaStream_t>(stream));
+}
+
+kvq_status kvq_exp2_probe(const float* x, float* y, int64_t n, void* stream) {
+  if (n < 0) return KVQ_EINVAL;
+  if (n == 0) return KVQ_OK;
+  if (!x || !y) return KVQ_EINVAL;
+  if ((reinterpret_cast<uintptr_t>(x) % 4) != 0 || (reinterpret_cast<uintptr_t>(y) % 4) != 0) return KVQ_EALIGN;
+  const kvq_status st = kvq_device_check();
+  if (st != KVQ_OK) return st;
+  return launch_exp2_probe(x, y, n, static_cast<cudaStream_t>(stream));
 }
 
 kvq_status kvq_wait_probe(void* workspace, void* stream) {

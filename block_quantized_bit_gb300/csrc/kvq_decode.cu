@@ -57,7 +57,7 @@ struct CCConfig {
   using G = RowGeom<D>;
   static constexpr int NKV = MLA ? 1 : 2;
   static constexpr int CODE_BYTES = kPage * D;           // one page of one head
-  static constexpr int SCALE_BYTES = kPage * G::NB * 2;
+  static constexpr int SCALE_BYTES = KindTraits<KIND>::kScaled ? kPage * G::NB * 2 : 0;  // none when unscaled
   static constexpr int STAGE_BYTES = NKV * (CODE_BYTES + SCALE_BYTES);
   static constexpr int PIPE_BYTES = WARPS * STAGES * STAGE_BYTES;
   static constexpr int COMBINE_BYTES = WARPS * GT * (DV + 2) * 4;
@@ -196,7 +196,7 @@ __global__ void __launch_bounds__(WARPS * 32, MINB) decode_cc_kernel(KParams p) 
     const int s = i % STAGES;
     if (lane == 0) {
       const int32_t pg = pg0 + warp + i * WARPS;
-      int32_t phys = __ldg(p.block_table + static_cast<int64_t>(b) * p.max_pages + pg);
+      int32_t phys = bt_entry(p, b, pg);
       if (phys >= p.num_pages) {  // out-of-range page: never dereferenced, reported in the status word
         set_status(p.status, kStatusBadPage);
         phys = -1;
@@ -209,8 +209,9 @@ __global__ void __launch_bounds__(WARPS * 32, MINB) decode_cc_kernel(KParams p) 
         for (int kv = 0; kv < Cfg::NKV; ++kv) {
           const int64_t row = (static_cast<int64_t>(phys) * Cfg::NKV + kv) * p.num_kv_heads + g;
           bulk_g2s(dst + kv * Cfg::CODE_BYTES, p.codes + row * head_chunk, Cfg::CODE_BYTES, &wbar[s]);
-          bulk_g2s(dst + Cfg::NKV * Cfg::CODE_BYTES + kv * Cfg::SCALE_BYTES, p.scales + row * head_scale,
-                   Cfg::SCALE_BYTES, &wbar[s]);
+          if (KindTraits<KIND>::kScaled)
+            bulk_g2s(dst + Cfg::NKV * Cfg::CODE_BYTES + kv * Cfg::SCALE_BYTES, p.scales + row * head_scale,
+                     Cfg::SCALE_BYTES, &wbar[s]);
         }
       } else {
         asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(&wbar[s])) : "memory");
@@ -254,7 +255,7 @@ __global__ void __launch_bounds__(WARPS * 32, MINB) decode_cc_kernel(KParams p) 
           if (c < NCH) {
             const uint4 code = *reinterpret_cast<const uint4*>(kc + t * D + c * 16);
             uint32_t kd[8];
-            dequant16<KIND>(code, ks[t * NB + (c >> 1)], kd);
+            dequant16<KIND>(code, KindTraits<KIND>::kScaled ? ks[t * NB + (c >> 1)] : kHalfOne, kd);
 #pragma unroll
             for (int e = 0; e < 8; ++e)
 #pragma unroll
@@ -312,7 +313,7 @@ __global__ void __launch_bounds__(WARPS * 32, MINB) decode_cc_kernel(KParams p) 
           if (c * 16 < DV) {
             const uint4 code = *reinterpret_cast<const uint4*>(vc + t * D + c * 16);
             uint32_t vd[8];
-            dequant16<KIND>(code, vs[t * NB + (c >> 1)], vd);
+            dequant16<KIND>(code, KindTraits<KIND>::kScaled ? vs[t * NB + (c >> 1)] : kHalfOne, vd);
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
               const float2 v2 = unpack_bf16x2(vd[e]);
@@ -579,7 +580,7 @@ __global__ void dequant_probe_kernel(const uint8_t* __restrict__ codes, const ui
   for (int64_t c = i; c < nchunks; c += stride) {
     const uint4 code = reinterpret_cast<const uint4*>(codes)[c];
     uint32_t kd[8];
-    dequant16<KIND>(code, scales[c], kd);
+    dequant16<KIND>(code, KindTraits<KIND>::kScaled ? scales[c] : kHalfOne, kd);
     uint4* dst = reinterpret_cast<uint4*>(out + c * 16);
     dst[0] = make_uint4(kd[0], kd[1], kd[2], kd[3]);
     dst[1] = make_uint4(kd[4], kd[5], kd[6], kd[7]);
@@ -601,8 +602,13 @@ kvq_status launch_cc(const DecodeArgs& a, cudaStream_t stream) {
 
 template <int D, int DV, int GT, bool MLA, int STAGES, int MINB>
 kvq_status launch_cc_kind(const DecodeArgs& a, cudaStream_t stream) {
-  if (a.kind == KVQ_FP8_E4M3) return launch_cc<D, DV, GT, KVQ_FP8_E4M3, MLA, STAGES, MINB>(a, stream);
-  return launch_cc<D, DV, GT, KVQ_Q8_0, MLA, STAGES, MINB>(a, stream);
+  switch (a.kind) {
+    case KVQ_FP8_E4M3: return launch_cc<D, DV, GT, KVQ_FP8_E4M3, MLA, STAGES, MINB>(a, stream);
+    case KVQ_Q8_0: return launch_cc<D, DV, GT, KVQ_Q8_0, MLA, STAGES, MINB>(a, stream);
+    case KVQ_FP8_E4M3_UNSCALED: return launch_cc<D, DV, GT, KVQ_FP8_E4M3_UNSCALED, MLA, STAGES, MINB>(a, stream);
+    case KVQ_FP8_E5M2_UNSCALED: return launch_cc<D, DV, GT, KVQ_FP8_E5M2_UNSCALED, MLA, STAGES, MINB>(a, stream);
+  }
+  return KVQ_EKIND;
 }
 
 }  // namespace
@@ -686,11 +692,17 @@ kvq_status launch_dequant_probe(kvq_kind kind, const uint8_t* codes, const uint1
   if (nchunks == 0) return KVQ_OK;
   const int threads = 256;
   const int64_t grid = std::min<int64_t>((nchunks + threads - 1) / threads, 152 * 16);
-  if (kind == KVQ_FP8_E4M3)
-    dequant_probe_kernel<KVQ_FP8_E4M3><<<static_cast<unsigned>(grid), threads, 0, stream>>>(codes, scales, out,
-                                                                                           nchunks);
-  else
-    dequant_probe_kernel<KVQ_Q8_0><<<static_cast<unsigned>(grid), threads, 0, stream>>>(codes, scales, out, nchunks);
+  const unsigned g = static_cast<unsigned>(grid);
+  switch (kind) {
+    case KVQ_FP8_E4M3: dequant_probe_kernel<KVQ_FP8_E4M3><<<g, threads, 0, stream>>>(codes, scales, out, nchunks); break;
+    case KVQ_Q8_0: dequant_probe_kernel<KVQ_Q8_0><<<g, threads, 0, stream>>>(codes, scales, out, nchunks); break;
+    case KVQ_FP8_E4M3_UNSCALED:
+      dequant_probe_kernel<KVQ_FP8_E4M3_UNSCALED><<<g, threads, 0, stream>>>(codes, scales, out, nchunks);
+      break;
+    case KVQ_FP8_E5M2_UNSCALED:
+      dequant_probe_kernel<KVQ_FP8_E5M2_UNSCALED><<<g, threads, 0, stream>>>(codes, scales, out, nchunks);
+      break;
+  }
   return cudaGetLastError() == cudaSuccess ? KVQ_OK : KVQ_ECUDA;
 }
 

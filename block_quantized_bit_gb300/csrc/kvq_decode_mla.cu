@@ -238,7 +238,7 @@ __device__ __forceinline__ int32_t mla_phys(const KParams& p, const MlaIter& t, 
   if (!t.live) return -1;
   const int32_t pg = t.pg0 + t.i * mla::kPagesPerTile + pi;
   if (pg >= t.pg1 || pg * kPage + off >= t.L) return -1;
-  const int32_t e = __ldg(p.block_table + static_cast<int64_t>(t.b) * p.max_pages + pg);
+  const int32_t e = bt_entry(p, t.b, pg);
   return (e >= 0 && e < p.num_pages) ? e : -1;
 }
 
@@ -331,7 +331,7 @@ __global__ void __launch_bounds__(mla::kThreads, 1) decode_mla_kernel(const KPar
       if (lane < kPagesPerTile) {
         const int32_t pg = t.pg0 + t.i * kPagesPerTile + lane;
         if (pg < t.pg1) {
-          phys = __ldg(p.block_table + static_cast<int64_t>(t.b) * p.max_pages + pg);
+          phys = bt_entry(p, t.b, pg);
           if (phys >= p.num_pages) {
             set_status(p.status, kStatusBadPage);
             phys = -1;
@@ -353,12 +353,12 @@ __global__ void __launch_bounds__(mla::kThreads, 1) decode_mla_kernel(const KPar
         if (lane == 0) {
 #pragma unroll
           for (int i = 0; i < kPagesPerTile; ++i) sMeta[rs * kPagesPerTile + i] = nv[i];
-          mbar_arrive_expect_tx(&bar_full[rs], npg * (kBox + (j == 0 ? kScPage : 0)));
+          mbar_arrive_expect_tx(&bar_full[rs], npg * (kBox + (j == 0 && KindTraits<KIND>::kScaled ? kScPage : 0)));
         }
         __syncwarp();
         if (phys >= 0) {
           mla_tma(smem_u32(sRing + rs * kSlab + lane * kBox), &tmap, j < 4 ? 128 * j : 448, phys, &bar_full[rs]);
-          if (j == 0)
+          if (j == 0 && KindTraits<KIND>::kScaled)  // an unscaled pool has codes only
             bulk_g2s(sSc + (n & 1) * kScTile + lane * kScPage,
                      reinterpret_cast<const uint8_t*>(p.scales) + static_cast<int64_t>(phys) * kScPage, kScPage,
                      &bar_full[rs]);
@@ -425,7 +425,8 @@ __global__ void __launch_bounds__(mla::kThreads, 1) decode_mla_kernel(const KPar
             const int c = 2 * c2 + h;
             if (v_ok) {
               uint32_t ww[8];
-              dequant16<KIND>(*reinterpret_cast<const uint4*>(slot + ((c ^ swz) * 16)), sc[blk], ww);
+              dequant16<KIND>(*reinterpret_cast<const uint4*>(slot + ((c ^ swz) * 16)),
+                              KindTraits<KIND>::kScaled ? sc[blk] : kHalfOne, ww);
 #pragma unroll
               for (int e = 0; e < 8; ++e) w[8 * h + e] = ww[e];
             } else {
@@ -468,7 +469,8 @@ __global__ void __launch_bounds__(mla::kThreads, 1) decode_mla_kernel(const KPar
 #pragma unroll
       for (int k = 0; k < 4; ++k) nxt[k] = __ldg(src + k);
       // a row's scales start 36 bytes apart: a 4-byte load is always aligned
-      nxt_s = __ldg(reinterpret_cast<const uint32_t*>(reinterpret_cast<const uint16_t*>(p.scales) + row * kNB + c * 4 +
+      if (KindTraits<KIND>::kScaled)
+        nxt_s = __ldg(reinterpret_cast<const uint32_t*>(reinterpret_cast<const uint16_t*>(p.scales) + row * kNB + c * 4 +
                                                       part * 2));
     };
     int32_t phys = mla_phys(p, t, pi, off);
@@ -817,7 +819,14 @@ bool decode_mla_tc_supported(int32_t head_dim, int32_t v_dim, int32_t is_mla, in
 }
 
 kvq_status launch_decode_mla_tc(const DecodeArgs& a, cudaStream_t stream) {
-  auto kern = (a.kind == KVQ_FP8_E4M3) ? decode_mla_kernel<KVQ_FP8_E4M3> : decode_mla_kernel<KVQ_Q8_0>;
+  decltype(&decode_mla_kernel<KVQ_FP8_E4M3>) kern = nullptr;
+  switch (a.kind) {
+    case KVQ_FP8_E4M3: kern = decode_mla_kernel<KVQ_FP8_E4M3>; break;
+    case KVQ_Q8_0: kern = decode_mla_kernel<KVQ_Q8_0>; break;
+    case KVQ_FP8_E4M3_UNSCALED: kern = decode_mla_kernel<KVQ_FP8_E4M3_UNSCALED>; break;
+    case KVQ_FP8_E5M2_UNSCALED: kern = decode_mla_kernel<KVQ_FP8_E5M2_UNSCALED>; break;
+  }
+  if (kern == nullptr) return KVQ_EKIND;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, mla::SMEM_BYTES) != cudaSuccess)
     return KVQ_ECUDA;
   CUtensorMap map;

@@ -56,7 +56,7 @@ constexpr int kN = 16;            // MMA N: query heads, padded
 constexpr int kSmWarps = 4;
 constexpr int kDwWarps = 16;
 constexpr int kMmaWarp = kSmWarps + kDwWarps;          // warp 20
-constexpr int kProdWarp = kMmaWarp + 1;                // warps 13 (K ring) and 14 (V ring)
+constexpr int kProdWarp = kMmaWarp + 1;                // warps 21 (K ring) and 22 (V ring)
 constexpr int kThreads = (kProdWarp + 2) * 32;         // 23 warps
 constexpr int kDwThreads = kDwWarps * 32;
 constexpr int kMaxPlanBatch = 2048;   // sequences whose item bases fit the shared table
@@ -266,7 +266,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const KParams p,
 
   if (warp >= kProdWarp) {
     // ===================================================================== producers
-    // Warp 13 fills the K ring, warp 14 the V ring, each running ahead on its own ring.  Lane pi (< 8)
+    // Warp 21 fills the K ring, warp 22 the V ring, each running ahead on its own ring.  Lane pi (< 8)
     // owns page pi of a tile: block-table entry (requested one tile ahead), valid tokens, its copies.
     const int kv = warp - kProdWarp;
     uint8_t* ring_base = kv ? sVr : sKr;
@@ -275,7 +275,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const KParams p,
     auto page_entry = [&](const TileIter& ti) -> int32_t {
       if (!ti.live || lane >= kPagesPerTile) return -1;
       const int32_t pg = ti.pg0 + ti.i * kPagesPerTile + lane;
-      return pg < ti.pg1 ? __ldg(p.block_table + static_cast<int64_t>(ti.b) * p.max_pages + pg) : -1;
+      return pg < ti.pg1 ? bt_entry(p, ti.b, pg) : -1;
     };
     uint32_t n = 0;              // tiles issued
     int32_t bt = page_entry(t);  // block-table entry of tile n
@@ -293,8 +293,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const KParams p,
       const int ring = kv * Cfg::STAGES + sl;
       const uint32_t use = n / Cfg::STAGES;
       if (use > 0 && !mbar_wait_bounded(&bar_empty[ring], (use - 1) & 1)) { ok = false; break; }
-      const uint32_t bytes =
-          __reduce_add_sync(0xffffffffu, phys >= 0 ? static_cast<uint32_t>(Cfg::NSL * kBox + Cfg::SC_KV) : 0u);
+      constexpr uint32_t kPageBytes = Cfg::NSL * kBox + (KindTraits<KIND>::kScaled ? Cfg::SC_KV : 0);
+      const uint32_t bytes = __reduce_add_sync(0xffffffffu, phys >= 0 ? kPageBytes : 0u);
       int32_t nv[kPagesPerTile];
 #pragma unroll
       for (int i = 0; i < kPagesPerTile; ++i) nv[i] = __shfl_sync(0xffffffffu, nvalid, i);
@@ -310,9 +310,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const KParams p,
         for (int c = 0; c < Cfg::NSL; ++c)
           tma_load_codes(smem_u32(slot + (lane * Cfg::NSL + c) * kBox), &tmap, c, t.g * kPage, kv, phys,
                          &bar_full[ring]);
-        const uint8_t* src = reinterpret_cast<const uint8_t*>(p.scales) +
-                             ((static_cast<int64_t>(phys) * 2 + kv) * p.num_kv_heads + t.g) * Cfg::SC_KV;
-        bulk_g2s(slot + Cfg::SL_SC + lane * Cfg::SC_KV, src, Cfg::SC_KV, &bar_full[ring]);
+        if (KindTraits<KIND>::kScaled) {  // an unscaled pool has codes only
+          const uint8_t* src = reinterpret_cast<const uint8_t*>(p.scales) +
+                               ((static_cast<int64_t>(phys) * 2 + kv) * p.num_kv_heads + t.g) * Cfg::SC_KV;
+          bulk_g2s(slot + Cfg::SL_SC + lane * Cfg::SC_KV, src, Cfg::SC_KV, &bar_full[ring]);
+        }
       }
       t = nx;
       ++n;
@@ -368,7 +370,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const KParams p,
         if (!mbar_wait_bounded(&bar_full[ring], (nk / Cfg::STAGES) & 1)) { ok = false; break; }
         const uint8_t* slot = sKr + ring * Cfg::SLOT_BYTES;
         const bool v_ok = off < sMeta[ring * kPagesPerTile + pi];
-        const uint64_t scw = load_scales<Cfg::NBT>(slot + sc_off);
+        const uint64_t scw = KindTraits<KIND>::kScaled ? load_scales<Cfg::NBT>(slot + sc_off) : 0u;
         // the buffer was last read by the QK of tile nk - 2
         if (nk >= 2 && !mbar_wait_bounded(&bar_qk_done[kb], ((nk >> 1) - 1) & 1)) { ok = false; break; }
         if (tk.i == 0) {
@@ -431,7 +433,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const KParams p,
         if (!mbar_wait_bounded(&bar_full[ring], (nv / Cfg::STAGES) & 1)) { ok = false; break; }
         const uint8_t* slot = sVr + (nv % Cfg::STAGES) * Cfg::SLOT_BYTES;
         const bool v_ok = off < sMeta[ring * kPagesPerTile + pi];
-        const uint64_t scw = load_scales<Cfg::NBT>(slot + sc_off);
+        const uint64_t scw = KindTraits<KIND>::kScaled ? load_scales<Cfg::NBT>(slot + sc_off) : 0u;
         // the previous PV must have read this thread's rows of the V tile (with two O^T slices, a part
         // that writes dims of slice 0 only waits for the first half of the PV)
         if (nv >= 1) {
@@ -552,8 +554,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const KParams p,
       const uint32_t ob = tO + item_obuf(pend_item) * 32;
 #pragma unroll
       for (int oc = 0; oc < Cfg::O_CHUNKS; ++oc) {
-        float o[16];
-        tmem_ld16(ob + oc * kN + lane_base, o);
+        float o[GN];  // the padding heads' columns are not read
+        tmem_ld_cols<GN>(ob + oc * kN + lane_base, o);
         const int d = oc * 128 + tt;
 #pragma unroll
         for (int h = 0; h < GN; ++h)
@@ -583,8 +585,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const KParams p,
         if (!mbar_wait_bounded(&bar_k_full[b], (gtile >> 1) & 1)) { ok = false; break; }
         tc_fence_after();
         const bool valid = sValid[b * kTile + tt] != 0;
-        float s[16];
-        tmem_ld16(tS + b * kN + lane_base, s);
+        float s[GN];
+        tmem_ld_cols<GN>(tS + b * kN + lane_base, s);
         bool moved = false;
 #pragma unroll
         for (int h = 0; h < GN; ++h) {
@@ -647,11 +649,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const KParams p,
           tc_fence_after();
 #pragma unroll
           for (int oc = 0; oc < Cfg::O_CHUNKS; ++oc) {
-            float o[16];
-            tmem_ld16(ob + oc * kN + lane_base, o);
+            float o[GN];
+            tmem_ld_cols<GN>(ob + oc * kN + lane_base, o);
 #pragma unroll
             for (int h = 0; h < GN; ++h) o[h] *= alpha[h];
-            tmem_st16(ob + oc * kN + lane_base, o);
+            tmem_st_cols<GN>(ob + oc * kN + lane_base, o);
           }
         }
         uint8_t* pb = sP + b * Cfg::P_BYTES;
@@ -705,8 +707,17 @@ template <int D>
 kvq_status launch_tc_d(const DecodeArgs& a, cudaStream_t stream) {
   using Cfg = TcCfg<D>;
   const bool g16 = (a.num_q_heads / a.num_kv_heads) > 8;
-  auto kern = (a.kind == KVQ_FP8_E4M3) ? (g16 ? decode_tc_kernel<D, KVQ_FP8_E4M3, 16> : decode_tc_kernel<D, KVQ_FP8_E4M3, 8>)
-                                       : (g16 ? decode_tc_kernel<D, KVQ_Q8_0, 16> : decode_tc_kernel<D, KVQ_Q8_0, 8>);
+  decltype(&decode_tc_kernel<D, KVQ_FP8_E4M3, 8>) kern = nullptr;
+  switch (a.kind) {
+#define KVQ_TC_KIND(K) \
+  case K: kern = g16 ? decode_tc_kernel<D, K, 16> : decode_tc_kernel<D, K, 8>; break;
+    KVQ_TC_KIND(KVQ_FP8_E4M3)
+    KVQ_TC_KIND(KVQ_Q8_0)
+    KVQ_TC_KIND(KVQ_FP8_E4M3_UNSCALED)
+    KVQ_TC_KIND(KVQ_FP8_E5M2_UNSCALED)
+#undef KVQ_TC_KIND
+  }
+  if (kern == nullptr) return KVQ_EKIND;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES) != cudaSuccess)
     return KVQ_ECUDA;
   CUtensorMap map;

@@ -171,22 +171,38 @@ __device__ __forceinline__ float2 unpack_bf16x2(uint32_t v) {
 __device__ __forceinline__ uint16_t lo16(uint32_t v) { return static_cast<uint16_t>(v & 0xFFFFu); }
 __device__ __forceinline__ uint16_t hi16(uint32_t v) { return static_cast<uint16_t>(v >> 16); }
 
+// Kinds with one fp16 scale per 32 elements (a scale array beside the codes); the unscaled kinds
+// ("Add fp8 KV-cache quantization (--kv-dtype)", section "How it works": the plain fp8 cast, scale 1.0)
+// have codes only.
+template <int KIND>
+struct KindTraits {
+  static constexpr bool kScaled = (KIND == KVQ_FP8_E4M3 || KIND == KVQ_Q8_0);
+};
+
+// fp16 bits of 1.0: the scale of every element of an unscaled pool.
+constexpr uint16_t kHalfOne = 0x3C00u;
+
 // Addend that completes step 2 for a block with fp16 scale bits s_bits.
 template <int KIND>
 __device__ __forceinline__ float dequant_addend(uint16_t s_bits) {
-  if (KIND == KVQ_FP8_E4M3) return -0.0f;
+  if (KIND != KVQ_Q8_0) return -0.0f;
   return -1152.0f * __half2float(__ushort_as_half(s_bits));
 }
 
 // Exact f16 values of the four codes of a 32-bit word: lo = codes 0-1, hi = codes 2-3.  The 16-bit
 // halves are taken with mov.b32 {l, h} inside the asm, so the conversions read register halves
 // instead of shifted and masked copies.
+// E5M2 codes are the upper byte of the binary16 of the same value (1 sign, 5 exponent bits with
+// bias 15, the leading 2 fraction bits), so each code only moves into the high byte of a half.
 template <int KIND>
 __device__ __forceinline__ void codes_to_f16x2(uint32_t word, uint32_t& lo, uint32_t& hi) {
-  if (KIND == KVQ_FP8_E4M3) {
+  if (KIND == KVQ_FP8_E4M3 || KIND == KVQ_FP8_E4M3_UNSCALED) {
     asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\tcvt.rn.f16x2.e4m3x2 %0, l;\n\tcvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
         : "=r"(lo), "=r"(hi)
         : "r"(word));
+  } else if (KIND == KVQ_FP8_E5M2_UNSCALED) {
+    lo = __byte_perm(word, 0u, 0x1404u);  // codes 0, 1 -> bytes 1, 3
+    hi = __byte_perm(word, 0u, 0x3424u);  // codes 2, 3 -> bytes 1, 3
   } else {
     const uint32_t u = word ^ 0x80808080u;  // q + 128 in each byte
     lo = __byte_perm(u, 0x64646464u, 0x5140u);
@@ -205,9 +221,12 @@ __device__ __forceinline__ uint32_t scale_pack_bf16x2(uint32_t f16x2, uint16_t s
   return r;
 }
 
-// Dequantize 16 codes (one 16-byte chunk, one scale) into 8 bf16x2 words.
+// Dequantize 16 codes (one 16-byte chunk, one scale) into 8 bf16x2 words.  The unscaled kinds ignore
+// s_bits: their values are the codes' own, exact in bf16 (the FMA by 1.0 and the bf16 rounding change
+// nothing).
 template <int KIND>
 __device__ __forceinline__ void dequant16(const uint4 c, uint16_t s_bits, uint32_t kd[8]) {
+  if (!KindTraits<KIND>::kScaled) s_bits = kHalfOne;
   const float z = dequant_addend<KIND>(s_bits);
   const uint32_t w[4] = {c.x, c.y, c.z, c.w};
 #pragma unroll

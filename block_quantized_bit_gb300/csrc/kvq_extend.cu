@@ -249,9 +249,12 @@ __device__ __forceinline__ float ex2(float x) {
 
 // 2^x on the FMA pipe, for a share of the probabilities (the MUFU unit alone would pace the softmax):
 // x = j + f with j = round(x) by the 1.5 * 2^23 addition (the sum's low mantissa bits hold j) and f in
-// [-0.5, 0.5]; 2^f by a cubic fitted for relative error on that interval; j added to the exponent field.
-// Relative error at most 1.5e-4 over [-126, 8], far below the bf16 rounding of P that follows.  x is
-// clamped at -126 (the result is then 2^-126, not 0: callers zero masked keys themselves).
+// [-0.5, 0.5]; 2^f by a cubic; j added to the exponent field.  The cubic's coefficients are a minimax fit of
+// 2^f on [-0.5, 0.5] for relative error, computed by Lawson's iteratively reweighted least squares on
+// Chebyshev nodes (the weights grow where the error is largest until it equioscillates), then rounded to
+// fp32.  Relative error at most 1.5e-4 over [-126, 8] (kvq_exp2_probe exposes this routine so that a test
+// checks the bound on the GPU), far below the bf16 rounding of P that follows.  x is clamped at -126 (the
+// result is then about 2^-126, not 0: callers zero masked keys themselves).
 __device__ __forceinline__ float ex2_fma(float x) {
   x = fmaxf(x, -126.0f);
   const float t = x + 12582912.0f;
@@ -364,8 +367,8 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const ExtendArgs
       const int sl = base + static_cast<int>(n % stages);
       const uint32_t use = n / stages;
       if (use > 0 && !warp_wait(&bar_empty[sl], (use - 1) & 1)) { ok = false; break; }
-      const uint32_t bytes =
-          __reduce_add_sync(0xffffffffu, phys >= 0 ? static_cast<uint32_t>(Cfg::NSL * kBox + Cfg::SC_KV) : 0u);
+      constexpr uint32_t kPageBytes = Cfg::NSL * kBox + (KindTraits<KIND>::kScaled ? Cfg::SC_KV : 0);
+      const uint32_t bytes = __reduce_add_sync(0xffffffffu, phys >= 0 ? kPageBytes : 0u);
       int32_t nv[Cfg::PPT];
 #pragma unroll
       for (int i = 0; i < Cfg::PPT; ++i) nv[i] = __shfl_sync(0xffffffffu, nvalid, i);
@@ -381,9 +384,11 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const ExtendArgs
         for (int c = 0; c < Cfg::NSL; ++c)
           tma_load_codes(smem_u32(slot + (lane * Cfg::NSL + c) * kBox), &tmap, c, t.it.g * kPage, kv, phys,
                          &bar_full[sl]);
-        const uint8_t* src = reinterpret_cast<const uint8_t*>(a.scales) +
-                             ((static_cast<int64_t>(phys) * 2 + kv) * a.num_kv_heads + t.it.g) * Cfg::SC_KV;
-        bulk_g2s(slot + Cfg::CODE_BYTES + lane * Cfg::SC_KV, src, Cfg::SC_KV, &bar_full[sl]);
+        if (KindTraits<KIND>::kScaled) {  // an unscaled pool has codes only
+          const uint8_t* src = reinterpret_cast<const uint8_t*>(a.scales) +
+                               ((static_cast<int64_t>(phys) * 2 + kv) * a.num_kv_heads + t.it.g) * Cfg::SC_KV;
+          bulk_g2s(slot + Cfg::CODE_BYTES + lane * Cfg::SC_KV, src, Cfg::SC_KV, &bar_full[sl]);
+        }
       }
       t = nx;
       ++n;
@@ -404,8 +409,8 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const ExtendArgs
     // dequantize this thread's codes of K or V from a ring slot into a bf16 tile
     auto write_tile = [&](uint8_t* dst, const uint8_t* slot, bool v_ok) {
       const uint8_t* rows = slot + pi * Cfg::NSL * kBox + off * 128;
-      const uint32_t sc = *reinterpret_cast<const uint32_t*>(
-          slot + Cfg::CODE_BYTES + pi * Cfg::SC_KV + (off * Cfg::NB + part * Cfg::NBT) * 2);
+      const uint32_t sc = KindTraits<KIND>::kScaled ? *reinterpret_cast<const uint32_t*>(
+          slot + Cfg::CODE_BYTES + pi * Cfg::SC_KV + (off * Cfg::NB + part * Cfg::NBT) * 2) : 0u;
 #pragma unroll
       for (int k = 0; k < Cfg::NCH; ++k) {
         uint32_t w[8];
@@ -709,10 +714,23 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const ExtendArgs
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols));
 }
 
+__global__ void exp2_probe_kernel(const float* __restrict__ x, float* __restrict__ y, int64_t n) {
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride)
+    y[i] = ex2_fma(x[i]);
+}
+
 template <int D>
 kvq_status launch_extend_d(const ExtendArgs& a, cudaStream_t stream) {
   using Cfg = XCfg<D>;
-  auto kern = (a.kind == KVQ_FP8_E4M3) ? extend_tc_kernel<D, KVQ_FP8_E4M3> : extend_tc_kernel<D, KVQ_Q8_0>;
+  decltype(&extend_tc_kernel<D, KVQ_FP8_E4M3>) kern = nullptr;
+  switch (a.kind) {
+    case KVQ_FP8_E4M3: kern = extend_tc_kernel<D, KVQ_FP8_E4M3>; break;
+    case KVQ_Q8_0: kern = extend_tc_kernel<D, KVQ_Q8_0>; break;
+    case KVQ_FP8_E4M3_UNSCALED: kern = extend_tc_kernel<D, KVQ_FP8_E4M3_UNSCALED>; break;
+    case KVQ_FP8_E5M2_UNSCALED: kern = extend_tc_kernel<D, KVQ_FP8_E5M2_UNSCALED>; break;
+  }
+  if (kern == nullptr) return KVQ_EKIND;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES) != cudaSuccess)
     return KVQ_ECUDA;
   CUtensorMap map;
@@ -733,6 +751,42 @@ bool extend_tc_supported(int32_t head_dim, int32_t v_dim, int32_t mla, int32_t g
   if (mla || v_dim != head_dim) return false;
   if (head_dim != 128 && head_dim != 256) return false;
   return group >= 1 && group <= kM && kM % group == 0 && batch <= kMaxExtendBatch;
+}
+
+kvq_status launch_exp2_probe(const float* x, float* y, int64_t n, cudaStream_t stream) {
+  if (n == 0) return KVQ_OK;
+  const int threads = 256;
+  const int64_t grid = std::min<int64_t>((n + threads - 1) / threads, 152 * 8);
+  exp2_probe_kernel<<<static_cast<unsigned>(grid), threads, 0, stream>>>(x, y, n);
+  return cudaGetLastError() == cudaSuccess ? KVQ_OK : KVQ_ECUDA;
+}
+
+namespace {
+// One CTA per sequence: new token i of sequence b (query row q_start[b] + i) sits at position
+// seq_lens[b] - n_b + i and attends to the prefix of seq_lens[b] - n_b + i + 1 positions.
+__global__ void extend_expand_kernel(const int32_t* __restrict__ q_start, const int32_t* __restrict__ seq_lens,
+                                     int32_t total_q, int32_t* __restrict__ vlens, int32_t* __restrict__ vrow,
+                                     uint32_t* status) {
+  const int32_t b = blockIdx.x;
+  const int32_t q0 = __ldg(q_start + b), q1 = __ldg(q_start + b + 1), L = __ldg(seq_lens + b);
+  const int32_t n = q1 - q0;
+  if (q0 < 0 || n < 0 || n > L || q1 > total_q) {
+    if (threadIdx.x == 0) set_status(status, kStatusBadExtend);
+    return;
+  }
+  for (int32_t i = threadIdx.x; i < n; i += blockDim.x) {
+    vlens[q0 + i] = L - n + i + 1;
+    vrow[q0 + i] = b;
+  }
+}
+}  // namespace
+
+kvq_status launch_extend_expand(const int32_t* q_start, const int32_t* seq_lens, int32_t batch, int32_t total_q,
+                                int32_t* vlens, int32_t* vrow, uint32_t* status, cudaStream_t stream) {
+  if (batch == 0) return KVQ_OK;
+  extend_expand_kernel<<<static_cast<unsigned>(batch), 256, 0, stream>>>(q_start, seq_lens, total_q, vlens, vrow,
+                                                                         status);
+  return cudaGetLastError() == cudaSuccess ? KVQ_OK : KVQ_ECUDA;
 }
 
 kvq_status launch_extend_tc(const ExtendArgs& a, cudaStream_t stream) {

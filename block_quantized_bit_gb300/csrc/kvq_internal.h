@@ -14,6 +14,7 @@ struct DecodeArgs {
   const uint8_t* codes;
   const uint16_t* scales;
   const int32_t* block_table;
+  const int32_t* bt_row;  // block-table row of each sequence, or null (row b); set by the MLA extend
   int64_t num_pages;
   int32_t max_pages;
   const int32_t* seq_lens;
@@ -121,4 +122,9 @@ struct ExtendArgs {
 constexpr int32_t kMaxExtendBatch = 2048;  // sequences whose item bases fit the kernel's shared table
 bool extend_tc_supported(int32_t head_dim, int32_t v_dim, int32_t mla, int32_t group, int32_t batch);
 kvq_status launch_extend_tc(const ExtendArgs& a, cudaStream_t stream);
+kvq_status launch_exp2_probe(const float* x, float* y, int64_t n, cudaStream_t stream);
+// MLA extend: each new token's causal prefix length and block-table row (rows of inconsistent sequences
+// are left as they are and flagged in the status word).
+kvq_status launch_extend_expand(const int32_t* q_start, const int32_t* seq_lens, int32_t batch, int32_t total_q,
+                                int32_t* vlens, int32_t* vrow, uint32_t* status, cudaStream_t stream);
 }  // namespace kvq

@@ -27,6 +27,7 @@ struct KParams {
   const uint8_t* codes;
   const __half* scales;
   const int32_t* block_table;
+  const int32_t* bt_row;  // block-table row of each sequence, or null: row b (the extend's per-token prefixes)
   const int32_t* seq_lens;
   float* part_acc;
   float* part_ml;
@@ -49,6 +50,12 @@ struct KParams {
                           // that the kernel which merges in-kernel writes its zero output
   float score_scale;      // sm_scale * log2(e)
 };
+
+// Block-table entry of page pg of sequence b.
+__device__ __forceinline__ int32_t bt_entry(const KParams& p, int32_t b, int32_t pg) {
+  const int64_t row = p.bt_row ? __ldg(p.bt_row + b) : b;
+  return __ldg(p.block_table + row * p.max_pages + pg);
+}
 
 __device__ __forceinline__ int32_t seq_pages(const KParams& p, int32_t b) {
   const int32_t L = max(__ldg(p.seq_lens + b), 0);
@@ -142,6 +149,7 @@ inline KParams make_kparams(const DecodeArgs& a) {
   p.codes = a.codes;
   p.scales = reinterpret_cast<const __half*>(a.scales);
   p.block_table = a.block_table;
+  p.bt_row = a.bt_row;
   p.seq_lens = a.seq_lens;
   p.part_acc = a.part_acc;
   p.part_ml = a.part_ml;

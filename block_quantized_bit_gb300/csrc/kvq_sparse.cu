@@ -93,6 +93,7 @@ __global__ void __launch_bounds__(kGatherThreads) sparse_gather_kernel(SparseGat
     reinterpret_cast<uint4*>(a.dst_codes + drow * a.D)[k] =
         __ldg(reinterpret_cast<const uint4*>(a.codes + srow * a.D) + k);
   }
+  if (a.dst_scales == nullptr) return;           // an unscaled pool: codes only
   const int32_t words = a.D / 64;               // 4-byte words of scales per row (D/32 fp16 values)
   const int64_t total_words = static_cast<int64_t>(count) * rows * words;
   for (int64_t u = tid; u < total_words; u += kGatherThreads) {

@@ -34,7 +34,8 @@ EXPORTS = ["kvq_pool_bytes", "kvq_scale_bytes", "kvq_bytes_per_token", "kvq_num_
            "kvq_decode_sparse_workspace_bytes", "kvq_decode_sparse", "kvq_decode", "kvq_decode_ex",
            "kvq_workspace_status", "kvq_encode_probe", "kvq_quantize_probe", "kvq_dequant_probe", "kvq_strerror",
            "kvq_device_check", "kvq_version", "kvq_decode_noalloc", "kvq_noalloc_status", "kvq_wait_probe",
-           "kvq_extend_workspace_bytes", "kvq_extend", "kvq_store_act_quant", "kvq_store_unscaled"]
+           "kvq_extend_workspace_bytes", "kvq_extend", "kvq_store_act_quant", "kvq_store_unscaled",
+           "kvq_bytes_per_token_ex", "kvq_num_pages_ex", "kvq_exp2_probe", "kvq_extend_workspace_bytes_ex"]
 
 
 class kvq_layout(ctypes.Structure):
@@ -70,6 +71,8 @@ def lib():
             "kvq_scale_bytes": (sz, [LP]),
             "kvq_bytes_per_token": (ctypes.c_double, [LP]),
             "kvq_num_pages": (i64, [LP, sz]),
+            "kvq_bytes_per_token_ex": (ctypes.c_double, [LP, i32]),
+            "kvq_num_pages_ex": (i64, [LP, i32, sz]),
             "kvq_store": (i32, [P, P, P, P, P, i64, LP, i32, P]),
             "kvq_decode_workspace_bytes": (sz, [LP, i32, i32, i32]),
             "kvq_decode_workspace_bytes_ex": (sz, [LP, i32, i32, i32, OP]),
@@ -93,6 +96,8 @@ def lib():
             "kvq_decode_noalloc": (i32, [P, P, P, P, i32, P, i32, i32, ctypes.c_float, P, i32, LP, i32, P]),
             "kvq_wait_probe": (i32, [P, P]),
             "kvq_noalloc_status": (i32, [P]),
+            "kvq_exp2_probe": (i32, [P, P, i64, P]),
+            "kvq_extend_workspace_bytes_ex": (sz, [LP, i32, i32, i32]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -167,6 +172,14 @@ def kvq_bytes_per_token(layout: Layout) -> float:
 
 def kvq_num_pages(layout: Layout, budget_bytes: int) -> int:
     return lib().kvq_num_pages(ctypes.byref(layout.c()), int(budget_bytes))
+
+
+def kvq_bytes_per_token_ex(layout: Layout, kind) -> float:
+    return lib().kvq_bytes_per_token_ex(ctypes.byref(layout.c()), _kind(kind))
+
+
+def kvq_num_pages_ex(layout: Layout, kind, budget_bytes: int) -> int:
+    return lib().kvq_num_pages_ex(ctypes.byref(layout.c()), _kind(kind), int(budget_bytes))
 
 
 def alloc_pool(layout: Layout, device="cuda"):
@@ -286,8 +299,18 @@ def kvq_store_act_quant(pool: torch.Tensor, scales: torch.Tensor, kv: torch.Tens
            "kvq_store_act_quant")
 
 
-def alloc_extend_workspace(device="cuda"):
-    return torch.empty(lib().kvq_extend_workspace_bytes(), dtype=torch.uint8, device=device)
+def alloc_extend_workspace(device="cuda", layout: Optional[Layout] = None, total_q=0, num_q_heads=1,
+                           max_pages_per_seq=1):
+    """The extend's workspace: its status word for GQA; for an MLA layout (pass the sizes) also the decode
+    workspace of one chunk of per-token prefixes."""
+    if layout is None or not layout.mla:
+        n = lib().kvq_extend_workspace_bytes()
+    else:
+        n = lib().kvq_extend_workspace_bytes_ex(ctypes.byref(layout.c()), int(total_q), int(num_q_heads),
+                                                int(max_pages_per_seq))
+        if n == 0:
+            raise KvqError(-1, "kvq_extend_workspace_bytes_ex")
+    return torch.empty(n, dtype=torch.uint8, device=device)
 
 
 def kvq_extend(q: torch.Tensor, pool: torch.Tensor, scales: torch.Tensor, block_table: torch.Tensor,
@@ -333,6 +356,11 @@ def kvq_quantize_probe(kind, x_bits: torch.Tensor, s_bits: torch.Tensor, codes: 
 def kvq_dequant_probe(kind, codes: torch.Tensor, scales: torch.Tensor, out: torch.Tensor, stream=None):
     _check(lib().kvq_dequant_probe(_kind(kind), _ptr(codes), _ptr(scales), _ptr(out), int(codes.numel()),
                                    _stream(stream)), "kvq_dequant_probe")
+
+
+def kvq_exp2_probe(x: torch.Tensor, y: torch.Tensor, stream=None):
+    """y = 2^x by the extend kernel's FMA-pipe exponential (float32 device tensors of equal size)."""
+    _check(lib().kvq_exp2_probe(_ptr(x), _ptr(y), int(x.numel()), _stream(stream)), "kvq_exp2_probe")
 
 
 def kvq_wait_probe(workspace: torch.Tensor, stream=None):

@@ -37,7 +37,9 @@
 extern "C" {
 #endif
 
-/* Code format.  Both use one fp16 scale per 32 elements. */
+/* Code format.  The first two use one fp16 scale per 32 elements; the unscaled ones have no scale array
+ * (written by kvq_store_unscaled; every attention entry point reads all four, ignoring `scales` for the
+ * unscaled kinds, which may then be NULL). */
 typedef enum {
     KVQ_FP8_E4M3 = 1,          /* OCP E4M3 "fn" codes, s = amax / 448 */
     KVQ_Q8_0 = 2,              /* int8 codes,          s = amax / 127 */
@@ -54,7 +56,7 @@ typedef enum {
 typedef enum {
     KVQ_OK = 0,
     KVQ_EINVAL = -1,       /* null pointer, negative size, bad layout, Hq % Hkv != 0, ... */
-    KVQ_EKIND = -2,        /* kind is not a kvq_kind */
+    KVQ_EKIND = -2,        /* kind is not a kvq_kind this call accepts */
     KVQ_EHEADDIM = -3,     /* head_dim (or v_dim) not a positive multiple of 32 */
     KVQ_EALIGN = -4,       /* a device pointer is not 16-byte aligned */
     KVQ_EWORKSPACE = -5,   /* workspace smaller than kvq_decode_workspace_bytes() */
@@ -89,6 +91,11 @@ size_t kvq_scale_bytes(const kvq_layout* layout);
 double kvq_bytes_per_token(const kvq_layout* layout);
 /* Whole pages (codes + scales) that fit in `budget_bytes`; num_pages of `layout` is ignored.  -1 if invalid. */
 int64_t kvq_num_pages(const kvq_layout* layout, size_t budget_bytes);
+/* The same two for any kind: 17/16 bytes per element for the block-scaled kinds, 1 for the unscaled fp8 casts
+ * ("Add fp8 KV-cache quantization (--kv-dtype)", section "Benchmark": twice the bf16 token budget).  -1 if the
+ * layout or the kind is invalid. */
+double kvq_bytes_per_token_ex(const kvq_layout* layout, kvq_kind kind);
+int64_t kvq_num_pages_ex(const kvq_layout* layout, kvq_kind kind, size_t budget_bytes);
 
 /* ---------------------------------------------------------------- store */
 /*
@@ -123,7 +130,7 @@ size_t kvq_decode_workspace_bytes_ex(const kvq_layout* layout, int32_t batch, in
 /*
  * Decode attention for one new query token per sequence.
  *   q            device bf16 [batch][num_q_heads][head_dim]
- *   pool, scales device, filled by kvq_store
+ *   pool, scales device, filled by kvq_store (or by kvq_store_unscaled: then scales is ignored)
  *   block_table  device int32 [batch][max_pages_per_seq]; entry j is the physical page of tokens
  *                [16j, 16j+16); -1 masks that whole page.  Entries at or beyond ceil(seq_len/16) are
  *                never read.  An entry >= layout->num_pages is treated as masked and makes
@@ -186,8 +193,10 @@ kvq_status kvq_decode_sparse(const void* q, const void* pool, const void* scales
  * store casts the incoming bf16 k/v to the pool's fp8 type, scale 1.0; fp8_e5m2 is wired the same way).
  * kind is KVQ_FP8_E4M3_UNSCALED or KVQ_FP8_E5M2_UNSCALED; each bf16 element becomes one code by a single
  * nearest-even rounding that saturates at the largest finite value (448 / 57344): finite and infinite inputs
- * give finite codes.  NaN inputs are outside the domain (as for kvq_store) and give NaN codes.  The pool has the codes layout of kvq_pool_bytes and no scale array.  Other arguments as
- * kvq_store.  The other entry points do not accept these kinds yet (KVQ_EKIND).
+ * give finite codes.  NaN inputs are outside the domain (as for kvq_store) and give NaN codes.  The pool has
+ * the codes layout of kvq_pool_bytes and no scale array.  Other arguments as kvq_store.  kvq_decode,
+ * kvq_decode_sparse and kvq_extend read such a pool with the same kind: every E4M3 and E5M2 value is a bf16
+ * value, so K and V enter the attention exactly as stored.
  */
 kvq_status kvq_store_unscaled(void* pool, const void* k, const void* v, const int64_t* slot_mapping,
                               int64_t num_tokens, const kvq_layout* layout, kvq_kind kind, void* stream);
@@ -220,18 +229,28 @@ kvq_status kvq_store_act_quant(void* pool, void* scales, const void* kv, const i
  *   seq_lens     stored tokens per sequence, the new ones included: the n_b = q_start[b + 1] - q_start[b]
  *                new tokens are the last n_b, so new token i sits at position seq_lens[b] - n_b + i
  *   out          [total_q, num_q_heads, v_dim], bf16 or f32 (out_dtype), device
- *   workspace    at least kvq_extend_workspace_bytes() (its status word), 16-byte aligned, device
+ *   workspace    at least kvq_extend_workspace_bytes_ex() (kvq_extend_workspace_bytes() for GQA: its status
+ *                word), 16-byte aligned, device
  * sm_scale must be finite and > 0 (else KVQ_EINVAL).  Other arguments as kvq_decode.
  * Query row (b, i, h) gets softmax(sm_scale * q.K^T) V over the positions
  * 0 .. seq_lens[b] - n_b + i of sequence b whose pages are not masked (causal), with K and V dequantized to
- * bf16 and fp32 accumulation; no valid position gives zeros.  Runs on the tensor cores (tcgen05).
- * Supported: page_size 16, head_dim = v_dim in {128, 256}, not MLA, query heads per kv head dividing
- * 128, batch <= 2048; otherwise KVQ_EUNSUPPORTED.  q_start and seq_lens are read on the device: a
- * sequence with n_b < 0, n_b > seq_lens[b] or q_start[b + 1] > total_q is skipped and makes
- * kvq_workspace_status report KVQ_EINVAL, as does a block-table entry >= layout->num_pages (that page is
- * skipped).  Asynchronous on `stream`.
+ * bf16 and fp32 accumulation; no valid position gives zeros.
+ * GQA (head_dim = v_dim in {128, 256}, query heads per kv head dividing 128): one flash-style tcgen05 kernel,
+ * each dequantized K/V tile shared by a block of 128 query rows.
+ * MLA (the latent row, head_dim 576 / v_dim 512, "feat(kvcache): 8-bit DSV4 window/compressed KV", section
+ * "What this adds"): every new token is decoded as a sequence of its own over its causal prefix, by the
+ * decode kernels of kvq_decode (chosen as kvq_decode chooses them for a batch of up to 1024 such prefixes;
+ * the tokens run in chunks of 1024), so its precision is the decode's; rows of a skipped sequence are zeros.
+ * Supported: page_size 16, batch <= 2048, and the two shapes above; otherwise KVQ_EUNSUPPORTED.  q_start
+ * and seq_lens are read on the device: a sequence with n_b < 0, n_b > seq_lens[b] or q_start[b + 1] >
+ * total_q is skipped and makes kvq_workspace_status report KVQ_EINVAL, as does a block-table entry >=
+ * layout->num_pages (that page is skipped).  Asynchronous on `stream`.
  */
 size_t kvq_extend_workspace_bytes(void);
+/* Workspace bytes kvq_extend needs for these sizes (a GQA layout: kvq_extend_workspace_bytes(); an MLA layout:
+ * the decode workspace of one chunk of prefixes plus two int32 per query row).  0 if invalid. */
+size_t kvq_extend_workspace_bytes_ex(const kvq_layout* layout, int32_t total_q, int32_t num_q_heads,
+                                     int32_t max_pages_per_seq);
 kvq_status kvq_extend(const void* q, const void* pool, const void* scales, const int32_t* block_table,
                       int32_t max_pages_per_seq, const int32_t* seq_lens, const int32_t* q_start, int32_t total_q,
                       int32_t batch, int32_t num_q_heads, float sm_scale, void* out, kvq_out_dtype out_dtype,
@@ -307,6 +326,14 @@ kvq_status kvq_quantize_probe(kvq_kind kind, const uint16_t* x, int64_t nx, cons
  */
 kvq_status kvq_dequant_probe(kvq_kind kind, const uint8_t* codes, const uint16_t* scales, uint16_t* out,
                              int64_t n, void* stream);
+/*
+ * Exponential step of the extend's softmax, by the extend kernel's own routine: y[i] = 2^x[i] for fp32 device
+ * arrays of n, as the FMA-pipe path computes a share of the probabilities (a cubic for 2^f on [-0.5, 0.5]
+ * and the integer part added to the exponent; x clamped at -126).  Relative error at most 1.5e-4 for x in
+ * [-126, 8].  Exposes the routine so that its bound can be checked on the GPU; the pages print no such
+ * step (they exponentiate in Triton / FlashInfer kernels).  4-byte aligned pointers.
+ */
+kvq_status kvq_exp2_probe(const float* x, float* y, int64_t n, void* stream);
 /*
  * Bounded-wait probe: one kernel waits, with the decode kernels' own bounded wait, on an mbarrier
  * that nothing completes.  The wait gives up after the library's limit (2 s) and the kernel records a

@@ -43,7 +43,8 @@ def measure(case, seqs=None, nthreads=0):
     n_kv = 1 if case.mla else 2
     nth = nthreads or max(1, os.cpu_count() or 1)
     codes = np.zeros((case.num_pages, n_kv, Hkv, P, D), np.uint8)
-    scales = np.zeros((case.num_pages, n_kv, Hkv, P, D // 32), np.uint16)
+    unscaled = case.kind.endswith("_unscaled")   # the plain fp8 casts keep no scales
+    scales = None if unscaled else np.zeros((case.num_pages, n_kv, Hkv, P, D // 32), np.uint16)
     pool16 = np.zeros((case.num_pages, n_kv, Hkv, P, D), np.uint16)
     # only the rows of the chosen sequences are needed
     lens = [int(x) for x in case.seq_lens.cpu()]
@@ -84,7 +85,7 @@ REPORT = [
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--families", nargs="*", default=None)
-    ap.add_argument("--kinds", nargs="*", default=["fp8_e4m3", "q8_0"])
+    ap.add_argument("--kinds", nargs="*", default=["fp8_e4m3", "q8_0", "fp8_e4m3_unscaled", "fp8_e5m2_unscaled"])
     a = ap.parse_args()
     print("| Workload | Kind | max abs vs bf16 | mean abs vs bf16 | max abs output | oracle s |")
     print("|---|---|---|---|---|---|")

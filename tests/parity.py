@@ -72,12 +72,12 @@ def oracle_decode(case, oc, osc, nthreads=0):
 
 
 def abs_value_pool(oc, kind):
-    """The pool with every V code replaced by the code of its absolute value (fp8: sign bit cleared; q8_0:
-    |int8|, the store never writes -128) and K unchanged.  Attention over it gives, for each output row,
+    """The pool with every V code replaced by the code of its absolute value (fp8 of every kind: sign bit
+    cleared; q8_0: |int8|, the store never writes -128) and K unchanged.  Attention over it gives, for each output row,
     sum_t softmax_t * |V_t|: the scale of the error that rounding the probabilities to bf16 (relative
     2^-9 each, as the tensor-core kernels feed them to the MMA) can cause."""
     a = oc.copy()
-    if kind == "fp8_e4m3":
+    if kind != "q8_0":
         a[:, 1] &= 0x7F
     else:
         a[:, 1] = np.abs(a[:, 1].view(np.int8)).astype(np.uint8)

@@ -139,7 +139,14 @@ def test_extend_argument_errors(lib):
     assert _extend(lib, L(), total_q=-1) == -1
     assert _extend(lib, L(), out_dtype=7) == -1
     assert _extend(lib, L(head_dim=64, v_dim=64)) == -8        # KVQ_EUNSUPPORTED: head_dim 64
-    assert _extend(lib, L(mla=True, num_kv_heads=1, head_dim=576, v_dim=512), hq=16) == -8
+    mla = L(mla=True, num_kv_heads=1, head_dim=576, v_dim=512)
+    need = lib.kvq_extend_workspace_bytes_ex(ctypes.byref(mla.c()), 5, 16, 10)
+    assert need > 256                                           # the decode workspace of the prefixes
+    assert lib.kvq_extend_workspace_bytes_ex(ctypes.byref(L().c()), 5, 8, 10) == 256
+    assert lib.kvq_extend_workspace_bytes_ex(ctypes.byref(mla.c()), -1, 16, 10) == 0
+    assert _extend(lib, mla, hq=16) == -5                       # MLA with the GQA workspace: too small
+    assert _extend(lib, mla, hq=16, ws_bytes=need, ws=FAKE + 8) == -4
+    assert _extend(lib, L(mla=True, num_kv_heads=1, head_dim=512, v_dim=512), hq=16, ws_bytes=1 << 30) == -8
     assert _extend(lib, L(), hq=6) == -8                        # 3 heads per kv head do not divide 128
     assert _extend(lib, L(page_size=32)) == -8
     assert _extend(lib, L(), ws_bytes=16) == -5                 # KVQ_EWORKSPACE
@@ -256,6 +263,39 @@ def test_unscaled_store_argument_errors(lib):
     assert call(n=0) == 0
     assert call(k=FAKE + 4) == -4                               # KVQ_EALIGN
     assert call(kind=4) != -2                                   # e5m2 is accepted (fails later: no device here)
-    # the decode does not read unscaled pools yet
+    # the decode reads unscaled pools without a scale array (NULL scales pass validation; no device here)
+    for kind in (3, 4):
+        st = lib.kvq_decode(P(FAKE), P(FAKE), None, P(FAKE), 10, P(FAKE), 2, 8, ctypes.c_float(1.0), P(FAKE), 0,
+                            P(FAKE), 1 << 20, ctypes.byref(L().c()), kind, None)
+        assert st not in (-1, -2), st
+    # the block-scaled kinds still need their scales; an unknown kind is rejected
+    assert lib.kvq_decode(P(FAKE), P(FAKE), None, P(FAKE), 10, P(FAKE), 2, 8, ctypes.c_float(1.0), P(FAKE), 0,
+                          P(FAKE), 1 << 20, ctypes.byref(L().c()), 1, None) == -1
     assert lib.kvq_decode(P(FAKE), P(FAKE), P(FAKE), P(FAKE), 10, P(FAKE), 2, 8, ctypes.c_float(1.0), P(FAKE), 0,
-                          P(FAKE), 1 << 20, ctypes.byref(L().c()), 3, None) == -2
+                          P(FAKE), 1 << 20, ctypes.byref(L().c()), 5, None) == -2
+
+
+def test_unscaled_cost_model_is_one_byte_per_element_and_doubles_the_bf16_budget(lib):
+    """"Add fp8 KV-cache quantization (--kv-dtype)", section "Benchmark": at the same budget the unscaled fp8 pool
+    holds twice the bf16 tokens (27,142 -> 54,284); the block-scaled kinds keep 17/16 bytes per element."""
+    g = GOLDEN["unscaled_fp8_kv_budget_tokens"]
+    for hkv, d in ((8, 128), (2, 256), (4, 64)):
+        lay = L(num_kv_heads=hkv, head_dim=d, v_dim=d)
+        for kind in ("fp8_e4m3_unscaled", "fp8_e5m2_unscaled"):
+            assert kvq.kvq_bytes_per_token_ex(lay, kind) == 2 * hkv * d * O.bytes_per_element(kind)
+            bf16_per_page = 16 * 2 * hkv * d * GOLDEN["bytes_per_element_bf16"]["value"]
+            budget = g["bf16"] * bf16_per_page // 16        # a budget of exactly 27,142 bf16 tokens (whole pages)
+            assert kvq.kvq_num_pages_ex(lay, kind, budget) * 16 == 2 * (budget // bf16_per_page) * 16
+        for kind in ("fp8_e4m3", "q8_0"):
+            assert kvq.kvq_bytes_per_token_ex(lay, kind) == kvq.kvq_bytes_per_token(lay)
+            assert kvq.kvq_num_pages_ex(lay, kind, 10 ** 9) == kvq.kvq_num_pages(lay, 10 ** 9)
+        assert kvq.kvq_bytes_per_token_ex(lay, 7) == -1.0 and kvq.kvq_num_pages_ex(lay, 0, 10 ** 9) == -1
+    assert g["fp8_e4m3"] == 2 * g["bf16"]
+
+
+def test_exp2_probe_argument_errors(lib):
+    P = ctypes.c_void_p
+    assert lib.kvq_exp2_probe(P(FAKE), P(FAKE), -1, None) == -1
+    assert lib.kvq_exp2_probe(None, P(FAKE), 4, None) == -1
+    assert lib.kvq_exp2_probe(P(FAKE), P(FAKE), 0, None) == 0
+    assert lib.kvq_exp2_probe(P(FAKE + 2), P(FAKE), 4, None) == -4

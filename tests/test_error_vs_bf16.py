@@ -43,9 +43,14 @@ def _bound(case, r, seqs):
             continue
         pg, off = sl // P, sl % P
         for g in range(Hkv):
-            kq = O.dequant(case.kind, codes[pg, 0, g, off], np.repeat(scales[pg, 0, g, off], 32, axis=-1))
-            vq = kq[:, :Dv] if case.mla else O.dequant(case.kind, codes[pg, 1, g, off],
-                                                        np.repeat(scales[pg, 1, g, off], 32, axis=-1))
+            if scales is None:   # unscaled: the code's own value
+                val = np.vectorize(lambda c: O.code_value(case.kind, int(c)))
+                kq = val(codes[pg, 0, g, off])
+                vq = kq[:, :Dv] if case.mla else val(codes[pg, 1, g, off])
+            else:
+                kq = O.dequant(case.kind, codes[pg, 0, g, off], np.repeat(scales[pg, 0, g, off], 32, axis=-1))
+                vq = kq[:, :Dv] if case.mla else O.dequant(case.kind, codes[pg, 1, g, off],
+                                                            np.repeat(scales[pg, 1, g, off], 32, axis=-1))
             k16, v16 = kf[rr, g], (kf[rr, g, :Dv] if case.mla else vf[rr, g])
             dv = np.abs(vq - v16).max(0)
             vmax = np.abs(v16).max(0)
@@ -65,7 +70,7 @@ CASES = [
 ]
 
 
-@pytest.mark.parametrize("kind", ["fp8_e4m3", "q8_0"])
+@pytest.mark.parametrize("kind", ["fp8_e4m3", "q8_0", "fp8_e4m3_unscaled", "fp8_e5m2_unscaled"])
 @pytest.mark.parametrize("fam,kw", CASES, ids=[c[0] for c in CASES])
 def test_quantized_decode_stays_within_the_softmax_perturbation_bound_of_bf16(fam, kw, kind):
     case = workloads.make(fam, kind=kind, device="cpu", **kw)

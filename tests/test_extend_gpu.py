@@ -4,7 +4,8 @@ Each case stores every row of its sequences (kvq_store on the GPU, the oracle's 
 bit-exact by the store tests) and declares the last n_b stored tokens of sequence b new; the kernel's output
 for every (new token, query head) must meet the decode bound (max abs <= 1.5e-2, mean abs <= 2e-3).  The
 cases span several key tiles and query blocks with ragged tails, D = 128 and 256, 1 to 16 query heads per kv
-head, masked pages, a first prefill (every token new), single new tokens and sequences without new tokens."""
+head, masked pages, a first prefill (every token new), single new tokens and sequences without new tokens.
+The MLA latent row runs through the decode kernels, one causal prefix per new token, with the same bound."""
 import numpy as np
 import pytest
 import torch
@@ -130,8 +131,69 @@ def test_extend_with_no_new_token_is_a_no_op_and_a_bad_q_start_is_reported():
     assert torch.isnan(out[3:int(bad[2])]).all()  # the skipped sequence's rows are untouched
 
 
+def _mla_stored(kind, n_new, mask=(), **kw):
+    case = _case("mla", kind, **kw)
+    L, codes, scales = gpu_pool(case)
+    gpu_store(case, codes, scales)
+    oc, osc = oracle_pool(case)
+    oracle_store(case, oc, osc)
+    bt = case.block_table.clone()
+    for b, j in mask:          # pages masked after the store: their rows are hidden from the attention
+        bt[b, j] = -1
+    case.block_table = bt
+    lens = case.seq_lens.cpu().tolist()
+    n_new = [L_ if x is None else x for x, L_ in zip(n_new, lens)]
+    q, q_start, _ = workloads.extend_inputs(case, n_new)
+    return case, L, codes, scales, oc, osc, q, q_start
+
+
+def _gpu_extend_mla(case, L, codes, scales, q, q_start, out_dtype=torch.float32):
+    out = torch.full((q.shape[0], case.num_q_heads, case.v_dim), float("nan"), dtype=out_dtype, device="cuda")
+    ws = kvq.alloc_extend_workspace("cuda", L, q.shape[0], case.num_q_heads, case.max_pages)
+    ws.fill_(0x5A)
+    kvq.kvq_extend(q, codes, scales, case.block_table, case.seq_lens, q_start, out, ws, L, case.kind, case.sm_scale)
+    torch.cuda.synchronize()
+    return out, ws
+
+
+MLA_CASES = [
+    # 16 heads (one padded group of 64 on the tensor cores), a first prefill and a partial one, masked pages
+    (dict(batch=2, ctx=200, num_q_heads=16), [None, 30], [(0, 3), (1, 10)]),
+    # 128 heads (two groups of 64), one sequence
+    (dict(batch=1, ctx=130, num_q_heads=128), [20], []),
+    # more new tokens than one chunk of 1024 prefixes (one head, the oracle's cost kept small)
+    (dict(batch=2, ctx=560, num_q_heads=1), [None, 480], [(1, 2)]),
+]
+
+
+@pytest.mark.parametrize("kind", ["fp8_e4m3", "q8_0"])
+@pytest.mark.parametrize("ci", range(len(MLA_CASES)))
+def test_mla_extend_matches_the_oracle(ci, kind):
+    """The MLA latent row (576 / 512): each new token decoded over its causal prefix by the decode kernels."""
+    kw, n_new, mask = MLA_CASES[ci]
+    case, L, codes, scales, oc, osc, q, q_start = _mla_stored(kind, n_new, mask, **kw)
+    out, ws = _gpu_extend_mla(case, L, codes, scales, q, q_start)
+    assert kvq.kvq_workspace_status(ws) == 0
+    assert_decode_close(out.cpu().numpy().astype(np.float64), _oracle_extend(case, oc, osc, q, q_start))
+
+
+def test_mla_extend_skips_a_bad_sequence_with_zeros_and_reports_it():
+    case, L, codes, scales, oc, osc, q, q_start = _mla_stored("fp8_e4m3", [None, 40], [], batch=2, ctx=200,
+                                                              num_q_heads=16)
+    lens = case.seq_lens.cpu().tolist()
+    bad = torch.tensor([0, 5, 5 + lens[1] + 1], dtype=torch.int32, device="cuda")  # sequence 1: too many
+    qb = q[:1].repeat(int(bad[-1]), 1, 1)
+    out, ws = _gpu_extend_mla(case, L, codes, scales, qb, bad)
+    assert kvq.kvq_workspace_status(ws) == KVQ_EINVAL
+    assert not out[5:].any()
+    ref = O.extend(bits(qb[:5]), oc, osc, case.block_table.cpu().numpy(), case.seq_lens.cpu().numpy()[:1],
+                   np.array([0, 5], np.int32), num_q_heads=case.num_q_heads, num_kv_heads=1, head_dim=case.head_dim,
+                   v_dim=case.v_dim, page_size=16, mla=True, kind=case.kind, sm_scale=case.sm_scale, nthreads=0)
+    assert_decode_close(out[:5].cpu().numpy().astype(np.float64), ref)
+
+
 def test_extend_rejects_unsupported_shapes():
-    case = workloads.make("mla", kind="fp8_e4m3", device="cuda", ctx=64)
+    case = workloads.make("long_gqa", kind="fp8_e4m3", device="cuda", batch=1, ctx=64, head_dim=64)
     L = layout_of(case)
     codes, scales = kvq.alloc_pool(L, "cuda")
     q = torch.zeros((1, case.num_q_heads, case.head_dim), dtype=torch.bfloat16, device="cuda")

@@ -104,13 +104,20 @@ def _fp32_sweep():
     near = np.concatenate(near)
     special = np.array([0.0, -0.0, np.inf, -np.inf, 1e-45, -1e-45, 0.49999997, 0.5, 126.5, 127.5, -127.5, 1e30],
                        np.float32)
-    y = np.concatenate([pats, near, -near, special, np.linspace(-130, 130, 1 << 20, dtype=np.float32)])
+    # every integer tie k + 0.5 of the int8 range and its four fp32 neighbours on each side
+    ties = np.arange(-130, 131, dtype=np.float32) + np.float32(0.5)
+    tie_near = [ties] + [(ties.view(np.uint32) + d).view(np.float32) for d in range(1, 5)] + \
+        [(ties.view(np.uint32) - d).view(np.float32) for d in range(1, 5)]
+    tie_near = np.concatenate(tie_near)
+    y = np.concatenate([pats, near, -near, special, np.linspace(-130, 130, 1 << 20, dtype=np.float32), tie_near,
+                        -tie_near])
     return y
 
 
 @pytest.mark.parametrize("kind", KINDS)
 def test_encode_probe_matches_oracle_on_fp32_sweep(kind):
-    """The store's code step (hardware satfinite RNE for fp8; roundf + clamp for q8_0) vs the oracle."""
+    """The store's code step (hardware satfinite RNE for fp8; the truncated half-offset sum and saturating pack for
+    q8_0) vs the oracle."""
     y = _fp32_sweep()
     yd = torch.from_numpy(y).cuda()
     codes = torch.empty(y.size, dtype=torch.uint8, device="cuda")
@@ -171,3 +178,46 @@ def test_store_quotient_gives_ieee_codes_for_every_bf16_and_fp16_scale(kind):
         reachable = xf[None, :] <= (2.0 ** 64) * sf[:, None]
         bad = np.argwhere((got != ref) & reachable)
         assert bad.size == 0, [(hex(int(s[i])), hex(int(xb[j])), int(got[i, j]), int(ref[i, j])) for i, j in bad[:8]]
+
+
+@pytest.mark.parametrize("kind", KINDS)
+def test_store_quotient_at_the_saturated_scale_for_every_bf16(kind):
+    """A block whose amax / Q exceeds the largest fp16 gets the scale 65504 (0x7BFF) and its quotients reach
+    |x / s| ~ 2^112, beyond the 2^64 the general sweep covers: the store's division still gives the oracle's
+    code for every finite bf16 x at that scale (the large quotients saturate on both sides)."""
+    xb = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    xb = xb[((xb >> 7) & 0xFF) != 0xFF]
+    s = np.array([0x7BFF], np.uint16)
+    out = torch.empty(xb.size, dtype=torch.uint8, device="cuda")
+    kvq.kvq_quantize_probe(kind, torch.from_numpy(xb.view(np.int16)).cuda(), torch.from_numpy(s.view(np.int16)).cuda(),
+                           out)
+    got = out.cpu().numpy()
+    ref = O.code_table(kind, xb, s).reshape(-1)
+    assert np.array_equal(got, ref), int((got != ref).sum())
+
+
+@pytest.mark.parametrize("kind", KINDS)
+def test_store_blocks_beyond_the_largest_scale_are_bit_exact(kind):
+    """Rows whose blocks hold magnitudes up to 3e38 (amax far above 65504 * Q): the scale saturates at 0x7BFF
+    and the codes at +-448 / +-127, identically on the GPU and in the oracle."""
+    g = torch.Generator().manual_seed(12)
+    T, Hkv, D, P = 40, 2, 128, 16
+    k = torch.randn(T, Hkv, D, generator=g) * torch.exp(torch.rand(T, Hkv, 1, generator=g) * 80.0)  # up to ~1e34
+    k[0, 0, :32] = torch.linspace(-3.0e38, 3.0e38, 32)
+    k[1, 1, 32:64] = 3.0e7                                   # just above 65504 * 448
+    v = torch.randn(T, Hkv, D, generator=g) * 1e9
+    kb, vb = k.to(torch.bfloat16), v.to(torch.bfloat16)
+    assert torch.isfinite(kb.float()).all() and torch.isfinite(vb.float()).all()
+    slots = torch.randperm(4 * P, generator=g)[:T].to(torch.int64)
+    L = kvq.Layout(4, P, Hkv, D, D)
+    codes, scales = kvq.alloc_pool(L, "cuda")
+    codes.fill_(0x33)
+    scales.fill_(0x1111)
+    kvq.kvq_store(codes, scales, kb.cuda(), vb.cuda(), slots.cuda(), L, kind)
+    torch.cuda.synchronize()
+    oc = np.full(L.codes_shape(), 0x33, np.uint8)
+    osc = np.full(L.scales_shape(), 0x1111, np.uint16)
+    O.store(oc, osc, bits(kb), bits(vb), slots.numpy(), num_kv_heads=Hkv, head_dim=D, page_size=P, mla=False, kind=kind)
+    assert np.array_equal(codes.cpu().numpy(), oc)
+    assert np.array_equal(scales.cpu().numpy().view(np.uint16), osc)
+    assert (osc == 0x7BFF).any()                             # the saturated scale occurs
