@@ -503,6 +503,9 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(KParams p, OutT* _
   __shared__ float s_m[kMergeWarps];
   __shared__ __align__(16) float s_a[kMergeWarps][32];
   __shared__ float s_l[kMergeWarps];
+  // Launched as a programmatic dependent of the decode kernel: its CTAs may start while the decode's last
+  // CTAs still run; this waits until that grid has completed and its partials are visible.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int sub = lane >> 3, q = lane & 7;  // split of the four, float4 of the slice
   const int32_t b = blockIdx.x / units_per_seq;
@@ -660,13 +663,25 @@ kvq_status launch_merge(const DecodeArgs& a, int32_t query_groups, cudaStream_t 
   const int32_t units = query_groups * a.heads_per_item * (a.v_dim / 32);
   const int64_t grid = static_cast<int64_t>(a.batch) * units;
   if (grid == 0) return KVQ_OK;
+  // programmatic stream serialization: the merge grid launches as the decode grid winds down instead of after it
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(kMergeThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e;
   if (a.out_dtype == KVQ_OUT_BF16)
-    merge_kernel<__nv_bfloat16><<<static_cast<unsigned>(grid), kMergeThreads, 0, stream>>>(
-        p, static_cast<__nv_bfloat16*>(a.out), a.heads_per_item, a.v_dim, units);
+    e = cudaLaunchKernelEx(&cfg, merge_kernel<__nv_bfloat16>, p, static_cast<__nv_bfloat16*>(a.out), a.heads_per_item,
+                           a.v_dim, units);
   else
-    merge_kernel<float><<<static_cast<unsigned>(grid), kMergeThreads, 0, stream>>>(
-        p, static_cast<float*>(a.out), a.heads_per_item, a.v_dim, units);
-  return cudaGetLastError() == cudaSuccess ? KVQ_OK : KVQ_ECUDA;
+    e = cudaLaunchKernelEx(&cfg, merge_kernel<float>, p, static_cast<float*>(a.out), a.heads_per_item, a.v_dim,
+                           units);
+  return (e == cudaSuccess && cudaGetLastError() == cudaSuccess) ? KVQ_OK : KVQ_ECUDA;
 }
 
 // ------------------------------------------------------------------------------------ wait probe

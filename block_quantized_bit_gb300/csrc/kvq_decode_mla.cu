@@ -318,6 +318,8 @@ __global__ void __launch_bounds__(mla::kThreads, 1) decode_mla_kernel(const KPar
   const uint32_t tO = tmem + 128;   // O^T block c: columns [128 + 64 c, 192 + 64 c)
   const uint32_t tK = tmem + 384;   // K slots: columns [384 + 64 s, 448 + 64 s)
   const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+  // the merge kernel that follows may launch now; it waits for this grid to complete before it reads
+  asm volatile("griddepcontrol.launch_dependents;");
   bool ok = true;
 
   if (warp == kProdWarp) {

@@ -261,6 +261,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const KParams p,
   const uint32_t tK = tmem + 96;  // K tiles: buffer b at columns [96 + b * KCOLS, 96 + (b + 1) * KCOLS)
   const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
 
+  // the merge kernel that follows may launch now; it waits for this grid to complete before it reads
+  asm volatile("griddepcontrol.launch_dependents;");
   bool ok = true;
   uint32_t gtile = 0;  // tiles processed by this CTA so far
 

@@ -123,11 +123,32 @@ __device__ __forceinline__ uint16_t encode_fp8x2(float a, float b) {
   return static_cast<uint16_t>(__nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3));
 }
 
-// One q8_0 code: round half away from zero, clamp to +-127.
+// q8_0 codes: round half away from zero, clamp to +-127, in two steps.
+// (1) q8_trunc_code: truncating y + copysign(0.5 - 2^-25, y) toward zero rounds half away from zero exactly
+//     (the fp32 sum is correctly rounded).  At a tie k + 0.5 the sum k + 1 - 2^-25 rounds up to k + 1 (for
+//     k = 0 it is the midpoint below 1, which goes to the even 1.0).  Just below a tie the sum stays below
+//     k + 1, because its distance to k + 1 exceeds half an ulp there; and 0.5 - 2^-25 itself, whose sum
+//     with 0.5 would round up to 1, gives 1 - 2^-24 with this offset, truncated to 0.  The sum is clamped
+//     at -127.5 so that the negative side saturates at -127; infinities saturate in the conversion.
+// (2) pack_q8x4: four such integers to int8 with saturation at +127 (cvt.pack.sat), element 0 in the
+//     lowest byte.
+// The kernels' quantize and encode probes compare this with the oracle's exact round-half-away on every
+// bf16 value against every fp16 scale and on a dense fp32 sweep with every tie.
+__device__ __forceinline__ int32_t q8_trunc_code(float y) {
+  const float half_below = copysignf(__uint_as_float(0x3EFFFFFFu), y);  // 0.5 - 2^-25, signed as y
+  return __float2int_rz(fmaxf(y + half_below, -127.5f));
+}
+
+__device__ __forceinline__ uint32_t pack_q8x4(int32_t e0, int32_t e1, int32_t e2, int32_t e3) {
+  uint32_t hi, r;
+  asm("cvt.pack.sat.s8.s32.b32 %0, %1, %2, 0;" : "=r"(hi) : "r"(e3), "r"(e2));
+  asm("cvt.pack.sat.s8.s32.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(e1), "r"(e0), "r"(hi));
+  return r;
+}
+
+// One q8_0 code (the probe's single-element form).
 __device__ __forceinline__ uint8_t encode_q8(float y) {
-  float r = roundf(y);  // C semantics: halfway cases away from zero
-  r = fminf(fmaxf(r, -kQ8Max), kQ8Max);
-  return static_cast<uint8_t>(static_cast<int8_t>(static_cast<int>(r)));
+  return static_cast<uint8_t>(pack_q8x4(q8_trunc_code(y), 0, 0, 0) & 0xFFu);
 }
 
 // --------------------------------------------------------------------------- decode dequantization

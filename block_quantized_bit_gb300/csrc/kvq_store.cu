@@ -61,8 +61,7 @@ __device__ __forceinline__ uint32_t encode4(float a, float b, float c, float d) 
   if (KIND == KVQ_FP8_E4M3) {
     return static_cast<uint32_t>(encode_fp8x2(a, b)) | (static_cast<uint32_t>(encode_fp8x2(c, d)) << 16);
   } else {
-    return static_cast<uint32_t>(encode_q8(a)) | (static_cast<uint32_t>(encode_q8(b)) << 8) |
-           (static_cast<uint32_t>(encode_q8(c)) << 16) | (static_cast<uint32_t>(encode_q8(d)) << 24);
+    return pack_q8x4(q8_trunc_code(a), q8_trunc_code(b), q8_trunc_code(c), q8_trunc_code(d));
   }
 }
 

@@ -203,7 +203,7 @@ def test_store_blocks_beyond_the_largest_scale_are_bit_exact(kind):
     g = torch.Generator().manual_seed(12)
     T, Hkv, D, P = 40, 2, 128, 16
     k = torch.randn(T, Hkv, D, generator=g) * torch.exp(torch.rand(T, Hkv, 1, generator=g) * 80.0)  # up to ~1e34
-    k[0, 0, :32] = torch.linspace(-3.0e38, 3.0e38, 32)
+    k[0, 0, :32] = torch.linspace(-1.0, 1.0, 32) * 3.0e38    # (a linspace over +-3e38 overflows its fp32 step)
     k[1, 1, 32:64] = 3.0e7                                   # just above 65504 * 448
     v = torch.randn(T, Hkv, D, generator=g) * 1e9
     kb, vb = k.to(torch.bfloat16), v.to(torch.bfloat16)
