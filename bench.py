@@ -78,6 +78,12 @@ def parse():
                     help="sparse (top-K) decode: this many index-list columns per sequence (0: dense decode)")
     ap.add_argument("--extend", type=int, default=0,
                     help="extend (prefill) step: this many new tokens per sequence (0: the decode step)")
+    ap.add_argument("--precise-p", action="store_true",
+                    help="extend with P carried to 16+ bits (two bf16 terms on the flash kernel; fp32 on the "
+                         "CUDA-core decode)")
+    ap.add_argument("--extend-path", type=int, default=None, choices=[0, 1, 2],
+                    help="extend kernel: 0 automatic (the default), 1 each new token's prefix on the CUDA-core "
+                         "decode (fp32 P), 2 the flash kernel (GQA) / the tensor-core decode (MLA)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--seed", type=int, default=None)
     return ap.parse_args()
@@ -581,19 +587,32 @@ def run_reference(args, world, rank):
 EXTEND_METRIC = "quantized-KV extend (prefill) attention TFLOP/s (% of GB300 bf16 peak); kvq_store of the new rows"
 
 
-def extend_kernel_name(case):
-    if case.mla:
-        return "kvq_extend (decode kernels over each new token's causal prefix, + merge)"
-    return "kvq_extend (extend_tc_kernel)"
+def extend_choice(kvq, case, L, total_q, path, precise=False):
+    """The extend kernel the library picks: 3 (flash kernel), 4 (flash, P as two bf16 terms), 1 or 2 (prefixes
+    on the CUDA-core / tensor-core decode)."""
+    p = kvq.kvq_extend_path(L, total_q, case.num_q_heads, case.max_pages, path, precise)
+    if p < 0:
+        raise RuntimeError("no extend kernel for this shape and path (status %d)" % p)
+    return p
 
 
-def extend_launches(kvq, case, L, total_q):
-    """Kernels one extend step launches: the store, then the GQA extend kernel; for MLA the prefix expansion
-    and, per chunk of 1024 new tokens, the decode (with the merge on the tensor-core path)."""
-    if not case.mla:
+def extend_kernel_name(choice):
+    if choice == 3:
+        return "kvq_extend (extend_tc_kernel)"
+    if choice == 4:
+        return "kvq_extend (extend_tc_kernel, P as two bf16 terms)"
+    if choice == 1:
+        return "kvq_extend (CUDA-core decode over each new token's causal prefix)"
+    return "kvq_extend (tensor-core decode over each new token's causal prefix, + merge)"
+
+
+def extend_launches(choice, total_q):
+    """Kernels one extend step launches: the store, then the flash kernel; or the prefix expansion and, per
+    chunk of 1024 new tokens, the decode (with the merge on the tensor-core path)."""
+    if choice >= 3:
         return 2
     chunk = min(total_q, 1024)
-    per = 2 if kvq.kvq_decode_path(L, chunk, case.num_q_heads, case.max_pages) == 2 else 1
+    per = 2 if choice == 2 else 1
     return 2 + per * ((total_q + chunk - 1) // chunk)
 
 
@@ -635,12 +654,16 @@ def run_extend(args, world, rank):
     sk, ss = case.k[rows], case.slot_mapping[rows]  # the step re-stores its new rows
     sv = None if case.mla else case.v[rows]
     out = torch.empty(q.shape[0], case.num_q_heads, case.v_dim, dtype=torch.bfloat16, device=dev)
-    ws = kvq.alloc_extend_workspace(dev, L, q.shape[0], case.num_q_heads, case.max_pages)
+    path, precise = args.extend_path, args.precise_p
+    choice = extend_choice(kvq, case, L, int(q.shape[0]), path, precise)
+    ws = kvq.alloc_extend_workspace(dev, L, q.shape[0], case.num_q_heads, case.max_pages, path=path,
+                                    precise_p=precise)
     flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)  # 4x L2
     stream = torch.cuda.current_stream()
 
     def extend(q_, qs_, bt_, sl_, o):
-        kvq.kvq_extend(q_, codes, scales, bt_, sl_, qs_, o, ws, L, case.kind, case.sm_scale)
+        kvq.kvq_extend(q_, codes, scales, bt_, sl_, qs_, o, ws, L, case.kind, case.sm_scale, path=path,
+                       precise_p=precise)
 
     for _ in range(args.warmup):
         flush.fill_(1)
@@ -717,21 +740,22 @@ def run_extend(args, world, rank):
         "unit": "TFLOP/s",
         "n_gpus": world, "steps": K, "warmup": args.warmup, "ms_per_step": round(total_ms / K, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "bf16",  # K and V dequantized to bf16, P bf16, fp32 accumulation on the tensor cores
+        "dtype": "bf16",  # K and V dequantized to bf16, fp32 accumulation (P bf16 on the tensor cores)
         "data": "synthetic (seeded; workloads.py)",
         "config": dict(workload_config(args, case, store_rows, keys, world), new_tokens_per_seq=args.extend,
-                       total_new_tokens=int(q.shape[0]), keys_read=keys),
+                       total_new_tokens=int(q.shape[0]), keys_read=keys, extend_path=path or 0,
+                       precise_p=bool(precise)),
         "extend_us": round(ext_s * 1e6, 2),
         "extend_tflops": round(achieved, 1),
         "store_us": round(statistics.mean(store_ms) * 1e3, 2),
         "store_gbs": round(store_b / (statistics.mean(store_ms) / 1e3) / 1e9, 1),
-        "roofline": {"bound": "tensor", "kernel": extend_kernel_name(case), "achieved": round(achieved, 1),
+        "roofline": {"bound": "tensor", "kernel": extend_kernel_name(choice), "achieved": round(achieved, 1),
                      "peak": peak, "unit": "TFLOP/s", "frac": round(achieved / peak, 4) if peak else None,
                      "peak_source": "MEASURED_PEAKS.json bf16_tflops (burst; of measured)", "traffic": None},
         "clocks": clk,
         "e2e": {"value": round(world * flops / e2e_s / 1e12, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": hout.numel() * hout.element_size()},
-        "gpu_launches": extend_launches(kvq, case, L, int(q.shape[0])) * K,
+        "gpu_launches": extend_launches(choice, int(q.shape[0])) * K,
     }
     if rank == 0 and not args.no_cpu_baseline:
         res["cpu_baseline"] = extend_cpu_baseline(case, args)

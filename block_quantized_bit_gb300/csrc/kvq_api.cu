@@ -251,22 +251,47 @@ bool plan_sparse(const kvq_layout* layout, int32_t batch, int32_t num_q_heads, i
   return true;
 }
 
-// MLA extend: every new token is a sequence of its own (its causal prefix, the block-table row of the sequence
-// it belongs to), decoded in chunks of at most kExtendMlaChunk tokens by the MLA decode kernels.  Workspace:
-// the decode workspace of one chunk (its status word at offset 0 is the call's), then the per-token
-// prefix lengths and block-table rows.
-constexpr int32_t kExtendMlaChunk = 1024;
+// Extend by prefixes: every new token is a sequence of its own (its causal prefix, the block-table row of the
+// sequence it belongs to), decoded in chunks of at most kExtendChunk tokens by the decode kernels.  This is
+// how the MLA latent row is extended, and the GQA path when the flash kernel cannot serve the shape or the
+// caller asks for fp32 probabilities.  Workspace: the decode workspace of one chunk (its status word at
+// offset 0 is the call's), then the per-token prefix lengths and block-table rows.
+constexpr int32_t kExtendChunk = 1024;
 
-struct ExtendMlaPlan {
+struct ExtendPlan {
+  bool flash;              // the GQA flash-style tcgen05 kernel (else: prefixes through the decode kernels)
+  bool split;              // the flash kernel feeds P as two bf16 terms
+  kvq_decode_options dec;  // the decode kernel choice of the prefix path
   int32_t chunk;
   size_t dense_bytes, lens_offset, rows_offset, total;
 };
 
-bool plan_extend_mla(const kvq_layout& L, int32_t total_q, int32_t num_q_heads, int32_t max_pages,
-                     ExtendMlaPlan* ep) {
-  ep->chunk = std::max<int32_t>(1, std::min<int32_t>(total_q, kExtendMlaChunk));
+// The extend's kernel choice and workspace.  False: invalid sizes or options, or no kernel for the shape.
+bool plan_extend(const kvq_layout& L, int32_t total_q, int32_t num_q_heads, int32_t max_pages,
+                 const kvq_extend_options* o, ExtendPlan* ep) {
+  const int32_t path = o ? o->path : 0;
+  const bool precise = o && o->precise_p != 0;
+  if (path < 0 || path > 2 || total_q < 0 || num_q_heads <= 0 || max_pages <= 0) return false;
+  if (num_q_heads % L.num_kv_heads != 0) return false;
+  const int32_t group = num_q_heads / L.num_kv_heads;
+  // the batch bound is checked per call; any batch up to it gives the same choice
+  const bool flash_ok = extend_tc_supported(L.head_dim, L.v_dim, L.mla, group, 1);
+  ep->flash = !L.mla && (path == 2 || (path == 0 && flash_ok));
+  ep->split = ep->flash && precise;
+  ep->dec.pages_per_split = 0;
+  ep->dec.path = path == 1 ? 1 : (path == 2 ? 2 : 0);
+  if (!ep->flash && precise) {
+    if (path == 2) return false;  // the tensor-core decode keeps P in bf16
+    ep->dec.path = 1;
+  }
+  if (ep->flash) {
+    ep->chunk = 0;
+    ep->dense_bytes = ep->lens_offset = ep->rows_offset = ep->total = kWorkspaceHeader;
+    return flash_ok;
+  }
+  ep->chunk = std::max<int32_t>(1, std::min<int32_t>(total_q, kExtendChunk));
   WorkspacePlan w;
-  if (!plan_workspace(L, ep->chunk, num_q_heads, max_pages, nullptr, &w) || w.path < 0) return false;
+  if (!plan_workspace(L, ep->chunk, num_q_heads, max_pages, &ep->dec, &w) || w.path < 0) return false;
   auto up = [](size_t x) { return (x + 255) / 256 * 256; };
   const size_t n = static_cast<size_t>(std::max<int32_t>(total_q, 1)) * sizeof(int32_t);
   ep->dense_bytes = up(w.total);
@@ -276,35 +301,18 @@ bool plan_extend_mla(const kvq_layout& L, int32_t total_q, int32_t num_q_heads, 
   return true;
 }
 
-kvq_status extend_mla(const void* q, const void* pool, const void* scales, const int32_t* block_table,
-                      int32_t max_pages_per_seq, const int32_t* seq_lens, const int32_t* q_start, int32_t total_q,
-                      int32_t batch, int32_t num_q_heads, float sm_scale, void* out, kvq_out_dtype out_dtype,
-                      void* workspace, size_t workspace_bytes, const kvq_layout* layout, kvq_kind kind,
-                      void* stream) {
-  if (!decode_cc_supported(layout->head_dim, layout->v_dim, layout->mla)) return KVQ_EUNSUPPORTED;
-  if (batch > kMaxExtendBatch) return KVQ_EUNSUPPORTED;
-  ExtendMlaPlan ep;
-  if (!plan_extend_mla(*layout, total_q, num_q_heads, max_pages_per_seq, &ep)) return KVQ_EUNSUPPORTED;
-  if (!workspace) return KVQ_EINVAL;
-  if (workspace_bytes < ep.total) return KVQ_EWORKSPACE;
-  if (!aligned(workspace)) return KVQ_EALIGN;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
+kvq_status extend_prefixes(const ExtendPlan& ep, const void* q, const void* pool, const void* scales,
+                           const int32_t* block_table, int32_t max_pages_per_seq, const int32_t* seq_lens,
+                           const int32_t* q_start, int32_t total_q, int32_t batch, int32_t num_q_heads, float sm_scale,
+                           void* out, kvq_out_dtype out_dtype, void* workspace, const kvq_layout* layout,
+                           kvq_kind kind, cudaStream_t s) {
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  if (cudaMemsetAsync(ws, 0, sizeof(uint32_t), s) != cudaSuccess) return KVQ_ECUDA;
-  if (batch == 0 || total_q == 0) return KVQ_OK;
-  if (!q || !pool || (has_scales(kind) && !scales) || !block_table || !seq_lens || !q_start || !out)
-    return KVQ_EINVAL;
-  if (!aligned(q) || !aligned(pool) || !aligned(scales) || !aligned(out) ||
-      (reinterpret_cast<uintptr_t>(block_table) % 4) != 0 || (reinterpret_cast<uintptr_t>(seq_lens) % 4) != 0 ||
-      (reinterpret_cast<uintptr_t>(q_start) % 4) != 0)
-    return KVQ_EALIGN;
-  kvq_status st = kvq_device_check();
-  if (st != KVQ_OK) return st;
   int32_t* vlens = reinterpret_cast<int32_t*>(ws + ep.lens_offset);
   int32_t* vrow = reinterpret_cast<int32_t*>(ws + ep.rows_offset);
   // rows no sequence covers (an inconsistent q_start) keep length 0: zeros out
   if (cudaMemsetAsync(ws + ep.lens_offset, 0, ep.total - ep.lens_offset, s) != cudaSuccess) return KVQ_ECUDA;
-  st = launch_extend_expand(q_start, seq_lens, batch, total_q, vlens, vrow, reinterpret_cast<uint32_t*>(ws), s);
+  kvq_status st =
+      launch_extend_expand(q_start, seq_lens, batch, total_q, vlens, vrow, reinterpret_cast<uint32_t*>(ws), s);
   if (st != KVQ_OK) return st;
   const size_t q_row = static_cast<size_t>(num_q_heads) * layout->head_dim * 2;
   const size_t o_row = static_cast<size_t>(num_q_heads) * layout->v_dim * (out_dtype == KVQ_OUT_F32 ? 4 : 2);
@@ -312,7 +320,7 @@ kvq_status extend_mla(const void* q, const void* pool, const void* scales, const
     const int32_t n = std::min<int32_t>(ep.chunk, total_q - c0);
     st = decode_common(static_cast<const uint8_t*>(q) + c0 * q_row, pool, scales, block_table, max_pages_per_seq,
                        vlens + c0, n, num_q_heads, sm_scale, static_cast<uint8_t*>(out) + c0 * o_row, out_dtype,
-                       workspace, ep.dense_bytes, layout, kind, nullptr, stream, false, vrow + c0);
+                       workspace, ep.dense_bytes, layout, kind, &ep.dec, s, false, vrow + c0);
     if (st != KVQ_OK) return st;
   }
   return KVQ_OK;
@@ -510,19 +518,42 @@ kvq_status kvq_decode_sparse(const void* q, const void* pool, const void* scales
 size_t kvq_extend_workspace_bytes(void) { return kWorkspaceHeader; }
 
 size_t kvq_extend_workspace_bytes_ex(const kvq_layout* layout, int32_t total_q, int32_t num_q_heads,
-                                     int32_t max_pages_per_seq) {
-  if (check_layout(layout) != KVQ_OK || total_q < 0 || num_q_heads <= 0 || max_pages_per_seq <= 0) return 0;
-  if (num_q_heads % layout->num_kv_heads != 0) return 0;
-  if (!layout->mla) return kWorkspaceHeader;
-  ExtendMlaPlan ep;
-  if (!plan_extend_mla(*layout, total_q, num_q_heads, max_pages_per_seq, &ep)) return 0;
+                                     int32_t max_pages_per_seq, const kvq_extend_options* options) {
+  if (check_layout(layout) != KVQ_OK || layout->page_size != kPageTokens) return 0;
+  ExtendPlan ep;
+  if (!plan_extend(*layout, total_q, num_q_heads, max_pages_per_seq, options, &ep)) return 0;
   return ep.total;
+}
+
+int32_t kvq_extend_path(const kvq_layout* layout, int32_t total_q, int32_t num_q_heads, int32_t max_pages_per_seq,
+                        const kvq_extend_options* options) {
+  if (check_layout(layout) != KVQ_OK) return KVQ_EINVAL;
+  if (total_q < 0 || num_q_heads <= 0 || max_pages_per_seq <= 0 || num_q_heads % layout->num_kv_heads != 0)
+    return KVQ_EINVAL;
+  if (options && (options->path < 0 || options->path > 2)) return KVQ_EINVAL;
+  if (layout->page_size != kPageTokens) return KVQ_EUNSUPPORTED;
+  ExtendPlan ep;
+  if (!plan_extend(*layout, total_q, num_q_heads, max_pages_per_seq, options, &ep)) return KVQ_EUNSUPPORTED;
+  if (ep.flash) return ep.split ? 4 : 3;
+  WorkspacePlan w;
+  plan_workspace(*layout, ep.chunk, num_q_heads, max_pages_per_seq, &ep.dec, &w);
+  return w.path;
 }
 
 kvq_status kvq_extend(const void* q, const void* pool, const void* scales, const int32_t* block_table,
                       int32_t max_pages_per_seq, const int32_t* seq_lens, const int32_t* q_start, int32_t total_q,
                       int32_t batch, int32_t num_q_heads, float sm_scale, void* out, kvq_out_dtype out_dtype,
                       void* workspace, size_t workspace_bytes, const kvq_layout* layout, kvq_kind kind, void* stream) {
+  return kvq_extend_ex(q, pool, scales, block_table, max_pages_per_seq, seq_lens, q_start, total_q, batch,
+                       num_q_heads, sm_scale, out, out_dtype, workspace, workspace_bytes, layout, kind, nullptr,
+                       stream);
+}
+
+kvq_status kvq_extend_ex(const void* q, const void* pool, const void* scales, const int32_t* block_table,
+                         int32_t max_pages_per_seq, const int32_t* seq_lens, const int32_t* q_start,
+                         int32_t total_q, int32_t batch, int32_t num_q_heads, float sm_scale, void* out,
+                         kvq_out_dtype out_dtype, void* workspace, size_t workspace_bytes, const kvq_layout* layout,
+                         kvq_kind kind, const kvq_extend_options* options, void* stream) {
   kvq_status st = check_layout(layout);
   if (st != KVQ_OK) return st;
   if (!kind_read_ok(kind)) return KVQ_EKIND;
@@ -530,17 +561,16 @@ kvq_status kvq_extend(const void* q, const void* pool, const void* scales, const
   if (out_dtype != KVQ_OUT_BF16 && out_dtype != KVQ_OUT_F32) return KVQ_EINVAL;
   if (batch < 0 || total_q < 0 || num_q_heads <= 0 || max_pages_per_seq <= 0) return KVQ_EINVAL;
   if (num_q_heads % layout->num_kv_heads != 0) return KVQ_EINVAL;
+  if (options && (options->path < 0 || options->path > 2)) return KVQ_EINVAL;
   if (static_cast<int64_t>(total_q) * (num_q_heads / layout->num_kv_heads) > std::numeric_limits<int32_t>::max() - 128)
     return KVQ_EINVAL;  // the kernel counts query rows per sequence in 32 bits
   if (!(sm_scale > 0.0f) || sm_scale > std::numeric_limits<float>::max()) return KVQ_EINVAL;  // finite, > 0
   if (layout->page_size != kPageTokens) return KVQ_EUNSUPPORTED;
-  if (layout->mla)
-    return extend_mla(q, pool, scales, block_table, max_pages_per_seq, seq_lens, q_start, total_q, batch, num_q_heads,
-                      sm_scale, out, out_dtype, workspace, workspace_bytes, layout, kind, stream);
-  if (!extend_tc_supported(layout->head_dim, layout->v_dim, layout->mla, num_q_heads / layout->num_kv_heads, batch))
-    return KVQ_EUNSUPPORTED;
+  if (batch > kMaxExtendBatch) return KVQ_EUNSUPPORTED;
+  ExtendPlan ep;
+  if (!plan_extend(*layout, total_q, num_q_heads, max_pages_per_seq, options, &ep)) return KVQ_EUNSUPPORTED;
   if (!workspace) return KVQ_EINVAL;
-  if (workspace_bytes < kWorkspaceHeader) return KVQ_EWORKSPACE;
+  if (workspace_bytes < ep.total) return KVQ_EWORKSPACE;
   if (!aligned(workspace)) return KVQ_EALIGN;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (cudaMemsetAsync(workspace, 0, sizeof(uint32_t), s) != cudaSuccess) return KVQ_ECUDA;
@@ -553,6 +583,9 @@ kvq_status kvq_extend(const void* q, const void* pool, const void* scales, const
     return KVQ_EALIGN;
   st = kvq_device_check();
   if (st != KVQ_OK) return st;
+  if (!ep.flash)
+    return extend_prefixes(ep, q, pool, scales, block_table, max_pages_per_seq, seq_lens, q_start, total_q, batch,
+                           num_q_heads, sm_scale, out, out_dtype, workspace, layout, kind, s);
   ExtendArgs a;
   a.q = static_cast<const uint16_t*>(q);
   a.codes = static_cast<const uint8_t*>(pool);
@@ -572,6 +605,7 @@ kvq_status kvq_extend(const void* q, const void* pool, const void* scales, const
   a.score_scale = sm_scale * 1.4426950408889634f;  // log2(e)
   a.out_dtype = out_dtype;
   a.kind = kind;
+  a.split_p = ep.split ? 1 : 0;
   return launch_extend_tc(a, s);
 }
 

@@ -12,6 +12,10 @@
 // heads of a kv head share every dequantized K and V tile:
 //   S[128 rows][T keys]  = Q[128][D] . Kd[T][D]^T   (A = Q, B = the K tile; both K-major in shared memory)
 //   O[128 rows][D]      += P[128][T] . Vd[T][D]     (A = P in tensor memory, B = the V tile read MN-major)
+// P enters the MMA as bf16.  The SPLIT instances feed it as two bf16 terms, P = hi + lo with hi = bf16(p)
+// and lo = bf16(p - hi), through a second PV into the same O: the product then carries P to about 2^-17
+// relative instead of 2^-9, for twice the PV MMAs.  (All their exponentials run on the MUFU unit: the FMA-
+// pipe cubic's 1.5e-4 would otherwise dominate that error.)
 // with fp32 S and O in tensor memory.  Q, K and V use the canonical no-swizzle core-matrix layout
 //   off(t, d) = (t % 8) * 16 + (t / 8) * RS + (d % 8) * 2 + (d / 8) * 128,   RS = D * 16,
 // with t the row (query row or key): K-major descriptors take LBO = 128 and SBO = RS, the MN-major one
@@ -94,6 +98,13 @@ struct XCfg {
   // tensor-memory columns: O [0, D); S buffer b [D + b T, D + (b + 1) T); P buffer b [384 + b T / 2, ...)
   static constexpr int S_COL = D;
   static constexpr int P_COL = 384;
+  // the low P terms of the SPLIT instances: buffer b at [PLO_COL + b T / 2, ...) where those columns are
+  // free (D = 256); else (D = 128) inside S buffer b, which the softmax has read when it forms them: half hf
+  // of the keys puts its T / 4 columns at the start of its own T / 2 columns of S.  Tensor-core operations
+  // of different accumulators are not ordered among themselves, so then the QK that next writes S buffer b
+  // waits for the PV that read those columns.
+  static constexpr int PLO_COL = P_COL + T;
+  static constexpr bool LO_IN_S = PLO_COL + T > kTmemCols;
   static_assert(D == 128 || D == 256, "extend needs head_dim 128 or 256");
   static_assert(D + 2 * T <= P_COL && P_COL + T <= kTmemCols, "tensor-memory columns");
   static_assert(PARTS * T == kDwThreads && NCH % 2 == 0 && NBT == 2, "dequant split");
@@ -270,7 +281,7 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity) {
   return __all_sync(0xffffffffu, mbar_wait_bounded(bar, parity));
 }
 
-template <int D, int KIND>
+template <int D, int KIND, bool SPLIT>
 __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const ExtendArgs a, const __grid_constant__ CUtensorMap tmap) {
   using Cfg = XCfg<D>;
   constexpr int T = Cfg::T;
@@ -473,6 +484,13 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const ExtendArgs
     const uint64_t dK = smem_desc(smem_u32(sK), 128, Cfg::RS);
     const uint64_t dV = smem_desc(smem_u32(sV), Cfg::RS, 128);
     const uint32_t tS = tmem + Cfg::S_COL, tO = tmem, tP = tmem + Cfg::P_COL;
+    // column of the low P terms of k-step ks (16 keys) of buffer bp (SPLIT)
+    auto lo_col = [&](int bp, int ks) -> uint32_t {
+      if constexpr (Cfg::LO_IN_S)
+        return tmem + Cfg::S_COL + bp * T + (ks / (T / 32)) * (T / 2) + (ks % (T / 32)) * 8;
+      else
+        return tmem + Cfg::PLO_COL + bp * (T / 2) + ks * 8;
+    };
     uint32_t n = 0, items = 0;  // tiles QK'd; items finished
     // PV of tile m; the first tile of an item overwrites O, once the previous item's O has been read out
     auto pv = [&](uint32_t m, bool first) -> bool {
@@ -485,6 +503,11 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const ExtendArgs
       for (int ks = 0; ks < T / 16; ++ks)
         mma_bf16_tmem_a(tO, tP + bp * (T / 2) + ks * 8, dV + static_cast<uint64_t>((ks * 2 * Cfg::RS) >> 4),
                         idesc_pv, (!first || ks > 0) ? 1u : 0u);
+      if constexpr (SPLIT) {
+#pragma unroll
+        for (int ks = 0; ks < T / 16; ++ks)
+          mma_bf16_tmem_a(tO, lo_col(bp, ks), dV + static_cast<uint64_t>((ks * 2 * Cfg::RS) >> 4), idesc_pv, 1u);
+      }
       mma_commit(&bar_pv_done[bp]);
       __syncwarp();
       return true;
@@ -495,8 +518,11 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const ExtendArgs
       for (int32_t i = 0; i < it.ntiles; ++i, ++n) {
         const int b = n & 1;
         if (!warp_wait(bar_k_full, n & 1)) { ok = false; break; }
-        // S buffer b was read by the softmax of tile n - 2
+        // S buffer b was read by the softmax of tile n - 2 (and, holding low P terms, by the PV of tile n - 2)
         if (n >= 2 && !warp_wait(&bar_p_full[b], ((n >> 1) - 1) & 1)) { ok = false; break; }
+        if constexpr (SPLIT && Cfg::LO_IN_S) {
+          if (n >= 2 && !warp_wait(&bar_pv_done[b], ((n >> 1) - 1) & 1)) { ok = false; break; }
+        }
         tc_fence_after();
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks)
@@ -521,6 +547,9 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const ExtendArgs
     const uint32_t tS = tmem + Cfg::S_COL + lane_base + hf * (T / 2);
     const uint32_t tO = tmem + lane_base + hf * (D / 2);
     const uint32_t tP = tmem + Cfg::P_COL + lane_base + hf * (T / 4);
+    // this warp's low P terms of buffer b start at tPlo + b * PLO_STRIDE (SPLIT)
+    const uint32_t tPlo = Cfg::LO_IN_S ? tS : tmem + Cfg::PLO_COL + lane_base + hf * (T / 4);
+    constexpr int PLO_STRIDE = Cfg::LO_IN_S ? T : T / 2;
     float* sRed = reinterpret_cast<float*>(smem + Cfg::RED_OFF);
     float* sSum = reinterpret_cast<float*>(smem + Cfg::SUM_OFF);
     const int32_t tb = kM / G;  // new tokens per query block
@@ -635,14 +664,15 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const ExtendArgs
           for (int h = 0; h < T / 64; ++h) {
             uint32_t v[32];
             tmem_ld32(tS + b * T + h * 32, v);
-            uint32_t w[16];
+            uint32_t w[16], wl[SPLIT ? 16 : 1];
 #pragma unroll
             for (int e = 0; e < 16; ++e) {
               const float x0 = fmaf(__uint_as_float(v[2 * e]), a.score_scale, -m_used);
               const float x1 = fmaf(__uint_as_float(v[2 * e + 1]), a.score_scale, -m_used);
               // every fourth pair on the FMA pipe, the rest on the MUFU unit
-              float p0 = (e & 3) == 3 ? ex2_fma(x0) : ex2(x0);
-              float p1 = (e & 3) == 3 ? ex2_fma(x1) : ex2(x1);
+              const bool fma_pipe = !SPLIT && (e & 3) == 3;
+              float p0 = fma_pipe ? ex2_fma(x0) : ex2(x0);
+              float p1 = fma_pipe ? ex2_fma(x1) : ex2(x1);
               if constexpr (decltype(masked)::value) {
                 const int k = h * 32 + 2 * e;  // k and k + 1 share a page
                 const bool pg = ((hmask >> (k / kPage)) & 1u) != 0u;
@@ -652,8 +682,14 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const ExtendArgs
               ls[(2 * e) & 3] += p0;
               ls[(2 * e + 1) & 3] += p1;
               w[e] = pack_bf16x2(p0, p1);
+              if constexpr (SPLIT) {
+                const float2 hv = unpack_bf16x2(w[e]);  // p - bf16(p) is exact in fp32
+                wl[e] = pack_bf16x2(p0 - hv.x, p1 - hv.y);
+              }
             }
             tmem_st16u(tP + b * (T / 2) + h * 16, w);
+            // (in S: columns [16 h, 16 h + 16) of this half, all loaded by now)
+            if constexpr (SPLIT) tmem_st16u(tPlo + b * PLO_STRIDE + h * 16, wl);
           }
           l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
         };
@@ -720,15 +756,15 @@ __global__ void exp2_probe_kernel(const float* __restrict__ x, float* __restrict
     y[i] = ex2_fma(x[i]);
 }
 
-template <int D>
+template <int D, bool SPLIT>
 kvq_status launch_extend_d(const ExtendArgs& a, cudaStream_t stream) {
   using Cfg = XCfg<D>;
-  decltype(&extend_tc_kernel<D, KVQ_FP8_E4M3>) kern = nullptr;
+  decltype(&extend_tc_kernel<D, KVQ_FP8_E4M3, SPLIT>) kern = nullptr;
   switch (a.kind) {
-    case KVQ_FP8_E4M3: kern = extend_tc_kernel<D, KVQ_FP8_E4M3>; break;
-    case KVQ_Q8_0: kern = extend_tc_kernel<D, KVQ_Q8_0>; break;
-    case KVQ_FP8_E4M3_UNSCALED: kern = extend_tc_kernel<D, KVQ_FP8_E4M3_UNSCALED>; break;
-    case KVQ_FP8_E5M2_UNSCALED: kern = extend_tc_kernel<D, KVQ_FP8_E5M2_UNSCALED>; break;
+    case KVQ_FP8_E4M3: kern = extend_tc_kernel<D, KVQ_FP8_E4M3, SPLIT>; break;
+    case KVQ_Q8_0: kern = extend_tc_kernel<D, KVQ_Q8_0, SPLIT>; break;
+    case KVQ_FP8_E4M3_UNSCALED: kern = extend_tc_kernel<D, KVQ_FP8_E4M3_UNSCALED, SPLIT>; break;
+    case KVQ_FP8_E5M2_UNSCALED: kern = extend_tc_kernel<D, KVQ_FP8_E5M2_UNSCALED, SPLIT>; break;
   }
   if (kern == nullptr) return KVQ_EKIND;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES) != cudaSuccess)
@@ -790,8 +826,8 @@ kvq_status launch_extend_expand(const int32_t* q_start, const int32_t* seq_lens,
 }
 
 kvq_status launch_extend_tc(const ExtendArgs& a, cudaStream_t stream) {
-  if (a.head_dim == 128) return launch_extend_d<128>(a, stream);
-  if (a.head_dim == 256) return launch_extend_d<256>(a, stream);
+  if (a.head_dim == 128) return a.split_p ? launch_extend_d<128, true>(a, stream) : launch_extend_d<128, false>(a, stream);
+  if (a.head_dim == 256) return a.split_p ? launch_extend_d<256, true>(a, stream) : launch_extend_d<256, false>(a, stream);
   return KVQ_EUNSUPPORTED;
 }
 

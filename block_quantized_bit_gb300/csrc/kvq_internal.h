@@ -118,6 +118,7 @@ struct ExtendArgs {
   float score_scale;          // sm_scale * log2(e): the kernels work in the exp2 domain
   kvq_out_dtype out_dtype;
   kvq_kind kind;
+  int32_t split_p;            // nonzero: P enters the PV MMA as two bf16 terms (hi + lo)
 };
 constexpr int32_t kMaxExtendBatch = 2048;  // sequences whose item bases fit the kernel's shared table
 bool extend_tc_supported(int32_t head_dim, int32_t v_dim, int32_t mla, int32_t group, int32_t batch);

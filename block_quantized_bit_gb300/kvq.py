@@ -35,7 +35,8 @@ EXPORTS = ["kvq_pool_bytes", "kvq_scale_bytes", "kvq_bytes_per_token", "kvq_num_
            "kvq_workspace_status", "kvq_encode_probe", "kvq_quantize_probe", "kvq_dequant_probe", "kvq_strerror",
            "kvq_device_check", "kvq_version", "kvq_decode_noalloc", "kvq_noalloc_status", "kvq_wait_probe",
            "kvq_extend_workspace_bytes", "kvq_extend", "kvq_store_act_quant", "kvq_store_unscaled",
-           "kvq_bytes_per_token_ex", "kvq_num_pages_ex", "kvq_exp2_probe", "kvq_extend_workspace_bytes_ex"]
+           "kvq_bytes_per_token_ex", "kvq_num_pages_ex", "kvq_exp2_probe", "kvq_extend_workspace_bytes_ex",
+           "kvq_extend_ex", "kvq_extend_path"]
 
 
 class kvq_layout(ctypes.Structure):
@@ -45,6 +46,10 @@ class kvq_layout(ctypes.Structure):
 
 class kvq_decode_options(ctypes.Structure):
     _fields_ = [("pages_per_split", ctypes.c_int32), ("path", ctypes.c_int32)]
+
+
+class kvq_extend_options(ctypes.Structure):
+    _fields_ = [("path", ctypes.c_int32), ("precise_p", ctypes.c_int32)]
 
 
 class KvqError(RuntimeError):
@@ -66,6 +71,7 @@ def lib():
         P, i64, i32, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_size_t
         LP = ctypes.POINTER(kvq_layout)
         OP = ctypes.POINTER(kvq_decode_options)
+        EP = ctypes.POINTER(kvq_extend_options)
         sig = {
             "kvq_pool_bytes": (sz, [LP]),
             "kvq_scale_bytes": (sz, [LP]),
@@ -97,7 +103,10 @@ def lib():
             "kvq_wait_probe": (i32, [P, P]),
             "kvq_noalloc_status": (i32, [P]),
             "kvq_exp2_probe": (i32, [P, P, i64, P]),
-            "kvq_extend_workspace_bytes_ex": (sz, [LP, i32, i32, i32]),
+            "kvq_extend_workspace_bytes_ex": (sz, [LP, i32, i32, i32, EP]),
+            "kvq_extend_path": (i32, [LP, i32, i32, i32, EP]),
+            "kvq_extend_ex": (i32, [P, P, P, P, i32, P, P, i32, i32, i32, ctypes.c_float, P, i32, P, sz, LP, i32,
+                                    EP, P]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -299,25 +308,40 @@ def kvq_store_act_quant(pool: torch.Tensor, scales: torch.Tensor, kv: torch.Tens
            "kvq_store_act_quant")
 
 
+def _extend_opts(path, precise_p=False):
+    if path is None and not precise_p:
+        return None
+    return ctypes.byref(kvq_extend_options(int(path or 0), 1 if precise_p else 0))
+
+
 def alloc_extend_workspace(device="cuda", layout: Optional[Layout] = None, total_q=0, num_q_heads=1,
-                           max_pages_per_seq=1):
-    """The extend's workspace: its status word for GQA; for an MLA layout (pass the sizes) also the decode
-    workspace of one chunk of per-token prefixes."""
-    if layout is None or not layout.mla:
+                           max_pages_per_seq=1, path=None, precise_p=False):
+    """The extend's workspace for these sizes and kernel choice (path None or 0: automatic; 1: each new
+    token's prefix on the CUDA-core decode; 2: the flash kernel / the MLA tensor-core decode; precise_p: P
+    carried to 16 bits or more).  Without a layout: the flash kernel's status word."""
+    if layout is None:
         n = lib().kvq_extend_workspace_bytes()
     else:
         n = lib().kvq_extend_workspace_bytes_ex(ctypes.byref(layout.c()), int(total_q), int(num_q_heads),
-                                                int(max_pages_per_seq))
+                                                int(max_pages_per_seq), _extend_opts(path, precise_p))
         if n == 0:
             raise KvqError(-1, "kvq_extend_workspace_bytes_ex")
     return torch.empty(n, dtype=torch.uint8, device=device)
 
 
+def kvq_extend_path(layout: Layout, total_q, num_q_heads, max_pages_per_seq, path=None, precise_p=False) -> int:
+    """3 (flash kernel), 4 (flash, P as two bf16 terms), 1 or 2 (prefixes on the CUDA-core / tensor-core
+    decode), or a negative status."""
+    return lib().kvq_extend_path(ctypes.byref(layout.c()), int(total_q), int(num_q_heads), int(max_pages_per_seq),
+                                 _extend_opts(path, precise_p))
+
+
 def kvq_extend(q: torch.Tensor, pool: torch.Tensor, scales: torch.Tensor, block_table: torch.Tensor,
                seq_lens: torch.Tensor, q_start: torch.Tensor, out: torch.Tensor, workspace: torch.Tensor,
-               layout: Layout, kind, sm_scale: float = 1.0, stream=None):
+               layout: Layout, kind, sm_scale: float = 1.0, stream=None, path=None, precise_p=False):
     """Extend (prefill) attention: the q rows q_start[b] .. q_start[b+1]-1 ([total_q, Hq, D] bf16) are the
-    last new tokens of sequence b and attend causally over the pool; out is [total_q, Hq, Dv]."""
+    last new tokens of sequence b and attend causally over the pool; out is [total_q, Hq, Dv].  path None
+    (and no precise_p) calls kvq_extend (automatic), else kvq_extend_ex with those options."""
     if out.dtype == torch.bfloat16:
         od = KVQ_OUT_BF16
     elif out.dtype == torch.float32:
@@ -326,10 +350,14 @@ def kvq_extend(q: torch.Tensor, pool: torch.Tensor, scales: torch.Tensor, block_
         raise TypeError("out must be bfloat16 or float32")
     total_q, Hq = q.shape[0], q.shape[1]
     B = seq_lens.numel()
-    _check(lib().kvq_extend(_ptr(q), _ptr(pool), _ptr(scales), _ptr(block_table), int(block_table.shape[1]),
-                            _ptr(seq_lens), _ptr(q_start), int(total_q), int(B), int(Hq), float(sm_scale), _ptr(out),
-                            od, _ptr(workspace), int(workspace.numel() * workspace.element_size()),
-                            ctypes.byref(layout.c()), _kind(kind), _stream(stream)), "kvq_extend")
+    args = (_ptr(q), _ptr(pool), _ptr(scales), _ptr(block_table), int(block_table.shape[1]), _ptr(seq_lens),
+            _ptr(q_start), int(total_q), int(B), int(Hq), float(sm_scale), _ptr(out), od, _ptr(workspace),
+            int(workspace.numel() * workspace.element_size()), ctypes.byref(layout.c()), _kind(kind))
+    opts = _extend_opts(path, precise_p)
+    if opts is None:
+        _check(lib().kvq_extend(*args, _stream(stream)), "kvq_extend")
+    else:
+        _check(lib().kvq_extend_ex(*args, opts, _stream(stream)), "kvq_extend_ex")
 
 
 def kvq_workspace_status(workspace: torch.Tensor, stream=None) -> int:

@@ -229,33 +229,63 @@ kvq_status kvq_store_act_quant(void* pool, void* scales, const void* kv, const i
  *   seq_lens     stored tokens per sequence, the new ones included: the n_b = q_start[b + 1] - q_start[b]
  *                new tokens are the last n_b, so new token i sits at position seq_lens[b] - n_b + i
  *   out          [total_q, num_q_heads, v_dim], bf16 or f32 (out_dtype), device
- *   workspace    at least kvq_extend_workspace_bytes_ex() (kvq_extend_workspace_bytes() for GQA: its status
- *                word), 16-byte aligned, device
+ *   workspace    at least kvq_extend_workspace_bytes_ex() for the same sizes and options, 16-byte aligned,
+ *                device
  * sm_scale must be finite and > 0 (else KVQ_EINVAL).  Other arguments as kvq_decode.
  * Query row (b, i, h) gets softmax(sm_scale * q.K^T) V over the positions
  * 0 .. seq_lens[b] - n_b + i of sequence b whose pages are not masked (causal), with K and V dequantized to
  * bf16 and fp32 accumulation; no valid position gives zeros.
- * GQA (head_dim = v_dim in {128, 256}, query heads per kv head dividing 128): one flash-style tcgen05 kernel,
- * each dequantized K/V tile shared by a block of 128 query rows.
- * MLA (the latent row, head_dim 576 / v_dim 512, "feat(kvcache): 8-bit DSV4 window/compressed KV", section
- * "What this adds"): every new token is decoded as a sequence of its own over its causal prefix, by the
- * decode kernels of kvq_decode (chosen as kvq_decode chooses them for a batch of up to 1024 such prefixes;
- * the tokens run in chunks of 1024), so its precision is the decode's; rows of a skipped sequence are zeros.
- * Supported: page_size 16, batch <= 2048, and the two shapes above; otherwise KVQ_EUNSUPPORTED.  q_start
- * and seq_lens are read on the device: a sequence with n_b < 0, n_b > seq_lens[b] or q_start[b + 1] >
- * total_q is skipped and makes kvq_workspace_status report KVQ_EINVAL, as does a block-table entry >=
+ * Kernels (kvq_extend_options.path; kvq_extend passes none, i.e. automatic):
+ *   flash (GQA with head_dim = v_dim in {128, 256} and query heads per kv head dividing 128): one
+ *     flash-style tcgen05 kernel, each dequantized K/V tile shared by a block of 128 query rows.  It feeds
+ *     the probabilities P to the MMA as bf16, so its error grows with the magnitude of V (about 2^-9 of
+ *     sum p|V|), as the tensor-core decode's does.
+ *   prefixes: every new token is decoded as a sequence of its own over its causal prefix, by the decode
+ *     kernels of kvq_decode (the tokens run in chunks of 1024, each chunk one kvq_decode-like call with
+ *     that many sequences), so its precision is the decode's.  It reads each prefix once per new token,
+ *     so it costs about n_b times the flash kernel's K/V bytes; L2 absorbs much of it.
+ * path 0 (automatic): flash where it supports the shape, else prefixes with the decode's automatic choice
+ * (the MLA latent row, head_dim 576 / v_dim 512, "feat(kvcache): 8-bit DSV4 window/compressed KV", section
+ * "What this adds", always takes prefixes); 1: prefixes on the CUDA-core decode (fp32 P, every
+ * kvq_decode shape); 2: flash for GQA, prefixes on the tensor-core decode for MLA.  kvq_extend_path tells
+ * which.  With precise_p (below) every path keeps P's rounding under 2^-16 relative, so the error no longer
+ * grows with |V| beyond the decode bound.  The rows of a skipped sequence (below) are left as they are by the flash kernel and set to zero
+ * by the prefixes.
+ * Supported: page_size 16, batch <= 2048, and the shapes of the chosen kernels; otherwise KVQ_EUNSUPPORTED.
+ * q_start and seq_lens are read on the device: a sequence with n_b < 0, n_b > seq_lens[b] or q_start[b + 1]
+ * > total_q is skipped and makes kvq_workspace_status report KVQ_EINVAL, as does a block-table entry >=
  * layout->num_pages (that page is skipped).  Asynchronous on `stream`.
  */
+typedef struct kvq_extend_options {
+    int32_t path;       /* 0 = automatic; 1 = prefixes on the CUDA-core decode; 2 = flash (GQA) / tensor-core
+                           decode (MLA) */
+    int32_t precise_p;  /* nonzero: P reaches the PV product with at least 16 significant bits.  The flash
+                           kernel feeds it as two bf16 terms, hi = bf16(p) and lo = bf16(p - hi), through a
+                           second PV (about 2^-17 relative; its exponentials all on the MUFU unit); prefixes
+                           run on the CUDA-core decode (fp32 P); path 2 on MLA is then KVQ_EUNSUPPORTED */
+} kvq_extend_options;
+/* The flash kernel's workspace: its status word (enough for the automatic choice on a supported GQA shape). */
 size_t kvq_extend_workspace_bytes(void);
-/* Workspace bytes kvq_extend needs for these sizes (a GQA layout: kvq_extend_workspace_bytes(); an MLA layout:
- * the decode workspace of one chunk of prefixes plus two int32 per query row).  0 if invalid. */
+/* Workspace bytes kvq_extend_ex needs for these sizes and options (options may be NULL): the flash kernel's
+ * status word, or the decode workspace of one chunk of prefixes plus two int32 per query row.  0 if
+ * invalid or unsupported. */
 size_t kvq_extend_workspace_bytes_ex(const kvq_layout* layout, int32_t total_q, int32_t num_q_heads,
-                                     int32_t max_pages_per_seq);
+                                     int32_t max_pages_per_seq, const kvq_extend_options* options);
+/* The extend kernel kvq_extend_ex would run: 3 (flash), 4 (flash with P as two bf16 terms), or the decode
+ * kernel of the prefixes, 1 (CUDA cores) or 2 (tensor cores).  Otherwise a negative kvq_status (KVQ_EINVAL for invalid sizes or options,
+ * KVQ_EUNSUPPORTED when no kernel supports the shape).  Host only; options may be NULL. */
+int32_t kvq_extend_path(const kvq_layout* layout, int32_t total_q, int32_t num_q_heads, int32_t max_pages_per_seq,
+                        const kvq_extend_options* options);
 kvq_status kvq_extend(const void* q, const void* pool, const void* scales, const int32_t* block_table,
                       int32_t max_pages_per_seq, const int32_t* seq_lens, const int32_t* q_start, int32_t total_q,
                       int32_t batch, int32_t num_q_heads, float sm_scale, void* out, kvq_out_dtype out_dtype,
                       void* workspace, size_t workspace_bytes, const kvq_layout* layout, kvq_kind kind,
                       void* stream);
+kvq_status kvq_extend_ex(const void* q, const void* pool, const void* scales, const int32_t* block_table,
+                         int32_t max_pages_per_seq, const int32_t* seq_lens, const int32_t* q_start,
+                         int32_t total_q, int32_t batch, int32_t num_q_heads, float sm_scale, void* out,
+                         kvq_out_dtype out_dtype, void* workspace, size_t workspace_bytes, const kvq_layout* layout,
+                         kvq_kind kind, const kvq_extend_options* options, void* stream);
 
 /*
  * The decode kernel kvq_decode_ex would run for these sizes and options: 1 (CUDA cores, one launch) or

@@ -121,11 +121,52 @@ def test_decode_argument_errors(lib):
     assert _decode(lib, L(), opts=bad) == -1
 
 
-def _extend(lib, layout, *, hq=8, kind=1, sm_scale=1.0, ws=FAKE, ws_bytes=256, total_q=5, batch=2, out_dtype=0):
+def _extend(lib, layout, *, hq=8, kind=1, sm_scale=1.0, ws=FAKE, ws_bytes=256, total_q=5, batch=2, out_dtype=0,
+            path=None):
     P = ctypes.c_void_p
-    return lib.kvq_extend(P(FAKE), P(FAKE), P(FAKE), P(FAKE), 10, P(FAKE), P(FAKE), total_q, batch, hq,
-                          ctypes.c_float(sm_scale), P(FAKE), out_dtype, P(ws), ws_bytes, ctypes.byref(layout.c()), kind,
-                          None)
+    args = (P(FAKE), P(FAKE), P(FAKE), P(FAKE), 10, P(FAKE), P(FAKE), total_q, batch, hq, ctypes.c_float(sm_scale),
+            P(FAKE), out_dtype, P(ws), ws_bytes, ctypes.byref(layout.c()), kind)
+    if path is None:
+        return lib.kvq_extend(*args, None)
+    return lib.kvq_extend_ex(*args, ctypes.byref(kvq.kvq_extend_options(path)), None)
+
+
+def _extend_ws(lib, layout, total_q, hq, max_pages, path=None):
+    opts = None if path is None else ctypes.byref(kvq.kvq_extend_options(path))
+    return lib.kvq_extend_workspace_bytes_ex(ctypes.byref(layout.c()), total_q, hq, max_pages, opts)
+
+
+def test_extend_kernel_choice(lib):
+    """The flash kernel where it supports the shape, else the prefixes on the decode's own choice; path 1
+    forces the CUDA-core decode (fp32 P), path 2 the flash kernel (GQA) or the tensor-core decode (MLA)."""
+    def path(layout, total_q=5, hq=8, max_pages=10, opt=None, precise=0):
+        o = None if opt is None and not precise else ctypes.byref(kvq.kvq_extend_options(opt or 0, precise))
+        return lib.kvq_extend_path(ctypes.byref(layout.c()), total_q, hq, max_pages, o)
+    assert path(L()) == 3
+    assert path(L(), opt=1) == 1
+    assert path(L(), opt=2) == 3
+    assert path(L(head_dim=64, v_dim=64)) == 1                  # no flash kernel: the decode's choice
+    assert path(L(head_dim=64, v_dim=64), opt=2) == -8
+    assert path(L(), hq=6) == 1                                 # 3 heads per kv head: CUDA-core decode
+    assert path(L(num_kv_heads=2), hq=24) == 2                  # 12 heads per kv head: tensor-core decode
+    assert path(L(num_kv_heads=2), hq=24, opt=1) == 1
+    mla = L(mla=True, num_kv_heads=1, head_dim=576, v_dim=512)
+    assert path(mla, hq=16) == 1                                # 5 prefixes x 160 tokens: below the MLA cutoff
+    assert path(mla, total_q=2048, hq=16) == 2                  # chunks of 1024 prefixes
+    assert path(mla, total_q=2048, hq=16, opt=1) == 1
+    assert path(mla, hq=16, opt=2) == 2
+    assert path(L(), opt=5) == -1
+    assert path(L(page_size=32)) == -8
+    # precise_p: the flash kernel with P as two bf16 terms; prefixes only on the CUDA-core decode
+    assert path(L(), precise=1) == 4
+    assert path(L(), opt=2, precise=1) == 4
+    assert path(L(), opt=1, precise=1) == 1
+    assert path(L(head_dim=64, v_dim=64), precise=1) == 1
+    assert path(L(num_kv_heads=2), hq=24, precise=1) == 1
+    assert path(mla, total_q=2048, hq=16, precise=1) == 1
+    assert path(mla, hq=16, opt=2, precise=1) == -8
+    assert _extend_ws(lib, L(), 5, 8, 10) == lib.kvq_extend_workspace_bytes_ex(
+        ctypes.byref(L().c()), 5, 8, 10, ctypes.byref(kvq.kvq_extend_options(0, 1)))
 
 
 def test_extend_argument_errors(lib):
@@ -138,16 +179,22 @@ def test_extend_argument_errors(lib):
     assert _extend(lib, L(), sm_scale=float("nan")) == -1
     assert _extend(lib, L(), total_q=-1) == -1
     assert _extend(lib, L(), out_dtype=7) == -1
-    assert _extend(lib, L(head_dim=64, v_dim=64)) == -8        # KVQ_EUNSUPPORTED: head_dim 64
+    # head_dim 64 and 3 heads per kv head have no flash kernel: the prefixes take them, with their workspace
+    assert _extend(lib, L(head_dim=64, v_dim=64)) == -5
+    assert _extend(lib, L(), hq=6) == -5
+    assert _extend(lib, L(), hq=6, path=2) == -8                # the flash kernel asked for: KVQ_EUNSUPPORTED
+    assert _extend(lib, L(), path=3) == -1
+    assert _extend(lib, L(head_dim=96, v_dim=96), ws_bytes=1 << 30) == -8
     mla = L(mla=True, num_kv_heads=1, head_dim=576, v_dim=512)
-    need = lib.kvq_extend_workspace_bytes_ex(ctypes.byref(mla.c()), 5, 16, 10)
+    need = _extend_ws(lib, mla, 5, 16, 10)
     assert need > 256                                           # the decode workspace of the prefixes
-    assert lib.kvq_extend_workspace_bytes_ex(ctypes.byref(L().c()), 5, 8, 10) == 256
-    assert lib.kvq_extend_workspace_bytes_ex(ctypes.byref(mla.c()), -1, 16, 10) == 0
-    assert _extend(lib, mla, hq=16) == -5                       # MLA with the GQA workspace: too small
+    assert _extend_ws(lib, L(), 5, 8, 10) == 256
+    assert _extend_ws(lib, L(), 5, 8, 10, path=1) > 256
+    assert _extend_ws(lib, mla, -1, 16, 10) == 0
+    assert _extend_ws(lib, L(), 5, 8, 10, path=-1) == 0
+    assert _extend(lib, mla, hq=16) == -5                       # MLA with the flash kernel's workspace: too small
     assert _extend(lib, mla, hq=16, ws_bytes=need, ws=FAKE + 8) == -4
     assert _extend(lib, L(mla=True, num_kv_heads=1, head_dim=512, v_dim=512), hq=16, ws_bytes=1 << 30) == -8
-    assert _extend(lib, L(), hq=6) == -8                        # 3 heads per kv head do not divide 128
     assert _extend(lib, L(page_size=32)) == -8
     assert _extend(lib, L(), ws_bytes=16) == -5                 # KVQ_EWORKSPACE
     assert _extend(lib, L(), ws=FAKE + 8) == -4                 # KVQ_EALIGN

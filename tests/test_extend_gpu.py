@@ -5,7 +5,9 @@ bit-exact by the store tests) and declares the last n_b stored tokens of sequenc
 for every (new token, query head) must meet the decode bound (max abs <= 1.5e-2, mean abs <= 2e-3).  The
 cases span several key tiles and query blocks with ragged tails, D = 128 and 256, 1 to 16 query heads per kv
 head, masked pages, a first prefill (every token new), single new tokens and sequences without new tokens.
-The MLA latent row runs through the decode kernels, one causal prefix per new token, with the same bound."""
+The MLA latent row runs through the decode kernels, one causal prefix per new token, with the same bound.
+The same prefix path serves GQA shapes the flash kernel does not (head_dim 64, group sizes not dividing
+128), and, forced onto the CUDA-core decode, keeps P in fp32 and meets the plain bound on spiked V too."""
 import numpy as np
 import pytest
 import torch
@@ -53,11 +55,16 @@ def _stored(key, kind):
     return case, L, codes, scales, oc, osc, q, q_start
 
 
-def _gpu_extend(case, L, codes, scales, q, q_start, out_dtype=torch.float32):
+def _gpu_extend(case, L, codes, scales, q, q_start, out_dtype=torch.float32, path=None, precise_p=False):
     out = torch.full((q.shape[0], case.num_q_heads, case.v_dim), float("nan"), dtype=out_dtype, device="cuda")
-    ws = kvq.alloc_extend_workspace()
+    if path is None and not precise_p:
+        ws = kvq.alloc_extend_workspace()
+    else:
+        ws = kvq.alloc_extend_workspace("cuda", L, q.shape[0], case.num_q_heads, case.max_pages, path=path,
+                                        precise_p=precise_p)
     ws.fill_(0x5A)
-    kvq.kvq_extend(q, codes, scales, case.block_table, case.seq_lens, q_start, out, ws, L, case.kind, case.sm_scale)
+    kvq.kvq_extend(q, codes, scales, case.block_table, case.seq_lens, q_start, out, ws, L, case.kind, case.sm_scale,
+                   path=path, precise_p=precise_p)
     torch.cuda.synchronize()
     return out, ws
 
@@ -89,6 +96,36 @@ def test_extend_matches_the_oracle(key, kind):
         assert_decode_close(got, ref, rel=2.0 ** -8, scale=scale)
     else:
         assert_decode_close(got, ref)
+
+
+@pytest.mark.parametrize("kind", ["fp8_e4m3", "q8_0"])
+@pytest.mark.parametrize("key", list(CASES))
+def test_extend_on_the_cuda_core_decode_meets_the_plain_bound(key, kind):
+    """Path 1: every new token's causal prefix on the CUDA-core decode, P in fp32.  The x100 spikes of the
+    serving family get no widened bound here."""
+    case, L, codes, scales, oc, osc, q, q_start = _stored(key, kind)
+    assert kvq.kvq_extend_path(L, q.shape[0], case.num_q_heads, case.max_pages, path=1) == 1
+    out, ws = _gpu_extend(case, L, codes, scales, q, q_start, path=1)
+    assert kvq.kvq_workspace_status(ws) == 0
+    assert_decode_close(out.cpu().numpy().astype(np.float64), _oracle_extend(case, oc, osc, q, q_start))
+
+
+@pytest.mark.parametrize("kind", ["fp8_e4m3", "q8_0"])
+@pytest.mark.parametrize("key", list(CASES))
+def test_extend_with_p_as_two_bf16_terms_meets_the_plain_bound(key, kind):
+    """precise_p on the flash kernel: P = hi + lo through two PVs (lo in S's own columns at D = 128, in
+    columns of its own at D = 256), so the serving family's x100 spikes need no widened bound."""
+    case, L, codes, scales, oc, osc, q, q_start = _stored(key, kind)
+    assert kvq.kvq_extend_path(L, q.shape[0], case.num_q_heads, case.max_pages, precise_p=True) == 4
+    out, ws = _gpu_extend(case, L, codes, scales, q, q_start, precise_p=True)
+    assert kvq.kvq_workspace_status(ws) == 0
+    ref = _oracle_extend(case, oc, osc, q, q_start)
+    got = out.cpu().numpy().astype(np.float64)
+    assert_decode_close(got, ref)
+    if key in SPIKED:
+        # and it is closer to the oracle than the bf16-P kernel where the spikes dominate
+        plain, _ = _gpu_extend(case, L, codes, scales, q, q_start)
+        assert np.abs(got - ref).max() < np.abs(plain.cpu().numpy().astype(np.float64) - ref).max()
 
 
 def test_extend_bf16_output_is_the_rounded_f32_output():
@@ -192,14 +229,56 @@ def test_mla_extend_skips_a_bad_sequence_with_zeros_and_reports_it():
     assert_decode_close(out[:5].cpu().numpy().astype(np.float64), ref)
 
 
-def test_extend_rejects_unsupported_shapes():
-    case = workloads.make("long_gqa", kind="fp8_e4m3", device="cuda", batch=1, ctx=64, head_dim=64)
-    L = layout_of(case)
-    codes, scales = kvq.alloc_pool(L, "cuda")
-    q = torch.zeros((1, case.num_q_heads, case.head_dim), dtype=torch.bfloat16, device="cuda")
-    out = torch.zeros((1, case.num_q_heads, case.v_dim), dtype=torch.float32, device="cuda")
-    qs = torch.tensor([0, 1], dtype=torch.int32, device="cuda")
+@pytest.mark.parametrize("kind", ["fp8_e4m3", "q8_0"])
+@pytest.mark.parametrize("shape", ["d64", "g3", "g12"])
+def test_extend_shapes_without_a_flash_kernel_run_on_the_prefixes(shape, kind):
+    """head_dim 64, 3 and 12 query heads per kv head: the automatic choice runs each new token's prefix on
+    the decode (CUDA cores for the first two, tensor cores for 12 heads per kv head); asking for the flash
+    kernel is KVQ_EUNSUPPORTED."""
+    kw = {"d64": dict(head_dim=64, num_q_heads=8, num_kv_heads=2),
+          "g3": dict(head_dim=128, num_q_heads=6, num_kv_heads=2),
+          "g12": dict(head_dim=128, num_q_heads=24, num_kv_heads=2)}[shape]
+    case = _case("long_gqa", kind, batch=2, ctx=400, mask_frac=0.03, **kw)
+    L, codes, scales = gpu_pool(case)
+    gpu_store(case, codes, scales)
+    oc, osc = oracle_pool(case)
+    oracle_store(case, oc, osc)
+    q, q_start, _ = workloads.extend_inputs(case, [400, 77])
+    want = 2 if shape == "g12" else 1
+    assert kvq.kvq_extend_path(L, q.shape[0], case.num_q_heads, case.max_pages) == want
+    out, ws = _gpu_extend(case, L, codes, scales, q, q_start, path=0)
+    assert kvq.kvq_workspace_status(ws) == 0
+    assert_decode_close(out.cpu().numpy().astype(np.float64), _oracle_extend(case, oc, osc, q, q_start))
+    assert kvq.kvq_extend_path(L, q.shape[0], case.num_q_heads, case.max_pages, path=2) == KVQ_EUNSUPPORTED
     with pytest.raises(kvq.KvqError) as e:
-        kvq.kvq_extend(q, codes, scales, case.block_table, case.seq_lens, qs, out, kvq.alloc_extend_workspace(), L,
-                       case.kind)
+        kvq.kvq_extend(q, codes, scales, case.block_table, case.seq_lens, q_start, out, kvq.alloc_extend_workspace(),
+                       L, case.kind, case.sm_scale, path=2)
     assert e.value.status == KVQ_EUNSUPPORTED
+
+
+@pytest.mark.parametrize("path", [1, 2])
+def test_mla_extend_on_either_decode_kernel(path):
+    """The MLA prefixes forced onto the CUDA-core (fp32 P) or the tensor-core decode."""
+    kw, n_new, mask = MLA_CASES[0]
+    case, L, codes, scales, oc, osc, q, q_start = _mla_stored("q8_0", n_new, mask, **kw)
+    assert kvq.kvq_extend_path(L, q.shape[0], case.num_q_heads, case.max_pages, path=path) == path
+    out, ws = _gpu_extend(case, L, codes, scales, q, q_start, path=path)
+    assert kvq.kvq_workspace_status(ws) == 0
+    assert_decode_close(out.cpu().numpy().astype(np.float64), _oracle_extend(case, oc, osc, q, q_start))
+
+
+def test_gqa_extend_on_the_prefixes_zeroes_a_bad_sequence_and_reports_it():
+    case, L, codes, scales, oc, osc, q, q_start = _stored("qwen3_small", "fp8_e4m3")
+    lens = case.seq_lens.cpu().tolist()
+    bad = torch.tensor([0, 3, 3 + lens[1] + 1, 3 + lens[1] + 2], dtype=torch.int32, device="cuda")
+    qb = torch.randn((int(bad[-1]), case.num_q_heads, case.head_dim), device="cuda").to(torch.bfloat16) / 12
+    out, ws = _gpu_extend(case, L, codes, scales, qb, bad, path=1)
+    assert kvq.kvq_workspace_status(ws) == KVQ_EINVAL
+    good = np.r_[0:3, int(bad[2]):int(bad[3])]
+    ok_start = torch.tensor([0, 3, 3, 4], dtype=torch.int32)
+    ref = O.extend(bits(qb[good]), oc, osc, case.block_table.cpu().numpy(), case.seq_lens.cpu().numpy(),
+                   ok_start.numpy(), num_q_heads=case.num_q_heads, num_kv_heads=case.num_kv_heads,
+                   head_dim=case.head_dim, v_dim=case.v_dim, page_size=case.page_size, mla=False, kind=case.kind,
+                   sm_scale=case.sm_scale, nthreads=0)
+    assert_decode_close(out[good].cpu().numpy().astype(np.float64), ref)
+    assert not out[3:int(bad[2])].any()  # the skipped sequence's rows are zeros on this path

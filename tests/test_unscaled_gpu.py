@@ -81,16 +81,17 @@ def test_unscaled_sparse_decode_matches_oracle(kind):
     assert_decode_close(out.cpu().numpy().astype(np.float64), ref)
 
 
+@pytest.mark.parametrize("precise", [False, True])
 @pytest.mark.parametrize("kind", KINDS)
 @pytest.mark.parametrize("D", [128, 256])
-def test_unscaled_extend_matches_oracle(kind, D):
+def test_unscaled_extend_matches_oracle(kind, D, precise):
     case, codes, oc = _stored("long_gqa", kind, batch=2, ctx=700, head_dim=D, mask_frac=0.02)
     q, q_start, _ = workloads.extend_inputs(case, [300, 129])
     L = layout_of(case)
     out = torch.full((q.shape[0], case.num_q_heads, case.v_dim), float("nan"), device="cuda")
-    ws = kvq.alloc_extend_workspace("cuda")
+    ws = kvq.alloc_extend_workspace("cuda", L, q.shape[0], case.num_q_heads, case.max_pages, precise_p=precise)
     kvq.kvq_extend(q.cuda(), codes, None, case.block_table.cuda(), case.seq_lens.cuda(), q_start.cuda(), out, ws, L,
-                   kind, case.sm_scale)
+                   kind, case.sm_scale, precise_p=precise)
     torch.cuda.synchronize()
     assert kvq.kvq_workspace_status(ws) == 0
     ref = O.extend(bits(q), oc, None, case.block_table.numpy(), case.seq_lens.numpy(), q_start.numpy(),
