@@ -60,6 +60,9 @@ constexpr int kVRS = 128 * 16;                     // 2048: bytes between 8-toke
 constexpr int kPS = (kTile / 8) * 128;             // 2048: bytes between 8-head groups of P
 constexpr int kMaxBatch = 1024;                    // sequences whose item bases fit the shared table
 constexpr float kLazyRescale = 8.0f;
+// running max of a head before its first valid score: finite, so that s * scale - m stays finite and the
+// first tile's vote fires; padded heads keep +inf, so that their probabilities come out as 2^-inf = 0
+constexpr float kNoMax = -1.0e30f;
 constexpr int kTmemCols = 512;
 
 constexpr int kSmWarps = 8;   // 0-7: warp w covers TMEM lane quarter w % 4 and heads 32 (w / 4) ..
@@ -89,6 +92,14 @@ static_assert(kSlab % 1024 == 0 && VT_OFF % 1024 == 0, "swizzle atoms");
 static_assert(SMEM_BYTES <= 226 * 1024, "shared memory (with the plan's static part)");
 
 }  // namespace mla
+
+// 2^x by the hardware approximation, subnormal results flushed to 0 (far below the bf16 rounding of P);
+// 2^-inf = 0.
+__device__ __forceinline__ float mla_ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 
 __device__ __forceinline__ uint64_t mla_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
   uint64_t d = 0;
@@ -307,7 +318,7 @@ __global__ void __launch_bounds__(mla::kThreads, 1) decode_mla_kernel(const KPar
                  "r"(kTmemCols));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
-  for (int h = tid; h < kHG; h += kThreads) sM[h] = -INFINITY;
+  for (int h = tid; h < kHG; h += kThreads) sM[h] = h < HP ? kNoMax : INFINITY;
   for (int i = tid; i < kHG * kD * 2 / 16; i += kThreads) reinterpret_cast<uint4*>(sQ)[i] = make_uint4(0, 0, 0, 0);
   fence_proxy_async_smem();
   mla_fence_before();
@@ -625,24 +636,32 @@ __global__ void __launch_bounds__(mla::kThreads, 1) decode_mla_kernel(const KPar
         // barrier)?  P is formed with the current running maxima at the same time; it is final unless a
         // maximum moves, which the lazy rescale makes rare, and then it is formed again.
         uint32_t pw[kHS / 2];
+        // d = s * scale - m per head: a max moves when d > 2^8 headroom; p = 2^d (2^-inf = 0 for invalid
+        // tokens and padded heads; the +inf of a head without a max yet is never used: its vote fires)
         auto form_p = [&](bool& moved) {
 #pragma unroll
           for (int g = 0; g < kHS / 16; ++g) {
             float s[16];
             mla_ld16(s_base + g * 16, s);
+            float m[16];
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+              const float4 m4 = *reinterpret_cast<const float4*>(sM + h0 + g * 16 + 4 * q4);
+              m[4 * q4] = m4.x; m[4 * q4 + 1] = m4.y; m[4 * q4 + 2] = m4.z; m[4 * q4 + 3] = m4.w;
+            }
+            bool mv = false;
 #pragma unroll
             for (int h2 = 0; h2 < 8; ++h2) {
               float pr[2];
 #pragma unroll
               for (int e = 0; e < 2; ++e) {
-                const int hd = h0 + g * 16 + 2 * h2 + e;
-                const float m = sM[hd];
-                const float x = (valid && hd < HP) ? s[2 * h2 + e] * p.score_scale : -INFINITY;
-                moved |= (x > -INFINITY) && (m == -INFINITY || x > m + kLazyRescale);
-                pr[e] = (x == -INFINITY || m == -INFINITY) ? 0.0f : exp2f(x - m);
+                const float d = valid ? fmaf(s[2 * h2 + e], p.score_scale, -m[2 * h2 + e]) : -INFINITY;
+                mv |= d > kLazyRescale;
+                pr[e] = mla_ex2(d);
               }
               pw[g * 8 + h2] = pack_bf16x2(pr[0], pr[1]);
             }
+            moved |= mv;
           }
         };
         bool moved = false;
@@ -675,10 +694,10 @@ __global__ void __launch_bounds__(mla::kThreads, 1) decode_mla_kernel(const KPar
             float mx = -INFINITY;
 #pragma unroll
             for (int w = 0; w < 4; ++w) mx = fmaxf(mx, sRed[(half * 4 + w) * kHS + idx]);
-            const float m = sM[tid];
+            const float m = sM[tid];  // kNoMax before the head's first valid score; +inf for padded heads
             float a = 1.0f;
-            if (mx > -INFINITY && (m == -INFINITY || mx > m + kLazyRescale)) {
-              if (m != -INFINITY) a = exp2f(m - mx);
+            if (mx > -INFINITY && mx > m + kLazyRescale) {
+              if (m != kNoMax) a = exp2f(m - mx);
               sM[tid] = mx;
             }
             sA[tid] = a;
@@ -764,10 +783,11 @@ __global__ void __launch_bounds__(mla::kThreads, 1) decode_mla_kernel(const KPar
           float lsum = 0.0f;
 #pragma unroll
           for (int w = 0; w < 4; ++w) lsum += sRed[(half * 4 + w) * kHS + idx];
-          p.part_ml[(static_cast<int64_t>(item) * HP + tid) * 2 + 0] = sM[tid];
+          const float m = sM[tid];
+          p.part_ml[(static_cast<int64_t>(item) * HP + tid) * 2 + 0] = m == kNoMax ? -INFINITY : m;
           p.part_ml[(static_cast<int64_t>(item) * HP + tid) * 2 + 1] = lsum;
         }
-        sM[tid] = -INFINITY;  // the next item starts afresh
+        sM[tid] = tid < HP ? kNoMax : INFINITY;  // the next item starts afresh
       }
       mla_fence_before();
       mla_named_sync(1, kSmWarps * 32);
