@@ -61,8 +61,19 @@ constexpr int kThreads = (kProdWarp + 2) * 32;         // 23 warps
 constexpr int kDwThreads = kDwWarps * 32;
 constexpr int kMaxPlanBatch = 2048;   // sequences whose item bases fit the shared table
 constexpr float kLazyRescale = 8.0f;  // log2 headroom before the running max must move
+// running max of a head before its first valid score: finite, so that s * scale - m stays finite and the
+// tile's vote fires; padded heads (G .. GN - 1) hold +inf, so that their probabilities are 2^-inf = 0
+constexpr float kNoMax = -1.0e30f;
 constexpr int kTmemCols = 512;
 constexpr int kBox = kPage * 128;  // one TMA box: 16 tokens x 128 code bytes of K or of V
+
+// 2^x by the hardware approximation, subnormal results flushed to 0 (far below the bf16 rounding of P);
+// 2^-inf = 0.
+__device__ __forceinline__ float tc_ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 
 template <int D>
 struct TcCfg {
@@ -579,7 +590,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const KParams p,
       float m_used[GN], l_t[GN];
 #pragma unroll
       for (int h = 0; h < GN; ++h) {
-        m_used[h] = -INFINITY;
+        m_used[h] = h < G ? kNoMax : INFINITY;
         l_t[h] = 0.0f;
       }
       bool o_live = false;  // O holds contributions that a rescale must scale
@@ -592,12 +603,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const KParams p,
         const bool valid = sValid[b * kTile + tt] != 0;
         float s[GN];
         tmem_ld_cols<GN>(tS + b * kN + lane_base, s);
+        // d = s * scale - m per head (-inf for an invalid token or a padded head); a max moves when d > 2^8
+        // headroom, which a head without a max yet always reports
         bool moved = false;
 #pragma unroll
-        for (int h = 0; h < GN; ++h) {
-          s[h] = (valid && h < G) ? s[h] * p.score_scale : -INFINITY;
-          moved |= (s[h] > -INFINITY) && (m_used[h] == -INFINITY || s[h] > m_used[h] + kLazyRescale);
-        }
+        for (int h = 0; h < GN; ++h) moved |= valid && fmaf(s[h], p.score_scale, -m_used[h]) > kLazyRescale;
         // does any token of the tile move any head's running max?  (one vote per warp, one barrier)
         const int wv = __any_sync(0xffffffffu, moved);
         if (lane == 0) sFlag[warp] = wv;
@@ -611,7 +621,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const KParams p,
           named_sync(1, kSmWarps * 32);  // sFlag has been read by every warp
 #pragma unroll
           for (int h = 0; h < GN; ++h) {
-            float mx = s[h];
+            float mx = (valid && h < G) ? s[h] * p.score_scale : -INFINITY;
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
             if (lane == 0) sRed[warp * kN + h] = mx;
@@ -622,8 +632,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const KParams p,
             float mx = sRed[h];
 #pragma unroll
             for (int w = 1; w < kSmWarps; ++w) mx = fmaxf(mx, sRed[w * kN + h]);
-            if (mx > -INFINITY && (m_used[h] == -INFINITY || mx > m_used[h] + kLazyRescale)) {
-              if (m_used[h] != -INFINITY) {
+            if (mx > -INFINITY && mx > m_used[h] + kLazyRescale) {  // (never for a padded head: m = +inf)
+              if (m_used[h] != kNoMax) {
                 alpha[h] = exp2f(m_used[h] - mx);
                 rescale = true;
               }
@@ -640,7 +650,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const KParams p,
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
             const int h = 2 * h2 + e;
-            pr[e] = (s[h] == -INFINITY || m_used[h] == -INFINITY) ? 0.0f : exp2f(s[h] - m_used[h]);
+            pr[e] = tc_ex2(valid ? fmaf(s[h], p.score_scale, -m_used[h]) : -INFINITY);
           }
           pw[h2] = pack_bf16x2(pr[0], pr[1]);
           const float2 pb = unpack_bf16x2(pw[h2]);
@@ -691,7 +701,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const KParams p,
 #pragma unroll
         for (int h = 0; h < GN; ++h)
           if (h == tt) mh = m_used[h];
-        p.part_ml[(static_cast<int64_t>(item) * G + tt) * 2 + 0] = mh;
+        p.part_ml[(static_cast<int64_t>(item) * G + tt) * 2 + 0] = mh == kNoMax ? -INFINITY : mh;
         p.part_ml[(static_cast<int64_t>(item) * G + tt) * 2 + 1] = lsum;
       }
       named_sync(1, kSmWarps * 32);
