@@ -101,8 +101,8 @@ struct TcCfg {
   static constexpr int Q_OFF = V_OFF + TILE_BYTES;
   static constexpr int P_OFF = Q_OFF + Q_BYTES;
   static constexpr int RED_OFF = P_OFF + 2 * P_BYTES;
-  static constexpr int FLAG_OFF = RED_OFF + kSmWarps * kN * 4;  // per-warp "max moved" votes
-  static constexpr int VAL_OFF = FLAG_OFF + 16;                  // token validity of each K buffer's tile
+  static constexpr int FLAG_OFF = RED_OFF + kSmWarps * kN * 4;  // per-warp "max moved" votes [2 tile parities]
+  static constexpr int VAL_OFF = FLAG_OFF + 2 * 16;              // token validity of each K buffer's tile
   static constexpr int META_OFF = VAL_OFF + 2 * kTile;           // valid tokens per page: [ring][slot][page]
   static constexpr int TAB_OFF = META_OFF + 2 * STAGES * kPagesPerTile * 4;
   static constexpr int NBARS = 11 + 4 * STAGES;
@@ -610,15 +610,18 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const KParams p,
         for (int h = 0; h < GN; ++h) moved |= valid && fmaf(s[h], p.score_scale, -m_used[h]) > kLazyRescale;
         // does any token of the tile move any head's running max?  (one vote per warp, one barrier)
         const int wv = __any_sync(0xffffffffu, moved);
-        if (lane == 0) sFlag[warp] = wv;
+        // the votes alternate by tile parity: a warp writes the next tile's only after every warp has passed
+        // this tile's barrier below, and nobody reads this tile's after the next tile's barrier
+        int32_t* flags = sFlag + b * kSmWarps;
+        if (lane == 0) flags[warp] = wv;
         named_sync(1, kSmWarps * 32);
-        const bool any_moved = (sFlag[0] | sFlag[1] | sFlag[2] | sFlag[3]) != 0;
+        const bool any_moved = (flags[0] | flags[1] | flags[2] | flags[3]) != 0;
         float alpha[GN];
         bool rescale = false;
 #pragma unroll
         for (int h = 0; h < GN; ++h) alpha[h] = 1.0f;
         if (any_moved) {  // uniform branch: exact tile maxima, then the new running max per head
-          named_sync(1, kSmWarps * 32);  // sFlag has been read by every warp
+          named_sync(1, kSmWarps * 32);  // every warp has read the votes
 #pragma unroll
           for (int h = 0; h < GN; ++h) {
             float mx = (valid && h < G) ? s[h] * p.score_scale : -INFINITY;
@@ -641,7 +644,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const KParams p,
             }
           }
         }
-        named_sync(1, kSmWarps * 32);  // sFlag / sRed are rewritten next tile
         // P row of this token (bf16), and the row sums of exactly those bf16 values
         uint32_t pw[GN / 2];
 #pragma unroll
@@ -686,6 +688,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const KParams p,
       }
       if (!ok) break;
       // ---- item end: (m, l) per head now; O^T at the next item's first tile (or after the last item)
+      named_sync(1, kSmWarps * 32);  // the last tile's maxima in sRed have been read by every warp
 #pragma unroll
       for (int h = 0; h < GN; ++h) {
         float v = l_t[h];
