@@ -208,6 +208,9 @@ kvq_status decode_common(const void* q, const void* pool, const void* scales, co
   a.heads_per_item = w.heads_per_item;
   a.split_align = w.split_align;
   a.target_items = w.target_items;
+  // the GQA tensor-core kernel: one item per SM when the splits come out even (no second pipeline fill
+  // and O readout per SM, half the partials to merge), else about two
+  a.one_wave_items = (w.path == 2 && !layout->mla) ? sm_count() : 0;
   a.min_one_split = (w.path == 1) ? 1 : 0;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   // status word and split counters (the counters only on the CUDA-core path, which merges in-kernel)

@@ -40,6 +40,8 @@ struct DecodeArgs {
   int32_t heads_per_item;  // query heads one work item covers (a tile of the group)
   int32_t split_align;     // automatic split sizes are a multiple of this many pages
   int32_t target_items;    // automatic split sizes aim at about this many work items
+  int32_t one_wave_items;  // nonzero: first try splits sized for this many items (one per resident CTA),
+                           // kept when the batch's items fit; else target_items
   int32_t min_one_split;   // nonzero: every (sequence, group) has at least one split (an empty one when
                            // the sequence has no page), as the kernel that merges in-kernel needs
 };

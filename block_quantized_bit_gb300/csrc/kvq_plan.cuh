@@ -5,6 +5,8 @@
 // C = pages_per_split when the caller fixes it; otherwise C = max(4, ceil(sum_b pages_b * groups /
 // target)) rounded up to `split_align` pages; the host sets the target per kernel (about two waves of
 // the CUDA-core kernel's resident CTAs, two items per SM for the GQA tensor-core kernel, one for MLA).
+// The GQA tensor-core kernel first tries the target of one item per SM and keeps it when the batch's
+// items fit in that many (the rounding of C can push them over; then two per SM).
 // Every CTA derives the same plan from seq_lens on the device, so no planning launch and no host
 // read-back are needed.
 #pragma once
@@ -46,6 +48,7 @@ struct KParams {
   int32_t head_tiles;     // group / heads_per_item
   int32_t pages_per_split;
   int32_t target_items;   // automatic split sizes aim at about this many items
+  int32_t one_wave_items; // nonzero: first try about this many items, kept when the items fit in it
   int32_t min_one_split;  // nonzero: a sequence without pages still gets one (empty) split per group, so
                           // that the kernel which merges in-kernel writes its zero output
   float score_scale;      // sm_scale * log2(e)
@@ -74,7 +77,7 @@ struct Plan {
 
 __device__ Plan make_plan(const KParams& p, int32_t want_item, int32_t want_b) {
   __shared__ long long s_red[32];
-  __shared__ int32_t s_scan[32];
+  __shared__ unsigned long long s_scan[32];
   __shared__ Plan s_plan;
   const int tid = threadIdx.x, nthr = blockDim.x, nwarp = nthr >> 5;
   const int lane = tid & 31, warp = tid >> 5;
@@ -90,31 +93,40 @@ __device__ Plan make_plan(const KParams& p, int32_t want_item, int32_t want_b) {
   long long tot = 0;
   for (int w = 0; w < nwarp; ++w) tot += s_red[w];
   tot *= groups;
-  int32_t C = p.pages_per_split;
-  if (C <= 0) {
-    long long c = (tot + p.target_items - 1) / p.target_items;
-    C = static_cast<int32_t>(c > kMinPagesPerSplit ? c : static_cast<long long>(kMinPagesPerSplit));
-    C = (C + p.split_align - 1) / p.split_align * p.split_align;
-  }
-  // 2) items per sequence, exclusive scan over the batch
-  int32_t mine = 0;
-  auto splits_of = [&](int32_t b) { return max((seq_pages(p, b) + C - 1) / C, p.min_one_split ? 1 : 0); };
-  for (int32_t b = b0; b < b1; ++b) mine += groups * splits_of(b);
-  int32_t incl = mine;
+  auto split_size = [&](int32_t target) {
+    long long c = (tot + target - 1) / target;
+    int32_t cc = static_cast<int32_t>(c > kMinPagesPerSplit ? c : static_cast<long long>(kMinPagesPerSplit));
+    return (cc + p.split_align - 1) / p.split_align * p.split_align;
+  };
+  // C2: the fixed or the target split size; C1: the one-wave size (C2 when there is none)
+  const int32_t C2 = p.pages_per_split > 0 ? p.pages_per_split : split_size(p.target_items);
+  const int32_t C1 = (p.pages_per_split <= 0 && p.one_wave_items > 0) ? split_size(p.one_wave_items) : C2;
+  auto splits_of = [&](int32_t b, int32_t c) { return max((seq_pages(p, b) + c - 1) / c, p.min_one_split ? 1 : 0); };
+  // 2) items per sequence under both sizes (low half C1, high half C2), exclusive scan over the batch
+  unsigned long long mine = 0;
+  for (int32_t b = b0; b < b1; ++b)
+    mine += static_cast<unsigned long long>(groups * splits_of(b, C1)) |
+            (static_cast<unsigned long long>(groups * splits_of(b, C2)) << 32);
+  unsigned long long incl = mine;
   for (int o = 1; o < 32; o <<= 1) {
-    const int32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+    const unsigned long long y = __shfl_up_sync(0xffffffffu, incl, o);
     if (lane >= o) incl += y;
   }
   if (lane == 31) s_scan[warp] = incl;
   __syncthreads();
-  int32_t warp_off = 0, total_items = 0;
+  unsigned long long warp_off = 0, totals = 0;
   for (int w = 0; w < nwarp; ++w) {
     if (w < warp) warp_off += s_scan[w];
-    total_items += s_scan[w];
+    totals += s_scan[w];
   }
-  int32_t run = warp_off + incl - mine;  // first item of b0
+  // one wave when every item has a resident CTA
+  const bool one = C1 != C2 && static_cast<uint32_t>(totals) <= static_cast<uint32_t>(p.one_wave_items);
+  const int32_t C = one ? C1 : C2;
+  auto pick = [&](unsigned long long v) { return static_cast<int32_t>(one ? (v & 0xFFFFFFFFull) : (v >> 32)); };
+  const int32_t total_items = pick(totals);
+  int32_t run = pick(warp_off + incl - mine);  // first item of b0
   for (int32_t b = b0; b < b1; ++b) {
-    const int32_t ns = splits_of(b);
+    const int32_t ns = splits_of(b, C);
     const int32_t n = groups * ns;
     if (blockIdx.x == 0 && p.plan_tab) {  // for the merge, which then needs no plan of its own
       p.plan_tab[2 * b] = run;
@@ -170,6 +182,7 @@ inline KParams make_kparams(const DecodeArgs& a) {
   p.score_scale = a.sm_scale * kLog2e;
   p.split_align = a.split_align;
   p.target_items = a.target_items > 0 ? a.target_items : kTargetItems;
+  p.one_wave_items = a.one_wave_items;
   p.min_one_split = a.min_one_split;
   return p;
 }
