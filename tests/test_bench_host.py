@@ -124,3 +124,18 @@ def test_oracle_sample_with_a_token_cap_counts_the_prefix_it_decodes():
     finally:
         _sys.argv = argv
     assert a.workload == "long_gqa" and a.kind == "fp8_e4m3" and a.batch is None and a.ctx is None
+
+
+def test_extend_launch_count_and_kernel_name_follow_the_kernel_choice():
+    """The extend's gpu_launches claim: the store plus the flash kernel (choice 3 or 4), or the store, the
+    prefix expansion and per chunk of 1024 new tokens the decode (with its merge on the tensor-core path)."""
+    assert bench.extend_launches(3, 16384) == 2
+    assert bench.extend_launches(4, 16384) == 2
+    assert bench.extend_launches(1, 1000) == 3
+    assert bench.extend_launches(1, 2049) == 2 + 3
+    assert bench.extend_launches(2, 2048) == 2 + 2 * 2
+    assert bench.extend_launches(2, 1) == 4
+    assert "two bf16 terms" in bench.extend_kernel_name(4)
+    assert "extend_tc_kernel" in bench.extend_kernel_name(3)
+    assert "CUDA-core" in bench.extend_kernel_name(1)
+    assert "tensor-core" in bench.extend_kernel_name(2)
