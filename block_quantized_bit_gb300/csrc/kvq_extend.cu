@@ -12,14 +12,14 @@
 // heads of a kv head share every dequantized K and V tile:
 //   S[128 rows][T keys]  = Q[128][D] . Kd[T][D]^T   (A = Q, B = the K tile; both K-major in shared memory)
 //   O[128 rows][D]      += P[128][T] . Vd[T][D]     (A = P in tensor memory, B = the V tile read MN-major)
-// P enters the MMA as bf16.  The SPLIT instances feed it as two bf16 terms, P = hi + lo with hi = bf16(p)
-// and lo = bf16(p - hi), through a second PV into the same O: the product then carries P to about 2^-17
-// relative instead of 2^-9, for twice the PV MMAs.  (All their exponentials run on the MUFU unit: the FMA-
-// pipe cubic's 1.5e-4 would otherwise dominate that error.)
 // with fp32 S and O in tensor memory.  Q, K and V use the canonical no-swizzle core-matrix layout
 //   off(t, d) = (t % 8) * 16 + (t / 8) * RS + (d % 8) * 2 + (d / 8) * 128,   RS = D * 16,
 // with t the row (query row or key): K-major descriptors take LBO = 128 and SBO = RS, the MN-major one
 // LBO = RS and SBO = 128.  T = 128 keys per tile at D = 128 and 64 at D = 256 (shared memory).
+// P enters the MMA as bf16.  The SPLIT instances feed it as two bf16 terms, P = hi + lo with hi = bf16(p)
+// and lo = bf16(p - hi), through a second PV into the same O: the product then carries P to about 2^-17
+// relative instead of 2^-9, for twice the PV MMAs.  (All their exponentials run on the MUFU unit: the FMA-
+// pipe cubic's 1.5e-4 would otherwise dominate that error.)
 //
 // One persistent CTA per SM, 19 warps:
 //   warps 17-18 producers, one for K and one for V: TMA copies of a tile's codes (128-byte swizzled boxes of
