@@ -282,3 +282,15 @@ def test_gqa_extend_on_the_prefixes_zeroes_a_bad_sequence_and_reports_it():
                    sm_scale=case.sm_scale, nthreads=0)
     assert_decode_close(out[good].cpu().numpy().astype(np.float64), ref)
     assert not out[3:int(bad[2])].any()  # the skipped sequence's rows are zeros on this path
+
+
+@pytest.mark.parametrize("precise", [False, True])
+@pytest.mark.parametrize("path", [None, 1, 2])
+def test_extend_with_no_new_token_is_a_no_op_on_every_kernel_choice(path, precise):
+    """total_q = 0 (every q_start entry 0): nothing is written and the status word is clear, on the flash
+    kernel, the prefixes and the two-term P instances alike."""
+    case, L, codes, scales, oc, osc, q, q_start = _stored("qwen3_small", "fp8_e4m3")
+    empty_q = q[:0]
+    zeros = torch.zeros_like(q_start)
+    out, ws = _gpu_extend(case, L, codes, scales, empty_q, zeros, path=path, precise_p=precise)
+    assert out.numel() == 0 and kvq.kvq_workspace_status(ws) == 0
