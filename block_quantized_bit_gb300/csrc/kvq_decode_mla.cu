@@ -39,6 +39,7 @@
 #include "kvq_device.cuh"
 #include "kvq_internal.h"
 #include "kvq_plan.cuh"
+#include "kvq_tc.cuh"
 
 namespace kvq {
 namespace {
@@ -550,10 +551,9 @@ __global__ void __launch_bounds__(mla::kThreads, 1) decode_mla_kernel(const KPar
         if (__shfl_sync(0xffffffffu, ready, 0)) {
           mla_fence_after();
           const uint64_t dV = dV0 + static_cast<uint64_t>((vb * kTile * 128 * 2) >> 4);
-#pragma unroll
-          for (int ks = 0; ks < kTile / 16; ++ks)
-            mla_mma_ss(tO + cp * 64, dV + static_cast<uint64_t>((ks * 2 * kVRS) >> 4),
-                       dP + static_cast<uint64_t>((ks * 2 * 128) >> 4), idesc_pv, (tp.i > 0 || ks > 0) ? 1u : 0u);
+          static_assert(kTile / 16 == 8, "one group of eight k-steps per V block");
+          mma8_bf16(tO + cp * 64, dV, static_cast<uint64_t>((2 * kVRS) >> 4), dP, static_cast<uint64_t>((2 * 128) >> 4),
+                    idesc_pv, tp.i > 0 ? 1u : 0u);
           mla_commit(&bar_v_free[vb]);
           if (cp == kVBlocks - 1) mla_commit(&bar_pv_done[np & 1]);
           __syncwarp();
@@ -577,10 +577,8 @@ __global__ void __launch_bounds__(mla::kThreads, 1) decode_mla_kernel(const KPar
           const uint32_t d_s = tS + (nq & 1) * 64;
           const uint32_t a0 = tK + ks * 64;
           if (jq < 4) {
-#pragma unroll
-            for (int k = 0; k < 8; ++k)
-              mla_mma_ts(d_s, a0 + k * 8, dQ + static_cast<uint64_t>(((16 * jq + 2 * k) * 128) >> 4), idesc_qk,
-                         (jq > 0 || k > 0) ? 1u : 0u);
+            mma8_bf16_tmem_a(d_s, a0, 8u, dQ + static_cast<uint64_t>(((16 * jq) * 128) >> 4),
+                             static_cast<uint64_t>((2 * 128) >> 4), idesc_qk, jq > 0 ? 1u : 0u);
           } else {
 #pragma unroll
             for (int k = 4; k < 8; ++k)  // dims 512..575 sit in the upper half of the slot

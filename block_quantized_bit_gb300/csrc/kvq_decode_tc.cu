@@ -507,10 +507,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const KParams p,
             const uint64_t dP = dP0 + static_cast<uint64_t>((b * Cfg::P_BYTES) >> 4);
 #pragma unroll
             for (int oc = 0; oc < Cfg::O_CHUNKS; ++oc) {
-#pragma unroll
-              for (int ks = 0; ks < kTile / 16; ++ks)
-                mma_bf16(o + oc * kN, dV + static_cast<uint64_t>((oc * 16 * 128 + ks * 2 * Cfg::RS) >> 4),
-                         dP + static_cast<uint64_t>((ks * 2 * 128) >> 4), idesc_pv, (tp.i > 0 || ks > 0) ? 1u : 0u);
+              static_assert(kTile / 16 == 8, "one group of eight k-steps per O chunk");
+              mma8_bf16(o + oc * kN, dV + static_cast<uint64_t>((oc * 16 * 128) >> 4),
+                        static_cast<uint64_t>((2 * Cfg::RS) >> 4), dP, static_cast<uint64_t>((2 * 128) >> 4),
+                        idesc_pv, tp.i > 0 ? 1u : 0u);
               if (oc == 0 && Cfg::O_CHUNKS == 2) mma_commit(&bar_pv_lo[b]);
             }
             mma_commit(&bar_pv_done[b]);
@@ -532,8 +532,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const KParams p,
           {
             const uint32_t ka = tK + b * Cfg::KCOLS;
 #pragma unroll
-            for (int ks = 0; ks < D / 16; ++ks)
-              mma_bf16_tmem_a(tS + b * kN, ka + ks * 8, dQ + static_cast<uint64_t>((ks * 256) >> 4), idesc_qk, ks > 0);
+            for (int g8 = 0; g8 < D / 128; ++g8)  // k-steps 8 g8 .. 8 g8 + 7
+              mma8_bf16_tmem_a(tS + b * kN, ka + g8 * 64, 8u, dQ + static_cast<uint64_t>((g8 * 8 * 256) >> 4),
+                               static_cast<uint64_t>(256 >> 4), idesc_qk, g8 > 0 ? 1u : 0u);
             mma_commit(&bar_qk_done[b]);
           }
           __syncwarp();
