@@ -33,10 +33,9 @@ __device__ __forceinline__ void tmem_st16u(uint32_t taddr, const uint32_t (&r)[1
 }
 
 // The MMA and commit helpers are warp-collective: all 32 lanes of the converged MMA warp call them with the
-// same operands and the lane chosen by elect.sync issues.  The descriptors then stay in uniform registers
-// (a probe measured 15 clocks per MMA with A in tensor memory and 40 with A in shared memory, against 56
-// from a lane-0 branch).  The full mask elects the same lane every time, so a commit tracks every MMA
-// issued before it.
+// same operands and the lane chosen by elect.sync issues, so the descriptors stay in uniform registers (an
+// elected issue beat a lane-0 branch).  The full mask elects the same lane every time, so a commit tracks
+// every MMA issued before it.
 __device__ __forceinline__ void mma_bf16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc,
                                                 uint32_t acc) {
   asm volatile(
